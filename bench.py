@@ -1,0 +1,520 @@
+#!/usr/bin/env python3
+"""Benchmark of the reduce-copy and batched-copy engine on GB300.
+
+Default line (rank 0 prints one JSON object):
+  workload  3-source reduce-copy, 3 x 67,108,864 float32 (256 MiB each),
+            src_k = PrepSrcValue(k, i), SRC_ROTATE_BYTES = 256 MiB (K = 1);
+  step      one reduce-copy launch over the whole transfer (1 GiB moved:
+            3 x 256 MiB read + 256 MiB written); inputs (1 GiB) exceed the
+            129 MB L2, so no flush is needed between steps;
+  value     HBM GB/s counting read + write bytes, summed over ranks;
+  e2e       the same transfer through tb_reduce_copy_host from pinned host
+            buffers: host-to-device sources, the kernel, device-to-host dst;
+  batch     the 47,540-descriptor batch (47,520 head-sliced pages of
+            64 B-16 KiB + 16 x 16 MiB + 4 x 8 MiB) through tb_batch_copy,
+            with one cudaMemcpyAsync per copy (tb_copy_each) timed beside it;
+  roofline  achieved algorithmic GB/s of the reduce kernel against the
+            measured HBM copy bandwidth (MEASURED_PEAKS.json);
+  cpu_baseline  the CPU oracle on a bounded sample, one host core.
+
+``--impl reference`` times the CPU oracle itself (the reference arm of this
+benchmark) on the same metric.  Under torchrun every rank runs its own
+replica on its own GPU (no data exchange); timings are the max over ranks.
+``--study`` prints extra lines (single 4 MiB transfer, the fillCompress
+sweep with rotation on and off, cold and warm) instead of the default line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MiB = 1 << 20
+GiB = 1 << 30
+METRIC = ("HBM GB/s (read+write) and % of GB300 HBM peak; copies/s for batched small copies")
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("3-source reduce-copy: 3 x 67,108,864 float32 (256 MiB each), src_k = "
+            "PrepSrcValue(k, i), k = 0..2, dst = src0 + src1 + src2 left to right in fp32, "
+            "SRC_ROTATE_BYTES = 256 MiB (K = 1)")
+
+
+# ---------------------------------------------------------------------------
+# Process group (torchrun) and timing helpers
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Ranks:
+    """Barrier and max/sum over ranks; a no-op for one process."""
+
+    def __init__(self, world: int, backend: str):
+        self.world = world
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+            self.backend = backend
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def reduce(self, value: float, op: str) -> float:
+        if not self.dist:
+            return value
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([value], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=getattr(self.dist.ReduceOp, op))
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+def combine(ranks: Ranks, units: float, seconds: float):
+    """Whole-job throughput: units summed over ranks / the slowest rank's time."""
+    total_units = ranks.reduce(units, "SUM")
+    worst = ranks.reduce(seconds, "MAX")
+    return total_units, worst
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def kernel_source_sha() -> str:
+    with open(os.path.join(ROOT, "copy_reduce_dst_gb300", "csrc", "tb_kernels.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel source changed after the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            entry = json.load(f)[key]
+    except (OSError, KeyError, ValueError):
+        return None
+    if entry.get("kernel_source_sha256") != kernel_source_sha():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            self.out = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and time.time() - t0 < timeout:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Reduce-copy (default line)
+# ---------------------------------------------------------------------------
+def run_reduce(args, tb, torch, ranks, local):
+    nb = 256 * MiB
+    n_src = 3
+    rotate = 256 * MiB
+    plan = tb.rotation_plan(nb, rotate)
+    ctx = tb.Context(local)
+    stream = torch.cuda.current_stream()
+    srcs = [torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda") for _ in range(n_src)]
+    for k, s in enumerate(srcs):
+        ctx.fill_source(s, nb, tb.default_pattern(), k, stream)
+    ctx.prepare_sources(srcs, nb, rotate)
+    dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    bytes_per_step = (n_src + 1) * nb
+    subexec = 32
+
+    # Sub-executor sweep with the library's own per-iteration events
+    # (TransferBench's loop: 3 warm-up + 20 timed iterations each).
+    sweep = {}
+    for se in (1, 4, 16, 32):
+        r = ctx.run_transfer(srcs, dst, nb, num_subexec=se, iters=20, rotate_bytes=rotate)
+        sweep[str(se)] = {"gbps": round(r["gbps"], 1), "ctas": r["ctas"],
+                          "median_ms": round(r["median_ms"], 4)}
+    strict = {}
+    with tb.Context(local, tb.options(ctas_per_subexec=1)) as c1:
+        for se in (1, 4, 16, 32):
+            r = c1.run_transfer(srcs, dst, nb, num_subexec=se, iters=5, rotate_bytes=rotate)
+            strict[str(se)] = {"gbps": round(r["gbps"], 1), "ctas": r["ctas"]}
+
+    def srcs_at(step):
+        off = tb.slice_for_iteration(step, plan.K) * plan.slice_stride
+        return [s.data_ptr() + off for s in srcs]
+
+    def step(i):
+        ctx.reduce_copy(srcs_at(i), dst, nb, subexec, stream)
+
+    for i in range(-args.warmup, 0):
+        step(i)
+    sampler = ClockSampler(local)
+    sampler.wait_first()
+    # Untimed soak so the clock samples cover a steady load, then the timed loop.
+    t_end = time.time() + 0.5
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    units, worst_s = combine(ranks, bytes_per_step * args.steps, ms / 1e3)
+    value = units / worst_s / 1e9
+    per_launch_s = (ms / 1e3) / args.steps
+    achieved = bytes_per_step / per_launch_s / 1e9
+    peak, peak_kind = read_peaks()
+
+    # End to end from pinned host memory (public API: tb_reduce_copy_host).
+    hsrc = [torch.empty(nb, dtype=torch.uint8).pin_memory() for _ in range(n_src)]
+    for h, s in zip(hsrc, srcs):
+        h.copy_(s[:nb].cpu())
+    hdst = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    dsrc = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(n_src)]
+    for i in range(args.warmup):
+        ctx.reduce_copy_host(hsrc, hdst, nb, dsrc, dst, subexec, stream)
+    e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    ranks.barrier()
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(e_steps):
+        ctx.reduce_copy_host(hsrc, hdst, nb, dsrc, dst, subexec, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ranks.barrier()
+    e_ms = ev0.elapsed_time(ev1)
+    e_units, e_worst = combine(ranks, bytes_per_step * e_steps, max(e_ms / 1e3, wall))
+    e2e = {"value": round(e_units / e_worst / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": n_src * nb, "d2h_bytes_per_step": nb,
+           "api": "tb_reduce_copy_host", "steps": e_steps}
+    ctx.close()
+    del srcs, dsrc, hsrc, hdst
+    torch.cuda.empty_cache()
+
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic("reduce_3src_256MiB"),
+                "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": bytes_per_step,
+                "kernel": "k_reduce (3 sources, 32-byte vectors)"}
+    result = {"value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "e2e": e2e,
+              "clocks": clocks, "gpu_launches": args.steps,
+              "subexec_sweep": sweep, "strict_one_cta_per_subexec": strict,
+              "subexec": subexec}
+    return result
+
+
+# ---------------------------------------------------------------------------
+# Batched copy (47,540 descriptors)
+# ---------------------------------------------------------------------------
+def run_batch(args, tb, torch, ranks, local):
+    from copy_reduce_dst_gb300 import workloads
+    layout = workloads.batch_head_sliced()
+    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    stream = torch.cuda.current_stream()
+    ctx = tb.Context(local, tb.options(time_kernels=1))
+    n = layout.n
+    payload = 2 * layout.total_bytes
+
+    for _ in range(args.warmup):
+        ctx.batch_copy(desc, stream)
+    torch.cuda.synchronize()
+    # device time of back-to-back calls (descriptor upload + kernel)
+    ranks.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ctx.batch_copy(desc, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall_total = time.perf_counter() - t0
+    ranks.barrier()
+    dev_ms = ev0.elapsed_time(ev1) / args.steps
+    stats = ctx.last_batch_stats()
+    # kernel-only device time and per-call wall time (pack + upload + kernel + sync)
+    kern, walls = [], []
+    for _ in range(max(3, min(args.steps, 10))):
+        t0 = time.perf_counter()
+        ctx.batch_copy(desc, stream)
+        stream.synchronize()
+        walls.append(time.perf_counter() - t0)
+        kern.append(ctx.last_batch_kernel_ms())
+    kernel_ms = statistics.median(kern)
+    wall_ms = statistics.median(walls) * 1e3
+    # one cudaMemcpyAsync per copy, timed the same way
+    each = []
+    for _ in range(2):
+        t0 = time.perf_counter()
+        ctx.copy_each(desc, stream)
+        stream.synchronize()
+        each.append(time.perf_counter() - t0)
+    each_ms = min(each) * 1e3
+    ctx.close()
+    peak, peak_kind = read_peaks()
+    algo = payload + stats["upload_bytes"]  # the kernel also reads each work item once
+    units, worst = combine(ranks, n * args.steps, wall_total)
+    return {
+        "workload": layout.name + " (uint8, two 2 GiB pools, seeded layout)",
+        "descriptors": n, "bytes_copied": layout.total_bytes,
+        "copies_per_s": round(units / worst, 1),
+        "gbps_rw_device": round(payload / (dev_ms / 1e3) / 1e9, 1),
+        "device_ms_per_batch": round(dev_ms, 4),
+        "kernel_ms": round(kernel_ms, 4),
+        "wall_ms_per_batch": round(wall_ms, 4),
+        "memcpy_each_wall_ms": round(each_ms, 3),
+        "speedup_vs_memcpy_each": round(each_ms / wall_ms, 1),
+        "work_items": {"warp": stats["warp_items"], "cta": stats["cta_items"],
+                       "launches": stats["launches"], "upload_bytes": stats["upload_bytes"]},
+        "roofline": {"bound": "hbm", "achieved": round(algo / (kernel_ms / 1e3) / 1e9, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(algo / (kernel_ms / 1e3) / 1e9 / peak, 4),
+                     "traffic": profiled_traffic("batch_head_sliced"),
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
+                     "kernel": "k_batch"},
+    }
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings
+# ---------------------------------------------------------------------------
+def oracle_sample(budget_s: float, n: int = 4 * MiB):
+    """The oracle's dstReference over 3 default-pattern sources of n float32,
+    repeated until budget_s has passed; returns (GB/s, reps, seconds)."""
+    import oracle
+    refs = [oracle.prepare_reference(n, k) for k in range(3)]
+    oracle.dst_reference(refs)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.dst_reference(refs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return 4 * 4 * n * reps / el / 1e9, reps, el
+
+
+def cpu_baseline(budget_s: float):
+    gbps, reps, el = oracle_sample(budget_s)
+    return {"value": round(gbps, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"dstReference[3] over 3 x 4,194,304 float32 default-pattern sources "
+                      f"(64 MiB moved per call), {reps} calls in {el:.1f} s, single thread"}
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    n = 4 * MiB
+    refs = [oracle.prepare_reference(n, k) for k in range(3)]
+    for _ in range(args.warmup):
+        oracle.dst_reference(refs)
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.dst_reference(refs)
+        times.append(time.perf_counter() - t)
+    el = time.perf_counter() - t0
+    value = 4 * 4 * n * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "3 x 4,194,304 float32 per step",
+                   "parallelism": "none (CPU, 1 thread)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"dstReference[3] over 3 x 4,194,304 float32 per step, "
+                                   f"{args.steps} steps"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Study lines (not the default): single transfer and the fillCompress sweep
+# ---------------------------------------------------------------------------
+def study(args, tb, torch, local):
+    import statistics as st
+    peak, _ = read_peaks()
+    flush = torch.empty(512 * MiB, dtype=torch.uint8, device="cuda")
+    with tb.Context(local) as ctx:
+        nb = 4 * MiB
+        plan = tb.rotation_plan(nb, 256 * MiB)
+        src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
+        ctx.fill_source(src, nb, tb.default_pattern(), 0)
+        ctx.prepare_sources([src], nb, 256 * MiB)
+        dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        r = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
+        print(json.dumps({"study": "single transfer 4 MiB, K=64", "gbps": r["gbps"],
+                          "median_ms": r["median_ms"], "K": r["K"],
+                          "alloc_bytes": r["alloc_bytes"], "gated": r["gated"]}), flush=True)
+        del src
+        pct = (40, 20, 0, 20, 20)
+        for mib in (8, 16, 32, 64, 128, 256, 512):
+            nb = mib * MiB
+            row = {"study": "fillCompress sweep", "MiB": mib}
+            for rot in (256 * MiB, 0):
+                plan = tb.rotation_plan(nb, rot)
+                src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
+                ctx.fill_source(src, nb, tb.compress_pattern(pct, 0x5EED), 0)
+                ctx.prepare_sources([src], nb, rot)
+                dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+                cold, warm = [], []
+                for rep in range(3):
+                    flush.fill_(rep)
+                    rc = ctx.run_transfer([src], dst, nb, iters=1, rotate_bytes=rot)
+                    cold.append(rc["gbps"])
+                    rw = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=rot)
+                    warm.append(rw["median_ms"])
+                tag = "on" if rot else "off"
+                warm_gbps = 2 * nb / (st.median(warm) / 1e3) / 1e9
+                row[f"{tag}_cold_gbps"] = round(st.median(cold), 1)
+                row[f"{tag}_warm_gbps"] = round(warm_gbps, 1)
+                row[f"{tag}_w_over_c"] = round(warm_gbps / st.median(cold), 3)
+                row[f"{tag}_K"] = plan.K
+                del src, dst
+            print(json.dumps(row), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-batch", action="store_true")
+    ap.add_argument("--study", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    from copy_reduce_dst_gb300 import tb  # fails loudly if libtb.so is missing
+    if args.study:
+        return study(args, tb, torch, local)
+    ranks = Ranks(world, "nccl")
+    red = run_reduce(args, tb, torch, ranks, local)
+    batch = None if args.no_batch else run_batch(args, tb, torch, ranks, local)
+    cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(red["value"], 1), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(red["ms_per_step"], 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "num_subexec": red["subexec"],
+                       "step": "one reduce-copy launch over 3 x 256 MiB -> 256 MiB "
+                               "(1,073,741,824 B moved)",
+                       "l2": "inputs larger than L2 (1 GiB per step vs 129 MB), no flush",
+                       "parallelism": f"replicas x{world} (no data exchange)",
+                       "subexec_sweep": red["subexec_sweep"],
+                       "strict_one_cta_per_subexec": red["strict_one_cta_per_subexec"],
+                       "pct_of_peak": round(red["value"] / world / read_peaks()[0] * 100, 1)},
+            "roofline": red["roofline"], "cpu_baseline": cpu, "e2e": red["e2e"],
+            "clocks": red["clocks"], "gpu_launches": red["gpu_launches"], "batch": batch,
+        }
+        print(json.dumps(line), flush=True)
+    ranks.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,984 @@
+// Host runtime of libtb: options, contexts, the rotation allocator's plan and
+// slice fill, TransferBench's timed iteration loop, the descriptor-slot ring
+// of the batched copy, and validation.  Every GPU step is one of the kernels
+// in tb_kernels.cu; this file only plans, enqueues and times them.
+
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "tb_internal.h"
+
+using tb::WorkItem;
+
+namespace {
+
+constexpr uint64_t kMiB = 1ull << 20;
+constexpr uint64_t kValidateChunk = 64 * kMiB;
+// Most launches queued behind the gate kernel; beyond this the launch queue
+// could fill while the gate holds the stream, so longer loops run ungated.
+constexpr int kMaxGatedLaunches = 256;
+
+struct Slot {
+    WorkItem *dev = nullptr;   // device copy of the packed items
+    WorkItem *host = nullptr;  // pinned staging
+    cudaEvent_t done = nullptr;
+    bool pending = false;      // `done` recorded and maybe not reached yet
+    cudaEvent_t t0 = nullptr;  // kernel timing (time_kernels only)
+    cudaEvent_t t1 = nullptr;
+};
+
+}  // namespace
+
+struct tb_ctx {
+    int device = 0;
+    int num_sms = 0;
+    tb_options opt{};
+    cudaStream_t stream = nullptr;  // internal stream of the synchronous calls
+
+    // Gate: host-mapped words the gate kernel polls and reports through.
+    volatile uint32_t *gate_flag = nullptr;
+    volatile uint32_t *gate_status = nullptr;
+    uint32_t *gate_flag_dev = nullptr;
+    uint32_t *gate_status_dev = nullptr;
+
+    std::vector<cudaEvent_t> events;  // timing events of tb_run_transfer
+    std::vector<float> iter_ms;
+
+    std::vector<Slot> slots;
+    uint32_t next_slot = 0;
+    std::vector<WorkItem> pack;       // packing area when a batch spans slots
+    std::vector<uint32_t> bucket;     // counting-sort buckets
+    tb_batch_stats last_batch{};
+    std::vector<uint32_t> last_slots;  // slots the last batch launched on
+
+    void *val_stage = nullptr;        // pinned validation staging
+    uint64_t prep_h2d = 0;
+    std::string err;
+};
+
+namespace {
+
+// Records a message on ctx and returns code.
+int fail(tb_ctx *ctx, int code, const char *fmt, ...) __attribute__((format(printf, 3, 4)));
+int fail(tb_ctx *ctx, int code, const char *fmt, ...)
+{
+    if (ctx) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        ctx->err = buf;
+    }
+    return code;
+}
+
+int cuda_fail(tb_ctx *ctx, cudaError_t e, const char *what)
+{
+    return fail(ctx, TB_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define TB_CUDA(ctx, call)                                   \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess)                               \
+            return cuda_fail((ctx), e_, #call);              \
+    } while (0)
+
+// Makes ctx's device current for the scope and restores the caller's after.
+class DeviceScope {
+  public:
+    explicit DeviceScope(int device)
+    {
+        if (cudaGetDevice(&prev_) == cudaSuccess && prev_ != device)
+            ok_ = cudaSetDevice(device) == cudaSuccess;
+        else
+            prev_ = -1;
+    }
+    ~DeviceScope()
+    {
+        if (prev_ >= 0)
+            cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+  private:
+    int prev_ = -1;
+    bool ok_ = true;
+};
+
+bool env_u64(const char *name, uint64_t *out, bool *bad)
+{
+    const char *v = getenv(name);
+    if (!v)
+        return false;
+    if (tb_parse_bytes(v, out) != TB_OK)
+        *bad = true;
+    return true;
+}
+
+bool env_i32(const char *name, int32_t *out, bool *bad)
+{
+    uint64_t v = 0;
+    if (!env_u64(name, &v, bad))
+        return false;
+    if (v > (uint64_t)INT32_MAX)
+        *bad = true;
+    else
+        *out = (int32_t)v;
+    return true;
+}
+
+bool env_u32(const char *name, uint32_t *out, bool *bad)
+{
+    uint64_t v = 0;
+    if (!env_u64(name, &v, bad))
+        return false;
+    if (v > (uint64_t)UINT32_MAX)
+        *bad = true;
+    else
+        *out = (uint32_t)v;
+    return true;
+}
+
+int check_options(tb_ctx *ctx, const tb_options &o)
+{
+    if (o.byte_offset % 4 != 0)
+        return fail(ctx, TB_EINVAL, "byte_offset must be a multiple of 4");
+    if (o.warmup < 0)
+        return fail(ctx, TB_EINVAL, "warmup must be >= 0");
+    if (o.memset_byte > 255)
+        return fail(ctx, TB_EINVAL, "memset_byte must be a byte");
+    if (o.ctas_per_subexec < 0)
+        return fail(ctx, TB_EINVAL, "ctas_per_subexec must be >= 0");
+    if (o.block_threads < 0 || o.block_threads > 512 || o.block_threads % 32 != 0)
+        return fail(ctx, TB_EINVAL, "block_threads must be a multiple of 32 up to 512");
+    if (o.small_max_bytes == 0 || o.small_max_bytes > 16 * kMiB)
+        return fail(ctx, TB_EINVAL, "small_max_bytes must be in [1, 16 MiB]");
+    if (o.chunk_bytes < 4096 || o.chunk_bytes % 4096 != 0 || o.chunk_bytes > (1ull << 31))
+        return fail(ctx, TB_EINVAL, "chunk_bytes must be a multiple of 4096 up to 2 GiB");
+    if (o.slot_items < 1024 || o.slot_items > (1u << 24))
+        return fail(ctx, TB_EINVAL, "slot_items must be in [1024, 2^24]");
+    if (o.num_slots < 1 || o.num_slots > 64)
+        return fail(ctx, TB_EINVAL, "num_slots must be in [1, 64]");
+    if (o.wait_timeout_ns == 0)
+        return fail(ctx, TB_EINVAL, "wait_timeout_ns must be > 0");
+    if (o.vec_bytes != 0 && o.vec_bytes != 4 && o.vec_bytes != 16 && o.vec_bytes != 32)
+        return fail(ctx, TB_EINVAL, "vec_bytes must be 0, 4, 16 or 32");
+    if (o.unroll != 0 && o.unroll != 1 && o.unroll != 2 && o.unroll != 4)
+        return fail(ctx, TB_EINVAL, "unroll must be 0, 1, 2 or 4");
+    return TB_OK;
+}
+
+uint64_t now_ns()
+{
+    return (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(
+               std::chrono::steady_clock::now().time_since_epoch())
+        .count();
+}
+
+// Waits for a slot's previous launch, bounded by the context's timeout.
+int wait_slot(tb_ctx *ctx, Slot &s)
+{
+    if (!s.pending)
+        return TB_OK;
+    const uint64_t deadline = now_ns() + ctx->opt.wait_timeout_ns;
+    for (;;) {
+        cudaError_t e = cudaEventQuery(s.done);
+        if (e == cudaSuccess)
+            break;
+        if (e != cudaErrorNotReady)
+            return cuda_fail(ctx, e, "cudaEventQuery(slot)");
+        if (now_ns() > deadline)
+            return fail(ctx, TB_ETIMEOUT, "no descriptor slot came free within %llu ns",
+                        (unsigned long long)ctx->opt.wait_timeout_ns);
+        std::this_thread::yield();
+    }
+    s.pending = false;
+    return TB_OK;
+}
+
+int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src, void *dst,
+             uint64_t num_bytes, int num_subexec)
+{
+    const tb_options &o = ctx->opt;
+    int rc = tb::plan_reduce(p, srcs, n_src, dst, num_bytes, num_subexec, o.ctas_per_subexec,
+                             o.block_threads, o.vec_bytes, o.unroll, o.memset_byte, ctx->num_sms);
+    if (rc == TB_EINVAL)
+        return fail(ctx, rc,
+                    "reduce-copy arguments rejected (nSrc in [0,%d], numBytes %% 4 == 0, "
+                    "4-byte aligned non-null pointers, numSubExec >= 0)",
+                    TB_MAX_SRCS);
+    if (rc != TB_OK)
+        return fail(ctx, rc, "vec_bytes=%d is not allowed by the pointers' alignment", o.vec_bytes);
+    return TB_OK;
+}
+
+double median_of(std::vector<float> v)
+{
+    if (v.empty())
+        return 0.0;
+    std::sort(v.begin(), v.end());
+    const size_t m = v.size() / 2;
+    return v.size() % 2 ? v[m] : 0.5 * ((double)v[m - 1] + (double)v[m]);
+}
+
+int validate_impl(tb_ctx *ctx, const void *dev, const void *expected, uint64_t num_bytes,
+                  uint32_t elem, tb_mismatch *out)
+{
+    if (out) {
+        out->index = -1;
+        out->expected = out->actual = 0;
+    }
+    if (!ctx->val_stage)
+        TB_CUDA(ctx, cudaHostAlloc(&ctx->val_stage, kValidateChunk, cudaHostAllocDefault));
+    const uint8_t *d = static_cast<const uint8_t *>(dev);
+    const uint8_t *e = static_cast<const uint8_t *>(expected);
+    uint8_t *h = static_cast<uint8_t *>(ctx->val_stage);
+    for (uint64_t off = 0; off < num_bytes; off += kValidateChunk) {
+        const uint64_t len = std::min<uint64_t>(kValidateChunk, num_bytes - off);
+        TB_CUDA(ctx, cudaMemcpyAsync(h, d + off, len, cudaMemcpyDeviceToHost, ctx->stream));
+        TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+        if (memcmp(h, e + off, len) == 0)
+            continue;
+        uint64_t b = 0;
+        while (h[b] == e[off + b])
+            ++b;
+        const uint64_t byte = off + b;
+        const uint64_t idx = byte / elem;
+        if (out) {
+            out->index = (int64_t)idx;
+            // The element's bytes, fetched whole (it may straddle two chunks).
+            uint32_t act = 0, exp = 0;
+            TB_CUDA(ctx, cudaMemcpy(&act, d + idx * elem, elem, cudaMemcpyDeviceToHost));
+            memcpy(&exp, e + idx * elem, elem);
+            out->expected = exp;
+            out->actual = act;
+        }
+        return fail(ctx, TB_EVALIDATE, "destination differs from expected at element %llu",
+                    (unsigned long long)idx);
+    }
+    return TB_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char *tb_strerror(int code)
+{
+    switch (code) {
+    case TB_OK: return "TB_OK";
+    case TB_EINVAL: return "TB_EINVAL: invalid argument";
+    case TB_ENOMEM: return "TB_ENOMEM: out of memory";
+    case TB_ECUDA: return "TB_ECUDA: CUDA error";
+    case TB_EVALIDATE: return "TB_EVALIDATE: destination differs from expected";
+    case TB_ETIMEOUT: return "TB_ETIMEOUT: bounded wait expired";
+    case TB_ENOTSUP: return "TB_ENOTSUP: not supported";
+    default: return "unknown tb error code";
+    }
+}
+
+const char *tb_last_error(const tb_ctx *ctx)
+{
+    return ctx ? ctx->err.c_str() : "";
+}
+
+void tb_options_default(tb_options *o)
+{
+    if (!o)
+        return;
+    memset(o, 0, sizeof *o);
+    o->rotate_bytes = 256 * kMiB;
+    o->byte_offset = 0;
+    o->warmup = 3;
+    o->always_validate = 0;
+    o->memset_byte = 0;
+    o->ctas_per_subexec = 0;
+    o->block_threads = 0;
+    o->small_max_bytes = 16384;
+    o->chunk_bytes = 65536;
+    o->slot_items = 65536;
+    o->num_slots = 4;
+    o->wait_timeout_ns = 5000000000ull;
+    o->use_gate = 1;
+    o->vec_bytes = 0;
+    o->unroll = 0;
+    o->time_kernels = 0;
+}
+
+int tb_parse_bytes(const char *text, uint64_t *out)
+{
+    if (!text || !out)
+        return TB_EINVAL;
+    const char *p = text;
+    while (*p == ' ' || *p == '\t')
+        ++p;
+    if (*p < '0' || *p > '9')
+        return TB_EINVAL;
+    uint64_t v = 0;
+    for (; *p >= '0' && *p <= '9'; ++p) {
+        const uint64_t digit = (uint64_t)(*p - '0');
+        if (v > (UINT64_MAX - digit) / 10)
+            return TB_EINVAL;
+        v = v * 10 + digit;
+    }
+    unsigned shift = 0;
+    switch (*p) {
+    case 'k': case 'K': shift = 10; break;
+    case 'm': case 'M': shift = 20; break;
+    case 'g': case 'G': shift = 30; break;
+    case 't': case 'T': shift = 40; break;
+    default: break;
+    }
+    if (shift) {
+        ++p;
+        if (*p == 'i' || *p == 'I')
+            ++p;
+    }
+    if (*p == 'b' || *p == 'B')
+        ++p;
+    while (*p == ' ' || *p == '\t' || *p == '\n')
+        ++p;
+    if (*p != '\0')
+        return TB_EINVAL;
+    if (shift && v > (UINT64_MAX >> shift))
+        return TB_EINVAL;
+    *out = v << shift;
+    return TB_OK;
+}
+
+int tb_options_from_env(tb_options *o)
+{
+    if (!o)
+        return TB_EINVAL;
+    bool bad = false;
+    if (!env_u64("TB_SRC_ROTATE_BYTES", &o->rotate_bytes, &bad))
+        env_u64("SRC_ROTATE_BYTES", &o->rotate_bytes, &bad);
+    env_u64("TB_BYTE_OFFSET", &o->byte_offset, &bad);
+    env_i32("TB_WARMUP", &o->warmup, &bad);
+    if (!env_i32("TB_ALWAYS_VALIDATE", &o->always_validate, &bad))
+        env_i32("ALWAYS_VALIDATE", &o->always_validate, &bad);
+    env_u32("TB_MEMSET_CHAR", &o->memset_byte, &bad);
+    env_i32("TB_CTAS_PER_SUBEXEC", &o->ctas_per_subexec, &bad);
+    env_i32("TB_BLOCK_THREADS", &o->block_threads, &bad);
+    env_u64("TB_SMALL_MAX_BYTES", &o->small_max_bytes, &bad);
+    env_u64("TB_CHUNK_BYTES", &o->chunk_bytes, &bad);
+    env_u32("TB_SLOT_ITEMS", &o->slot_items, &bad);
+    env_u32("TB_NUM_SLOTS", &o->num_slots, &bad);
+    env_u64("TB_WAIT_TIMEOUT_NS", &o->wait_timeout_ns, &bad);
+    env_i32("TB_USE_GATE", &o->use_gate, &bad);
+    env_i32("TB_VEC_BYTES", &o->vec_bytes, &bad);
+    env_i32("TB_UNROLL", &o->unroll, &bad);
+    env_i32("TB_TIME_KERNELS", &o->time_kernels, &bad);
+    return bad ? TB_EINVAL : TB_OK;
+}
+
+int tb_rotation_plan(uint64_t num_bytes, uint64_t rotate_bytes, uint64_t byte_offset, uint64_t *K,
+                     uint64_t *slice_stride, uint64_t *alloc_bytes)
+{
+    if (num_bytes == 0 || num_bytes > UINT64_MAX - 255)
+        return TB_EINVAL;
+    // K = ceil(rotateBytes / numBytes); 0 disables rotation.
+    const uint64_t k = rotate_bytes == 0 ? 1 : rotate_bytes / num_bytes + (rotate_bytes % num_bytes != 0);
+    const uint64_t stride = (num_bytes + 255) & ~(uint64_t)255;
+    if (k - 1 > (UINT64_MAX - num_bytes) / stride)
+        return TB_EINVAL;
+    const uint64_t span = (k - 1) * stride + num_bytes;
+    if (span > UINT64_MAX - byte_offset)
+        return TB_EINVAL;
+    if (K)
+        *K = k;
+    if (slice_stride)
+        *slice_stride = stride;
+    if (alloc_bytes)
+        *alloc_bytes = span + byte_offset;
+    return TB_OK;
+}
+
+uint64_t tb_slice_for_iteration(int64_t iteration, uint64_t K)
+{
+    if (K == 0)
+        return 0;
+    if (iteration >= 0)
+        return (uint64_t)iteration % K;
+    // -1 -> K-1, -2 -> K-2, ...: fold the magnitude, then reflect.
+    const uint64_t mag = (uint64_t)(-(iteration + 1)) + 1;
+    const uint64_t r = mag % K;
+    return r == 0 ? 0 : K - r;
+}
+
+int tb_create(tb_ctx **out, int device, const tb_options *opt)
+{
+    if (!out)
+        return TB_EINVAL;
+    tb_options o;
+    if (opt) {
+        o = *opt;
+    } else {
+        tb_options_default(&o);
+        if (tb_options_from_env(&o) != TB_OK)
+            return TB_EINVAL;
+    }
+    if (check_options(nullptr, o) != TB_OK)
+        return TB_EINVAL;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return device < 0 ? TB_EINVAL : TB_ECUDA;
+
+    tb_ctx *ctx = new (std::nothrow) tb_ctx;
+    if (!ctx)
+        return TB_ENOMEM;
+    ctx->device = device;
+    ctx->opt = o;
+    DeviceScope scope(device);
+    auto bail = [&](int code) {
+        tb_destroy(ctx);
+        return code;
+    };
+    if (!scope.ok())
+        return bail(TB_ECUDA);
+    if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return bail(TB_ECUDA);
+    if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess)
+        return bail(TB_ECUDA);
+
+    void *gate = nullptr;
+    if (cudaHostAlloc(&gate, 2 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess)
+        return bail(TB_ENOMEM);
+    ctx->gate_flag = static_cast<volatile uint32_t *>(gate);
+    ctx->gate_status = ctx->gate_flag + 1;
+    ctx->gate_flag[0] = 0;
+    ctx->gate_status[0] = 0;
+    void *dgate = nullptr;
+    if (cudaHostGetDevicePointer(&dgate, gate, 0) != cudaSuccess)
+        return bail(TB_ECUDA);
+    ctx->gate_flag_dev = static_cast<uint32_t *>(dgate);
+    ctx->gate_status_dev = ctx->gate_flag_dev + 1;
+
+    ctx->slots.resize(o.num_slots);
+    const size_t slot_bytes = (size_t)o.slot_items * sizeof(WorkItem);
+    for (Slot &s : ctx->slots) {
+        if (cudaMalloc(&s.dev, slot_bytes) != cudaSuccess)
+            return bail(TB_ENOMEM);
+        if (cudaHostAlloc(&s.host, slot_bytes, cudaHostAllocDefault) != cudaSuccess)
+            return bail(TB_ENOMEM);
+        if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess)
+            return bail(TB_ECUDA);
+        if (o.time_kernels &&
+            (cudaEventCreate(&s.t0) != cudaSuccess || cudaEventCreate(&s.t1) != cudaSuccess))
+            return bail(TB_ECUDA);
+    }
+    *out = ctx;
+    return TB_OK;
+}
+
+void tb_destroy(tb_ctx *ctx)
+{
+    if (!ctx)
+        return;
+    DeviceScope scope(ctx->device);
+    for (Slot &s : ctx->slots) {
+        if (s.done) {
+            if (s.pending)
+                cudaEventSynchronize(s.done);
+            cudaEventDestroy(s.done);
+        }
+        if (s.t0)
+            cudaEventDestroy(s.t0);
+        if (s.t1)
+            cudaEventDestroy(s.t1);
+        if (s.dev)
+            cudaFree(s.dev);
+        if (s.host)
+            cudaFreeHost(s.host);
+    }
+    if (ctx->stream) {
+        cudaStreamSynchronize(ctx->stream);
+        cudaStreamDestroy(ctx->stream);
+    }
+    for (cudaEvent_t e : ctx->events)
+        cudaEventDestroy(e);
+    if (ctx->gate_flag)
+        cudaFreeHost((void *)ctx->gate_flag);
+    if (ctx->val_stage)
+        cudaFreeHost(ctx->val_stage);
+    delete ctx;
+}
+
+int tb_get_options(const tb_ctx *ctx, tb_options *opt)
+{
+    if (!ctx || !opt)
+        return TB_EINVAL;
+    *opt = ctx->opt;
+    return TB_OK;
+}
+
+int tb_fill_source(tb_ctx *ctx, void *dst, uint64_t num_bytes, const tb_pattern *pat,
+                   int buffer_idx, tb_stream stream)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (!dst || !pat || num_bytes % 4 != 0 || ((uintptr_t)dst & 3u) || buffer_idx < 0 ||
+        buffer_idx > 40000)
+        return fail(ctx, TB_EINVAL,
+                    "fill_source: dst 4-byte aligned, numBytes %% 4 == 0, bufferIdx in [0, 40000]");
+    if (pat->kind == TB_PATTERN_COMPRESS) {
+        uint32_t total = 0;
+        for (int m = 0; m < 5; ++m) {
+            if (pat->compress_pct[m] > 100)
+                return fail(ctx, TB_EINVAL, "fillCompress percentage above 100");
+            total += pat->compress_pct[m];
+        }
+        if (total != 100)
+            return fail(ctx, TB_EINVAL, "fillCompress percentages sum to %u, not 100", total);
+    } else if (pat->kind == TB_PATTERN_REPEAT) {
+        if (!pat->repeat || pat->repeat_len == 0 || pat->repeat_len > 4096)
+            return fail(ctx, TB_EINVAL, "fillPattern needs 1..4096 values");
+    } else if (pat->kind != TB_PATTERN_DEFAULT) {
+        return fail(ctx, TB_EINVAL, "unknown pattern kind %d", pat->kind);
+    }
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, tb::launch_fill_source(static_cast<float *>(dst), num_bytes / 4, *pat, buffer_idx,
+                                        ctx->num_sms, static_cast<cudaStream_t>(stream)));
+    return TB_OK;
+}
+
+int tb_upload_sources(tb_ctx *ctx, void *const *srcs, const void *const *host_srcs, int n_src,
+                      uint64_t num_bytes)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (n_src < 0 || n_src > TB_MAX_SRCS || (n_src > 0 && (!srcs || !host_srcs)))
+        return fail(ctx, TB_EINVAL, "upload_sources: bad source list");
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, cudaDeviceSynchronize());
+    for (int k = 0; k < n_src; ++k) {
+        if (!srcs[k] || !host_srcs[k])
+            return fail(ctx, TB_EINVAL, "upload_sources: null pointer");
+        char *d = static_cast<char *>(srcs[k]) + ctx->opt.byte_offset;
+        TB_CUDA(ctx, cudaMemcpyAsync(d, host_srcs[k], num_bytes, cudaMemcpyHostToDevice, ctx->stream));
+        ctx->prep_h2d += num_bytes;
+    }
+    TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    return TB_OK;
+}
+
+int tb_prepare_sources(tb_ctx *ctx, void *const *srcs, int n_src, uint64_t num_bytes,
+                       uint64_t rotate_bytes)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (n_src < 0 || n_src > TB_MAX_SRCS || (n_src > 0 && !srcs) || num_bytes % 4 != 0)
+        return fail(ctx, TB_EINVAL, "prepare_sources: bad arguments");
+    uint64_t K = 0, stride = 0;
+    if (tb_rotation_plan(num_bytes, rotate_bytes, ctx->opt.byte_offset, &K, &stride, nullptr) != TB_OK)
+        return fail(ctx, TB_EINVAL, "prepare_sources: rotation plan overflows");
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, cudaDeviceSynchronize());
+    // Slices [0, m) are valid; copy them onto [m, 2m) until all K are.
+    const uint64_t span = (K - 1) * stride + num_bytes;
+    for (int k = 0; k < n_src; ++k) {
+        if (!srcs[k])
+            return fail(ctx, TB_EINVAL, "prepare_sources: null source");
+        char *base = static_cast<char *>(srcs[k]) + ctx->opt.byte_offset;
+        for (uint64_t m = 1; m < K; m *= 2) {
+            const uint64_t len = std::min<uint64_t>(m * stride, span - m * stride);
+            const void *from[1] = {base};
+            tb::ReducePlan p;
+            int rc = plan_for(ctx, &p, from, 1, base + m * stride, len, 0);
+            if (rc != TB_OK)
+                return rc;
+            TB_CUDA(ctx, tb::launch_reduce(p, ctx->stream));
+        }
+    }
+    TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    return TB_OK;
+}
+
+uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx)
+{
+    return ctx ? ctx->prep_h2d : 0;
+}
+
+int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
+                   int num_subexec, tb_stream stream)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    DeviceScope scope(ctx->device);
+    tb::ReducePlan p;
+    int rc = plan_for(ctx, &p, srcs, n_src, dst, num_bytes, num_subexec);
+    if (rc != TB_OK)
+        return rc;
+    TB_CUDA(ctx, tb::launch_reduce(p, static_cast<cudaStream_t>(stream)));
+    return TB_OK;
+}
+
+int tb_reduce_copy_host(tb_ctx *ctx, const void *const *host_srcs, int n_src, void *host_dst,
+                        uint64_t num_bytes, void *const *dev_srcs, void *dev_dst, int num_subexec,
+                        tb_stream stream)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (n_src < 0 || n_src > TB_MAX_SRCS || !host_dst || !dev_dst ||
+        (n_src > 0 && (!host_srcs || !dev_srcs)))
+        return fail(ctx, TB_EINVAL, "reduce_copy_host: bad arguments");
+    for (int k = 0; k < n_src; ++k)
+        if (!host_srcs[k] || !dev_srcs[k])
+            return fail(ctx, TB_EINVAL, "reduce_copy_host: null source");
+    DeviceScope scope(ctx->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    tb::ReducePlan p;
+    int rc = plan_for(ctx, &p, (const void *const *)dev_srcs, n_src, dev_dst, num_bytes, num_subexec);
+    if (rc != TB_OK)
+        return rc;
+    for (int k = 0; k < n_src; ++k)
+        TB_CUDA(ctx, cudaMemcpyAsync(dev_srcs[k], host_srcs[k], num_bytes, cudaMemcpyHostToDevice, st));
+    TB_CUDA(ctx, tb::launch_reduce(p, st));
+    TB_CUDA(ctx, cudaMemcpyAsync(host_dst, dev_dst, num_bytes, cudaMemcpyDeviceToHost, st));
+    return TB_OK;
+}
+
+int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (!t || !out || t->iters < 1 || t->n_src < 0 || t->n_src > TB_MAX_SRCS || !t->dst ||
+        (t->n_src > 0 && !t->srcs))
+        return fail(ctx, TB_EINVAL, "run_transfer: bad arguments");
+    memset(out, 0, sizeof *out);
+    out->mismatch_index = -1;
+    const tb_options &o = ctx->opt;
+    uint64_t K = 0, stride = 0, alloc = 0;
+    if (tb_rotation_plan(t->num_bytes, t->rotate_bytes, o.byte_offset, &K, &stride, &alloc) != TB_OK)
+        return fail(ctx, TB_EINVAL, "run_transfer: rotation plan overflows or numBytes == 0");
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, cudaDeviceSynchronize());
+
+    // Slice-0 pointers; the plan is made once and only the source pointers
+    // move between iterations (the stride keeps every slice's alignment).
+    const void *base[TB_MAX_SRCS];
+    for (int k = 0; k < t->n_src; ++k) {
+        if (!t->srcs[k])
+            return fail(ctx, TB_EINVAL, "run_transfer: null source");
+        base[k] = static_cast<const char *>(t->srcs[k]) + o.byte_offset;
+    }
+    char *dst = static_cast<char *>(t->dst) + o.byte_offset;
+    tb::ReducePlan plan;
+    int rc = plan_for(ctx, &plan, base, t->n_src, dst, t->num_bytes, t->num_subexec);
+    if (rc != TB_OK)
+        return rc;
+    auto at_iteration = [&](int64_t it) {
+        const uint64_t off = tb_slice_for_iteration(it, K) * stride;
+        for (int k = 0; k < t->n_src; ++k)
+            plan.src[k] = reinterpret_cast<const float *>(static_cast<const char *>(base[k]) + off);
+    };
+
+    const int iters = t->iters;
+    while ((int)ctx->events.size() < iters + 1) {
+        cudaEvent_t e;
+        TB_CUDA(ctx, cudaEventCreate(&e));
+        ctx->events.push_back(e);
+    }
+    ctx->iter_ms.assign(iters, 0.0f);
+    cudaStream_t st = ctx->stream;
+    const bool per_iter_validate = o.always_validate && t->expected;
+    const bool gated = o.use_gate && !per_iter_validate && o.warmup + iters <= kMaxGatedLaunches;
+
+    if (gated) {
+        ctx->gate_flag[0] = 0;
+        ctx->gate_status[0] = 0;
+        TB_CUDA(ctx, tb::launch_gate(ctx->gate_flag_dev, ctx->gate_status_dev, o.wait_timeout_ns, st));
+    }
+    int first_err = TB_OK;
+    for (int64_t it = -(int64_t)o.warmup; it < iters; ++it) {
+        at_iteration(it);
+        if (it == 0 || (per_iter_validate && it > 0))
+            TB_CUDA(ctx, cudaEventRecord(ctx->events[it], st));
+        cudaError_t e = tb::launch_reduce(plan, st);
+        if (e != cudaSuccess) {
+            if (gated)
+                __atomic_store_n(ctx->gate_flag, 1u, __ATOMIC_SEQ_CST);
+            cudaStreamSynchronize(st);
+            return cuda_fail(ctx, e, "reduce-copy launch");
+        }
+        if (it >= 0)
+            TB_CUDA(ctx, cudaEventRecord(ctx->events[it + 1], st));
+        if (per_iter_validate && it >= 0) {
+            tb_mismatch mm;
+            first_err = validate_impl(ctx, dst, t->expected, t->num_bytes, 4, &mm);
+            if (first_err != TB_OK) {
+                out->mismatch_index = mm.index;
+                out->mismatch_expected = mm.expected;
+                out->mismatch_actual = mm.actual;
+                out->iters = (int)it + 1;
+                break;
+            }
+        }
+    }
+    if (gated)
+        __atomic_store_n(ctx->gate_flag, 1u, __ATOMIC_SEQ_CST);
+    TB_CUDA(ctx, cudaStreamSynchronize(st));
+    if (gated && ctx->gate_status[0] != 1u)
+        return fail(ctx, TB_ETIMEOUT, "gate kernel was not released within %llu ns",
+                    (unsigned long long)o.wait_timeout_ns);
+
+    const int done = first_err != TB_OK ? out->iters : iters;
+    double total = 0.0;
+    for (int i = 0; i < done; ++i) {
+        float ms = 0.0f;
+        TB_CUDA(ctx, cudaEventElapsedTime(&ms, ctx->events[i], ctx->events[i + 1]));
+        ctx->iter_ms[i] = ms;
+        total += ms;
+    }
+    out->K = K;
+    out->slice_stride = stride;
+    out->alloc_bytes = alloc;
+    out->prep_h2d_bytes = ctx->prep_h2d;
+    out->iters = done;
+    out->num_subexec = plan.num_subexec;
+    out->ctas = plan.num_subexec * plan.ctas_per_sub;
+    out->block_threads = plan.block_threads;
+    out->gated = gated ? 1 : 0;
+    out->total_ms = total;
+    if (done > 0) {
+        std::vector<float> v(ctx->iter_ms.begin(), ctx->iter_ms.begin() + done);
+        out->mean_ms = total / done;
+        out->median_ms = median_of(v);
+        out->min_ms = *std::min_element(v.begin(), v.end());
+        out->max_ms = *std::max_element(v.begin(), v.end());
+        out->gbps = total > 0 ? (double)(t->n_src + 1) * (double)t->num_bytes * done / (total * 1e6)
+                              : 0.0;
+    }
+    out->iter_ms = ctx->iter_ms.data();
+    if (first_err != TB_OK) {
+        out->validated = 1;
+        return first_err;
+    }
+    if (t->expected) {
+        out->validated = 1;
+        tb_mismatch mm;
+        rc = validate_impl(ctx, dst, t->expected, t->num_bytes, 4, &mm);
+        if (rc != TB_OK) {
+            out->mismatch_index = mm.index;
+            out->mismatch_expected = mm.expected;
+            out->mismatch_actual = mm.actual;
+            return rc;
+        }
+    }
+    return TB_OK;
+}
+
+int tb_run_transfer(tb_ctx *ctx, void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
+                    int num_subexec, int iters, uint64_t rotate_bytes, tb_result *out)
+{
+    tb_transfer t;
+    t.srcs = srcs;
+    t.n_src = n_src;
+    t.dst = dst;
+    t.num_bytes = num_bytes;
+    t.num_subexec = num_subexec;
+    t.iters = iters;
+    t.rotate_bytes = rotate_bytes;
+    t.expected = nullptr;
+    return tb_run_transfer_ex(ctx, &t, out);
+}
+
+int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (n > 0 && !desc)
+        return fail(ctx, TB_EINVAL, "batch_copy: null descriptor array");
+    const tb_options &o = ctx->opt;
+    tb_batch_stats st{};
+
+    // Pass 1: check every descriptor; count warp items per length bucket and
+    // CTA chunks.  Buckets sort warp items longest first (coarsely).
+    const uint64_t small = o.small_max_bytes;
+    unsigned shift = 6;
+    while ((small >> shift) > 4096)
+        ++shift;
+    const size_t nb = (size_t)(small >> shift) + 1;
+    ctx->bucket.assign(nb + 1, 0);
+    uint64_t n_cta = 0, n_long = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const tb_copy_desc &d = desc[i];
+        if (d.len == 0)
+            continue;
+        if (d.src == 0 || d.dst == 0 || d.src + d.len < d.src || d.dst + d.len < d.dst)
+            return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range", i);
+        ++st.descs;
+        st.bytes += d.len;
+        if (d.len <= small) {
+            ++ctx->bucket[nb - 1 - (size_t)(d.len >> shift)];
+        } else {
+            ++n_long;
+            n_cta += (d.len + o.chunk_bytes - 1) / o.chunk_bytes;
+        }
+    }
+    const uint64_t n_warp = st.descs - n_long;
+    st.warp_items = n_warp;
+    st.cta_items = n_cta;
+    const uint64_t total = n_cta + n_warp;
+    if (total == 0) {
+        ctx->last_batch = st;
+        return TB_OK;
+    }
+    // Bucket counts -> first position of each bucket among the warp items.
+    uint32_t run = 0;
+    for (size_t b = 0; b < nb; ++b) {
+        const uint32_t c = ctx->bucket[b];
+        ctx->bucket[b] = run;
+        run += c;
+    }
+
+    // Pass 2: place items.  Into the first slot's staging directly when the
+    // batch fits one slot, else into the packing area.
+    DeviceScope scope(ctx->device);
+    Slot *first = &ctx->slots[ctx->next_slot];
+    const bool one_slot = total <= o.slot_items;
+    WorkItem *items;
+    if (one_slot) {
+        int rc = wait_slot(ctx, *first);
+        if (rc != TB_OK)
+            return rc;
+        items = first->host;
+    } else {
+        ctx->pack.resize(total);
+        items = ctx->pack.data();
+    }
+    uint64_t ci = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const tb_copy_desc &d = desc[i];
+        if (d.len == 0)
+            continue;
+        if (d.len <= small) {
+            uint32_t &pos = ctx->bucket[nb - 1 - (size_t)(d.len >> shift)];
+            items[n_cta + pos++] = WorkItem{d.src, d.dst, d.len};
+        } else {
+            for (uint64_t off = 0; off < d.len; off += o.chunk_bytes)
+                items[ci++] = WorkItem{d.src + off, d.dst + off, std::min(o.chunk_bytes, d.len - off)};
+        }
+    }
+
+    // Launch: each slot takes up to slot_items items, CTA chunks first.
+    ctx->last_slots.clear();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int full_grid = ctx->num_sms * tb::batch_ctas_per_sm();
+    const uint32_t warps_per_cta = tb::kBatchThreads / 32;
+    uint64_t cta_left = n_cta, warp_left = n_warp;
+    while (cta_left + warp_left > 0) {
+        Slot &slot = ctx->slots[ctx->next_slot];
+        ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
+        int rc = wait_slot(ctx, slot);
+        if (rc != TB_OK)
+            return rc;
+        const uint64_t c = std::min<uint64_t>(cta_left, o.slot_items);
+        const uint64_t w = std::min<uint64_t>(warp_left, o.slot_items - c);
+        const uint64_t cnt = c + w;
+        if (!one_slot) {
+            // CTA items are a prefix of the packing area, warp items follow.
+            memcpy(slot.host, items + (n_cta - cta_left), c * sizeof(WorkItem));
+            memcpy(slot.host + c, items + n_cta + (n_warp - warp_left), w * sizeof(WorkItem));
+        }
+        TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, cnt * sizeof(WorkItem),
+                                     cudaMemcpyHostToDevice, s));
+        const uint64_t want = std::max<uint64_t>(c, (w + warps_per_cta - 1) / warps_per_cta);
+        const int grid = (int)std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)full_grid, want));
+        if (slot.t0)
+            TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
+        TB_CUDA(ctx, tb::launch_batch(slot.dev, (uint32_t)c, (uint32_t)w, grid, s));
+        if (slot.t1)
+            TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
+        TB_CUDA(ctx, cudaEventRecord(slot.done, s));
+        ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
+        slot.pending = true;
+        st.launches += 1;
+        st.upload_bytes += cnt * sizeof(WorkItem);
+        cta_left -= c;
+        warp_left -= w;
+    }
+    ctx->last_batch = st;
+    return TB_OK;
+}
+
+int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms)
+{
+    if (!ctx || !ms)
+        return TB_EINVAL;
+    if (!ctx->opt.time_kernels)
+        return fail(ctx, TB_ENOTSUP, "the context was created without time_kernels");
+    DeviceScope scope(ctx->device);
+    double total = 0.0;
+    for (uint32_t i : ctx->last_slots) {
+        Slot &s = ctx->slots[i];
+        TB_CUDA(ctx, cudaEventSynchronize(s.t1));
+        float t = 0.0f;
+        TB_CUDA(ctx, cudaEventElapsedTime(&t, s.t0, s.t1));
+        total += t;
+    }
+    *ms = total;
+    return TB_OK;
+}
+
+int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (n > 0 && !desc)
+        return fail(ctx, TB_EINVAL, "copy_each: null descriptor array");
+    for (size_t i = 0; i < n; ++i) {
+        const tb_copy_desc &d = desc[i];
+        if (d.len && (d.src == 0 || d.dst == 0 || d.src + d.len < d.src || d.dst + d.len < d.dst))
+            return fail(ctx, TB_EINVAL, "copy_each: descriptor %zu has a null or wrapping range", i);
+    }
+    DeviceScope scope(ctx->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (size_t i = 0; i < n; ++i) {
+        const tb_copy_desc &d = desc[i];
+        if (d.len)
+            TB_CUDA(ctx, cudaMemcpyAsync(reinterpret_cast<void *>(d.dst),
+                                         reinterpret_cast<const void *>(d.src), d.len,
+                                         cudaMemcpyDeviceToDevice, s));
+    }
+    return TB_OK;
+}
+
+int tb_last_batch_stats(const tb_ctx *ctx, tb_batch_stats *out)
+{
+    if (!ctx || !out)
+        return TB_EINVAL;
+    *out = ctx->last_batch;
+    return TB_OK;
+}
+
+int tb_validate(tb_ctx *ctx, const void *dst_device, const void *expected_host, uint64_t num_bytes,
+                uint32_t elem_size, tb_mismatch *out)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if ((num_bytes > 0 && (!dst_device || !expected_host)) ||
+        (elem_size != 1 && elem_size != 2 && elem_size != 4) || num_bytes % elem_size != 0)
+        return fail(ctx, TB_EINVAL, "validate: bad arguments");
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, cudaDeviceSynchronize());
+    return validate_impl(ctx, dst_device, expected_host, num_bytes, elem_size, out);
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Internal interface between the host runtime (tb_host.cpp) and the kernels
+// (tb_kernels.cu) of libtb.  Not installed; the public ABI is include/tb.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tb.h"
+
+namespace tb {
+
+// ---------------------------------------------------------------------------
+// Reduce-copy (K1)
+// ---------------------------------------------------------------------------
+
+// One reduce-copy launch, fully resolved on the host.  The element range
+// [0, n) splits into head (scalar, until dst reaches vector alignment), body
+// (nvec vectors of vec_bytes) and tail (scalar).  Sub-executor s owns body
+// vectors [s * sub_vecs, min(nvec, (s + 1) * sub_vecs)); the ctas_per_sub
+// CTAs of a sub-executor share its range tile by tile.
+struct ReducePlan {
+    const float *src[TB_MAX_SRCS];
+    float *dst;
+    uint64_t n;            // elements
+    uint64_t head;         // scalar elements before the body
+    uint64_t nvec;         // body vectors
+    uint64_t sub_vecs;     // body vectors per sub-executor
+    int n_src;
+    int vec_bytes;         // 32, 16, or 0 (no common alignment: scalar path)
+    int num_subexec;
+    int ctas_per_sub;
+    int block_threads;
+    int unroll;            // vectors per source a thread holds in flight
+    uint32_t memset_word;  // 0-source fill, the memset byte repeated
+};
+
+// Picks vector width, head/tail, sub-executor split, grid and unroll for one
+// launch.  num_subexec, ctas_per_subexec, block_threads, vec_bytes and unroll
+// of 0 take the defaults.  Returns TB_OK, TB_EINVAL or TB_ENOTSUP (a forced
+// vector width the pointers' alignment does not allow).
+int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
+                int num_subexec, int ctas_per_subexec, int block_threads, int vec_bytes, int unroll,
+                uint32_t memset_byte, int num_sms);
+
+// Launches the plan on `stream` (asynchronous).
+cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream);
+
+// Default CTAs resident per SM for the reduce kernel of this plan shape.
+int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll);
+
+// ---------------------------------------------------------------------------
+// Source patterns
+// ---------------------------------------------------------------------------
+cudaError_t launch_fill_source(float *dst, uint64_t n, const tb_pattern &pat, int buffer_idx,
+                               int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Gate kernel: waits, with a %globaltimer deadline, until *flag != 0.
+// Writes *status = 1 when released, 2 when the deadline passed first.
+// ---------------------------------------------------------------------------
+cudaError_t launch_gate(const volatile uint32_t *flag, uint32_t *status, uint64_t timeout_ns,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Batched copy (K2)
+// ---------------------------------------------------------------------------
+
+// One packed work item: copy len bytes from src to dst.  A slot holds
+// n_cta items (chunks of long descriptors, one CTA each) followed by n_warp
+// items (short descriptors, one warp each, sorted longest first).
+struct WorkItem {
+    uint64_t src;
+    uint64_t dst;
+    uint64_t len;
+};
+static_assert(sizeof(WorkItem) == 24, "WorkItem is packed as three 64-bit words");
+
+constexpr int kBatchThreads = 256;
+
+cudaError_t launch_batch(const WorkItem *items, uint32_t n_cta, uint32_t n_warp, int grid,
+                         cudaStream_t stream);
+
+// CTAs resident per SM for the batch kernel.
+int batch_ctas_per_sm();
+
+}  // namespace tb

@@ -1,0 +1,385 @@
+/*
+ * tb.h - C ABI of libtb, a single-GPU GB300 (sm_103a) reduce-copy and
+ * batched-copy engine.
+ *
+ * Two operations sit on the hot path:
+ *
+ *  1. The GPU-executor transfer of TransferBench: dst[i] = src0[i] + ... +
+ *     srcN-1[i] over float32 buffers, with source-slice rotation so that
+ *     repeated iterations read HBM rather than L2.
+ *       - "TransferBench data validation" (ROCm docs 1.66.02), table
+ *         "Number of sources / Expected value" and section
+ *         "Expected destination (dstReference)": 0 sources -> memset value,
+ *         1 source -> dst == src0, N sources -> the left-to-right float sum.
+ *       - TransferBench PR #365 "source-slice rotation (SRC_ROTATE_BYTES)",
+ *         section "Technical Details": K = ceil(SRC_ROTATE_BYTES / numBytes),
+ *         allocation K * numBytes + byteOffset, slices 1..K-1 filled
+ *         device-to-device from slice 0, iteration i reads slice i % K, the
+ *         rotation kept outside the timed region.
+ *
+ *  2. The batched descriptor copy of the Mooncake RFC #5041
+ *     ("HipTransport: fast, correct intra-node XGMI", section
+ *     "Design of #5040"): many scattered copies of 64 B - 16 MiB run as one
+ *     kernel over a (src, dst, len) descriptor array instead of one memcpy
+ *     call each; the caller's stream orders it (section "Item 4: ordering
+ *     after the caller's stream", first option: an explicit stream argument).
+ *
+ * Conventions for every entry point:
+ *   - Return 0 (TB_OK) or a negative TB_E* code; tb_strerror() names it and
+ *     tb_last_error() returns a sentence about the last failure on a context.
+ *   - Device pointers are plain CUDA device addresses of the context's device
+ *     (interior pointers into caching-allocator blocks are fine).  The caller
+ *     owns every buffer it passes; the library owns only what it allocates
+ *     inside a context (staging, descriptor slots, events, timing arrays).
+ *   - tb_stream is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.
+ *   - Nothing falls back to a different copy method on failure: an error is
+ *     returned instead, so a benchmark never silently measures something else.
+ *   - Synchronous calls (tb_upload_sources, tb_prepare_sources,
+ *     tb_run_transfer*, tb_validate) first wait until all work already queued
+ *     on the device has finished, so they see the results of earlier
+ *     asynchronous calls on any stream.
+ *   - A context is not thread-safe; use one context per host thread.
+ */
+#ifndef TB_H
+#define TB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------------- */
+/* Error codes                                                              */
+/* ----------------------------------------------------------------------- */
+#define TB_OK          0
+#define TB_EINVAL     (-1)  /* bad argument: null pointer, bad size, overflow */
+#define TB_ENOMEM     (-2)  /* a host or device allocation of the library failed */
+#define TB_ECUDA      (-3)  /* a CUDA call failed; tb_last_error() has the text */
+#define TB_EVALIDATE  (-4)  /* destination differs from the expected bytes */
+#define TB_ETIMEOUT   (-5)  /* a bounded wait (descriptor slot, gate) expired */
+#define TB_ENOTSUP    (-6)  /* request outside what this build supports */
+
+/* Most sources one reduce-copy accepts. */
+#define TB_MAX_SRCS 16
+
+typedef struct tb_ctx tb_ctx;
+typedef void *tb_stream;
+
+/* ----------------------------------------------------------------------- */
+/* Options                                                                  */
+/* ----------------------------------------------------------------------- */
+typedef struct {
+    /* SRC_ROTATE_BYTES of PR #365: bytes of rotation per source.
+       Default 256 MiB; 0 disables rotation (K = 1). */
+    uint64_t rotate_bytes;
+    /* Bytes between the start of each source allocation (and of dst) and the
+       first data byte ("K * numBytes + byteOffset").  Multiple of 4. Default 0. */
+    uint64_t byte_offset;
+    /* Untimed iterations before the timed ones (indices -warmup .. -1).
+       Default 3. */
+    int32_t warmup;
+    /* ALWAYS_VALIDATE: 1 = validate after every timed iteration and stop at
+       the first error; 0 = once after the loop.  Default 0. */
+    int32_t always_validate;
+    /* MEMSET_CHAR: the byte a 0-source transfer writes.  Default 0. */
+    uint32_t memset_byte;
+    /* Reduce-copy CTAs per sub-executor; 0 = enough to fill every SM.
+       1 gives one CTA per sub-executor.  Default 0. */
+    int32_t ctas_per_subexec;
+    /* Reduce-copy threads per CTA (multiple of 32, <= 512); 0 = 512. */
+    int32_t block_threads;
+    /* Batched copy: descriptors up to this many bytes are copied by one warp;
+       longer ones are split into chunks copied by a whole CTA.
+       Default 16384. */
+    uint64_t small_max_bytes;
+    /* Batched copy: bytes per CTA chunk of a long descriptor (multiple of
+       4096).  Default 65536. */
+    uint64_t chunk_bytes;
+    /* Batched copy: work items (warp items + CTA chunks) one descriptor slot
+       holds, and how many slots the ring has.  A batch larger than one slot
+       runs as several launches.  Defaults 65536 and 4. */
+    uint32_t slot_items;
+    uint32_t num_slots;
+    /* Limit of every bounded wait (descriptor slot reuse, gate kernel), in
+       nanoseconds.  Default 5e9. */
+    uint64_t wait_timeout_ns;
+    /* 1 = tb_run_transfer enqueues its iterations behind a gate kernel that
+       the host releases once everything is queued, so host launch overhead
+       never separates iterations (nvbandwidth's spin-kernel method).
+       Default 1. */
+    int32_t use_gate;
+    /* Reduce-copy vector width in bytes: 32, 16, or 0 = the widest that every
+       pointer of the launch shares the alignment of (4-byte scalar loads when
+       they share no 16-byte alignment).  Default 0. */
+    int32_t vec_bytes;
+    /* Reduce-copy vectors per source each thread keeps in flight (1, 2 or 4);
+       0 = chosen from the source count.  Default 0. */
+    int32_t unroll;
+    /* 1 = bracket every batched-copy kernel with CUDA events so that
+       tb_last_batch_kernel_ms can report its device time.  Default 0. */
+    int32_t time_kernels;
+} tb_options;
+
+/* Fills *opt with the defaults above. */
+void tb_options_default(tb_options *opt);
+
+/* Overrides fields of *opt from the environment:
+     TB_SRC_ROTATE_BYTES (or SRC_ROTATE_BYTES), TB_BYTE_OFFSET, TB_WARMUP,
+     TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
+     TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_CHUNK_BYTES, TB_SLOT_ITEMS,
+     TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
+     TB_TIME_KERNELS.
+   Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
+   partly updated) if a variable does not parse. */
+int tb_options_from_env(tb_options *opt);
+
+/* Parses an unsigned byte count: decimal digits, optionally followed by one of
+   K, M, G, T (binary: 2^10, 2^20, 2^30, 2^40), optionally followed by "B" or
+   "iB", case-insensitive; surrounding blanks are allowed.  "256M" and "256MB"
+   are 268,435,456.  Rejects signs, empty input, trailing junk and any value
+   that does not fit in 64 bits (TB_EINVAL) - PR #365's review asks that
+   SRC_ROTATE_BYTES never overflow a signed type. */
+int tb_parse_bytes(const char *text, uint64_t *out);
+
+/* ----------------------------------------------------------------------- */
+/* Context                                                                  */
+/* ----------------------------------------------------------------------- */
+
+/* Creates a context on CUDA device `device`.  opt == NULL takes the defaults
+   with environment overrides.  Allocates pinned staging, descriptor slots and
+   events.  *out is set only on success. */
+int tb_create(tb_ctx **out, int device, const tb_options *opt);
+
+/* Waits for the context's outstanding work, then frees everything it owns.
+   NULL is accepted. */
+void tb_destroy(tb_ctx *ctx);
+
+/* Copies the context's options to *opt. */
+int tb_get_options(const tb_ctx *ctx, tb_options *opt);
+
+/* Text of the last error recorded on ctx ("" if none). Valid until the next
+   call on ctx. */
+const char *tb_last_error(const tb_ctx *ctx);
+
+/* Static name of an error code. */
+const char *tb_strerror(int code);
+
+/* ----------------------------------------------------------------------- */
+/* Rotation plan (host only, no GPU needed)                                 */
+/* ----------------------------------------------------------------------- */
+
+/* PR #365 "Technical Details": K = ceil(rotateBytes / numBytes), or 1 when
+   rotateBytes == 0.  Slice j starts at byteOffset + j * sliceStride, where
+   sliceStride = numBytes rounded up to 256 bytes so every slice keeps the
+   alignment of slice 0 for vector loads.  allocBytes = (K - 1) * sliceStride
+   + numBytes + byteOffset, i.e. the page's K * numBytes + byteOffset whenever
+   numBytes is a multiple of 256 (4 MiB at the 256 MiB default: K = 64,
+   268,435,456 bytes).  Any output pointer may be NULL.  TB_EINVAL for
+   numBytes == 0 or 64-bit overflow. */
+int tb_rotation_plan(uint64_t numBytes, uint64_t rotateBytes, uint64_t byteOffset,
+                     uint64_t *K, uint64_t *sliceStride, uint64_t *allocBytes);
+
+/* The slice iteration `iteration` reads: iteration folded into [0, K), so the
+   negative warm-up indices -warmup..-1 read slices K-warmup..K-1. */
+uint64_t tb_slice_for_iteration(int64_t iteration, uint64_t K);
+
+/* ----------------------------------------------------------------------- */
+/* Source preparation ("TransferBench data validation", section            */
+/* "Expected source pattern" and "Initializing source and destination       */
+/* memories")                                                               */
+/* ----------------------------------------------------------------------- */
+
+#define TB_PATTERN_DEFAULT   0  /* PrepSrcValue(bufferIdx, i) */
+#define TB_PATTERN_COMPRESS  1  /* fillCompress */
+#define TB_PATTERN_REPEAT    2  /* fillPattern */
+
+typedef struct {
+    int32_t kind;             /* TB_PATTERN_* */
+    /* TB_PATTERN_COMPRESS: percentages of 64-byte lines in mode 0 (random),
+       1 (1B0), 2 (2B0), 3 (4B0), 4 (32B0); they must sum to 100.  Mode nB0
+       zeroes every odd-numbered aligned n-byte chunk of its line.  Line L of
+       buffer k draws SplitMix64 outputs number 17L .. 17L+16 of the stream
+       seeded with seed + k: the first picks the mode ((draw % 100) against
+       the running sum of the percentages), the next 16 give the floats
+       (draw >> 40) * 2^-23 - 1 in [-1, 1). */
+    uint32_t compress_pct[5];
+    uint64_t seed;
+    /* TB_PATTERN_REPEAT: host array of repeat_len floats, repeated over the
+       buffer (copied by the call; at most 4096 values). */
+    const float *repeat;
+    uint32_t repeat_len;
+} tb_pattern;
+
+/* Writes source pattern `pat` for SRC number bufferIdx into numBytes bytes of
+   device memory at dst (slice 0 of a source: the allocation base plus
+   byte_offset), with a kernel on `stream`, asynchronously.  numBytes must be
+   a multiple of 4 and dst 4-byte aligned.  Default pattern:
+   PrepSrcValue(bufferIdx, i) = (((i % 383) * 517) % 383 + 31) * (bufferIdx+1)
+   as a float32. */
+int tb_fill_source(tb_ctx *ctx, void *dst, uint64_t numBytes, const tb_pattern *pat,
+                   int bufferIdx, tb_stream stream);
+
+/* Host-to-device prep copy: for each k, copies numBytes bytes from hostSrcs[k]
+   into slice 0 of srcs[k] (srcs[k] + byte_offset).  Synchronous.  Adds
+   nSrc * numBytes to the context's prep-H2D counter. */
+int tb_upload_sources(tb_ctx *ctx, void *const *srcs, const void *const *hostSrcs,
+                      int nSrc, uint64_t numBytes);
+
+/* Prep fill of PR #365: with slice 0 of every source already written, fills
+   slices 1..K-1 from slice 0 device-to-device (by doubling, log2(K) copies,
+   with the library's own copy kernel), K from tb_rotation_plan(numBytes,
+   rotateBytes, byte_offset).  srcs[k] are allocation bases of at least
+   allocBytes.  Synchronous.  Moves no host data. */
+int tb_prepare_sources(tb_ctx *ctx, void *const *srcs, int nSrc, uint64_t numBytes,
+                       uint64_t rotateBytes);
+
+/* Bytes the context has copied host-to-device to prepare sources so far. */
+uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
+
+/* ----------------------------------------------------------------------- */
+/* Reduce-copy                                                              */
+/* ----------------------------------------------------------------------- */
+
+/* One reduce-copy launch on `stream`, asynchronous:
+     nSrc == 0: every byte of dst[0 .. numBytes) = memset_byte;
+     nSrc == 1: dst = srcs[0], bit for bit;
+     nSrc >= 2: dst[i] = (...((srcs[0][i] + srcs[1][i]) + srcs[2][i]) ...)
+                in float32, each add rounded to nearest even, no fused
+                multiply-add, subnormals kept.
+   srcs[k] and dst point at the data itself (no byte_offset or slice offset
+   is added).  numBytes must be a multiple of 4, every pointer 4-byte aligned,
+   nSrc <= TB_MAX_SRCS.  The elements are split into numSubExec contiguous
+   ranges (sub-executors), each a multiple of 4 elements except the last;
+   numSubExec == 0 means one per CTA of the default grid.  Ranges must not
+   overlap between dst and any source. */
+int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int nSrc, void *dst,
+                   uint64_t numBytes, int numSubExec, tb_stream stream);
+
+typedef struct {
+    uint64_t K;               /* slices per source */
+    uint64_t slice_stride;    /* bytes between slices */
+    uint64_t alloc_bytes;     /* bytes each source allocation needs */
+    uint64_t prep_h2d_bytes;  /* the context's prep-H2D counter */
+    int32_t  iters;           /* timed iterations run */
+    int32_t  num_subexec;     /* sub-executors used */
+    int32_t  ctas;            /* CTAs per launch */
+    int32_t  block_threads;   /* threads per CTA */
+    int32_t  gated;           /* 1 if the iterations ran behind the gate */
+    int32_t  validated;       /* 1 if dst was compared with expected bytes */
+    double   total_ms;        /* device time of all timed iterations */
+    double   mean_ms, median_ms, min_ms, max_ms;
+    double   gbps;            /* (nSrc + 1) * numBytes * iters / total, 1e9 B/s */
+    const float *iter_ms;     /* iters per-iteration times (owned by ctx,
+                                 valid until the next tb_run_transfer) */
+    int64_t  mismatch_index;  /* first bad element when validation failed, else -1 */
+    uint32_t mismatch_expected, mismatch_actual;  /* its bits */
+} tb_result;
+
+typedef struct {
+    void *const *srcs;        /* nSrc device allocation bases (>= alloc_bytes) */
+    int32_t n_src;
+    void *dst;                /* device allocation base (>= numBytes + byte_offset) */
+    uint64_t num_bytes;       /* bytes per source slice and of dst */
+    int32_t num_subexec;      /* 0 = auto */
+    int32_t iters;            /* timed iterations, >= 1 */
+    uint64_t rotate_bytes;    /* SRC_ROTATE_BYTES for this transfer */
+    const void *expected;     /* NULL, or host bytes dst must equal (validation
+                                 after the loop, or after every iteration when
+                                 always_validate is set) */
+} tb_transfer;
+
+/* TransferBench's timed iteration loop for one transfer, synchronous on an
+   internal stream: for it = -warmup .. iters-1, iteration it reads slice
+   tb_slice_for_iteration(it, K) of every source (the slice offset is a kernel
+   argument, so rotation costs no host-to-device traffic and sits outside
+   the timed region) and writes dst + byte_offset.  Each timed iteration is
+   bracketed by CUDA events.  Sources must already hold their slices
+   (tb_fill_source or tb_upload_sources, then tb_prepare_sources).  On a
+   validation failure returns TB_EVALIDATE with the mismatch in *out. */
+int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out);
+
+/* tb_run_transfer_ex without expected bytes. */
+int tb_run_transfer(tb_ctx *ctx, void *const *srcs, int nSrc, void *dst,
+                    uint64_t numBytes, int numSubExec, int iters, uint64_t rotateBytes,
+                    tb_result *out);
+
+/* The transfer with host buffers, end to end, asynchronous on `stream`:
+   copies numBytes from each hostSrcs[k] into devSrcs[k], runs one
+   tb_reduce_copy into devDst, and copies devDst back into hostDst.  Host
+   buffers should be page-locked for the copies to be asynchronous.  The
+   device buffers are the caller's (numBytes each, no offsets added). */
+int tb_reduce_copy_host(tb_ctx *ctx, const void *const *hostSrcs, int nSrc, void *hostDst,
+                        uint64_t numBytes, void *const *devSrcs, void *devDst,
+                        int numSubExec, tb_stream stream);
+
+/* ----------------------------------------------------------------------- */
+/* Batched copy                                                             */
+/* ----------------------------------------------------------------------- */
+
+typedef struct {
+    uint64_t src;  /* device address of the first source byte */
+    uint64_t dst;  /* device address of the first destination byte */
+    uint64_t len;  /* bytes; 0 is a no-op */
+} tb_copy_desc;
+
+/* Copies every descriptor's len bytes from src to dst, byte-exact, any
+   alignment, with one kernel launch per descriptor slot, asynchronously on
+   `stream` (ordered after the caller's earlier work on it).  The descriptor
+   array is read and packed before return, so the caller may reuse it at
+   once.  Descriptors of at most small_max_bytes go to one warp each
+   (largest first); longer ones are split into chunk_bytes pieces that
+   whole CTAs copy.  Destinations must not overlap one another or any source
+   of the batch (the order of copies is unspecified).  TB_EINVAL for a null
+   address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
+   slot came free within wait_timeout_ns. */
+int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
+
+typedef struct {
+    uint64_t descs;        /* descriptors with len > 0 */
+    uint64_t warp_items;   /* descriptors copied by one warp */
+    uint64_t cta_items;    /* chunks copied by a whole CTA */
+    uint64_t launches;     /* kernel launches (slots) used */
+    uint64_t bytes;        /* sum of len */
+    uint64_t upload_bytes; /* packed work-item bytes copied host-to-device */
+} tb_batch_stats;
+
+/* Statistics of the last tb_batch_copy on ctx. */
+int tb_last_batch_stats(const tb_ctx *ctx, tb_batch_stats *out);
+
+/* Device time, in milliseconds, of the kernel launches of the last
+   tb_batch_copy (summed over its launches).  Waits for them to finish.
+   TB_ENOTSUP unless the context was created with time_kernels = 1. */
+int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms);
+
+/* The per-copy baseline the Mooncake RFC measures against ("Every request is
+   one hipMemcpyAsync"): one cudaMemcpyAsync (device to device) per
+   descriptor with len > 0, in array order, on `stream`.  Same arguments and
+   checks as tb_batch_copy; provided so the two can be timed side by side. */
+int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
+
+/* ----------------------------------------------------------------------- */
+/* Validation ("How validation (ValidateAllTransfers) works")               */
+/* ----------------------------------------------------------------------- */
+
+typedef struct {
+    int64_t  index;     /* first differing element, -1 if none */
+    uint32_t expected;  /* its expected bits (elemSize bytes, zero-extended) */
+    uint32_t actual;    /* its actual bits */
+} tb_mismatch;
+
+/* Copies numBytes of device memory at dstDevice to the host (in bounded
+   chunks through pinned staging) and compares it with expectedHost by
+   memcmp; elemSize (1, 2 or 4) sets the unit of the reported index.
+   Synchronous.  Returns TB_OK when equal, TB_EVALIDATE with *out filled at
+   the first difference otherwise.  out may be NULL. */
+int tb_validate(tb_ctx *ctx, const void *dstDevice, const void *expectedHost,
+                uint64_t numBytes, uint32_t elemSize, tb_mismatch *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TB_H */

@@ -1,0 +1,174 @@
+"""GPU parity of the batched descriptor copy (through the C ABI) against the
+oracle's batch apply.  Bar: bit-exact over the whole destination pool, whose
+untouched bytes keep a seeded random fill, so a stray write anywhere shows."""
+import numpy as np
+import pytest
+
+import oracle
+from copy_reduce_dst_gb300 import workloads
+from gpu_helpers import to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from copy_reduce_dst_gb300 import _build
+    _build.build()
+    from copy_reduce_dst_gb300 import tb as mod
+    return mod
+
+
+def run_layout(tb, ctx, layout, seed=1, stream=None, src_shift=0, dst_shift=0):
+    """Random pools, one tb_batch_copy of the layout, whole-pool comparison.
+    src_shift / dst_shift move every copy by a few bytes to vary alignment."""
+    import torch
+    src_h = workloads.random_bytes(layout.src_pool_bytes + 64, seed)
+    dst_h = workloads.random_bytes(layout.dst_pool_bytes + 64, seed + 1000)
+    src_d = to_dev(src_h)
+    dst_d = to_dev(dst_h)
+    so = layout.src_off + np.uint64(src_shift)
+    do = layout.dst_off + np.uint64(dst_shift)
+    desc = np.stack([np.uint64(src_d.data_ptr()) + so, np.uint64(dst_d.data_ptr()) + do,
+                     layout.lens], axis=1)
+    ctx.batch_copy(desc, stream)
+    if stream is not None:
+        stream.synchronize()
+    got = to_host(dst_d)
+    exp = dst_h.copy()
+    oracle.apply_batch(exp, src_h, so, do, layout.lens)
+    mm = oracle.first_mismatch(got, exp)
+    assert mm == -1, f"first differing byte {mm}"
+    return ctx.last_batch_stats()
+
+
+@pytest.fixture(scope="module")
+def ctx(tb):
+    with tb.Context(0) as c:
+        yield c
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tiny_any_alignment(tb, ctx, seed):
+    # lengths 0..300 B at any byte offset of src and dst
+    layout = workloads.random_batch(seed, 2000, 300, 4 * MiB, align=1)
+    st = run_layout(tb, ctx, layout, seed)
+    assert st["descs"] == int((layout.lens > 0).sum())
+
+
+@pytest.mark.parametrize("ss,ds", [(0, 0), (1, 0), (0, 1), (3, 7), (15, 1), (4, 12), (8, 8)])
+def test_misalignment_pairs(tb, ctx, ss, ds):
+    # every src/dst alignment pair over lengths that cross vector and tile edges
+    layout = workloads.random_batch(ss * 16 + ds, 3000, 5000, 64 * MiB, align=16)
+    run_layout(tb, ctx, layout, 7, src_shift=ss, dst_shift=ds)
+
+
+def test_lengths_one_byte_to_three_mib(tb, ctx):
+    # Mooncake RFC "Correctness": lengths from 1 B to 3 MiB, unaligned ranges
+    g = np.random.default_rng(11)
+    lens = np.exp(g.uniform(0, np.log(3 * MiB), 600)).astype(np.uint64)
+    lens = np.maximum(lens, 1)
+    gen = workloads.rng(12)
+    so = workloads.scatter_offsets(gen, lens, 0, 1024 * MiB, 1)
+    do = workloads.scatter_offsets(gen, lens, 0, 1024 * MiB, 1)
+    layout = workloads.BatchLayout("1B-3MiB", so, do, lens, 1024 * MiB, 1024 * MiB)
+    st = run_layout(tb, ctx, layout, 13)
+    assert st["cta_items"] > 0 and st["warp_items"] > 0
+
+
+def test_more_launches_than_slots(tb):
+    # 1024 items per slot and 2 slots: the batch needs many launches and every
+    # slot is reused while earlier launches may still be running.
+    with tb.Context(0, tb.options(slot_items=1024, num_slots=2, chunk_bytes=4096)) as c:
+        layout = workloads.random_batch(21, 9000, 20000, 512 * MiB, align=1)
+        st = run_layout(tb, c, layout, 22)
+        assert st["launches"] > 2 * 2
+        for i in range(3):
+            run_layout(tb, c, workloads.random_batch(30 + i, 3000, 4000, 64 * MiB), 40 + i)
+
+
+@pytest.mark.parametrize("small,chunk", [(1, 4096), (64, 8192), (16384, 65536), (1 << 20, 1 << 20),
+                                         (16 << 20, 4096)])
+def test_size_bins(tb, small, chunk):
+    with tb.Context(0, tb.options(small_max_bytes=small, chunk_bytes=chunk)) as c:
+        layout = workloads.random_batch(5, 1500, 100000, 512 * MiB, align=4)
+        run_layout(tb, c, layout, 6, src_shift=1)
+
+
+def test_user_stream_ordering(tb, ctx):
+    """The copy runs after earlier work on the caller's stream: a fill queued
+    just before on the same stream is what gets copied."""
+    import torch
+    st = torch.cuda.Stream()
+    src = torch.zeros(8 * MiB, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(8 * MiB, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        big = torch.empty(256 * MiB, dtype=torch.uint8, device="cuda")
+        for _ in range(4):
+            big.fill_(1)               # keep the stream busy for a while
+        src.fill_(0xAB)
+    desc = np.array([[src.data_ptr(), dst.data_ptr(), 8 * MiB]], dtype=np.uint64)
+    ctx.batch_copy(desc, st)
+    st.synchronize()
+    assert np.all(to_host(dst) == 0xAB)
+
+
+def test_bad_descriptors(tb, ctx):
+    import torch
+    d = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tb.TBError) as e:
+        ctx.batch_copy(np.array([[0, d.data_ptr(), 8]], dtype=np.uint64))
+    assert e.value.code == tb.TB_EINVAL
+    with pytest.raises(tb.TBError):
+        ctx.batch_copy(np.array([[d.data_ptr(), 2**64 - 4, 8]], dtype=np.uint64))
+    ctx.batch_copy(np.array([[0, 0, 0]], dtype=np.uint64))         # len 0 is a no-op
+    ctx.batch_copy(np.zeros((0, 3), dtype=np.uint64))
+
+
+def test_slot_wait_deadline(tb):
+    """With one slot, a second batch waits for the first launch; a 1 ns limit
+    expires first and the call returns TB_ETIMEOUT instead of blocking."""
+    import torch
+    with tb.Context(0, tb.options(num_slots=1, wait_timeout_ns=1)) as c:
+        layout = workloads.random_batch(3, 40000, 16384, 1024 * MiB, align=64)
+        src = torch.empty(1024 * MiB, dtype=torch.uint8, device="cuda")
+        dst = torch.empty(1024 * MiB, dtype=torch.uint8, device="cuda")
+        desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            for _ in range(8):
+                src.fill_(3)           # the launch queues behind these
+        c.batch_copy(desc, st)
+        with pytest.raises(tb.TBError) as e:
+            c.batch_copy(desc, st)
+        assert e.value.code == tb.TB_ETIMEOUT
+        st.synchronize()
+        c.batch_copy(desc, st)         # the slot is free again
+        st.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# Full-size layouts, in the launch configuration the bench times
+# ---------------------------------------------------------------------------
+def test_index_pages_full(tb, ctx):
+    st = run_layout(tb, ctx, workloads.batch_index_pages(), 101)
+    assert st["descs"] == 3840 and st["warp_items"] == 3840
+
+
+def test_block_pages_full(tb, ctx):
+    st = run_layout(tb, ctx, workloads.batch_block_pages(), 102)
+    assert st["descs"] == 7200
+
+
+def test_head_sliced_full(tb, ctx):
+    layout = workloads.batch_head_sliced()
+    st = run_layout(tb, ctx, layout, 103)
+    assert st["descs"] == 47540 and st["warp_items"] == 47520
+    assert st["cta_items"] == (16 * 16 * MiB + 4 * 8 * MiB) // (64 * 1024)
+    assert st["launches"] == 1

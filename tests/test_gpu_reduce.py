@@ -1,0 +1,379 @@
+"""GPU parity of the reduce-copy path (through the C ABI) against the oracle.
+
+Bar: bit-exact.  Every float add on both sides is one IEEE binary32
+round-to-nearest-even add taken left to right, so dst must equal
+dstReference[nSrc] byte for byte (inputs are finite and NaN-free; a NaN's
+payload after an add is not fixed by IEEE 754 and is not compared here).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import dev_bytes, finite_floats, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from copy_reduce_dst_gb300 import _build
+    _build.build()
+    from copy_reduce_dst_gb300 import tb as mod
+    return mod
+
+
+@pytest.fixture(scope="module")
+def ctx(tb):
+    with tb.Context(0) as c:
+        yield c
+
+
+def reduce_and_compare(tb, ctx, srcs_host, byte_offsets=None, dst_offset=0, num_subexec=0,
+                       memset_byte=0):
+    """Uploads the sources at the given byte offsets inside padded buffers,
+    runs one tb_reduce_copy, and compares dst (and the guard bytes around it)
+    with the oracle."""
+    n = srcs_host[0].size if srcs_host else 0
+    nbytes = 4 * n
+    offs = byte_offsets or [0] * len(srcs_host)
+    pad = 256
+    bufs = []
+    for a, off in zip(srcs_host, offs):
+        b = dev_bytes(nbytes + off + pad, fill=0x5A)
+        b[off:off + nbytes].copy_(to_dev(a)[:nbytes]) if nbytes else None
+        bufs.append((b, off))
+    dst = dev_bytes(nbytes + dst_offset + pad, fill=0xC3)
+    ctx.reduce_copy([b.data_ptr() + off for b, off in bufs], dst.data_ptr() + dst_offset, nbytes,
+                    num_subexec)
+    got = to_host(dst)
+    exp = oracle.dst_reference(srcs_host, n=n, memset_byte=memset_byte)
+    body = got[dst_offset:dst_offset + nbytes]
+    mm = oracle.first_mismatch(body.view(np.uint32) if nbytes else body, exp.view(np.uint32))
+    assert mm == -1, f"first mismatch at element {mm}"
+    assert np.all(got[:dst_offset] == 0xC3) and np.all(got[dst_offset + nbytes:] == 0xC3), \
+        "write outside dst"
+
+
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16])
+def test_reduce_parity_source_counts(tb, ctx, nsrc):
+    g = np.random.default_rng(100 + nsrc)
+    n = 3 * 512 * 4 * 8 + 13          # several tiles plus a ragged tail
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    reduce_and_compare(tb, ctx, srcs)
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 1000, 4097, 65536 + 3])
+def test_reduce_parity_sizes(tb, ctx, n):
+    g = np.random.default_rng(n)
+    srcs = [finite_floats(g, n) for _ in range(3)]
+    if n == 0:
+        dst = dev_bytes(64, fill=0xC3)
+        ctx.reduce_copy([dev_bytes(16).data_ptr()] * 3, dst.data_ptr(), 0)
+        assert np.all(to_host(dst) == 0xC3)
+        return
+    reduce_and_compare(tb, ctx, srcs)
+
+
+@pytest.mark.parametrize("offs,doff", [
+    ([4, 4, 4], 4),          # co-aligned, head of 7 elements to 32 B
+    ([20, 20, 20], 20),      # co-aligned mod 32 with a 3-element head
+    ([16, 16, 16], 16),      # co-aligned mod 16, not mod 32
+    ([48, 16, 80], 16),      # co-aligned mod 16 only, different mod 32
+    ([0, 4, 8], 12),         # no common alignment: scalar path
+    ([0, 0, 0], 4),          # dst misaligned against the sources
+])
+def test_reduce_parity_alignment(tb, ctx, offs, doff):
+    g = np.random.default_rng(sum(offs) + doff)
+    n = 100003
+    srcs = [finite_floats(g, n) for _ in range(3)]
+    reduce_and_compare(tb, ctx, srcs, byte_offsets=offs, dst_offset=doff)
+
+
+@pytest.mark.parametrize("nsrc", [1, 2, 9])
+def test_reduce_parity_alignment_many(tb, ctx, nsrc):
+    g = np.random.default_rng(7 * nsrc)
+    n = 50001
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    reduce_and_compare(tb, ctx, srcs, byte_offsets=[4 * (k % 3) for k in range(nsrc)],
+                       dst_offset=8)
+    reduce_and_compare(tb, ctx, srcs, byte_offsets=[12] * nsrc, dst_offset=12)
+
+
+@pytest.mark.parametrize("subexec", [1, 3, 4, 16, 32, 1000, 0])
+@pytest.mark.parametrize("ctas", [0, 1, 3])
+def test_reduce_parity_subexecutors(tb, subexec, ctas):
+    g = np.random.default_rng(subexec * 10 + ctas)
+    n = 262144 + 5
+    srcs = [finite_floats(g, n) for _ in range(3)]
+    with tb.Context(0, tb.options(ctas_per_subexec=ctas)) as c:
+        reduce_and_compare(tb, c, srcs, num_subexec=subexec)
+
+
+@pytest.mark.parametrize("vec,unroll,threads", [(4, 0, 0), (16, 1, 256), (16, 2, 0), (16, 4, 512),
+                                               (32, 1, 128), (32, 2, 512), (32, 4, 0), (0, 0, 64)])
+@pytest.mark.parametrize("nsrc", [1, 3, 8])
+def test_reduce_parity_kernel_shapes(tb, vec, unroll, threads, nsrc):
+    g = np.random.default_rng(vec + unroll + threads + nsrc)
+    n = 131072 + 9
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    with tb.Context(0, tb.options(vec_bytes=vec, unroll=unroll, block_threads=threads)) as c:
+        reduce_and_compare(tb, c, srcs, num_subexec=7)
+
+
+@pytest.mark.parametrize("byte", [0x00, 0xA5])
+def test_zero_sources_is_memset(tb, byte):
+    with tb.Context(0, tb.options(memset_byte=byte)) as c:
+        for n, doff in ((1, 0), (77777, 4), (4096, 20)):
+            dst = dev_bytes(4 * n + doff + 64, fill=0x11)
+            c.reduce_copy([], dst.data_ptr() + doff, 4 * n)
+            got = to_host(dst)
+            assert np.all(got[doff:doff + 4 * n] == byte)
+            assert np.all(got[:doff] == 0x11) and np.all(got[doff + 4 * n:] == 0x11)
+
+
+def test_one_source_copies_bits(tb, ctx):
+    bits = np.array([0x80000000, 0x7FC00001, 0xFF800001, 0x7FA00000, 0x00000001, 0x807FFFFF,
+                     0x7F800000, 0xFF800000] * 5001, dtype=np.uint32)
+    reduce_and_compare(tb, ctx, [bits.view(np.float32)])
+    reduce_and_compare(tb, ctx, [bits.view(np.float32)], byte_offsets=[4], dst_offset=12)
+
+
+def test_left_to_right_association(tb, ctx):
+    one = np.ones(1000, np.float32)
+    eps = np.full(1000, 2.0**-24, np.float32)
+    reduce_and_compare(tb, ctx, [one, eps, eps])
+    reduce_and_compare(tb, ctx, [eps, eps, one])
+
+
+def test_bad_arguments(tb, ctx):
+    d = dev_bytes(64)
+    with pytest.raises(tb.TBError) as e:
+        ctx.reduce_copy([d.data_ptr()], d.data_ptr() + 32, 6)          # not a multiple of 4
+    assert e.value.code == tb.TB_EINVAL
+    with pytest.raises(tb.TBError):
+        ctx.reduce_copy([d.data_ptr() + 2], d.data_ptr() + 32, 8)      # misaligned
+    with pytest.raises(tb.TBError):
+        ctx.reduce_copy([d.data_ptr()] * 17, d.data_ptr(), 8)          # too many sources
+    with pytest.raises(tb.TBError):
+        ctx.reduce_copy([0], d.data_ptr(), 8)                          # null source
+
+
+# ---------------------------------------------------------------------------
+# Source patterns written by the library's fill kernels
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("k", [0, 1, 2, 15])
+def test_fill_default_pattern(tb, ctx, k):
+    n = 383 * 1000 + 77
+    d = dev_bytes(4 * n + 4)
+    ctx.fill_source(d.data_ptr() + 4, 4 * n, tb.default_pattern(), k)
+    got = to_host(d, 4 * n, 4).view(np.float32)
+    assert oracle.first_mismatch(got, oracle.prepare_reference(n, k)) == -1
+
+
+@pytest.mark.parametrize("pct,k,n", [((40, 20, 0, 20, 20), 0, 16 * 20000),
+                                     ((40, 20, 0, 20, 20), 1, 16 * 3000 + 7),
+                                     ((0, 25, 25, 25, 25), 2, 16 * 999 + 15),
+                                     ((100, 0, 0, 0, 0), 0, 33)])
+def test_fill_compress_pattern(tb, ctx, pct, k, n):
+    d = dev_bytes(4 * n)
+    ctx.fill_source(d, 4 * n, tb.compress_pattern(pct, 0x5EED), k)
+    got = to_host(d, 4 * n).view(np.uint32)
+    exp = oracle.fill_compress(n, pct, 0x5EED, k).view(np.uint32)
+    assert oracle.first_mismatch(got, exp) == -1
+
+
+def test_fill_repeat_pattern(tb, ctx):
+    vals = [1.5, -2.0, 0.25, 7.0, -0.0]
+    pat, keep = tb.repeat_pattern(vals)
+    n = 100001
+    d = dev_bytes(4 * n)
+    ctx.fill_source(d, 4 * n, pat, 0)
+    got = to_host(d).view(np.float32)
+    assert oracle.first_mismatch(got, oracle.fill_pattern(n, np.array(vals, np.float32))) == -1
+
+
+def test_fill_rejects_bad_patterns(tb, ctx):
+    d = dev_bytes(64)
+    with pytest.raises(tb.TBError):
+        ctx.fill_source(d, 64, tb.compress_pattern((50, 0, 0, 0, 0), 1), 0)
+    with pytest.raises(tb.TBError):
+        ctx.fill_source(d, 62, tb.default_pattern(), 0)
+
+
+# ---------------------------------------------------------------------------
+# Rotation, timed loop and validation (tb_run_transfer)
+# ---------------------------------------------------------------------------
+def test_single_transfer_mechanism(tb):
+    """PR #365's mechanism check: a 4 MiB transfer at the 256 MiB default
+    allocates 268,435,456 B (K = 64) while the prep host-to-device copy stays
+    4 MiB; every slice holds slice 0's data; validation passes with rotation
+    on, once at the end and after every iteration."""
+    nb = 4 * MiB
+    n = nb // 4
+    plan = tb.rotation_plan(nb, 256 * MiB)
+    assert (plan.K, plan.alloc_bytes) == (64, 268435456)
+    ref = oracle.prepare_reference(n, 0)
+    for always in (0, 1):
+        with tb.Context(0, tb.options(always_validate=always)) as c:
+            src = dev_bytes(plan.alloc_bytes)
+            dst = dev_bytes(nb, fill=0)
+            c.upload_sources([src], [ref], nb)
+            assert c.prep_h2d_bytes == nb
+            c.prepare_sources([src], nb, 256 * MiB)
+            assert c.prep_h2d_bytes == nb
+            whole = to_host(src).view(np.float32).reshape(64, n)
+            for j in range(64):
+                assert oracle.first_mismatch(whole[j], ref) == -1, f"slice {j}"
+            r = c.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB, expected=ref)
+            assert r["K"] == 64 and r["alloc_bytes"] == 268435456 and r["prep_h2d_bytes"] == nb
+            assert r["iters"] == 10 and r["validated"] == 1 and r["mismatch_index"] == -1
+            assert len(r["iter_ms"]) == 10 and all(t > 0 for t in r["iter_ms"])
+            assert r["gated"] == (0 if always else 1)
+
+
+@pytest.mark.parametrize("iters,warmup,K", [(5, 3, 8), (1, 3, 8), (8, 0, 8), (3, 5, 4), (7, 2, 1)])
+def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K):
+    """Slices filled with different patterns: after the loop dst holds the
+    last iteration's slice, (iters - 1) % K."""
+    nb = 64 * 1024
+    n = nb // 4
+    with tb.Context(0, tb.options(warmup=warmup)) as c:
+        plan = tb.rotation_plan(nb, K * nb)
+        assert plan.K == K
+        src = dev_bytes(plan.alloc_bytes)
+        for j in range(K):
+            c.fill_source(src.data_ptr() + j * plan.slice_stride, nb, tb.default_pattern(), j)
+        dst = dev_bytes(nb, fill=0)
+        last = oracle.slice_for_iteration(iters - 1, K)
+        expect = oracle.prepare_reference(n, last)
+        r = c.run_transfer([src], dst, nb, iters=iters, rotate_bytes=K * nb, expected=expect)
+        assert r["mismatch_index"] == -1
+
+
+def test_byte_offset(tb):
+    nb = 1 * MiB + 64
+    n = nb // 4
+    with tb.Context(0, tb.options(byte_offset=20)) as c:
+        plan = tb.rotation_plan(nb, 4 * MiB, 20)
+        srcs = [dev_bytes(plan.alloc_bytes) for _ in range(2)]
+        refs = [oracle.prepare_reference(n, k) for k in range(2)]
+        c.upload_sources(srcs, refs, nb)
+        c.prepare_sources(srcs, nb, 4 * MiB)
+        dst = dev_bytes(nb + 20, fill=0x77)
+        r = c.run_transfer(srcs, dst, nb, iters=6, rotate_bytes=4 * MiB,
+                           expected=oracle.dst_reference(refs))
+        assert r["K"] == plan.K == 4 and r["mismatch_index"] == -1
+        assert np.all(to_host(dst, 20) == 0x77)
+
+
+@pytest.mark.parametrize("always", [0, 1])
+def test_validation_reports_first_mismatch(tb, always):
+    nb = 256 * 1024
+    n = nb // 4
+    with tb.Context(0, tb.options(always_validate=always)) as c:
+        src = dev_bytes(nb)
+        c.fill_source(src, nb, tb.default_pattern(), 0)
+        dst = dev_bytes(nb)
+        wrong = oracle.prepare_reference(n, 0)
+        wrong[12345] = 1.0        # a planted error in the expected copy
+        with pytest.raises(tb.TBError) as e:
+            c.run_transfer([src], dst, nb, iters=3, rotate_bytes=0, expected=wrong)
+        assert e.value.code == tb.TB_EVALIDATE
+        r = e.value.result
+        assert r["mismatch_index"] == 12345
+        assert r["mismatch_expected"] == np.float32(1.0).view(np.uint32)
+        assert r["mismatch_actual"] == np.float32(oracle.prep_src_value(0, 12345)).view(np.uint32)
+        if always:
+            assert r["iters"] == 1       # stopped at the first iteration
+        assert c.validate(dst, wrong, nb) == (12345, int(r["mismatch_expected"]),
+                                              int(r["mismatch_actual"]))
+        assert c.validate(dst, oracle.prepare_reference(n, 0), nb) is None
+
+
+def test_gate_deadline_returns_timeout(tb):
+    """A gate whose deadline (1 microsecond) passes before the host releases
+    it returns on its own; the call reports TB_ETIMEOUT and the context stays
+    usable."""
+    nb = 1 * MiB
+    with tb.Context(0, tb.options(wait_timeout_ns=1000, warmup=3)) as c:
+        src = dev_bytes(nb)
+        c.fill_source(src, nb, tb.default_pattern(), 0)
+        dst = dev_bytes(nb)
+        with pytest.raises(tb.TBError) as e:
+            c.run_transfer([src], dst, nb, iters=200, rotate_bytes=0)
+        assert e.value.code == tb.TB_ETIMEOUT
+        ref = oracle.prepare_reference(nb // 4, 0)
+        assert c.validate(dst, ref, nb) is None
+        c2 = tb.options(use_gate=0)
+    with tb.Context(0, c2) as c:
+        src = dev_bytes(nb)
+        c.fill_source(src, nb, tb.default_pattern(), 0)
+        dst = dev_bytes(nb)
+        r = c.run_transfer([src], dst, nb, iters=4, rotate_bytes=0, expected=ref)
+        assert r["gated"] == 0
+
+
+def test_reduce_copy_host_end_to_end(tb, ctx):
+    import torch
+    g = np.random.default_rng(9)
+    n = 1000003
+    srcs = [finite_floats(g, n) for _ in range(3)]
+    hs = [torch.from_numpy(s).pin_memory() for s in srcs]
+    hd = torch.empty(n, dtype=torch.float32).pin_memory()
+    ds = [dev_bytes(4 * n) for _ in range(3)]
+    dd = dev_bytes(4 * n)
+    st = torch.cuda.Stream()
+    ctx.reduce_copy_host(hs, hd, 4 * n, ds, dd, 0, st)
+    st.synchronize()
+    assert oracle.first_mismatch(hd.numpy(), oracle.dst_reference(srcs)) == -1
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the bench times
+# ---------------------------------------------------------------------------
+def test_three_source_256mib_all_subexecutors(tb):
+    """3 x 256 MiB, src_k = PrepSrcValue(k, i), K = 1; sub-executor counts
+    1, 4, 16, 32 and auto.  dst = 6 * PrepSrcValue(0, i) exactly."""
+    nb = 256 * MiB
+    n = nb // 4
+    refs = [oracle.prepare_reference(n, k) for k in range(3)]
+    exp = oracle.dst_reference(refs)
+    with tb.Context(0) as c:
+        srcs = [dev_bytes(nb) for _ in range(3)]
+        for k, s in enumerate(srcs):
+            c.fill_source(s, nb, tb.default_pattern(), k)
+        for k, s in enumerate(srcs):
+            assert c.validate(s, refs[k], nb) is None
+        for se in (1, 4, 16, 32, 0):
+            dst = dev_bytes(nb, fill=0)
+            r = c.run_transfer(srcs, dst, nb, num_subexec=se, iters=2, rotate_bytes=256 * MiB,
+                               expected=exp)
+            assert r["K"] == 1 and r["mismatch_index"] == -1, se
+            got = to_host(dst).view(np.float32)
+            assert oracle.first_mismatch(got, exp) == -1
+            assert got[:4].tolist() == [186.0, 990.0, 1794.0, 300.0]
+
+
+@pytest.mark.parametrize("mib", [8, 64, 512])
+@pytest.mark.parametrize("rotate", [256 * MiB, 0])
+def test_compress_sweep_sizes(tb, mib, rotate):
+    nb = mib * MiB
+    n = nb // 4
+    pct = (40, 20, 0, 20, 20)
+    ref = oracle.fill_compress(n, pct, 0x5EED, 0)
+    with tb.Context(0) as c:
+        plan = tb.rotation_plan(nb, rotate)
+        src = dev_bytes(plan.alloc_bytes)
+        c.fill_source(src, nb, tb.compress_pattern(pct, 0x5EED), 0)
+        assert c.validate(src, ref, nb) is None
+        c.prepare_sources([src], nb, rotate)
+        last = plan.K - 1
+        assert c.validate(src.data_ptr() + last * plan.slice_stride, ref, nb) is None
+        dst = dev_bytes(nb, fill=0)
+        r = c.run_transfer([src], dst, nb, iters=3, rotate_bytes=rotate, expected=ref)
+        assert r["mismatch_index"] == -1 and r["K"] == plan.K
