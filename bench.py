@@ -467,6 +467,36 @@ def study(args, tb, torch, local):
 
 
 # ---------------------------------------------------------------------------
+# Profiling target: 3 warm-up + 3 launches of one kernel on the bench's own
+# workload, nothing else (for ncu -k ... -s 3 -c 1..3).
+# ---------------------------------------------------------------------------
+def profile_target(kind, tb, torch, local):
+    stream = torch.cuda.current_stream()
+    if kind == "reduce":
+        nb = 256 * MiB
+        with tb.Context(local) as ctx:
+            srcs = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(3)]
+            for k, s in enumerate(srcs):
+                ctx.fill_source(s, nb, tb.default_pattern(), k, stream)
+            dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            for _ in range(6):
+                ctx.reduce_copy(srcs, dst, nb, 32, stream)
+            torch.cuda.synchronize()
+    else:
+        from copy_reduce_dst_gb300 import workloads
+        layout = workloads.batch_head_sliced()
+        src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+        dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+        desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+        with tb.Context(local) as ctx:
+            for _ in range(6):
+                ctx.batch_copy(desc, stream)
+            torch.cuda.synchronize()
+    print(f"profile target {kind}: 6 launches done", flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,6 +506,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--study", action="store_true")
+    ap.add_argument("--profile", choices=["reduce", "batch"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -490,6 +521,8 @@ def main():
     from copy_reduce_dst_gb300 import tb  # fails loudly if libtb.so is missing
     if args.study:
         return study(args, tb, torch, local)
+    if args.profile:
+        return profile_target(args.profile, tb, torch, local)
     ranks = Ranks(world, "nccl")
     red = run_reduce(args, tb, torch, ranks, local)
     batch = None if args.no_batch else run_batch(args, tb, torch, ranks, local)

@@ -752,7 +752,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     out->prep_h2d_bytes = ctx->prep_h2d;
     out->iters = done;
     out->num_subexec = plan.num_subexec;
-    out->ctas = plan.num_subexec * plan.ctas_per_sub;
+    out->ctas = plan.grid;
     out->block_threads = plan.block_threads;
     out->gated = gated ? 1 : 0;
     out->total_ms = total;

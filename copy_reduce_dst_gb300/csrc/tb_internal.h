@@ -15,20 +15,20 @@ namespace tb {
 
 // One reduce-copy launch, fully resolved on the host.  The element range
 // [0, n) splits into head (scalar, until dst reaches vector alignment), body
-// (nvec vectors of vec_bytes) and tail (scalar).  Sub-executor s owns body
-// vectors [s * sub_vecs, min(nvec, (s + 1) * sub_vecs)); the ctas_per_sub
-// CTAs of a sub-executor share its range tile by tile.
+// (nvec vectors of vec_bytes) and tail (scalar).  The grid's CTAs are dealt to
+// the num_subexec sub-executors as evenly as integers allow; each
+// sub-executor owns a contiguous run of body vectors in proportion to its
+// CTAs (equal runs when num_subexec divides the grid).
 struct ReducePlan {
     const float *src[TB_MAX_SRCS];
     float *dst;
     uint64_t n;            // elements
     uint64_t head;         // scalar elements before the body
     uint64_t nvec;         // body vectors
-    uint64_t sub_vecs;     // body vectors per sub-executor
     int n_src;
-    int vec_bytes;         // 32, 16, or 0 (no common alignment: scalar path)
+    int vec_bytes;         // 32, 16, or 4 (no common 16-byte alignment: scalar)
     int num_subexec;
-    int ctas_per_sub;
+    int grid;              // CTAs of the launch (>= num_subexec)
     int block_threads;
     int unroll;            // vectors per source a thread holds in flight
     uint32_t memset_word;  // 0-source fill, the memset byte repeated

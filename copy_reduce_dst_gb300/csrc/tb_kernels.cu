@@ -97,10 +97,33 @@ struct ReduceArgs {
     uint64_t n;
     uint64_t head;
     uint64_t nvec;
-    uint64_t sub_vecs;
-    uint32_t ctas_per_sub;
+    uint32_t nsub;         // sub-executors; never more than the grid's CTAs
     uint32_t memset_word;
 };
+
+// The CTAs of a launch are dealt to the sub-executors as evenly as integers
+// allow (sub-executor s gets CTAs [s*G/S, (s+1)*G/S)), and each sub-executor
+// owns a contiguous range of body vectors in proportion to its CTAs, so every
+// CTA streams the same share whether or not S divides the grid G.
+struct SubRange {
+    uint32_t part, nparts;   // this CTA's rank within its sub-executor, and their count
+    uint64_t vbeg, vend;     // the sub-executor's body vectors
+};
+
+__device__ __forceinline__ SubRange sub_range(uint64_t nvec, uint32_t S)
+{
+    const uint32_t G = gridDim.x, b = blockIdx.x;
+    const uint32_t sub = (uint32_t)(((uint64_t)(b + 1) * S - 1) / G);
+    const uint32_t c0 = (uint32_t)((uint64_t)sub * G / S);
+    const uint32_t c1 = (uint32_t)((uint64_t)(sub + 1) * G / S);
+    const uint64_t q = nvec / G, r = nvec % G;
+    SubRange sr;
+    sr.part = b - c0;
+    sr.nparts = c1 - c0;
+    sr.vbeg = q * c0 + (r * c0) / G;
+    sr.vend = q * c1 + (r * c1) / G;
+    return sr;
+}
 
 // Scalar element i, used for the head and the tail of a launch.
 template <int N>
@@ -158,8 +181,7 @@ __global__ void __launch_bounds__(512) k_reduce(const ReduceArgs a)
 {
     const uint32_t tid = threadIdx.x;
     const uint32_t bd = blockDim.x;
-    const uint32_t sub = blockIdx.x / a.ctas_per_sub;
-    const uint32_t part = blockIdx.x - sub * a.ctas_per_sub;
+    const SubRange sr = sub_range(a.nvec, a.nsub);
 
     const char *s[N > 0 ? N : 1];
 #pragma unroll
@@ -167,11 +189,10 @@ __global__ void __launch_bounds__(512) k_reduce(const ReduceArgs a)
         s[k] = reinterpret_cast<const char *>(a.src[k] + a.head);
     char *d = reinterpret_cast<char *>(a.dst + a.head);
 
-    const uint64_t vbeg = (uint64_t)sub * a.sub_vecs;
-    const uint64_t vend = min(a.nvec, vbeg + a.sub_vecs);
+    const uint64_t vend = sr.vend;
     const uint64_t tile = (uint64_t)bd * U;
-    const uint64_t step = (uint64_t)a.ctas_per_sub * tile;
-    for (uint64_t t = vbeg + part * tile; t < vend; t += step) {
+    const uint64_t step = (uint64_t)sr.nparts * tile;
+    for (uint64_t t = sr.vbeg + sr.part * tile; t < vend; t += step) {
         if (t + tile <= vend)
             reduce_vectors<N, VB, U>(a, s, d, t + tid, bd, vend, true);
         else
@@ -192,14 +213,12 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
 {
     const uint32_t tid = threadIdx.x;
     const uint32_t bd = blockDim.x;
-    const uint32_t sub = blockIdx.x / a.ctas_per_sub;
-    const uint32_t part = blockIdx.x - sub * a.ctas_per_sub;
-    const uint64_t vbeg = (uint64_t)sub * a.sub_vecs;
-    const uint64_t vend = min(a.nvec, vbeg + a.sub_vecs);
+    const SubRange sr = sub_range(a.nvec, a.nsub);
+    const uint64_t vend = sr.vend;
     const uint64_t tile = (uint64_t)bd * 2;
-    const uint64_t step = (uint64_t)a.ctas_per_sub * tile;
+    const uint64_t step = (uint64_t)sr.nparts * tile;
     const uint64_t W = VB / 4;
-    for (uint64_t t = vbeg + part * tile; t < vend; t += step) {
+    for (uint64_t t = sr.vbeg + sr.part * tile; t < vend; t += step) {
         const uint64_t v0 = t + tid, v1 = t + bd + tid;
         if (v0 >= vend)
             break;
@@ -621,16 +640,17 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     p->block_threads = block_threads ? block_threads : 512;
     p->unroll = vb == 4 ? 4 : std::min(unroll ? unroll : default_unroll(n_src, vb), max_unroll(n_src, vb));
 
+    // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
+    // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
+    // sub-executor); never fewer CTAs than sub-executors.
     const int per_sm = reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
     const int64_t full = (int64_t)num_sms * per_sm;
     const int64_t S = num_subexec > 0 ? num_subexec : full;
-    const int64_t C =
-        ctas_per_subexec > 0 ? ctas_per_subexec : std::max<int64_t>(1, (full + S - 1) / S);
-    if (S * C > (int64_t)INT32_MAX)
+    const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, full);
+    if (G > (int64_t)INT32_MAX)
         return TB_EINVAL;
     p->num_subexec = (int)S;
-    p->ctas_per_sub = (int)C;
-    p->sub_vecs = std::max<uint64_t>(1, (p->nvec + (uint64_t)S - 1) / (uint64_t)S);
+    p->grid = (int)G;
     return TB_OK;
 }
 
@@ -643,10 +663,9 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.n = p.n;
     a.head = p.head;
     a.nvec = p.nvec;
-    a.sub_vecs = p.sub_vecs;
-    a.ctas_per_sub = (uint32_t)p.ctas_per_sub;
+    a.nsub = (uint32_t)p.num_subexec;
     a.memset_word = p.memset_word;
-    const unsigned grid = (unsigned)p.num_subexec * (unsigned)p.ctas_per_sub;
+    const unsigned grid = (unsigned)p.grid;
     if (p.n == 0)
         return cudaSuccess;
     if (p.n_src > 8) {

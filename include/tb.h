@@ -86,8 +86,9 @@ typedef struct {
     int32_t always_validate;
     /* MEMSET_CHAR: the byte a 0-source transfer writes.  Default 0. */
     uint32_t memset_byte;
-    /* Reduce-copy CTAs per sub-executor; 0 = enough to fill every SM.
-       1 gives one CTA per sub-executor.  Default 0. */
+    /* Reduce-copy CTAs per sub-executor.  0 = one full wave of resident CTAs
+       dealt to the sub-executors as evenly as possible (at least one each);
+       1 gives TransferBench's one CTA per sub-executor.  Default 0. */
     int32_t ctas_per_subexec;
     /* Reduce-copy threads per CTA (multiple of 32, <= 512); 0 = 512. */
     int32_t block_threads;
@@ -252,9 +253,10 @@ uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
    srcs[k] and dst point at the data itself (no byte_offset or slice offset
    is added).  numBytes must be a multiple of 4, every pointer 4-byte aligned,
    nSrc <= TB_MAX_SRCS.  The elements are split into numSubExec contiguous
-   ranges (sub-executors), each a multiple of 4 elements except the last;
-   numSubExec == 0 means one per CTA of the default grid.  Ranges must not
-   overlap between dst and any source. */
+   ranges (sub-executors), each served by its own CTAs and sized in
+   proportion to them (equal when numSubExec divides the grid);
+   numSubExec == 0 means one per CTA of the default grid.  The split does not
+   change the result.  dst must not overlap any source. */
 int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int nSrc, void *dst,
                    uint64_t numBytes, int numSubExec, tb_stream stream);
 
