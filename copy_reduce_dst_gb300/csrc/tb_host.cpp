@@ -181,6 +181,15 @@ int check_options(tb_ctx *ctx, const tb_options &o)
     return TB_OK;
 }
 
+// CUDA profiling tools (ncu, nsys) are injected through CUDA_INJECTION64_PATH
+// and run each launch to completion before the launch call returns; a gate
+// kernel would then hold the host inside its own launch until its deadline.
+bool profiler_attached()
+{
+    const char *v = getenv("CUDA_INJECTION64_PATH");
+    return v && *v;
+}
+
 uint64_t now_ns()
 {
     return (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(
@@ -698,7 +707,8 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     ctx->iter_ms.assign(iters, 0.0f);
     cudaStream_t st = ctx->stream;
     const bool per_iter_validate = o.always_validate && t->expected;
-    const bool gated = o.use_gate && !per_iter_validate && o.warmup + iters <= kMaxGatedLaunches;
+    const bool gated = o.use_gate && !per_iter_validate && o.warmup + iters <= kMaxGatedLaunches &&
+                       !profiler_attached();
 
     if (gated) {
         ctx->gate_flag[0] = 0;

@@ -110,6 +110,8 @@ typedef struct {
     /* 1 = tb_run_transfer enqueues its iterations behind a gate kernel that
        the host releases once everything is queued, so host launch overhead
        never separates iterations (nvbandwidth's spin-kernel method).
+       Ignored when a CUDA profiling tool is injected (CUDA_INJECTION64_PATH
+       set): such tools finish each launch before the launch call returns.
        Default 1. */
     int32_t use_gate;
     /* Reduce-copy vector width in bytes: 32, 16, or 0 = the widest that every
