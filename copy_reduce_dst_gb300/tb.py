@@ -163,6 +163,9 @@ _sig("tb_last_batch_stats", ct.c_int, _vp, _P(BatchStats))
 _sig("tb_last_batch_kernel_ms", ct.c_int, _vp, _P(ct.c_double))
 _sig("tb_copy_each", ct.c_int, _vp, _P(CopyDesc), ct.c_size_t, _vp)
 _sig("tb_validate", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
+_sig("tb_batch_copy_noalloc", ct.c_int, _P(CopyDesc), ct.c_size_t, _vp)
+
+TB_NOALLOC_MAX_ITEMS = 65536
 
 
 class TBError(RuntimeError):
@@ -414,3 +417,13 @@ class Context:
             return (m.index, m.expected, m.actual)
         self._ok(code, "tb_validate")
         return None
+
+
+def batch_copy_noalloc(descs, stream=None) -> None:
+    """tb_batch_copy_noalloc on the current CUDA device: the batched copy for
+    callers that cannot allocate device memory (its work items live in a
+    fixed array inside the library).  Raises TBError on a nonzero code."""
+    ptr, n, keep = Context.descriptor_array(descs)
+    code = lib.tb_batch_copy_noalloc(ptr, n, stream_handle(stream))
+    del keep
+    _check(code, None, "tb_batch_copy_noalloc")

@@ -364,6 +364,32 @@ int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms);
    checks as tb_batch_copy; provided so the two can be timed side by side. */
 int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
 
+/* Work items tb_batch_copy_noalloc can hold: 65,536 (1.5 MiB of device
+   memory per GPU, 24 bytes each). */
+#define TB_NOALLOC_MAX_ITEMS 65536
+
+/* The batched copy without any allocation.  The pages have no counterpart:
+   it exists for callers that cannot call cudaMalloc - a serving engine that
+   has handed all free HBM to its own allocator (a KV cache reserved up
+   front) has nothing left for one, and a latency-sensitive loop cannot
+   afford cudaMalloc / cudaFree, which may synchronize the whole device.
+   Same copy semantics as tb_batch_copy with default options (copies up to
+   16 KiB go to one warp, longer ones to 64 KiB CTA chunks), on the current
+   CUDA device, asynchronously on `stream`; no context is needed.
+   The packed work items live in a fixed __device__ array that every GPU
+   loading this library holds until the process exits.  The first call on a
+   device looks up that array's device address (with that device current);
+   make that first call before any stream capture.  Every call on a device
+   shares the one array and leaves the last batch's items in it: calls whose
+   work overlaps on the GPU (different streams, no ordering between them)
+   race; calls on one stream run in order.  Host-side packing is serialized
+   by a lock.  Returns TB_EINVAL for a null or wrapping range, TB_ENOTSUP
+   when the batch needs more than TB_NOALLOC_MAX_ITEMS work items (each copy
+   up to 16 KiB is one item, a longer one ceil(len / 64 KiB) items; nothing
+   is copied then), TB_ECUDA when a CUDA call fails.  It calls no cudaMalloc,
+   cudaFree or other allocating routine. */
+int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stream stream);
+
 /* ----------------------------------------------------------------------- */
 /* Validation ("How validation (ValidateAllTransfers) works")               */
 /* ----------------------------------------------------------------------- */
