@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libtb.so")
 
-SOURCES = ["tb_kernels.cu", "tb_host.cpp", "tb_static.cu"]
+SOURCES = ["tb_kernels.cu", "tb_host.cpp", "tb_pack.cpp", "tb_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-ftz=false",
               "-Xcompiler", "-fPIC,-O2,-Wall,-Wextra", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -30,8 +30,8 @@ constexpr uint64_t kValidateChunk = 64 * kMiB;
 constexpr int kMaxGatedLaunches = 256;
 
 struct Slot {
-    WorkItem *dev = nullptr;   // device copy of the packed items
-    WorkItem *host = nullptr;  // pinned staging
+    void *dev = nullptr;       // device copy of one packed launch
+    void *host = nullptr;      // pinned staging of it
     cudaEvent_t done = nullptr;
     bool pending = false;      // `done` recorded and maybe not reached yet
     cudaEvent_t t0 = nullptr;  // kernel timing (time_kernels only)
@@ -57,7 +57,7 @@ struct tb_ctx {
 
     std::vector<Slot> slots;
     uint32_t next_slot = 0;
-    std::vector<WorkItem> pack;       // packing area when a batch spans slots
+    int batch_grid = 0;               // one wave of batch-kernel CTAs
     std::vector<uint32_t> bucket;     // counting-sort buckets
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
@@ -166,8 +166,6 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "block_threads must be a multiple of 32 up to 512");
     if (o.small_max_bytes == 0 || o.small_max_bytes > 16 * kMiB)
         return fail(ctx, TB_EINVAL, "small_max_bytes must be in [1, 16 MiB]");
-    if (o.chunk_bytes < 4096 || o.chunk_bytes % 4096 != 0 || o.chunk_bytes > (1ull << 31))
-        return fail(ctx, TB_EINVAL, "chunk_bytes must be a multiple of 4096 up to 2 GiB");
     if (o.slot_items < 1024 || o.slot_items > (1u << 24))
         return fail(ctx, TB_EINVAL, "slot_items must be in [1024, 2^24]");
     if (o.num_slots < 1 || o.num_slots > 64)
@@ -320,7 +318,6 @@ void tb_options_default(tb_options *o)
     o->ctas_per_subexec = 0;
     o->block_threads = 0;
     o->small_max_bytes = 16384;
-    o->chunk_bytes = 65536;
     o->slot_items = 65536;
     o->num_slots = 4;
     o->wait_timeout_ns = 5000000000ull;
@@ -386,7 +383,6 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_CTAS_PER_SUBEXEC", &o->ctas_per_subexec, &bad);
     env_i32("TB_BLOCK_THREADS", &o->block_threads, &bad);
     env_u64("TB_SMALL_MAX_BYTES", &o->small_max_bytes, &bad);
-    env_u64("TB_CHUNK_BYTES", &o->chunk_bytes, &bad);
     env_u32("TB_SLOT_ITEMS", &o->slot_items, &bad);
     env_u32("TB_NUM_SLOTS", &o->num_slots, &bad);
     env_u64("TB_WAIT_TIMEOUT_NS", &o->wait_timeout_ns, &bad);
@@ -479,8 +475,9 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     ctx->gate_flag_dev = static_cast<uint32_t *>(dgate);
     ctx->gate_status_dev = ctx->gate_flag_dev + 1;
 
+    ctx->batch_grid = ctx->num_sms * tb::batch_ctas_per_sm();
     ctx->slots.resize(o.num_slots);
-    const size_t slot_bytes = (size_t)o.slot_items * sizeof(WorkItem);
+    const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items, ctx->batch_grid);
     for (Slot &s : ctx->slots) {
         if (cudaMalloc(&s.dev, slot_bytes) != cudaSuccess)
             return bail(TB_ENOMEM);
@@ -816,113 +813,61 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     if (n > 0 && !desc)
         return fail(ctx, TB_EINVAL, "batch_copy: null descriptor array");
     const tb_options &o = ctx->opt;
-    tb_batch_stats st{};
-
-    // Pass 1: check every descriptor; count warp items per length bucket and
-    // CTA chunks.  Buckets sort warp items longest first (coarsely).
     const uint64_t small = o.small_max_bytes;
-    unsigned shift = 6;
-    while ((small >> shift) > 4096)
-        ++shift;
-    const size_t nb = (size_t)(small >> shift) + 1;
-    ctx->bucket.assign(nb + 1, 0);
-    uint64_t n_cta = 0, n_long = 0;
-    for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
-            continue;
-        if (d.src == 0 || d.dst == 0 || d.src + d.len < d.src || d.dst + d.len < d.dst)
-            return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range", i);
-        ++st.descs;
-        st.bytes += d.len;
-        if (d.len <= small) {
-            ++ctx->bucket[nb - 1 - (size_t)(d.len >> shift)];
-        } else {
-            ++n_long;
-            n_cta += (d.len + o.chunk_bytes - 1) / o.chunk_bytes;
-        }
-    }
-    const uint64_t n_warp = st.descs - n_long;
-    st.warp_items = n_warp;
-    st.cta_items = n_cta;
-    const uint64_t total = n_cta + n_warp;
-    if (total == 0) {
+    tb::BatchCounts all;
+    size_t bad = 0;
+    if (tb::count_batch(desc, n, small, &all, &bad) != TB_OK)
+        return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range", bad);
+    tb_batch_stats st{};
+    st.descs = all.descs;
+    st.bytes = all.bytes;
+    ctx->last_slots.clear();
+    if (all.descs == 0) {
         ctx->last_batch = st;
         return TB_OK;
     }
-    // Bucket counts -> first position of each bucket among the warp items.
-    uint32_t run = 0;
-    for (size_t b = 0; b < nb; ++b) {
-        const uint32_t c = ctx->bucket[b];
-        ctx->bucket[b] = run;
-        run += c;
-    }
-
-    // Pass 2: place items.  Into the first slot's staging directly when the
-    // batch fits one slot, else into the packing area.
     DeviceScope scope(ctx->device);
-    Slot *first = &ctx->slots[ctx->next_slot];
-    const bool one_slot = total <= o.slot_items;
-    WorkItem *items;
-    if (one_slot) {
-        int rc = wait_slot(ctx, *first);
-        if (rc != TB_OK)
-            return rc;
-        items = first->host;
-    } else {
-        ctx->pack.resize(total);
-        items = ctx->pack.data();
-    }
-    uint64_t ci = 0;
-    for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
-            continue;
-        if (d.len <= small) {
-            uint32_t &pos = ctx->bucket[nb - 1 - (size_t)(d.len >> shift)];
-            items[n_cta + pos++] = WorkItem{d.src, d.dst, d.len};
-        } else {
-            for (uint64_t off = 0; off < d.len; off += o.chunk_bytes)
-                items[ci++] = WorkItem{d.src + off, d.dst + off, std::min(o.chunk_bytes, d.len - off)};
-        }
-    }
-
-    // Launch: each slot takes up to slot_items items, CTA chunks first.
-    ctx->last_slots.clear();
+    ctx->bucket.resize(tb::bucket_count(small));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int full_grid = ctx->num_sms * tb::batch_ctas_per_sm();
-    const uint32_t warps_per_cta = tb::kBatchThreads / 32;
-    uint64_t cta_left = n_cta, warp_left = n_warp;
-    while (cta_left + warp_left > 0) {
+
+    // One launch per run of at most slot_items non-empty descriptors (one
+    // run for every batch that fits a slot).
+    size_t begin = 0;
+    while (begin < n) {
+        size_t end = begin;
+        uint64_t taken = 0;
+        while (end < n && (taken < o.slot_items || desc[end].len == 0)) {
+            taken += desc[end].len != 0;
+            ++end;
+        }
+        tb::BatchCounts c = all;
+        if (begin != 0 || end != n)
+            tb::count_batch(desc + begin, end - begin, small, &c, nullptr);
+        const int grid = tb::batch_grid(c, ctx->batch_grid);
+
         Slot &slot = ctx->slots[ctx->next_slot];
         ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
         int rc = wait_slot(ctx, slot);
         if (rc != TB_OK)
             return rc;
-        const uint64_t c = std::min<uint64_t>(cta_left, o.slot_items);
-        const uint64_t w = std::min<uint64_t>(warp_left, o.slot_items - c);
-        const uint64_t cnt = c + w;
-        if (!one_slot) {
-            // CTA items are a prefix of the packing area, warp items follow.
-            memcpy(slot.host, items + (n_cta - cta_left), c * sizeof(WorkItem));
-            memcpy(slot.host + c, items + n_cta + (n_warp - warp_left), w * sizeof(WorkItem));
-        }
-        TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, cnt * sizeof(WorkItem),
+        tb::BatchPlan plan;
+        tb::pack_batch(desc + begin, end - begin, small, c, grid, slot.host, ctx->bucket.data(),
+                       &plan);
+        TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
                                      cudaMemcpyHostToDevice, s));
-        const uint64_t want = std::max<uint64_t>(c, (w + warps_per_cta - 1) / warps_per_cta);
-        const int grid = (int)std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)full_grid, want));
         if (slot.t0)
             TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-        TB_CUDA(ctx, tb::launch_batch(slot.dev, (uint32_t)c, (uint32_t)w, grid, s));
+        TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s));
         if (slot.t1)
             TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
         TB_CUDA(ctx, cudaEventRecord(slot.done, s));
         ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
         slot.pending = true;
         st.launches += 1;
-        st.upload_bytes += cnt * sizeof(WorkItem);
-        cta_left -= c;
-        warp_left -= w;
+        st.warp_items += plan.n_short;
+        st.cta_items += plan.n_long_items;
+        st.upload_bytes += plan.upload_bytes;
+        begin = end;
     }
     ctx->last_batch = st;
     return TB_OK;

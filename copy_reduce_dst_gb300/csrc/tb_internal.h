@@ -65,9 +65,7 @@ cudaError_t launch_gate(const volatile uint32_t *flag, uint32_t *status, uint64_
 // Batched copy (K2)
 // ---------------------------------------------------------------------------
 
-// One packed work item: copy len bytes from src to dst.  A slot holds
-// n_cta items (chunks of long descriptors, one CTA each) followed by n_warp
-// items (short descriptors, one warp each, sorted longest first).
+// One packed work item: copy len bytes from src to dst.
 struct WorkItem {
     uint64_t src;
     uint64_t dst;
@@ -77,8 +75,41 @@ static_assert(sizeof(WorkItem) == 24, "WorkItem is packed as three 64-bit words"
 
 constexpr int kBatchThreads = 256;
 
-cudaError_t launch_batch(const WorkItem *items, uint32_t n_cta, uint32_t n_warp, int grid,
-                         cudaStream_t stream);
+// Descriptor counts of a batch (descriptors with len == 0 are skipped).
+struct BatchCounts {
+    uint64_t descs;       // len > 0
+    uint64_t n_short;     // len <= small_max: one warp each
+    uint64_t n_long;      // len > small_max: CTA phase
+    uint64_t long_bytes;  // sum of the long lengths
+    uint64_t bytes;       // sum of all lengths
+};
+
+// One packed launch (see tb_pack.cpp for the buffer layout).
+struct BatchPlan {
+    uint32_t n_long_items;  // pieces of long copies
+    uint32_t n_short;       // short copies
+    uint32_t grid;          // CTAs of the launch
+    size_t table_offset;    // byte offset of cta_first[] in the buffer
+    size_t upload_bytes;    // items + table
+};
+
+unsigned bucket_shift(uint64_t small_max);
+size_t bucket_count(uint64_t small_max);
+// Bytes a packed launch of at most `items` descriptors over `grid` CTAs needs.
+size_t batch_buffer_bytes(uint64_t items, int grid);
+// Checks and counts descriptors; TB_EINVAL (index in *bad) for a null or
+// wrapping range.
+int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCounts *c,
+                size_t *bad);
+// CTAs for a batch: one full wave at most, fewer for small batches.
+int batch_grid(const BatchCounts &c, int full_grid);
+// Packs the (checked, counted) descriptors into buf; bucket: scratch of
+// bucket_count(small_max) words.
+void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const BatchCounts &c,
+                int grid, void *buf, uint32_t *bucket, BatchPlan *out);
+
+// Launches k_batch over a packed buffer (device copy at `dev`).
+cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream);
 
 // CTAs resident per SM for the batch kernel.
 int batch_ctas_per_sm();

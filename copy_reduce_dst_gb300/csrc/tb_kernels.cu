@@ -532,14 +532,18 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem *p)
     return w;
 }
 
-// Persistent grid.  Phase 1: CTA items (chunks of long descriptors) round
-// robin over CTAs.  Phase 2: warp items, longest first, dealt to warps in
+// Persistent grid of one wave.  Phase 1: CTA b copies the long-copy pieces
+// [first[b], first[b+1]) - equal byte shares, so all CTAs finish it
+// together.  Phase 2: short copies, longest first, dealt to warps in
 // boustrophedon order (round r goes up the warp list when r is even and down
-// when it is odd) so each warp's byte total stays close to the mean.
+// when it is odd) so each warp's byte total stays close to the mean; each
+// warp fetches its next item before copying the current one.
 __global__ void __launch_bounds__(kBatchThreads) k_batch(const WorkItem *__restrict__ items,
-                                                         uint32_t n_cta, uint32_t n_warp)
+                                                         const uint32_t *__restrict__ first,
+                                                         uint32_t n_short)
 {
-    for (uint32_t i = blockIdx.x; i < n_cta; i += gridDim.x) {
+    const uint32_t i1 = __ldg(first + blockIdx.x + 1);
+    for (uint32_t i = __ldg(first + blockIdx.x); i < i1; ++i) {
         const WorkItem w = load_item(items + i);
         copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
                    w.len, threadIdx.x, blockDim.x);
@@ -549,14 +553,28 @@ __global__ void __launch_bounds__(kBatchThreads) k_batch(const WorkItem *__restr
     const uint32_t warps_per_cta = blockDim.x >> 5;
     const uint64_t W = (uint64_t)gridDim.x * warps_per_cta;
     const uint64_t wid = (uint64_t)blockIdx.x * warps_per_cta + (threadIdx.x >> 5);
-    const WorkItem *witems = items + n_cta;
-    for (uint64_t r = 0; r * W < n_warp; ++r) {
-        const uint64_t idx = r * W + ((r & 1) ? (W - 1 - wid) : wid);
-        if (idx >= n_warp)
-            continue;
-        const WorkItem w = load_item(witems + idx);
-        copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
-                   w.len, lane, 32u);
+    const WorkItem *shorts = items + __ldg(first + gridDim.x);
+    auto index = [&](uint64_t r) { return r * W + ((r & 1) ? (W - 1 - wid) : wid); };
+    uint64_t r = 0;
+    while (r * W < n_short && index(r) >= n_short)
+        ++r;
+    if (r * W >= n_short)
+        return;
+    WorkItem cur = load_item(shorts + index(r));
+    for (;;) {
+        uint64_t rn = r + 1;
+        while (rn * W < n_short && index(rn) >= n_short)
+            ++rn;
+        const bool more = rn * W < n_short;
+        WorkItem nxt = cur;
+        if (more)
+            nxt = load_item(shorts + index(rn));
+        copy_range(reinterpret_cast<uint8_t *>(cur.dst), reinterpret_cast<const uint8_t *>(cur.src),
+                   cur.len, lane, 32u);
+        if (!more)
+            break;
+        cur = nxt;
+        r = rn;
     }
 }
 
@@ -744,12 +762,14 @@ int batch_ctas_per_sm()
     return g_batch_ctas_per_sm;
 }
 
-cudaError_t launch_batch(const WorkItem *items, uint32_t n_cta, uint32_t n_warp, int grid,
-                         cudaStream_t stream)
+cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream)
 {
-    if (n_cta == 0 && n_warp == 0)
+    if (plan.n_long_items == 0 && plan.n_short == 0)
         return cudaSuccess;
-    k_batch<<<grid, kBatchThreads, 0, stream>>>(items, n_cta, n_warp);
+    const WorkItem *items = static_cast<const WorkItem *>(dev);
+    const uint32_t *first =
+        reinterpret_cast<const uint32_t *>(static_cast<const char *>(dev) + plan.table_offset);
+    k_batch<<<plan.grid, kBatchThreads, 0, stream>>>(items, first, plan.n_short);
     return cudaGetLastError();
 }
 

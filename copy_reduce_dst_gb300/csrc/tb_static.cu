@@ -28,18 +28,21 @@ namespace {
 
 using tb::WorkItem;
 
-constexpr uint64_t kSmallMax = 16384;   // one warp per copy up to this size
-constexpr uint64_t kChunk = 65536;      // longer copies: 64 KiB CTA chunks
-constexpr unsigned kShift = 6;          // length buckets of 64 bytes
-constexpr size_t kBuckets = (kSmallMax >> kShift) + 1;
+constexpr uint64_t kSmallMax = 16384;  // one warp per copy up to this size
 constexpr int kMaxDevices = 64;
+constexpr int kMaxGrid = 2048;         // CTAs of one launch at most
+// Packed launch: TB_NOALLOC_MAX_ITEMS descriptors, up to kMaxGrid extra
+// pieces where CTA shares cut a long copy, and the per-CTA table.
+constexpr size_t kScratchItems =
+    TB_NOALLOC_MAX_ITEMS + kMaxGrid + ((kMaxGrid + 1) * sizeof(uint32_t) + sizeof(WorkItem) - 1) /
+                                          sizeof(WorkItem);
 
-// The scratch: packed work items of the batch in flight.
-static __device__ __align__(256) WorkItem g_scratch_items[TB_NOALLOC_MAX_ITEMS];
+// The scratch: the packed launch of the batch in flight.
+static __device__ __align__(256) WorkItem g_scratch_items[kScratchItems];
 
 // Host-side packing area (static storage, no heap) and its lock.
-WorkItem g_host_items[TB_NOALLOC_MAX_ITEMS];
-uint32_t g_bucket[kBuckets];
+WorkItem g_host_items[kScratchItems];
+uint32_t g_bucket[(kSmallMax >> 6) + 1];
 std::mutex g_lock;
 
 // Per-device set-up: the scratch array's device address and the grid size.
@@ -58,7 +61,7 @@ int setup_current_device(int *device)
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
         return TB_ECUDA;
-    g_dev_grid[*device] = sms * tb::batch_ctas_per_sm();
+    g_dev_grid[*device] = std::min(kMaxGrid, sms * tb::batch_ctas_per_sm());
     g_dev_items[*device] = static_cast<WorkItem *>(ptr);
     return TB_OK;
 }
@@ -69,66 +72,31 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
 {
     if (n > 0 && !desc)
         return TB_EINVAL;
+    tb::BatchCounts c;
+    if (tb::count_batch(desc, n, kSmallMax, &c, nullptr) != TB_OK)
+        return TB_EINVAL;
+    if (c.descs > TB_NOALLOC_MAX_ITEMS)
+        return TB_ENOTSUP;
+    if (c.descs == 0)
+        return TB_OK;
     std::lock_guard<std::mutex> hold(g_lock);
     int device = -1;
     int rc = setup_current_device(&device);
     if (rc != TB_OK)
         return rc;
+    static_assert(sizeof(g_bucket) / sizeof(g_bucket[0]) >= (kSmallMax >> 6) + 1, "bucket area");
 
-    // Pass 1: check, count long-copy chunks and short copies per length bucket.
-    std::fill(g_bucket, g_bucket + kBuckets, 0u);
-    uint64_t n_cta = 0, n_warp = 0;
-    for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
-            continue;
-        if (d.src == 0 || d.dst == 0 || d.src + d.len < d.src || d.dst + d.len < d.dst)
-            return TB_EINVAL;
-        if (d.len <= kSmallMax) {
-            ++g_bucket[kBuckets - 1 - (size_t)(d.len >> kShift)];
-            ++n_warp;
-        } else {
-            n_cta += (d.len + kChunk - 1) / kChunk;
-        }
-    }
-    const uint64_t total = n_cta + n_warp;
-    if (total > TB_NOALLOC_MAX_ITEMS)
-        return TB_ENOTSUP;
-    if (total == 0)
-        return TB_OK;
-
-    // Pass 2: chunks first, then short copies longest first.
-    uint32_t run = 0;
-    for (size_t b = 0; b < kBuckets; ++b) {
-        const uint32_t c = g_bucket[b];
-        g_bucket[b] = run;
-        run += c;
-    }
-    uint64_t ci = 0;
-    for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
-            continue;
-        if (d.len <= kSmallMax) {
-            uint32_t &pos = g_bucket[kBuckets - 1 - (size_t)(d.len >> kShift)];
-            g_host_items[n_cta + pos++] = WorkItem{d.src, d.dst, d.len};
-        } else {
-            for (uint64_t off = 0; off < d.len; off += kChunk)
-                g_host_items[ci++] = WorkItem{d.src + off, d.dst + off, std::min(kChunk, d.len - off)};
-        }
-    }
-
+    tb::BatchPlan plan;
+    tb::pack_batch(desc, n, kSmallMax, c, tb::batch_grid(c, g_dev_grid[device]), g_host_items,
+                   g_bucket, &plan);
     // The copy from pageable host memory returns once the bytes are staged,
     // so the host area is free again when this call returns.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WorkItem *items = g_dev_items[device];
-    if (cudaMemcpyAsync(items, g_host_items, total * sizeof(WorkItem), cudaMemcpyHostToDevice, s) !=
+    if (cudaMemcpyAsync(items, g_host_items, plan.upload_bytes, cudaMemcpyHostToDevice, s) !=
         cudaSuccess)
         return TB_ECUDA;
-    const uint64_t warps_per_cta = tb::kBatchThreads / 32;
-    const uint64_t want = std::max<uint64_t>(n_cta, (n_warp + warps_per_cta - 1) / warps_per_cta);
-    const int grid = (int)std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)g_dev_grid[device], want));
-    if (tb::launch_batch(items, (uint32_t)n_cta, (uint32_t)n_warp, grid, s) != cudaSuccess)
+    if (tb::launch_batch(items, plan, s) != cudaSuccess)
         return TB_ECUDA;
     return TB_OK;
 }

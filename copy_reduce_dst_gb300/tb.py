@@ -52,7 +52,6 @@ class Options(ct.Structure):
         ("ctas_per_subexec", _i32),
         ("block_threads", _i32),
         ("small_max_bytes", _u64),
-        ("chunk_bytes", _u64),
         ("slot_items", _u32),
         ("num_slots", _u32),
         ("wait_timeout_ns", _u64),

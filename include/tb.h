@@ -92,16 +92,13 @@ typedef struct {
     int32_t ctas_per_subexec;
     /* Reduce-copy threads per CTA (multiple of 32, <= 512); 0 = 512. */
     int32_t block_threads;
-    /* Batched copy: descriptors up to this many bytes are copied by one warp;
-       longer ones are split into chunks copied by a whole CTA.
-       Default 16384. */
+    /* Batched copy: descriptors up to this many bytes are copied by one
+       warp; the bytes of all longer ones are shared equally among the CTAs.
+       Default 16384, at most 16 MiB. */
     uint64_t small_max_bytes;
-    /* Batched copy: bytes per CTA chunk of a long descriptor (multiple of
-       4096).  Default 65536. */
-    uint64_t chunk_bytes;
-    /* Batched copy: work items (warp items + CTA chunks) one descriptor slot
-       holds, and how many slots the ring has.  A batch larger than one slot
-       runs as several launches.  Defaults 65536 and 4. */
+    /* Batched copy: non-empty descriptors one descriptor slot holds, and how
+       many slots the ring has.  A batch with more runs as several launches.
+       Defaults 65536 and 4. */
     uint32_t slot_items;
     uint32_t num_slots;
     /* Limit of every bounded wait (descriptor slot reuse, gate kernel), in
@@ -132,7 +129,7 @@ void tb_options_default(tb_options *opt);
 /* Overrides fields of *opt from the environment:
      TB_SRC_ROTATE_BYTES (or SRC_ROTATE_BYTES), TB_BYTE_OFFSET, TB_WARMUP,
      TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
-     TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_CHUNK_BYTES, TB_SLOT_ITEMS,
+     TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
      TB_TIME_KERNELS.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
@@ -333,10 +330,11 @@ typedef struct {
    alignment, with one kernel launch per descriptor slot, asynchronously on
    `stream` (ordered after the caller's earlier work on it).  The descriptor
    array is read and packed before return, so the caller may reuse it at
-   once.  Descriptors of at most small_max_bytes go to one warp each
-   (largest first); longer ones are split into chunk_bytes pieces that
-   whole CTAs copy.  Destinations must not overlap one another or any source
-   of the batch (the order of copies is unspecified).  TB_EINVAL for a null
+   once.  The bytes of all descriptors longer than small_max_bytes form one
+   stream cut into equal shares, one per CTA; then descriptors of at most
+   small_max_bytes go to one warp each, longest first.  Destinations must not
+   overlap one another or any source of the batch (the order of copies is
+   unspecified).  TB_EINVAL for a null
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
    slot came free within wait_timeout_ns. */
 int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
@@ -344,7 +342,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
 typedef struct {
     uint64_t descs;        /* descriptors with len > 0 */
     uint64_t warp_items;   /* descriptors copied by one warp */
-    uint64_t cta_items;    /* chunks copied by a whole CTA */
+    uint64_t cta_items;    /* pieces of long descriptors copied by whole CTAs */
     uint64_t launches;     /* kernel launches (slots) used */
     uint64_t bytes;        /* sum of len */
     uint64_t upload_bytes; /* packed work-item bytes copied host-to-device */
@@ -364,8 +362,7 @@ int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms);
    checks as tb_batch_copy; provided so the two can be timed side by side. */
 int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
 
-/* Work items tb_batch_copy_noalloc can hold: 65,536 (1.5 MiB of device
-   memory per GPU, 24 bytes each). */
+/* Non-empty descriptors one tb_batch_copy_noalloc call can take. */
 #define TB_NOALLOC_MAX_ITEMS 65536
 
 /* The batched copy without any allocation.  The pages have no counterpart:
@@ -373,20 +370,19 @@ int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stre
    has handed all free HBM to its own allocator (a KV cache reserved up
    front) has nothing left for one, and a latency-sensitive loop cannot
    afford cudaMalloc / cudaFree, which may synchronize the whole device.
-   Same copy semantics as tb_batch_copy with default options (copies up to
-   16 KiB go to one warp, longer ones to 64 KiB CTA chunks), on the current
-   CUDA device, asynchronously on `stream`; no context is needed.
-   The packed work items live in a fixed __device__ array that every GPU
-   loading this library holds until the process exits.  The first call on a
+   Same copy semantics and scheduling as tb_batch_copy with default options
+   (copies up to 16 KiB go to one warp each), on the current CUDA device,
+   asynchronously on `stream`; no context is needed.
+   The packed work items live in a fixed __device__ array of about 1.6 MiB
+   that every GPU loading this library holds until the process exits.  The first call on a
    device looks up that array's device address (with that device current);
    make that first call before any stream capture.  Every call on a device
    shares the one array and leaves the last batch's items in it: calls whose
    work overlaps on the GPU (different streams, no ordering between them)
    race; calls on one stream run in order.  Host-side packing is serialized
    by a lock.  Returns TB_EINVAL for a null or wrapping range, TB_ENOTSUP
-   when the batch needs more than TB_NOALLOC_MAX_ITEMS work items (each copy
-   up to 16 KiB is one item, a longer one ceil(len / 64 KiB) items; nothing
-   is copied then), TB_ECUDA when a CUDA call fails.  It calls no cudaMalloc,
+   when the batch has more than TB_NOALLOC_MAX_ITEMS descriptors with
+   len > 0 (nothing is copied then), TB_ECUDA when a CUDA call fails.  It calls no cudaMalloc,
    cudaFree or other allocating routine. */
 int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stream stream);
 

@@ -84,7 +84,7 @@ def test_lengths_one_byte_to_three_mib(tb, ctx):
 def test_more_launches_than_slots(tb):
     # 1024 items per slot and 2 slots: the batch needs many launches and every
     # slot is reused while earlier launches may still be running.
-    with tb.Context(0, tb.options(slot_items=1024, num_slots=2, chunk_bytes=4096)) as c:
+    with tb.Context(0, tb.options(slot_items=1024, num_slots=2)) as c:
         layout = workloads.random_batch(21, 9000, 20000, 512 * MiB, align=1)
         st = run_layout(tb, c, layout, 22)
         assert st["launches"] > 2 * 2
@@ -92,10 +92,9 @@ def test_more_launches_than_slots(tb):
             run_layout(tb, c, workloads.random_batch(30 + i, 3000, 4000, 64 * MiB), 40 + i)
 
 
-@pytest.mark.parametrize("small,chunk", [(1, 4096), (64, 8192), (16384, 65536), (1 << 20, 1 << 20),
-                                         (16 << 20, 4096)])
-def test_size_bins(tb, small, chunk):
-    with tb.Context(0, tb.options(small_max_bytes=small, chunk_bytes=chunk)) as c:
+@pytest.mark.parametrize("small", [1, 64, 1000, 16384, 1 << 20, 16 << 20])
+def test_size_bins(tb, small):
+    with tb.Context(0, tb.options(small_max_bytes=small)) as c:
         layout = workloads.random_batch(5, 1500, 100000, 512 * MiB, align=4)
         run_layout(tb, c, layout, 6, src_shift=1)
 
@@ -170,5 +169,5 @@ def test_head_sliced_full(tb, ctx):
     layout = workloads.batch_head_sliced()
     st = run_layout(tb, ctx, layout, 103)
     assert st["descs"] == 47540 and st["warp_items"] == 47520
-    assert st["cta_items"] == (16 * 16 * MiB + 4 * 8 * MiB) // (64 * 1024)
+    assert 20 <= st["cta_items"] <= 20 + 2048      # 20 long copies, cut at CTA shares
     assert st["launches"] == 1
