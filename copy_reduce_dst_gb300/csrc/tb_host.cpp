@@ -36,6 +36,8 @@ struct Slot {
     bool pending = false;      // `done` recorded and maybe not reached yet
     cudaEvent_t t0 = nullptr;  // kernel timing (time_kernels only)
     cudaEvent_t t1 = nullptr;
+    volatile uint32_t *status = nullptr;  // host-mapped: 1 if a kernel wait expired
+    uint32_t *status_dev = nullptr;
 };
 
 }  // namespace
@@ -56,6 +58,7 @@ struct tb_ctx {
     std::vector<float> iter_ms;
 
     std::vector<Slot> slots;
+    void *slot_status = nullptr;      // host-mapped status words, one per slot
     uint32_t next_slot = 0;
     int batch_grid = 0;               // one wave of batch-kernel CTAs
     std::vector<uint32_t> bucket;     // counting-sort buckets
@@ -213,6 +216,12 @@ int wait_slot(tb_ctx *ctx, Slot &s)
         std::this_thread::yield();
     }
     s.pending = false;
+    if (s.status && *s.status != 0u) {
+        *s.status = 0u;
+        return fail(ctx, TB_ETIMEOUT,
+                    "an earlier batch on this descriptor slot stopped early: a bounded wait "
+                    "inside the kernel expired");
+    }
     return TB_OK;
 }
 
@@ -477,7 +486,17 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
 
     ctx->batch_grid = ctx->num_sms * tb::batch_ctas_per_sm();
     ctx->slots.resize(o.num_slots);
-    const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items, ctx->batch_grid);
+    const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items);
+    void *status_dev = nullptr;
+    if (cudaHostAlloc(&ctx->slot_status, o.num_slots * sizeof(uint32_t), cudaHostAllocMapped) !=
+            cudaSuccess ||
+        cudaHostGetDevicePointer(&status_dev, ctx->slot_status, 0) != cudaSuccess)
+        return bail(TB_ENOMEM);
+    for (uint32_t i = 0; i < o.num_slots; ++i) {
+        ctx->slots[i].status = static_cast<volatile uint32_t *>(ctx->slot_status) + i;
+        ctx->slots[i].status_dev = static_cast<uint32_t *>(status_dev) + i;
+        *ctx->slots[i].status = 0u;
+    }
     for (Slot &s : ctx->slots) {
         if (cudaMalloc(&s.dev, slot_bytes) != cudaSuccess)
             return bail(TB_ENOMEM);
@@ -521,6 +540,8 @@ void tb_destroy(tb_ctx *ctx)
         cudaEventDestroy(e);
     if (ctx->gate_flag)
         cudaFreeHost((void *)ctx->gate_flag);
+    if (ctx->slot_status)
+        cudaFreeHost(ctx->slot_status);
     if (ctx->val_stage)
         cudaFreeHost(ctx->val_stage);
     delete ctx;
@@ -816,7 +837,8 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     const uint64_t small = o.small_max_bytes;
     tb::BatchCounts all;
     size_t bad = 0;
-    if (tb::count_batch(desc, n, small, &all, &bad) != TB_OK)
+    ctx->bucket.resize(tb::bucket_count(small));
+    if (tb::count_batch(desc, n, small, &all, &bad, ctx->bucket.data()) != TB_OK)
         return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range", bad);
     tb_batch_stats st{};
     st.descs = all.descs;
@@ -827,7 +849,6 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         return TB_OK;
     }
     DeviceScope scope(ctx->device);
-    ctx->bucket.resize(tb::bucket_count(small));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     // One launch per run of at most slot_items non-empty descriptors (one
@@ -842,7 +863,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         }
         tb::BatchCounts c = all;
         if (begin != 0 || end != n)
-            tb::count_batch(desc + begin, end - begin, small, &c, nullptr);
+            tb::count_batch(desc + begin, end - begin, small, &c, nullptr, ctx->bucket.data());
         const int grid = tb::batch_grid(c, ctx->batch_grid);
 
         Slot &slot = ctx->slots[ctx->next_slot];
@@ -857,7 +878,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
                                      cudaMemcpyHostToDevice, s));
         if (slot.t0)
             TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-        TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s));
+        TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev));
         if (slot.t1)
             TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
         TB_CUDA(ctx, cudaEventRecord(slot.done, s));
@@ -865,7 +886,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         slot.pending = true;
         st.launches += 1;
         st.warp_items += plan.n_short;
-        st.cta_items += plan.n_long_items;
+        st.cta_items += plan.chunks;
         st.upload_bytes += plan.upload_bytes;
         begin = end;
     }
@@ -884,6 +905,9 @@ int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms)
     for (uint32_t i : ctx->last_slots) {
         Slot &s = ctx->slots[i];
         TB_CUDA(ctx, cudaEventSynchronize(s.t1));
+        if (*s.status != 0u)
+            return fail(ctx, TB_ETIMEOUT, "the last batch stopped early: a bounded wait inside "
+                                          "the kernel expired");
         float t = 0.0f;
         TB_CUDA(ctx, cudaEventElapsedTime(&t, s.t0, s.t1));
         total += t;

@@ -74,6 +74,8 @@ struct WorkItem {
 static_assert(sizeof(WorkItem) == 24, "WorkItem is packed as three 64-bit words");
 
 constexpr int kBatchThreads = 256;
+constexpr uint64_t kChunkBytes = 65536;  // target size of a long-copy chunk
+constexpr uint32_t kMaxChunks = 16384;   // chunks of one launch at most
 
 // Descriptor counts of a batch (descriptors with len == 0 are skipped).
 struct BatchCounts {
@@ -86,30 +88,47 @@ struct BatchCounts {
 
 // One packed launch (see tb_pack.cpp for the buffer layout).
 struct BatchPlan {
-    uint32_t n_long_items;  // pieces of long copies
     uint32_t n_short;       // short copies
+    uint32_t n_long;        // long copies
     uint32_t grid;          // CTAs of the launch
-    size_t table_offset;    // byte offset of cta_first[] in the buffer
-    size_t upload_bytes;    // items + table
+    uint32_t chunks;        // long-stream chunks (a multiple of grid)
+    uint64_t long_bytes;    // bytes of the long-copy stream
+    size_t prefix_offset;   // byte offsets of prefix[] and chunk_desc[]
+    size_t chunk_offset;
+    size_t upload_bytes;    // bytes of the packed buffer
 };
+
+// Start of chunk c of `chunks` equal chunks of a `total`-byte stream, on a
+// 64-byte offset; chunk `chunks` starts at total.
+__host__ __device__ inline uint64_t chunk_start(uint64_t total, uint64_t chunks, uint64_t c)
+{
+    if (c >= chunks)
+        return total;
+    const uint64_t raw = (total / chunks) * c + ((total % chunks) * c) / chunks;
+    return raw & ~(uint64_t)63;
+}
 
 unsigned bucket_shift(uint64_t small_max);
 size_t bucket_count(uint64_t small_max);
-// Bytes a packed launch of at most `items` descriptors over `grid` CTAs needs.
-size_t batch_buffer_bytes(uint64_t items, int grid);
+// Bytes a packed launch of at most `descs` non-empty descriptors needs.
+size_t batch_buffer_bytes(uint64_t descs);
 // Checks and counts descriptors; TB_EINVAL (index in *bad) for a null or
-// wrapping range.
+// wrapping range.  With `bucket` (bucket_count(small_max) words) it also
+// counts the short copies per length bucket, which pack_batch needs.
 int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCounts *c,
-                size_t *bad);
+                size_t *bad, uint32_t *bucket);
 // CTAs for a batch: one full wave at most, fewer for small batches.
 int batch_grid(const BatchCounts &c, int full_grid);
-// Packs the (checked, counted) descriptors into buf; bucket: scratch of
-// bucket_count(small_max) words.
+// Packs the descriptors into buf; c and bucket come from count_batch over
+// exactly these descriptors.
 void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const BatchCounts &c,
                 int grid, void *buf, uint32_t *bucket, BatchPlan *out);
 
-// Launches k_batch over a packed buffer (device copy at `dev`).
-cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream);
+// Launches k_batch over a packed buffer (device copy at `dev`).  status
+// (nullable, device-visible) is set to 1 if a bounded wait inside the kernel
+// expired.
+cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
+                         uint32_t *status = nullptr);
 
 // CTAs resident per SM for the batch kernel.
 int batch_ctas_per_sm();

@@ -2,14 +2,15 @@
 // array into the work list one k_batch launch reads.
 //
 // Layout of a packed launch (one device buffer):
-//   WorkItem items[n_long_items + n_short]   pieces of long copies, then
-//                                            short copies longest first
-//   uint32_t cta_first[grid + 1]             CTA b copies long pieces
-//                                            [cta_first[b], cta_first[b+1])
-// The bytes of all long copies (len > small_max) form one stream, cut into
-// grid shares of equal size (cuts on 64-byte stream offsets), so every CTA
-// leaves the long-copy phase at the same time; a cut inside a copy splits it
-// into two pieces.  Short copies are then dealt to warps by the kernel.
+//   WorkItem shorts[n_short]     copies of at most small_max bytes, longest
+//                                first (one warp each)
+//   WorkItem longs[n_long]       the longer copies, in descriptor order
+//   uint64_t prefix[n_long + 1]  offset of each long copy in the stream of
+//                                all long-copy bytes; prefix[n_long] = total
+//   uint32_t chunk_desc[C + 1]   the long copy holding chunk c's first byte
+// The long-copy stream is cut into C = grid * m chunks of equal size (cuts
+// on 64-byte stream offsets); CTA b copies chunks b, b + grid, ... so every
+// CTA gets exactly m chunks and the grid sweeps the stream front to back.
 
 #include <algorithm>
 #include <cstring>
@@ -17,11 +18,6 @@
 #include "tb_internal.h"
 
 namespace tb {
-
-size_t bucket_count(uint64_t small_max)
-{
-    return (size_t)(small_max >> bucket_shift(small_max)) + 1;
-}
 
 unsigned bucket_shift(uint64_t small_max)
 {
@@ -31,15 +27,25 @@ unsigned bucket_shift(uint64_t small_max)
     return shift;
 }
 
-size_t batch_buffer_bytes(uint64_t items, int grid)
+size_t bucket_count(uint64_t small_max)
 {
-    return (size_t)(items + (uint64_t)grid) * sizeof(WorkItem) + ((size_t)grid + 1) * sizeof(uint32_t);
+    return (size_t)(small_max >> bucket_shift(small_max)) + 1;
+}
+
+size_t batch_buffer_bytes(uint64_t descs)
+{
+    return (size_t)descs * (sizeof(WorkItem) + sizeof(uint64_t)) + sizeof(uint64_t) +
+           ((size_t)kMaxChunks + 1) * sizeof(uint32_t);
 }
 
 int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCounts *c,
-                size_t *bad)
+                size_t *bad, uint32_t *bucket)
 {
     *c = BatchCounts{};
+    const unsigned shift = bucket_shift(small_max);
+    const size_t nb = bucket_count(small_max);
+    if (bucket)
+        std::fill(bucket, bucket + nb, 0u);
     for (size_t i = 0; i < n; ++i) {
         const tb_copy_desc &d = desc[i];
         if (d.len == 0)
@@ -53,6 +59,8 @@ int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCou
         c->bytes += d.len;
         if (d.len <= small_max) {
             ++c->n_short;
+            if (bucket)
+                ++bucket[nb - 1 - (size_t)(d.len >> shift)];
         } else {
             ++c->n_long;
             c->long_bytes += d.len;
@@ -65,18 +73,9 @@ int batch_grid(const BatchCounts &c, int full_grid)
 {
     const uint64_t warps = kBatchThreads / 32;
     const uint64_t for_short = (c.n_short + warps - 1) / warps;
-    const uint64_t for_long = (c.long_bytes + 65535) / 65536;  // at least 64 KiB per CTA
+    const uint64_t for_long = (c.long_bytes + kChunkBytes - 1) / kChunkBytes;
     const uint64_t want = std::max<uint64_t>(1, std::max(for_short, for_long));
-    return (int)std::min<uint64_t>((uint64_t)full_grid, want);
-}
-
-// Start of CTA b's share of a T-byte stream over G CTAs, on a 64-byte offset.
-static uint64_t share_start(uint64_t T, uint32_t G, uint32_t b)
-{
-    if (b >= G)
-        return T;
-    const uint64_t raw = (T / G) * b + ((T % G) * b) / G;
-    return raw & ~(uint64_t)63;
+    return (int)std::min<uint64_t>(std::min<uint64_t>((uint64_t)full_grid, kMaxChunks), want);
 }
 
 void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const BatchCounts &c,
@@ -84,79 +83,59 @@ void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const Ba
 {
     const unsigned shift = bucket_shift(small_max);
     const size_t nb = bucket_count(small_max);
-    const uint32_t G = (uint32_t)grid;
 
-    // Long copies: walk the stream, cutting at every CTA share boundary.
-    WorkItem *items = static_cast<WorkItem *>(buf);
-    uint32_t n_long_items = 0;
-    {
-        // The table goes after the items; its position needs the item count,
-        // which is at most n_long + G - 1, so fill it in a local pass first.
-        uint64_t pos = 0;
-        uint32_t b = 0;
-        uint64_t next = share_start(c.long_bytes, G, 1);
-        std::fill(bucket, bucket + nb, 0u);
-        for (size_t i = 0; i < n; ++i) {
-            const tb_copy_desc &d = desc[i];
-            if (d.len == 0)
-                continue;
-            if (d.len <= small_max) {
-                ++bucket[nb - 1 - (size_t)(d.len >> shift)];
-                continue;
-            }
-            uint64_t off = 0;
-            while (off < d.len) {
-                while (next <= pos) {  // CTA b's share is complete
-                    ++b;
-                    next = share_start(c.long_bytes, G, b + 1);
-                }
-                const uint64_t take = std::min(d.len - off, next - pos);
-                items[n_long_items++] = WorkItem{d.src + off, d.dst + off, take};
-                off += take;
-                pos += take;
-            }
-        }
-    }
-    // Per-CTA table: second walk over the pieces (cheap: at most n_long + G).
-    uint32_t *first = reinterpret_cast<uint32_t *>(items + n_long_items + c.n_short);
-    {
-        uint64_t pos = 0;
-        uint32_t b = 0;
-        first[0] = 0;
-        uint64_t next = share_start(c.long_bytes, G, 1);
-        for (uint32_t k = 0; k < n_long_items; ++k) {
-            while (next <= pos && b < G) {
-                ++b;
-                first[b] = k;
-                next = share_start(c.long_bytes, G, b + 1);
-            }
-            pos += items[k].len;
-        }
-        while (b < G)
-            first[++b] = n_long_items;
-    }
+    // Chunks: about kChunkBytes each, a whole number per CTA.
+    uint64_t m = (c.long_bytes + (uint64_t)grid * kChunkBytes / 2) / ((uint64_t)grid * kChunkBytes);
+    m = std::max<uint64_t>(1, std::min<uint64_t>(m, kMaxChunks / (uint64_t)grid));
+    const uint64_t chunks = c.n_long ? (uint64_t)grid * m : 0;
 
-    // Short copies, longest first (counting sort on 2^shift-byte buckets).
+    WorkItem *shorts = static_cast<WorkItem *>(buf);
+    WorkItem *longs = shorts + c.n_short;
+    uint64_t *prefix = reinterpret_cast<uint64_t *>(longs + c.n_long);
+    uint32_t *chunk_desc = reinterpret_cast<uint32_t *>(prefix + c.n_long + 1);
+
+    // Bucket counts (from count_batch) -> starts; short copies longest first.
     uint32_t run = 0;
     for (size_t k = 0; k < nb; ++k) {
         const uint32_t cnt = bucket[k];
         bucket[k] = run;
         run += cnt;
     }
-    WorkItem *shorts = items + n_long_items;
+    // Place every copy.
+    uint32_t nl = 0;
+    uint64_t pos = 0;
     for (size_t i = 0; i < n; ++i) {
         const tb_copy_desc &d = desc[i];
-        if (d.len == 0 || d.len > small_max)
+        if (d.len == 0)
             continue;
-        uint32_t &p = bucket[nb - 1 - (size_t)(d.len >> shift)];
-        shorts[p++] = WorkItem{d.src, d.dst, d.len};
+        if (d.len <= small_max) {
+            uint32_t &p = bucket[nb - 1 - (size_t)(d.len >> shift)];
+            shorts[p++] = WorkItem{d.src, d.dst, d.len};
+        } else {
+            prefix[nl] = pos;
+            longs[nl++] = WorkItem{d.src, d.dst, d.len};
+            pos += d.len;
+        }
     }
+    prefix[nl] = pos;
+    // Chunk -> first long copy it touches.
+    uint32_t dcur = 0;
+    for (uint64_t k = 0; k < chunks; ++k) {
+        const uint64_t s0 = chunk_start(pos, chunks, k);
+        while (dcur + 1 < nl && prefix[dcur + 1] <= s0)
+            ++dcur;
+        chunk_desc[k] = dcur;
+    }
+    chunk_desc[chunks] = nl;
 
-    out->n_long_items = n_long_items;
     out->n_short = (uint32_t)c.n_short;
-    out->grid = G;
-    out->table_offset = (size_t)(n_long_items + c.n_short) * sizeof(WorkItem);
-    out->upload_bytes = out->table_offset + ((size_t)G + 1) * sizeof(uint32_t);
+    out->n_long = nl;
+    out->grid = (uint32_t)grid;
+    out->chunks = (uint32_t)chunks;
+    out->long_bytes = pos;
+    out->prefix_offset = (size_t)((const char *)prefix - (const char *)buf);
+    out->chunk_offset = (size_t)((const char *)chunk_desc - (const char *)buf);
+    out->upload_bytes = out->chunk_offset + ((size_t)chunks + 1) * sizeof(uint32_t);
 }
 
 }  // namespace tb

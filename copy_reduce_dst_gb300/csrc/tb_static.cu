@@ -31,11 +31,11 @@ using tb::WorkItem;
 constexpr uint64_t kSmallMax = 16384;  // one warp per copy up to this size
 constexpr int kMaxDevices = 64;
 constexpr int kMaxGrid = 2048;         // CTAs of one launch at most
-// Packed launch: TB_NOALLOC_MAX_ITEMS descriptors, up to kMaxGrid extra
-// pieces where CTA shares cut a long copy, and the per-CTA table.
-constexpr size_t kScratchItems =
-    TB_NOALLOC_MAX_ITEMS + kMaxGrid + ((kMaxGrid + 1) * sizeof(uint32_t) + sizeof(WorkItem) - 1) /
-                                          sizeof(WorkItem);
+// Bytes of one packed launch of TB_NOALLOC_MAX_ITEMS descriptors.
+constexpr size_t kScratchBytes =
+    TB_NOALLOC_MAX_ITEMS * (sizeof(WorkItem) + sizeof(uint64_t)) + sizeof(uint64_t) +
+    ((size_t)tb::kMaxChunks + 1) * sizeof(uint32_t);
+constexpr size_t kScratchItems = (kScratchBytes + sizeof(WorkItem) - 1) / sizeof(WorkItem);
 
 // The scratch: the packed launch of the batch in flight.
 static __device__ __align__(256) WorkItem g_scratch_items[kScratchItems];
@@ -72,14 +72,14 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
 {
     if (n > 0 && !desc)
         return TB_EINVAL;
+    std::lock_guard<std::mutex> hold(g_lock);
     tb::BatchCounts c;
-    if (tb::count_batch(desc, n, kSmallMax, &c, nullptr) != TB_OK)
+    if (tb::count_batch(desc, n, kSmallMax, &c, nullptr, g_bucket) != TB_OK)
         return TB_EINVAL;
     if (c.descs > TB_NOALLOC_MAX_ITEMS)
         return TB_ENOTSUP;
     if (c.descs == 0)
         return TB_OK;
-    std::lock_guard<std::mutex> hold(g_lock);
     int device = -1;
     int rc = setup_current_device(&device);
     if (rc != TB_OK)

@@ -336,7 +336,9 @@ typedef struct {
    overlap one another or any source of the batch (the order of copies is
    unspecified).  TB_EINVAL for a null
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
-   slot came free within wait_timeout_ns. */
+   slot came free within wait_timeout_ns, or when the previous batch that
+   used the chosen slot stopped early because a bounded wait inside the
+   kernel (2 s per wait) expired. */
 int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
 
 typedef struct {

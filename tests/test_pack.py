@@ -31,18 +31,27 @@ def harness(tmp_path_factory):
 def pack(lib, desc, small_max=16384, full_grid=608):
     desc = np.ascontiguousarray(desc, dtype=np.uint64).reshape(-1, 3)
     n = desc.shape[0]
-    cap = (n + full_grid) * 24 + (full_grid + 1) * 4
+    cap = n * 32 + 8 + (16384 + 1) * 4
     buf = np.zeros(cap, dtype=np.uint8)
     bucket = np.zeros(8192, dtype=np.uint32)
-    out = np.zeros(8, dtype=np.uint64)
+    out = np.zeros(9, dtype=np.uint64)
     rc = lib.harness_pack(desc.ctypes.data if n else None, n, small_max, full_grid,
                           buf.ctypes.data, bucket.ctypes.data, out.ctypes.data)
     assert rc == 0
-    n_long, n_short, grid, toff, upload, bound = (int(x) for x in out[:6])
+    n_short, n_long, grid, chunks, total, poff, coff, upload, bound = (int(x) for x in out)
     assert upload <= bound <= cap
-    items = buf[: (n_long + n_short) * 24].view(np.uint64).reshape(-1, 3)
-    first = buf[toff: toff + (grid + 1) * 4].view(np.uint32)
-    return items[:n_long], items[n_long:], first, grid
+    items = buf[: (n_short + n_long) * 24].view(np.uint64).reshape(-1, 3)
+    prefix = buf[poff: poff + (n_long + 1) * 8].view(np.uint64)
+    cdesc = buf[coff: coff + (chunks + 1) * 4].view(np.uint32)
+    return dict(shorts=items[:n_short], longs=items[n_short:], prefix=prefix, chunk_desc=cdesc,
+                grid=grid, chunks=chunks, total=total)
+
+
+def chunk_bytes(lib, p, c):
+    lib.harness_chunk_start.restype = ct.c_uint64
+    lib.harness_chunk_start.argtypes = [ct.c_uint64, ct.c_uint64, ct.c_uint64]
+    return (lib.harness_chunk_start(p["total"], p["chunks"], c + 1) -
+            lib.harness_chunk_start(p["total"], p["chunks"], c))
 
 
 def random_desc(g, n, long_frac, small_max):
@@ -55,38 +64,43 @@ def random_desc(g, n, long_frac, small_max):
 
 @pytest.mark.parametrize("seed,n,long_frac,small,grid", [
     (0, 1000, 0.05, 16384, 608), (1, 47540, 0.0005, 16384, 608), (2, 50, 0.5, 1000, 608),
-    (3, 3000, 0.0, 16384, 608), (4, 200, 1.0, 64, 16), (5, 7, 0.3, 16384, 1), (6, 0, 0.0, 16384, 608)])
+    (3, 3000, 0.0, 16384, 608), (4, 200, 1.0, 64, 16), (5, 7, 0.3, 16384, 1), (6, 0, 0.0, 16384, 608),
+    (7, 300, 1.0, 16384, 608)])
 def test_packer_invariants(harness, seed, n, long_frac, small, grid):
     g = np.random.default_rng(seed)
     desc = random_desc(g, n, long_frac, small)
-    longs, shorts, first, G = pack(harness, desc, small, grid)
+    p = pack(harness, desc, small, grid)
     lens = desc[:, 2] if n else np.zeros(0, np.uint64)
     is_long = lens > small
-    assert G >= 1 and G <= grid
+    G = p["grid"]
+    assert 1 <= G <= grid
 
-    # long copies: pieces in stream order, each descriptor covered exactly once
-    k = 0
-    for s, d, ln in desc[is_long]:
-        off = 0
-        while off < ln:
-            ps, pd, pl = (int(x) for x in longs[k])
-            assert ps == int(s) + off and pd == int(d) + off and pl > 0
-            off += pl
-            k += 1
-        assert off == ln
-    assert k == longs.shape[0]
+    # long copies in descriptor order, prefix = running stream offset
+    assert np.array_equal(p["longs"], desc[is_long])
+    want_prefix = np.concatenate([[0], np.cumsum(lens[is_long])]).astype(np.uint64)
+    assert np.array_equal(p["prefix"], want_prefix)
+    total = int(want_prefix[-1])
+    assert p["total"] == total
 
-    # per-CTA table and equal shares (cuts on 64-byte stream offsets)
-    assert first[0] == 0 and first[G] == longs.shape[0]
-    assert np.all(np.diff(first.astype(np.int64)) >= 0)
-    total = int(lens[is_long].sum())
-    share = np.array([int(longs[first[b]:first[b + 1], 2].sum()) for b in range(G)])
-    assert share.sum() == total
-    if total:
-        assert share.max() - share.min() <= 64 + 64
-        assert share.max() <= total // G + 128
+    # chunks: a whole number per CTA, equal sizes within 64 bytes, each chunk's
+    # first byte inside the long copy the table names
+    if is_long.any():
+        assert p["chunks"] % G == 0 and p["chunks"] >= G
+        sizes = np.array([chunk_bytes(harness, p, c) for c in range(p["chunks"])])
+        # both cut points floor to 64 bytes, so every chunk is within 64 of T/C
+        assert sizes.sum() == total and np.all(np.abs(sizes - total / p["chunks"]) < 64)
+        per_cta = sizes.reshape(-1, G).sum(axis=0)
+        assert np.all(np.abs(per_cta - total / G) < 64 * (p["chunks"] // G))
+        for c in range(p["chunks"]):
+            s0 = total - sizes[c:].sum()
+            d = p["chunk_desc"][c]
+            assert p["prefix"][d] <= s0 and (s0 < p["prefix"][d + 1] or sizes[c] == 0)
+        assert p["chunk_desc"][p["chunks"]] == is_long.sum()
+    else:
+        assert p["chunks"] == 0
 
-    # short copies: the same multiset, longest first by 64-byte bucket
+    # short copies: the same multiset, longest first by bucket
+    shorts = p["shorts"]
     want = sorted(map(tuple, desc[(lens > 0) & ~is_long].tolist()))
     assert sorted(map(tuple, shorts.tolist())) == want
     shift = 6
@@ -100,8 +114,6 @@ def test_packer_batch_47540(harness):
     from copy_reduce_dst_gb300 import workloads
     lay = workloads.batch_head_sliced()
     desc = lay.descriptors(1 << 32, 1 << 36)
-    longs, shorts, first, G = pack(harness, desc)
-    assert G == 608 and shorts.shape[0] == 47520
-    share = np.array([int(longs[first[b]:first[b + 1], 2].sum()) for b in range(G)])
-    assert share.sum() == 288 << 20
-    assert share.max() - share.min() <= 128
+    p = pack(harness, desc)
+    assert p["grid"] == 608 and p["shorts"].shape[0] == 47520 and p["longs"].shape[0] == 20
+    assert p["total"] == 288 << 20 and p["chunks"] == 608 * 8
