@@ -111,20 +111,28 @@ def ctx_options(tb, **fields):
     return tb.options_from_env(tb.options(**fields))
 
 
-def kernel_source_sha() -> str:
-    with open(os.path.join(ROOT, "copy_reduce_dst_gb300", "csrc", "tb_kernels.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def kernel_source_sha(source: str) -> str:
+    """SHA-256 of a kernel's source file together with the shared device
+    header, so a recorded ncu figure goes stale when either changes."""
+    h = hashlib.sha256()
+    for name in (source, "tb_device.cuh"):
+        with open(os.path.join(ROOT, "copy_reduce_dst_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def profiled_traffic(key: str):
-    """Per-launch DRAM bytes from the committed ncu summary, or None when the
-    kernel source changed after the capture."""
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary,
+    or None when the kernel's source changed after the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             entry = json.load(f)[key]
     except (OSError, KeyError, ValueError):
         return None
-    if entry.get("kernel_source_sha256") != kernel_source_sha():
+    try:
+        if entry.get("kernel_source_sha256") != kernel_source_sha(entry["source"]):
+            return None
+    except (OSError, KeyError):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -433,10 +441,15 @@ def reference_arm(args):
 # Study lines (not the default): single transfer and the fillCompress sweep
 # ---------------------------------------------------------------------------
 def study(args, tb, torch, local):
+    """Single 4 MiB transfer (K = 64) and the fillCompress sweep with rotation
+    on and off.  Warm = total device time of 20 back-to-back iterations after
+    3 warm-ups (per-iteration events telescope, so their ~1 us resolution
+    does not bias the sum); cold = mean of 10 single iterations, each after
+    writing a 512 MiB buffer (> L2).  Each figure is the median of 3 reps."""
     import statistics as st
-    peak, _ = read_peaks()
     flush = torch.empty(512 * MiB, dtype=torch.uint8, device="cuda")
-    with tb.Context(local, ctx_options(tb)) as ctx:
+    with tb.Context(local, ctx_options(tb)) as ctx, \
+            tb.Context(local, ctx_options(tb, warmup=0)) as cold_ctx:
         nb = 4 * MiB
         plan = tb.rotation_plan(nb, 256 * MiB)
         src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
@@ -445,7 +458,7 @@ def study(args, tb, torch, local):
         dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
         r = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
         print(json.dumps({"study": "single transfer 4 MiB, K=64", "gbps": r["gbps"],
-                          "median_ms": r["median_ms"], "K": r["K"],
+                          "mean_ms": r["mean_ms"], "K": r["K"],
                           "alloc_bytes": r["alloc_bytes"], "gated": r["gated"]}), flush=True)
         del src
         pct = (40, 20, 0, 20, 20)
@@ -460,16 +473,17 @@ def study(args, tb, torch, local):
                 dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
                 cold, warm = [], []
                 for rep in range(3):
-                    flush.fill_(rep)
-                    rc = ctx.run_transfer([src], dst, nb, iters=1, rotate_bytes=rot)
-                    cold.append(rc["gbps"])
-                    rw = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=rot)
-                    warm.append(rw["median_ms"])
+                    c = []
+                    for _ in range(10):
+                        flush.fill_(rep)
+                        c.append(cold_ctx.run_transfer([src], dst, nb, iters=1,
+                                                       rotate_bytes=rot)["total_ms"])
+                    cold.append(2 * nb / (st.mean(c) / 1e3) / 1e9)
+                    warm.append(ctx.run_transfer([src], dst, nb, iters=20, rotate_bytes=rot)["gbps"])
                 tag = "on" if rot else "off"
-                warm_gbps = 2 * nb / (st.median(warm) / 1e3) / 1e9
                 row[f"{tag}_cold_gbps"] = round(st.median(cold), 1)
-                row[f"{tag}_warm_gbps"] = round(warm_gbps, 1)
-                row[f"{tag}_w_over_c"] = round(warm_gbps / st.median(cold), 3)
+                row[f"{tag}_warm_gbps"] = round(st.median(warm), 1)
+                row[f"{tag}_w_over_c"] = round(st.median(warm) / st.median(cold), 3)
                 row[f"{tag}_K"] = plan.K
                 del src, dst
             print(json.dumps(row), flush=True)
@@ -479,7 +493,7 @@ def study(args, tb, torch, local):
 # Profiling target: 3 warm-up + 3 launches of one kernel on the bench's own
 # workload, nothing else (for ncu -k ... -s 3 -c 1..3).
 # ---------------------------------------------------------------------------
-def profile_target(kind, tb, torch, local):
+def profile_target(kind, args, tb, torch, local):
     stream = torch.cuda.current_stream()
     if kind == "reduce":
         nb = 256 * MiB
@@ -491,6 +505,24 @@ def profile_target(kind, tb, torch, local):
             for _ in range(6):
                 ctx.reduce_copy(srcs, dst, nb, 32, stream)
             torch.cuda.synchronize()
+    elif kind == "rotation":
+        # One fillCompress transfer of args.mib MiB with SRC_ROTATE_BYTES =
+        # args.rotate_mib MiB: 4 timed iterations inside an NVTX range "timed"
+        # (profile with --nvtx --nvtx-include timed/ --cache-control none).
+        nb = args.mib * MiB
+        rot = args.rotate_mib * MiB
+        with tb.Context(local, ctx_options(tb, warmup=0)) as ctx:
+            plan = tb.rotation_plan(nb, rot)
+            src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
+            ctx.fill_source(src, nb, tb.compress_pattern((40, 20, 0, 20, 20), 0x5EED), 0)
+            ctx.prepare_sources([src], nb, rot)
+            dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+            ctx.run_transfer([src], dst, nb, iters=4, rotate_bytes=rot)
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("timed")
+            r = ctx.run_transfer([src], dst, nb, iters=4, rotate_bytes=rot)
+            torch.cuda.nvtx.range_pop()
+            print(json.dumps({"K": r["K"], "iter_ms": r["iter_ms"]}), flush=True)
     else:
         from copy_reduce_dst_gb300 import workloads
         layout = workloads.batch_head_sliced()
@@ -515,7 +547,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--study", action="store_true")
-    ap.add_argument("--profile", choices=["reduce", "batch"])
+    ap.add_argument("--profile", choices=["reduce", "batch", "rotation"])
+    ap.add_argument("--mib", type=int, default=16, help="--profile rotation: transfer MiB")
+    ap.add_argument("--rotate-mib", type=int, default=256,
+                    help="--profile rotation: SRC_ROTATE_BYTES in MiB (0 = off)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -531,7 +566,7 @@ def main():
     if args.study:
         return study(args, tb, torch, local)
     if args.profile:
-        return profile_target(args.profile, tb, torch, local)
+        return profile_target(args.profile, args, tb, torch, local)
     ranks = Ranks(world, "nccl")
     red = run_reduce(args, tb, torch, ranks, local)
     batch = None if args.no_batch else run_batch(args, tb, torch, ranks, local)

@@ -1,9 +1,8 @@
 """Builds libtb.so, the CUDA library of this package, in-tree.
 
-Two translation units (kernels and host runtime) compile in parallel with
-nvcc for sm_103a only, then link into ``lib/libtb.so`` with the CUDA runtime
-linked statically, so the library needs nothing at run time beyond the
-driver.  Device code is built without fused multiply-add contraction and
+The kernel and host translation units compile in parallel with nvcc for
+sm_103a only, then link into ``lib/libtb.so`` with the CUDA runtime linked
+statically, so the library needs nothing at run time beyond the driver.  Device code is built without fused multiply-add contraction and
 without flush-to-zero, so every float add of the reduce-copy is one IEEE
 binary32 round-to-nearest-even add.
 """
@@ -20,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libtb.so")
 
-SOURCES = ["tb_kernels.cu", "tb_host.cpp", "tb_pack.cpp", "tb_static.cu"]
+SOURCES = ["tb_reduce.cu", "tb_batch.cu", "tb_fill.cu", "tb_host.cpp", "tb_pack.cpp",
+           "tb_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-ftz=false",
               "-Xcompiler", "-fPIC,-O2,-Wall,-Wextra", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,0 +1,469 @@
+// K2, the batched descriptor copy of libtb (sm_103a): one launch over a
+// packed (src, dst, len) work list (Mooncake RFC #5041, "Design of #5040").
+// Long copies stream through a bulk (TMA) pipeline in shared memory; short
+// copies go to warps.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tb_device.cuh"
+#include "tb_internal.h"
+
+namespace tb {
+namespace {
+
+using namespace dev;
+
+// ---------------------------------------------------------------------------
+// K2: batched copy.  copy_range copies len bytes with `size` cooperating
+// threads (a warp or a CTA), any alignment:
+//   - head bytes until dst is 16-byte aligned, one byte per thread;
+//   - body in 16-byte vectors: direct when src is then 16-byte aligned too,
+//     otherwise every output vector is funnel-shifted out of the two aligned
+//     source vectors that hold its bytes (both contain bytes of the range,
+//     so no load leaves the source's aligned 16-byte words);
+//   - tail bytes, one byte per thread.
+// ---------------------------------------------------------------------------
+constexpr int kCopyUnroll = 4;
+
+__device__ __forceinline__ uint4 ld16(const uint4 *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st16(uint4 *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w));
+}
+
+// Bytes sh .. sh+15 of the 32-byte concatenation lo|hi (little-endian).
+__device__ __forceinline__ uint4 shift_pair(const uint4 &lo, const uint4 &hi, uint32_t q, uint32_t rbits)
+{
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+        o[j] = q == 0 ? w[j] : (q == 1 ? w[j + 1] : (q == 2 ? w[j + 2] : w[j + 3]));
+    uint4 r;
+    r.x = __funnelshift_r(o[0], o[1], rbits);
+    r.y = __funnelshift_r(o[1], o[2], rbits);
+    r.z = __funnelshift_r(o[2], o[3], rbits);
+    r.w = __funnelshift_r(o[3], o[4], rbits);
+    return r;
+}
+
+__device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, uint64_t len,
+                                           uint32_t rank, uint32_t size)
+{
+    uint64_t h = (16u - ((uintptr_t)dst & 15u)) & 15u;
+    if (h > len)
+        h = len;
+    if (rank < h)
+        dst[rank] = src[rank];
+    dst += h;
+    src += h;
+    len -= h;
+
+    const uint64_t nv = len >> 4;
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    const uint32_t sh = (uint32_t)((uintptr_t)src & 15u);
+    uint64_t v = rank;
+    if (sh == 0) {
+        const uint4 *s = reinterpret_cast<const uint4 *>(src);
+        for (; v + (kCopyUnroll - 1) * (uint64_t)size < nv; v += kCopyUnroll * (uint64_t)size) {
+            uint4 r[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u)
+                r[u] = ld16(s + v + u * size);
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u)
+                st16(d + v + u * size, r[u]);
+        }
+        for (; v < nv; v += size)
+            st16(d + v, ld16(s + v));
+    } else {
+        const uint4 *s = reinterpret_cast<const uint4 *>(src - sh);
+        const uint32_t q = sh >> 2, rbits = (sh & 3u) * 8u;
+        for (; v + (kCopyUnroll - 1) * (uint64_t)size < nv; v += kCopyUnroll * (uint64_t)size) {
+            uint4 lo[kCopyUnroll], hi[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                lo[u] = ld16(s + v + u * size);
+                hi[u] = ld16(s + v + u * size + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u)
+                st16(d + v + u * size, shift_pair(lo[u], hi[u], q, rbits));
+        }
+        for (; v < nv; v += size)
+            st16(d + v, shift_pair(ld16(s + v), ld16(s + v + 1), q, rbits));
+    }
+
+    const uint64_t done = nv << 4;
+    if (rank < len - done)
+        dst[done + rank] = src[done + rank];
+}
+
+__device__ __forceinline__ WorkItem load_item(const WorkItem *p)
+{
+    WorkItem w;
+    w.src = __ldg(&p->src);
+    w.dst = __ldg(&p->dst);
+    w.len = __ldg(&p->len);
+    return w;
+}
+
+struct BatchArgs {
+    const WorkItem *shorts;      // n_short copies, longest first
+    const WorkItem *longs;       // n_long copies
+    const uint64_t *prefix;      // stream offset of each long copy
+    const uint32_t *chunk_desc;  // long copy holding each chunk's first byte
+    uint32_t *status;            // nullable: set to 1 if a bounded wait expired
+    uint64_t long_bytes;
+    uint32_t n_short;
+    uint32_t chunks;
+};
+
+// ---------------------------------------------------------------------------
+// Bulk (TMA) copies through shared memory: cp.async.bulk global -> shared
+// completes on an mbarrier; cp.async.bulk shared -> global is tracked by
+// bulk groups.  No tensor map, no cluster multicast.
+// ---------------------------------------------------------------------------
+constexpr int kStages = 3;
+constexpr uint32_t kBlock = 16384;                 // bytes per bulk copy
+constexpr size_t kBarBytes = 128;                  // mbarriers, then stages
+constexpr size_t kBatchSmem = kBarBytes + (size_t)kStages * kBlock;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs)
+            return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t smem, uint64_t gsrc, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem),
+        "l"(gsrc), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(uint64_t gdst, uint32_t smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Newest group may still be reading shared memory; all older ones are done.
+__device__ __forceinline__ void bulk_wait_read_all_but_newest()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Walks this CTA's chunks of the long-copy stream (chunks b, b + G, ...),
+// one piece (a contiguous part of one long copy) at a time.
+struct PieceWalker {
+    const BatchArgs &a;
+    uint32_t c;
+    uint64_t pos, end;
+    uint32_t d;
+
+    __device__ explicit PieceWalker(const BatchArgs &args) : a(args), c(blockIdx.x), pos(0), end(0), d(0)
+    {
+        open();
+    }
+    __device__ void open()
+    {
+        if (c < a.chunks) {
+            pos = chunk_start(a.long_bytes, a.chunks, c);
+            end = chunk_start(a.long_bytes, a.chunks, c + 1);
+            d = __ldg(a.chunk_desc + c);
+        }
+    }
+    __device__ bool next(uint64_t &src, uint64_t &dst, uint64_t &len)
+    {
+        while (c < a.chunks) {
+            if (pos < end) {
+                const WorkItem w = load_item(a.longs + d);
+                const uint64_t off = pos - __ldg(a.prefix + d);
+                const uint64_t take = min(w.len - off, end - pos);
+                src = w.src + off;
+                dst = w.dst + off;
+                len = take;
+                pos += take;
+                if (off + take == w.len)
+                    ++d;
+                return true;
+            }
+            c += gridDim.x;
+            open();
+        }
+        return false;
+    }
+};
+
+// A piece is copied by bulk copies when src and dst share their address
+// modulo 16: a byte head brings both to 16 bytes, the body moves in bulk,
+// a byte tail (< 16 bytes) ends it.  Other pieces are copied by threads.
+__device__ __forceinline__ bool bulk_split(uint64_t src, uint64_t dst, uint64_t len, uint64_t &head,
+                                           uint64_t &body)
+{
+    if (((src ^ dst) & 15u) != 0)
+        return false;
+    head = min((16u - (dst & 15u)) & 15u, len);
+    body = (len - head) & ~(uint64_t)15;
+    return true;
+}
+
+// Thread 0's bulk pipeline over the bodies of this CTA's pieces: kStages
+// blocks of up to kBlock bytes in flight; block k uses stage k % kStages.
+// Returns false if a wait expired (status recorded, copies drained).
+__device__ bool bulk_pipeline(const BatchArgs &a, uint32_t bars, uint32_t stages)
+{
+    PieceWalker walk(a);
+    uint64_t bsrc = 0, bdst = 0, bleft = 0;
+    auto next_block = [&](uint64_t &gs, uint64_t &gd, uint32_t &nb) -> bool {
+        while (bleft == 0) {
+            uint64_t s, d, l, h, body;
+            if (!walk.next(s, d, l))
+                return false;
+            if (bulk_split(s, d, l, h, body) && body > 0) {
+                bsrc = s + h;
+                bdst = d + h;
+                bleft = body;
+            }
+        }
+        nb = (uint32_t)(bleft < kBlock ? bleft : kBlock);
+        gs = bsrc;
+        gd = bdst;
+        bsrc += nb;
+        bdst += nb;
+        bleft -= nb;
+        return true;
+    };
+
+    uint64_t gdst[kStages];
+    uint32_t nbytes[kStages];
+    uint32_t uses = 0;  // bit s: parity of stage s's next phase
+    uint32_t issued = 0;
+    for (int s = 0; s < kStages; ++s) {
+        uint64_t gs;
+        if (!next_block(gs, gdst[s], nbytes[s]))
+            break;
+        bulk_load(stages + s * kBlock, gs, nbytes[s], bars + 8 * s);
+        ++issued;
+    }
+    bool ok = true;
+    for (uint32_t i = 0; i < issued; ++i) {
+        const uint32_t s = i % kStages;
+        if (!mbar_wait_bounded(bars + 8 * s, (uses >> s) & 1u)) {
+            ok = false;
+            break;
+        }
+        uses ^= 1u << s;
+        bulk_store(gdst[s], stages + s * kBlock, nbytes[s]);
+        if (i >= 1) {
+            const uint32_t sp = (i - 1) % kStages;
+            uint64_t gs;
+            if (next_block(gs, gdst[sp], nbytes[sp])) {
+                bulk_wait_read_all_but_newest();
+                bulk_load(stages + sp * kBlock, gs, nbytes[sp], bars + 8 * sp);
+                ++issued;
+            }
+        }
+    }
+    if (!ok) {
+        if (a.status)
+            *reinterpret_cast<volatile uint32_t *>(a.status) = 1u;
+        // Let the loads still in flight land (each wait bounded again).
+        for (uint32_t k = 0; k < kStages; ++k)
+            mbar_wait_bounded(bars + 8 * k, (uses >> k) & 1u);
+    }
+    bulk_wait_all();
+    return ok;
+}
+
+// Threads other than warp 0: the bytes of this CTA's pieces that the bulk
+// pipeline does not move (heads, tails, pieces whose src and dst differ
+// modulo 16).
+__device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
+{
+    PieceWalker walk(a);
+    uint64_t s, d, l, h, body;
+    while (walk.next(s, d, l)) {
+        if (bulk_split(s, d, l, h, body)) {
+            if (rank < h)
+                reinterpret_cast<uint8_t *>(d)[rank] = reinterpret_cast<const uint8_t *>(s)[rank];
+            const uint64_t t = h + body;
+            if (rank < l - t)
+                reinterpret_cast<uint8_t *>(d)[t + rank] = reinterpret_cast<const uint8_t *>(s)[t + rank];
+        } else {
+            copy_range(reinterpret_cast<uint8_t *>(d), reinterpret_cast<const uint8_t *>(s), l, rank,
+                       size);
+        }
+    }
+}
+
+// Persistent grid of one wave.
+//   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
+//   owns chunks b, b + G, ... (the same number for every CTA, the grid
+//   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned
+//   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
+//   the leftover edges.
+//   Short copies (longest first in memory) go to warps 1.. (all warps when
+//   there are no long copies), dealt in boustrophedon order: round r goes up
+//   the warp list when r is even and down when it is odd, which keeps every
+//   warp's byte total close to the mean.  Odd warps walk their rounds from
+//   the smallest item up, so small latency-bound copies overlap large ones.
+//   Each warp fetches its next item before copying the current one.
+__global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const bool has_long = a.chunks > 0;
+    if (has_long) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kStages; ++s)
+                mbar_init(smem_u32(smem) + 8 * s);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (warp == 0) {
+            if (lane == 0)
+                bulk_pipeline(a, smem_u32(smem), smem_u32(smem + kBarBytes));
+            return;
+        }
+        long_edges(a, threadIdx.x - 32, blockDim.x - 32);
+    }
+
+    const uint32_t w0 = has_long ? 1u : 0u;
+    const uint32_t warps_per_cta = (blockDim.x >> 5) - w0;
+    const uint64_t W = (uint64_t)gridDim.x * warps_per_cta;
+    const uint64_t wid = (uint64_t)blockIdx.x * warps_per_cta + (warp - w0);
+    const uint64_t n_short = a.n_short;
+    const uint64_t R = (n_short + W - 1) / W;
+    const bool reverse = wid & 1u;
+    // The k-th item this warp copies (k in [0, R)), or n_short if none.
+    auto item_at = [&](uint64_t k) {
+        const uint64_t r = reverse ? (R - 1 - k) : k;
+        return r * W + ((r & 1) ? (W - 1 - wid) : wid);
+    };
+    uint64_t k = 0;
+    while (k < R && item_at(k) >= n_short)
+        ++k;
+    if (k >= R)
+        return;
+    WorkItem cur = load_item(a.shorts + item_at(k));
+    for (;;) {
+        uint64_t kn = k + 1;
+        while (kn < R && item_at(kn) >= n_short)
+            ++kn;
+        const bool more = kn < R;
+        WorkItem nxt = cur;
+        if (more)
+            nxt = load_item(a.shorts + item_at(kn));
+        copy_range(reinterpret_cast<uint8_t *>(cur.dst), reinterpret_cast<const uint8_t *>(cur.src),
+                   cur.len, lane, 32u);
+        if (!more)
+            break;
+        cur = nxt;
+        k = kn;
+    }
+}
+
+int g_batch_ctas_per_sm = 0;
+
+}  // namespace
+
+
+static bool batch_kernel_setup()
+{
+    static bool done = false;
+    if (!done)
+        done = cudaFuncSetAttribute(k_batch, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kBatchSmem) == cudaSuccess;
+    return done;
+}
+
+int batch_ctas_per_sm()
+{
+    if (g_batch_ctas_per_sm == 0) {
+        int blocks = 0;
+        if (!batch_kernel_setup() ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_batch, kBatchThreads,
+                                                          kBatchSmem) != cudaSuccess ||
+            blocks < 1)
+            blocks = 1;
+        g_batch_ctas_per_sm = blocks;
+    }
+    return g_batch_ctas_per_sm;
+}
+
+cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
+                         uint32_t *status)
+{
+    if (plan.n_short == 0 && plan.n_long == 0)
+        return cudaSuccess;
+    if (!batch_kernel_setup())
+        return cudaErrorInvalidValue;
+    const char *base = static_cast<const char *>(dev);
+    BatchArgs a;
+    a.shorts = reinterpret_cast<const WorkItem *>(base);
+    a.longs = a.shorts + plan.n_short;
+    a.prefix = reinterpret_cast<const uint64_t *>(base + plan.prefix_offset);
+    a.chunk_desc = reinterpret_cast<const uint32_t *>(base + plan.chunk_offset);
+    a.status = status;
+    a.long_bytes = plan.long_bytes;
+    a.n_short = plan.n_short;
+    a.chunks = plan.chunks;
+    // Short copies only: no shared memory needed.
+    const size_t smem = plan.chunks ? kBatchSmem : 0;
+    k_batch<<<plan.grid, kBatchThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace tb

@@ -40,6 +40,16 @@ struct Slot {
     uint32_t *status_dev = nullptr;
 };
 
+// Chunk size of the staged tb_reduce_copy_host pipeline.
+constexpr uint64_t kStageChunk = 32 * kMiB;
+
+// Streams and events of the staged host <-> device pipeline, made on first use.
+struct Pipeline {
+    cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
+    cudaEvent_t begin = nullptr, end = nullptr;
+    std::vector<cudaEvent_t> in, out;  // per chunk
+};
+
 }  // namespace
 
 struct tb_ctx {
@@ -64,6 +74,8 @@ struct tb_ctx {
     std::vector<uint32_t> bucket;     // counting-sort buckets
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
+
+    Pipeline pipe;                    // staged host <-> device transfers
 
     void *val_stage = nullptr;        // pinned validation staging
     uint64_t prep_h2d = 0;
@@ -238,6 +250,46 @@ int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src,
                     TB_MAX_SRCS);
     if (rc != TB_OK)
         return fail(ctx, rc, "vec_bytes=%d is not allowed by the pointers' alignment", o.vec_bytes);
+    return TB_OK;
+}
+
+// Device address of a page-locked host buffer mapped into the device's
+// address space, or nullptr for any other memory.
+void *mapped_host_pointer(const void *p)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer)
+        return nullptr;
+    return attr.devicePointer;
+}
+
+int ensure_pipeline(tb_ctx *ctx)
+{
+    Pipeline &pl = ctx->pipe;
+    if (pl.h2d)
+        return TB_OK;
+    for (cudaStream_t *s : {&pl.h2d, &pl.cmp, &pl.d2h})
+        TB_CUDA(ctx, cudaStreamCreateWithFlags(s, cudaStreamNonBlocking));
+    TB_CUDA(ctx, cudaEventCreateWithFlags(&pl.begin, cudaEventDisableTiming));
+    TB_CUDA(ctx, cudaEventCreateWithFlags(&pl.end, cudaEventDisableTiming));
+    return TB_OK;
+}
+
+// Grows the per-chunk events of the staged pipeline to n.
+int pipeline_events(tb_ctx *ctx, uint64_t n)
+{
+    Pipeline &pl = ctx->pipe;
+    while (pl.in.size() < n) {
+        cudaEvent_t a = nullptr, b = nullptr;
+        TB_CUDA(ctx, cudaEventCreateWithFlags(&a, cudaEventDisableTiming));
+        pl.in.push_back(a);
+        TB_CUDA(ctx, cudaEventCreateWithFlags(&b, cudaEventDisableTiming));
+        pl.out.push_back(b);
+    }
     return TB_OK;
 }
 
@@ -538,6 +590,19 @@ void tb_destroy(tb_ctx *ctx)
     }
     for (cudaEvent_t e : ctx->events)
         cudaEventDestroy(e);
+    Pipeline &pl = ctx->pipe;
+    for (cudaStream_t s : {pl.h2d, pl.cmp, pl.d2h})
+        if (s) {
+            cudaStreamSynchronize(s);
+            cudaStreamDestroy(s);
+        }
+    for (cudaEvent_t e : {pl.begin, pl.end})
+        if (e)
+            cudaEventDestroy(e);
+    for (cudaEvent_t e : pl.in)
+        cudaEventDestroy(e);
+    for (cudaEvent_t e : pl.out)
+        cudaEventDestroy(e);
     if (ctx->gate_flag)
         cudaFreeHost((void *)ctx->gate_flag);
     if (ctx->slot_status)
@@ -662,22 +727,76 @@ int tb_reduce_copy_host(tb_ctx *ctx, const void *const *host_srcs, int n_src, vo
 {
     if (!ctx)
         return TB_EINVAL;
-    if (n_src < 0 || n_src > TB_MAX_SRCS || !host_dst || !dev_dst ||
-        (n_src > 0 && (!host_srcs || !dev_srcs)))
+    if (n_src < 0 || n_src > TB_MAX_SRCS || !host_dst || (n_src > 0 && !host_srcs))
         return fail(ctx, TB_EINVAL, "reduce_copy_host: bad arguments");
     for (int k = 0; k < n_src; ++k)
-        if (!host_srcs[k] || !dev_srcs[k])
-            return fail(ctx, TB_EINVAL, "reduce_copy_host: null source");
+        if (!host_srcs[k])
+            return fail(ctx, TB_EINVAL, "reduce_copy_host: null host source");
     DeviceScope scope(ctx->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    tb::ReducePlan p;
-    int rc = plan_for(ctx, &p, (const void *const *)dev_srcs, n_src, dev_dst, num_bytes, num_subexec);
+
+    // Direct: every host buffer is page-locked and mapped into the device's
+    // address space, so one reduce-copy kernel reads the sources and writes
+    // the destination across the host link (both directions at once).
+    const void *mapped[TB_MAX_SRCS];
+    void *mapped_dst = mapped_host_pointer(host_dst);
+    bool direct = mapped_dst != nullptr;
+    for (int k = 0; direct && k < n_src; ++k)
+        direct = (mapped[k] = mapped_host_pointer(host_srcs[k])) != nullptr;
+    if (direct) {
+        tb::ReducePlan p;
+        int rc = plan_for(ctx, &p, mapped, n_src, mapped_dst, num_bytes, num_subexec);
+        if (rc != TB_OK)
+            return rc;
+        TB_CUDA(ctx, tb::launch_reduce(p, st));
+        return TB_OK;
+    }
+
+    // Staged: chunks flow host -> device copies, kernel, device -> host copy
+    // on three streams, so copies in both directions overlap the kernels.
+    if (!dev_dst || (n_src > 0 && !dev_srcs))
+        return fail(ctx, TB_EINVAL, "reduce_copy_host: device buffers are needed for host "
+                                    "memory that is not page-locked and mapped");
+    for (int k = 0; k < n_src; ++k)
+        if (!dev_srcs[k])
+            return fail(ctx, TB_EINVAL, "reduce_copy_host: null device source");
+    int rc = ensure_pipeline(ctx);
     if (rc != TB_OK)
         return rc;
-    for (int k = 0; k < n_src; ++k)
-        TB_CUDA(ctx, cudaMemcpyAsync(dev_srcs[k], host_srcs[k], num_bytes, cudaMemcpyHostToDevice, st));
-    TB_CUDA(ctx, tb::launch_reduce(p, st));
-    TB_CUDA(ctx, cudaMemcpyAsync(host_dst, dev_dst, num_bytes, cudaMemcpyDeviceToHost, st));
+    const uint64_t chunk = kStageChunk;
+    const uint64_t nchunks = num_bytes ? (num_bytes + chunk - 1) / chunk : 0;
+    rc = pipeline_events(ctx, nchunks);
+    if (rc != TB_OK)
+        return rc;
+    Pipeline &pl = ctx->pipe;
+    TB_CUDA(ctx, cudaEventRecord(pl.begin, st));
+    for (cudaStream_t s : {pl.h2d, pl.cmp, pl.d2h})
+        TB_CUDA(ctx, cudaStreamWaitEvent(s, pl.begin, 0));
+    for (uint64_t c = 0; c < nchunks; ++c) {
+        const uint64_t off = c * chunk;
+        const uint64_t len = std::min(chunk, num_bytes - off);
+        const void *ds[TB_MAX_SRCS];
+        for (int k = 0; k < n_src; ++k) {
+            char *d = static_cast<char *>(dev_srcs[k]) + off;
+            TB_CUDA(ctx, cudaMemcpyAsync(d, static_cast<const char *>(host_srcs[k]) + off, len,
+                                         cudaMemcpyHostToDevice, pl.h2d));
+            ds[k] = d;
+        }
+        TB_CUDA(ctx, cudaEventRecord(pl.in[c], pl.h2d));
+        TB_CUDA(ctx, cudaStreamWaitEvent(pl.cmp, pl.in[c], 0));
+        tb::ReducePlan p;
+        rc = plan_for(ctx, &p, ds, n_src, static_cast<char *>(dev_dst) + off, len, num_subexec);
+        if (rc != TB_OK)
+            return rc;
+        TB_CUDA(ctx, tb::launch_reduce(p, pl.cmp));
+        TB_CUDA(ctx, cudaEventRecord(pl.out[c], pl.cmp));
+        TB_CUDA(ctx, cudaStreamWaitEvent(pl.d2h, pl.out[c], 0));
+        TB_CUDA(ctx, cudaMemcpyAsync(static_cast<char *>(host_dst) + off,
+                                     static_cast<const char *>(dev_dst) + off, len,
+                                     cudaMemcpyDeviceToHost, pl.d2h));
+    }
+    TB_CUDA(ctx, cudaEventRecord(pl.end, pl.d2h));
+    TB_CUDA(ctx, cudaStreamWaitEvent(st, pl.end, 0));
     return TB_OK;
 }
 

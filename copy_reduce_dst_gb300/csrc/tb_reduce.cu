@@ -1,0 +1,363 @@
+// K1, the reduce-copy kernel of libtb (sm_103a), and its launch planning:
+// dst[i] = src0[i] + ... + srcN-1[i] in float32, left to right ("TransferBench
+// data validation", table "Number of sources / Expected value").
+//
+// HBM-bound streaming; no contraction, so no tensor cores.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "tb_device.cuh"
+#include "tb_internal.h"
+
+namespace tb {
+namespace {
+
+using namespace dev;
+
+// ---------------------------------------------------------------------------
+// K1: reduce-copy.  N = number of sources (0 = memset, 1 = bit copy).
+// Each thread keeps U vectors of every source in flight: all N*U loads are
+// issued before the first add, then the sums run left to right per element
+// and U vector stores follow.
+// ---------------------------------------------------------------------------
+struct ReduceArgs {
+    const float *src[TB_MAX_SRCS];
+    float *dst;
+    uint64_t n;
+    uint64_t head;
+    uint64_t nvec;
+    uint32_t nsub;         // sub-executors; never more than the grid's CTAs
+    uint32_t memset_word;
+};
+
+// The CTAs of a launch are dealt to the sub-executors as evenly as integers
+// allow (sub-executor s gets CTAs [s*G/S, (s+1)*G/S)), and each sub-executor
+// owns a contiguous range of body vectors in proportion to its CTAs, so every
+// CTA streams the same share whether or not S divides the grid G.
+struct SubRange {
+    uint32_t part, nparts;   // this CTA's rank within its sub-executor, and their count
+    uint64_t vbeg, vend;     // the sub-executor's body vectors
+};
+
+__device__ __forceinline__ SubRange sub_range(uint64_t nvec, uint32_t S)
+{
+    const uint32_t G = gridDim.x, b = blockIdx.x;
+    const uint32_t sub = (uint32_t)(((uint64_t)(b + 1) * S - 1) / G);
+    const uint32_t c0 = (uint32_t)((uint64_t)sub * G / S);
+    const uint32_t c1 = (uint32_t)((uint64_t)(sub + 1) * G / S);
+    const uint64_t q = nvec / G, r = nvec % G;
+    SubRange sr;
+    sr.part = b - c0;
+    sr.nparts = c1 - c0;
+    sr.vbeg = q * c0 + (r * c0) / G;
+    sr.vend = q * c1 + (r * c1) / G;
+    return sr;
+}
+
+// Scalar element i, used for the head and the tail of a launch.
+template <int N>
+__device__ __forceinline__ void reduce_one(const ReduceArgs &a, uint64_t i)
+{
+    if constexpr (N == 0) {
+        reinterpret_cast<uint32_t *>(a.dst)[i] = a.memset_word;
+    } else {
+        uint32_t acc = reinterpret_cast<const uint32_t *>(a.src[0])[i];
+#pragma unroll
+        for (int k = 1; k < N; ++k)
+            acc = __float_as_uint(__fadd_rn(__uint_as_float(acc), a.src[k][i]));
+        reinterpret_cast<uint32_t *>(a.dst)[i] = acc;
+    }
+}
+
+template <int N, int VB, int U>
+__device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, const char *const *s, char *d,
+                                               uint64_t v0, uint64_t stride, uint64_t vend,
+                                               bool full)
+{
+    Vec<VB> acc[U];
+    if constexpr (N == 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < VB / 4; ++e)
+                acc[u].w[e] = a.memset_word;
+    } else {
+        Vec<VB> x[N > 1 ? N - 1 : 1][U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (full || v0 + u * stride < vend)
+                vload<VB>(acc[u], s[0] + (v0 + u * stride) * VB);
+#pragma unroll
+        for (int k = 1; k < N; ++k)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (full || v0 + u * stride < vend)
+                    vload<VB>(x[k - 1][u], s[k] + (v0 + u * stride) * VB);
+#pragma unroll
+        for (int k = 1; k < N; ++k)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                vadd<VB>(acc[u], x[k - 1][u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (full || v0 + u * stride < vend)
+            vstore<VB>(d + (v0 + u * stride) * VB, acc[u]);
+}
+
+template <int N, int VB, int U>
+__global__ void __launch_bounds__(512) k_reduce(const ReduceArgs a)
+{
+    const uint32_t tid = threadIdx.x;
+    const uint32_t bd = blockDim.x;
+    const SubRange sr = sub_range(a.nvec, a.nsub);
+
+    const char *s[N > 0 ? N : 1];
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+        s[k] = reinterpret_cast<const char *>(a.src[k] + a.head);
+    char *d = reinterpret_cast<char *>(a.dst + a.head);
+
+    const uint64_t vend = sr.vend;
+    const uint64_t tile = (uint64_t)bd * U;
+    const uint64_t step = (uint64_t)sr.nparts * tile;
+    for (uint64_t t = sr.vbeg + sr.part * tile; t < vend; t += step) {
+        if (t + tile <= vend)
+            reduce_vectors<N, VB, U>(a, s, d, t + tid, bd, vend, true);
+        else
+            reduce_vectors<N, VB, U>(a, s, d, t + tid, bd, vend, false);
+    }
+
+    if (blockIdx.x == 0 && tid < a.head)
+        reduce_one<N>(a, tid);
+    const uint64_t tail0 = a.head + a.nvec * (VB / 4);
+    if (blockIdx.x == gridDim.x - 1 && tail0 + tid < a.n)
+        reduce_one<N>(a, tail0 + tid);
+}
+
+// More than 8 sources: the source loop runs at run time, each thread holding
+// two vectors of one source at a time.
+template <int VB>
+__global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_src)
+{
+    const uint32_t tid = threadIdx.x;
+    const uint32_t bd = blockDim.x;
+    const SubRange sr = sub_range(a.nvec, a.nsub);
+    const uint64_t vend = sr.vend;
+    const uint64_t tile = (uint64_t)bd * 2;
+    const uint64_t step = (uint64_t)sr.nparts * tile;
+    const uint64_t W = VB / 4;
+    for (uint64_t t = sr.vbeg + sr.part * tile; t < vend; t += step) {
+        const uint64_t v0 = t + tid, v1 = t + bd + tid;
+        if (v0 >= vend)
+            break;
+        const bool ok1 = v1 < vend;
+        Vec<VB> acc0, acc1, x0, x1;
+        vload<VB>(acc0, a.src[0] + a.head + v0 * W);
+        if (ok1)
+            vload<VB>(acc1, a.src[0] + a.head + v1 * W);
+        for (int k = 1; k < n_src; ++k) {
+            vload<VB>(x0, a.src[k] + a.head + v0 * W);
+            if (ok1)
+                vload<VB>(x1, a.src[k] + a.head + v1 * W);
+            vadd<VB>(acc0, x0);
+            if (ok1)
+                vadd<VB>(acc1, x1);
+        }
+        vstore<VB>(a.dst + a.head + v0 * W, acc0);
+        if (ok1)
+            vstore<VB>(a.dst + a.head + v1 * W, acc1);
+    }
+    const uint64_t tail0 = a.head + a.nvec * W;
+    auto one = [&](uint64_t i) {
+        uint32_t acc = reinterpret_cast<const uint32_t *>(a.src[0])[i];
+        for (int k = 1; k < n_src; ++k)
+            acc = __float_as_uint(__fadd_rn(__uint_as_float(acc), a.src[k][i]));
+        reinterpret_cast<uint32_t *>(a.dst)[i] = acc;
+    };
+    if (blockIdx.x == 0 && tid < a.head)
+        one(tid);
+    if (blockIdx.x == gridDim.x - 1 && tail0 + tid < a.n)
+        one(tail0 + tid);
+}
+
+using ReduceKernel = void (*)(const ReduceArgs);
+
+template <int N, int VB>
+ReduceKernel pick_unroll(int u)
+{
+    switch (u) {
+    case 1: return k_reduce<N, VB, 1>;
+    case 2: return k_reduce<N, VB, 2>;
+    default: return k_reduce<N, VB, 4>;
+    }
+}
+
+template <int N>
+ReduceKernel pick_vec(int vb, int u)
+{
+    switch (vb) {
+    case 32: return pick_unroll<N, 32>(u);
+    case 16: return pick_unroll<N, 16>(u);
+    default: return k_reduce<N, 4, 4>;
+    }
+}
+
+ReduceKernel pick_reduce(int n_src, int vb, int u)
+{
+    switch (n_src) {
+    case 0: return pick_vec<0>(vb, u);
+    case 1: return pick_vec<1>(vb, u);
+    case 2: return pick_vec<2>(vb, u);
+    case 3: return pick_vec<3>(vb, u);
+    case 4: return pick_vec<4>(vb, u);
+    case 5: return pick_vec<5>(vb, u);
+    case 6: return pick_vec<6>(vb, u);
+    case 7: return pick_vec<7>(vb, u);
+    case 8: return pick_vec<8>(vb, u);
+    default: return nullptr;
+    }
+}
+
+// Largest unroll whose in-flight words (sources x unroll x words per vector)
+// stay in registers without spilling at 512 threads per CTA.
+int max_unroll(int n_src, int vb)
+{
+    const int words = std::max(1, n_src) * (vb / 4);
+    const int budget = vb == 32 ? 48 : 64;
+    for (int u = 4; u > 1; u /= 2)
+        if (words * u <= budget)
+            return u;
+    return 1;
+}
+
+// Default: the largest unroll that still fits 64 registers, i.e. two
+// 512-thread CTAs per SM.
+int default_unroll(int n_src, int vb)
+{
+    const int words = std::max(1, n_src) * (vb / 4);
+    for (int u = 4; u > 1; u /= 2)
+        if (words * u <= 32)
+            return u;
+    return 1;
+}
+
+
+}  // namespace
+
+int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll)
+{
+    void *fn = n_src <= 8 ? (void *)pick_reduce(n_src, vec_bytes, unroll)
+                          : (vec_bytes == 16 ? (void *)k_reduce_many<16> : (void *)k_reduce_many<4>);
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, block_threads, 0) != cudaSuccess ||
+        blocks < 1)
+        blocks = 1;
+    return blocks;
+}
+
+int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
+                int num_subexec, int ctas_per_subexec, int block_threads, int vec_bytes, int unroll,
+                uint32_t memset_byte, int num_sms)
+{
+    if (!p || !dst || n_src < 0 || n_src > TB_MAX_SRCS || num_bytes % 4 != 0 || num_subexec < 0 ||
+        ctas_per_subexec < 0 || block_threads < 0 || block_threads > 512 || block_threads % 32 != 0 ||
+        unroll < 0 || unroll > 4 || unroll == 3 || num_sms < 1 ||
+        (vec_bytes != 0 && vec_bytes != 4 && vec_bytes != 16 && vec_bytes != 32))
+        return TB_EINVAL;
+    if (n_src > 0 && !srcs)
+        return TB_EINVAL;
+    uintptr_t any = (uintptr_t)dst;
+    for (int k = 0; k < n_src; ++k) {
+        if (!srcs[k])
+            return TB_EINVAL;
+        any |= (uintptr_t)srcs[k];
+    }
+    if (any & 3u)
+        return TB_EINVAL;
+
+    *p = ReducePlan{};
+    p->n_src = n_src;
+    for (int k = 0; k < n_src; ++k)
+        p->src[k] = static_cast<const float *>(srcs[k]);
+    p->dst = static_cast<float *>(dst);
+    p->n = num_bytes / 4;
+    const uint32_t b = memset_byte & 0xFFu;
+    p->memset_word = b | (b << 8) | (b << 16) | (b << 24);
+
+    // Widest vector whose alignment every pointer shares: then one head
+    // brings them all to a vector boundary together.
+    auto common = [&](uintptr_t mask) {
+        const uintptr_t m = (uintptr_t)dst & mask;
+        for (int k = 0; k < n_src; ++k)
+            if (((uintptr_t)srcs[k] & mask) != m)
+                return false;
+        return true;
+    };
+    int vb = common(31) ? 32 : (common(15) ? 16 : 4);
+    if (vec_bytes != 0) {
+        if (vec_bytes > vb)
+            return TB_ENOTSUP;
+        vb = vec_bytes;
+    }
+    if (n_src > 8) {  // the run-time source loop has 4- and 16-byte forms only
+        if (vec_bytes == 32)
+            return TB_ENOTSUP;
+        if (vb == 32)
+            vb = 16;
+    }
+    p->vec_bytes = vb;
+
+    if (vb > 4) {
+        const uintptr_t mis = (uintptr_t)dst & (uintptr_t)(vb - 1);
+        const uint64_t head = mis ? ((uint64_t)vb - mis) / 4 : 0;
+        p->head = std::min<uint64_t>(head, p->n);
+    }
+    p->nvec = (p->n - p->head) / ((uint64_t)vb / 4);
+    p->block_threads = block_threads ? block_threads : 512;
+    p->unroll = vb == 4 ? 4 : std::min(unroll ? unroll : default_unroll(n_src, vb), max_unroll(n_src, vb));
+
+    // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
+    // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
+    // sub-executor); never fewer CTAs than sub-executors.
+    const int per_sm = reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
+    const int64_t full = (int64_t)num_sms * per_sm;
+    const int64_t S = num_subexec > 0 ? num_subexec : full;
+    const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, full);
+    if (G > (int64_t)INT32_MAX)
+        return TB_EINVAL;
+    p->num_subexec = (int)S;
+    p->grid = (int)G;
+    return TB_OK;
+}
+
+cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
+{
+    ReduceArgs a{};
+    for (int k = 0; k < p.n_src; ++k)
+        a.src[k] = p.src[k];
+    a.dst = p.dst;
+    a.n = p.n;
+    a.head = p.head;
+    a.nvec = p.nvec;
+    a.nsub = (uint32_t)p.num_subexec;
+    a.memset_word = p.memset_word;
+    const unsigned grid = (unsigned)p.grid;
+    if (p.n == 0)
+        return cudaSuccess;
+    if (p.n_src > 8) {
+        if (p.vec_bytes == 16)
+            k_reduce_many<16><<<grid, p.block_threads, 0, stream>>>(a, p.n_src);
+        else
+            k_reduce_many<4><<<grid, p.block_threads, 0, stream>>>(a, p.n_src);
+    } else {
+        ReduceKernel k = pick_reduce(p.n_src, p.vec_bytes, p.unroll);
+        k<<<grid, p.block_threads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tb

@@ -307,11 +307,18 @@ int tb_run_transfer(tb_ctx *ctx, void *const *srcs, int nSrc, void *dst,
                     uint64_t numBytes, int numSubExec, int iters, uint64_t rotateBytes,
                     tb_result *out);
 
-/* The transfer with host buffers, end to end, asynchronous on `stream`:
-   copies numBytes from each hostSrcs[k] into devSrcs[k], runs one
-   tb_reduce_copy into devDst, and copies devDst back into hostDst.  Host
-   buffers should be page-locked for the copies to be asynchronous.  The
-   device buffers are the caller's (numBytes each, no offsets added). */
+/* The transfer with host buffers, end to end, asynchronous on `stream`
+   (ordered after the caller's earlier work on it): hostDst = the reduce-copy
+   of hostSrcs, numBytes each.
+   - When every host buffer is page-locked and mapped into the device's
+     address space (cudaHostAlloc, or cudaHostRegister with mapping), one
+     reduce-copy kernel reads the sources and writes hostDst across the host
+     link directly; devSrcs / devDst are not used and may be NULL.
+   - Otherwise the bytes are staged through the caller's device buffers
+     devSrcs[k] / devDst (numBytes each) in 32 MiB chunks: host-to-device
+     copies, the kernel and the device-to-host copy of successive chunks run
+     on three internal streams and overlap.  Pageable host memory makes the
+     copies synchronous with the host. */
 int tb_reduce_copy_host(tb_ctx *ctx, const void *const *hostSrcs, int nSrc, void *hostDst,
                         uint64_t numBytes, void *const *devSrcs, void *devDst,
                         int numSubExec, tb_stream stream);

@@ -318,6 +318,24 @@ def test_gate_deadline_returns_timeout(tb):
         assert r["gated"] == 0
 
 
+@pytest.mark.parametrize("n", [1, 1000003, (96 << 20) // 4 + 5])
+def test_reduce_copy_host_staged(tb, ctx, n):
+    """Pageable host memory: the bytes are staged through device buffers in
+    32 MiB chunks on three streams."""
+    import torch
+    g = np.random.default_rng(n)
+    srcs = [finite_floats(g, n) for _ in range(3)]
+    hd = np.zeros(n, np.float32)
+    ds = [dev_bytes(4 * n) for _ in range(3)]
+    dd = dev_bytes(4 * n)
+    st = torch.cuda.Stream()
+    ctx.reduce_copy_host(srcs, hd, 4 * n, ds, dd, 0, st)
+    st.synchronize()
+    assert oracle.first_mismatch(hd, oracle.dst_reference(srcs)) == -1
+    with pytest.raises(tb.TBError):
+        ctx.reduce_copy_host(srcs, hd, 4 * n, [None] * 3, None, 0, st)
+
+
 def test_reduce_copy_host_end_to_end(tb, ctx):
     import torch
     g = np.random.default_rng(9)
@@ -325,10 +343,9 @@ def test_reduce_copy_host_end_to_end(tb, ctx):
     srcs = [finite_floats(g, n) for _ in range(3)]
     hs = [torch.from_numpy(s).pin_memory() for s in srcs]
     hd = torch.empty(n, dtype=torch.float32).pin_memory()
-    ds = [dev_bytes(4 * n) for _ in range(3)]
-    dd = dev_bytes(4 * n)
     st = torch.cuda.Stream()
-    ctx.reduce_copy_host(hs, hd, 4 * n, ds, dd, 0, st)
+    # page-locked and mapped: one kernel across the host link, no device buffers
+    ctx.reduce_copy_host(hs, hd, 4 * n, [None] * 3, None, 0, st)
     st.synchronize()
     assert oracle.first_mismatch(hd.numpy(), oracle.dst_reference(srcs)) == -1
 
