@@ -218,6 +218,9 @@ def run_reduce(args, tb, torch, ranks, local):
     # count is reported in the line's config).
     subexec = max(sweep, key=lambda k: sweep[k]["gbps"])
     subexec = int(subexec)
+    info = ctx.reduce_plan(srcs, dst, nb, subexec)
+    kernel = (f"k_reduce_bulk<{n_src}> (bulk copies through shared memory)" if info["engine"] == 2
+              else f"k_reduce<{n_src}, {info['vec_bytes']}, {info['unroll']}> (vector loads)")
     strict = {}
     with tb.Context(local, ctx_options(tb, ctas_per_subexec=1)) as c1:
         for se in (1, 4, 16, 32):
@@ -295,7 +298,7 @@ def run_reduce(args, tb, torch, ranks, local):
                 "traffic": profiled_traffic("reduce_3src_256MiB"),
                 "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": bytes_per_step,
-                "kernel": "k_reduce (3 sources, 32-byte vectors)"}
+                "kernel": kernel, "grid": info["grid"], "block_threads": info["block_threads"]}
     result = {"value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "e2e": e2e,
               "clocks": clocks, "gpu_launches": args.steps,
               "subexec_sweep": sweep, "strict_one_cta_per_subexec": strict,

@@ -138,71 +138,6 @@ constexpr int kStages = 3;
 constexpr uint32_t kBlock = 16384;                 // bytes per bulk copy
 constexpr size_t kBarBytes = 128;                  // mbarriers, then stages
 constexpr size_t kBatchSmem = kBarBytes + (size_t)kStages * kBlock;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase of the given parity, for at most kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs)
-            return false;
-    return true;
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t smem, uint64_t gsrc, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem),
-        "l"(gsrc), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(uint64_t gdst, uint32_t smem, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem),
-                 "r"(bytes)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Newest group may still be reading shared memory; all older ones are done.
-__device__ __forceinline__ void bulk_wait_read_all_but_newest()
-{
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 
 // Walks this CTA's chunks of the long-copy stream (chunks b, b + G, ...),
 // one piece (a contiguous part of one long copy) at a time.

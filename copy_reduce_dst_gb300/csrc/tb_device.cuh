@@ -87,5 +87,96 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// ---------------------------------------------------------------------------
+// Bulk (TMA) copies between global and shared memory: cp.async.bulk
+// global -> shared completes on an mbarrier; shared -> global is tracked by
+// bulk groups.  No tensor map, no cluster multicast.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs)
+            return false;
+    return true;
+}
+
+// Announces `bytes` of bulk-copy traffic on an mbarrier (this thread's
+// arrival); the copies that complete it are issued with bulk_copy_in.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_in(uint32_t smem, uint64_t gsrc, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem),
+        "l"(gsrc), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// One bulk copy global -> shared that alone completes the mbarrier's phase.
+__device__ __forceinline__ void bulk_load(uint32_t smem, uint64_t gsrc, uint32_t bytes, uint32_t bar)
+{
+    mbar_expect_tx(bar, bytes);
+    bulk_copy_in(smem, gsrc, bytes, bar);
+}
+
+__device__ __forceinline__ void bulk_store(uint64_t gdst, uint32_t smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Newest group may still be reading shared memory; all older ones are done.
+__device__ __forceinline__ void bulk_wait_read_all_but_newest()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Makes this thread's ordinary shared-memory writes visible to later bulk
+// copies (the async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 }  // namespace dev
 }  // namespace tb

@@ -63,6 +63,9 @@ struct tb_ctx {
     volatile uint32_t *gate_status = nullptr;
     uint32_t *gate_flag_dev = nullptr;
     uint32_t *gate_status_dev = nullptr;
+    // Host-mapped word the bulk reduce kernel sets if a bounded wait expired.
+    volatile uint32_t *reduce_status = nullptr;
+    uint32_t *reduce_status_dev = nullptr;
 
     std::vector<cudaEvent_t> events;  // timing events of tb_run_transfer
     std::vector<float> iter_ms;
@@ -191,6 +194,8 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "vec_bytes must be 0, 4, 16 or 32");
     if (o.unroll != 0 && o.unroll != 1 && o.unroll != 2 && o.unroll != 4)
         return fail(ctx, TB_EINVAL, "unroll must be 0, 1, 2 or 4");
+    if (o.reduce_engine < 0 || o.reduce_engine > 2)
+        return fail(ctx, TB_EINVAL, "reduce_engine must be 0, 1 or 2");
     return TB_OK;
 }
 
@@ -242,14 +247,19 @@ int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src,
 {
     const tb_options &o = ctx->opt;
     int rc = tb::plan_reduce(p, srcs, n_src, dst, num_bytes, num_subexec, o.ctas_per_subexec,
-                             o.block_threads, o.vec_bytes, o.unroll, o.memset_byte, ctx->num_sms);
+                             o.block_threads, o.vec_bytes, o.unroll, o.memset_byte, ctx->num_sms,
+                             o.reduce_engine);
+    p->status = ctx->reduce_status_dev;
     if (rc == TB_EINVAL)
         return fail(ctx, rc,
                     "reduce-copy arguments rejected (nSrc in [0,%d], numBytes %% 4 == 0, "
                     "4-byte aligned non-null pointers, numSubExec >= 0)",
                     TB_MAX_SRCS);
     if (rc != TB_OK)
-        return fail(ctx, rc, "vec_bytes=%d is not allowed by the pointers' alignment", o.vec_bytes);
+        return fail(ctx, rc,
+                    "vec_bytes=%d / reduce_engine=%d not possible for %d sources at these "
+                    "pointers' alignment",
+                    o.vec_bytes, o.reduce_engine, n_src);
     return TB_OK;
 }
 
@@ -386,6 +396,7 @@ void tb_options_default(tb_options *o)
     o->vec_bytes = 0;
     o->unroll = 0;
     o->time_kernels = 0;
+    o->reduce_engine = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -451,6 +462,7 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_VEC_BYTES", &o->vec_bytes, &bad);
     env_i32("TB_UNROLL", &o->unroll, &bad);
     env_i32("TB_TIME_KERNELS", &o->time_kernels, &bad);
+    env_i32("TB_REDUCE_ENGINE", &o->reduce_engine, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -524,17 +536,20 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
         return bail(TB_ECUDA);
 
     void *gate = nullptr;
-    if (cudaHostAlloc(&gate, 2 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess)
+    if (cudaHostAlloc(&gate, 4 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess)
         return bail(TB_ENOMEM);
     ctx->gate_flag = static_cast<volatile uint32_t *>(gate);
     ctx->gate_status = ctx->gate_flag + 1;
+    ctx->reduce_status = ctx->gate_flag + 2;
     ctx->gate_flag[0] = 0;
     ctx->gate_status[0] = 0;
+    ctx->reduce_status[0] = 0;
     void *dgate = nullptr;
     if (cudaHostGetDevicePointer(&dgate, gate, 0) != cudaSuccess)
         return bail(TB_ECUDA);
     ctx->gate_flag_dev = static_cast<uint32_t *>(dgate);
     ctx->gate_status_dev = ctx->gate_flag_dev + 1;
+    ctx->reduce_status_dev = ctx->gate_flag_dev + 2;
 
     ctx->batch_grid = ctx->num_sms * tb::batch_ctas_per_sm();
     ctx->slots.resize(o.num_slots);
@@ -721,6 +736,31 @@ int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int n_src, void *dst, u
     return TB_OK;
 }
 
+int tb_reduce_plan(tb_ctx *ctx, const void *const *srcs, int n_src, const void *dst,
+                   uint64_t num_bytes, int num_subexec, tb_launch_info *out)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if (!out)
+        return fail(ctx, TB_EINVAL, "reduce_plan: null output");
+    DeviceScope scope(ctx->device);
+    tb::ReducePlan p;
+    int rc = plan_for(ctx, &p, srcs, n_src, const_cast<void *>(dst), num_bytes, num_subexec);
+    if (rc != TB_OK)
+        return rc;
+    out->engine = p.engine;
+    out->vec_bytes = p.vec_bytes;
+    out->unroll = p.unroll;
+    out->block_threads = p.block_threads;
+    out->grid = p.grid;
+    out->num_subexec = p.num_subexec;
+    out->head_elems = p.head;
+    out->body_vectors = p.nvec;
+    out->tail_elems = p.n - p.head - p.nvec * ((uint64_t)p.vec_bytes / 4);
+    out->smem_bytes = p.smem_bytes;
+    return TB_OK;
+}
+
 int tb_reduce_copy_host(tb_ctx *ctx, const void *const *host_srcs, int n_src, void *host_dst,
                         uint64_t num_bytes, void *const *dev_srcs, void *dev_dst, int num_subexec,
                         tb_stream stream)
@@ -884,6 +924,10 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     if (gated && ctx->gate_status[0] != 1u)
         return fail(ctx, TB_ETIMEOUT, "gate kernel was not released within %llu ns",
                     (unsigned long long)o.wait_timeout_ns);
+    if (ctx->reduce_status[0] != 0u) {
+        ctx->reduce_status[0] = 0u;
+        return fail(ctx, TB_ETIMEOUT, "a bounded wait inside the reduce-copy kernel expired");
+    }
 
     const int done = first_err != TB_OK ? out->iters : iters;
     double total = 0.0;
@@ -902,6 +946,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     out->ctas = plan.grid;
     out->block_threads = plan.block_threads;
     out->gated = gated ? 1 : 0;
+    out->engine = plan.engine;
     out->total_ms = total;
     if (done > 0) {
         std::vector<float> v(ctx->iter_ms.begin(), ctx->iter_ms.begin() + done);

@@ -31,16 +31,20 @@ struct ReducePlan {
     int grid;              // CTAs of the launch (>= num_subexec)
     int block_threads;
     int unroll;            // vectors per source a thread holds in flight
+    int engine;            // 1 = vector loads, 2 = bulk copies through shared memory
+    size_t smem_bytes;     // dynamic shared memory of the launch
     uint32_t memset_word;  // 0-source fill, the memset byte repeated
+    uint32_t *status;      // nullable, device-visible: 1 if a bounded wait expired
 };
 
-// Picks vector width, head/tail, sub-executor split, grid and unroll for one
-// launch.  num_subexec, ctas_per_subexec, block_threads, vec_bytes and unroll
-// of 0 take the defaults.  Returns TB_OK, TB_EINVAL or TB_ENOTSUP (a forced
-// vector width the pointers' alignment does not allow).
+// Picks engine, vector width, head/tail, sub-executor split, grid and unroll
+// for one launch.  num_subexec, ctas_per_subexec, block_threads, vec_bytes,
+// unroll and engine of 0 take the defaults.  Returns TB_OK, TB_EINVAL or
+// TB_ENOTSUP (a forced vector width or engine the sources or the pointers'
+// alignment do not allow).
 int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
                 int num_subexec, int ctas_per_subexec, int block_threads, int vec_bytes, int unroll,
-                uint32_t memset_byte, int num_sms);
+                uint32_t memset_byte, int num_sms, int engine);
 
 // Launches the plan on `stream` (asynchronous).
 cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream);

@@ -31,6 +31,7 @@ struct ReduceArgs {
     uint64_t nvec;
     uint32_t nsub;         // sub-executors; never more than the grid's CTAs
     uint32_t memset_word;
+    uint32_t *status;      // nullable: set to 1 if a bounded wait expired
 };
 
 // The CTAs of a launch are dealt to the sub-executors as evenly as integers
@@ -184,6 +185,159 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
         one(tail0 + tid);
 }
 
+// ---------------------------------------------------------------------------
+// K1, bulk form (1 to 4 sources, every pointer sharing its address modulo
+// 16).  The body is cut into tiles of kTile bytes per source.  Thread 0
+// streams each tile's N source pieces into one of kRStages shared-memory
+// stages with bulk copies (one mbarrier per stage); all threads add the
+// pieces in place, left to right with __fadd_rn, into the stage's first
+// buffer; after a proxy fence and a barrier, thread 0 writes that buffer out
+// with a bulk copy and refills the previous stage.  With one source the
+// tiles go straight from the load to the store (a bit copy).
+// ---------------------------------------------------------------------------
+constexpr int kRStages = 3;
+constexpr uint32_t kTile = 8192;
+constexpr uint32_t kTileVecs = kTile / 16;
+constexpr int kBulkThreads = 256;
+
+template <int N>
+constexpr size_t bulk_smem_bytes()
+{
+    return 128 + (size_t)kRStages * N * kTile;
+}
+
+template <int N>
+__global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t tid = threadIdx.x;
+    const SubRange sr = sub_range(a.nvec, a.nsub);
+    const uint64_t span = sr.vend > sr.vbeg ? sr.vend - sr.vbeg : 0;
+    const uint64_t ntiles = (span + kTileVecs - 1) / kTileVecs;
+    const uint64_t mine = ntiles > sr.part ? (ntiles - sr.part + sr.nparts - 1) / sr.nparts : 0;
+    const uint32_t bars = smem_u32(smem);
+    const uint32_t stages = smem_u32(smem + 128);
+    const uint64_t sbase = (uint64_t)(a.head) * 4;
+
+    // Tile j of this CTA: first body vector and vector count.
+    auto tile = [&](uint64_t j, uint64_t &v0, uint32_t &nv) {
+        v0 = sr.vbeg + (sr.part + j * sr.nparts) * kTileVecs;
+        const uint64_t left = sr.vend - v0;
+        nv = (uint32_t)(left < kTileVecs ? left : kTileVecs);
+    };
+    auto issue = [&](uint64_t j) {
+        uint64_t v0;
+        uint32_t nv;
+        tile(j, v0, nv);
+        const uint32_t s = (uint32_t)(j % kRStages);
+        const uint32_t bar = bars + 8 * s;
+        mbar_expect_tx(bar, N * nv * 16);
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+            bulk_copy_in(stages + (s * N + k) * kTile,
+                         reinterpret_cast<uint64_t>(a.src[k]) + sbase + v0 * 16, nv * 16, bar);
+    };
+
+    if (mine > 0) {
+        if (tid == 0) {
+            for (int s = 0; s < kRStages; ++s)
+                mbar_init(bars + 8 * s);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            for (uint64_t j = 0; j < mine && j < (uint64_t)kRStages; ++j)
+                issue(j);
+        }
+        __syncthreads();
+        for (uint64_t j = 0; j < mine; ++j) {
+            const uint32_t s = (uint32_t)(j % kRStages);
+            const uint32_t parity = (uint32_t)((j / kRStages) & 1);
+            uint64_t v0;
+            uint32_t nv;
+            tile(j, v0, nv);
+            bool expired = false;
+            if (N > 1 || tid == 0) {
+                expired = !mbar_wait_bounded(bars + 8 * s, parity);
+                if (N > 1 && !expired) {
+                    const uint32_t out = stages + s * N * kTile;
+                    for (uint32_t v = tid; v < nv; v += kBulkThreads) {
+                        Vec<16> acc, x;
+                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(acc.w[0]), "=r"(acc.w[1]), "=r"(acc.w[2]), "=r"(acc.w[3])
+                                     : "r"(out + v * 16));
+#pragma unroll
+                        for (int k = 1; k < N; ++k) {
+                            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(x.w[0]), "=r"(x.w[1]), "=r"(x.w[2]), "=r"(x.w[3])
+                                         : "r"(out + k * kTile + v * 16));
+                            vadd<16>(acc, x);
+                        }
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(out + v * 16),
+                                     "r"(acc.w[0]), "r"(acc.w[1]), "r"(acc.w[2]), "r"(acc.w[3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            if (N > 1)
+                expired = __syncthreads_or(expired);
+            if (expired) {
+                if (tid == 0) {
+                    if (a.status)
+                        *reinterpret_cast<volatile uint32_t *>(a.status) = 1u;
+                    // Let the loads already issued land (each wait bounded again).
+                    for (uint64_t m = j; m < mine && m < j + kRStages; ++m)
+                        mbar_wait_bounded(bars + 8 * (uint32_t)(m % kRStages),
+                                          (uint32_t)((m / kRStages) & 1));
+                    bulk_wait_all();
+                }
+                return;
+            }
+            if (tid == 0) {
+                bulk_store(reinterpret_cast<uint64_t>(a.dst) + sbase + v0 * 16,
+                           stages + s * N * kTile, nv * 16);
+                if (j >= 1 && j - 1 + kRStages < mine) {
+                    bulk_wait_read_all_but_newest();
+                    issue(j - 1 + kRStages);
+                }
+            }
+        }
+        if (tid == 0)
+            bulk_wait_all();
+    }
+
+    if (blockIdx.x == 0 && tid < a.head)
+        reduce_one<N>(a, tid);
+    const uint64_t tail0 = a.head + a.nvec * 4;
+    if (blockIdx.x == gridDim.x - 1 && tail0 + tid < a.n)
+        reduce_one<N>(a, tail0 + tid);
+}
+
+using BulkKernel = void (*)(const ReduceArgs);
+
+BulkKernel pick_bulk(int n_src, size_t *smem)
+{
+    switch (n_src) {
+    case 1: *smem = bulk_smem_bytes<1>(); return k_reduce_bulk<1>;
+    case 2: *smem = bulk_smem_bytes<2>(); return k_reduce_bulk<2>;
+    case 3: *smem = bulk_smem_bytes<3>(); return k_reduce_bulk<3>;
+    case 4: *smem = bulk_smem_bytes<4>(); return k_reduce_bulk<4>;
+    default: *smem = 0; return nullptr;
+    }
+}
+
+// Shared memory above 48 KiB must be allowed per kernel before its launch.
+bool bulk_kernel_setup(int n_src)
+{
+    static bool done[5] = {};
+    size_t smem = 0;
+    BulkKernel k = pick_bulk(n_src, &smem);
+    if (!k)
+        return false;
+    if (!done[n_src])
+        done[n_src] = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem) == cudaSuccess;
+    return done[n_src];
+}
+
 using ReduceKernel = void (*)(const ReduceArgs);
 
 template <int N, int VB>
@@ -248,6 +402,18 @@ int default_unroll(int n_src, int vb)
 
 }  // namespace
 
+static int bulk_ctas_per_sm(int n_src)
+{
+    size_t smem = 0;
+    BulkKernel k = pick_bulk(n_src, &smem);
+    int blocks = 0;
+    if (!k || !bulk_kernel_setup(n_src) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kBulkThreads, smem) != cudaSuccess ||
+        blocks < 1)
+        blocks = 1;
+    return blocks;
+}
+
 int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll)
 {
     void *fn = n_src <= 8 ? (void *)pick_reduce(n_src, vec_bytes, unroll)
@@ -261,8 +427,10 @@ int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll)
 
 int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
                 int num_subexec, int ctas_per_subexec, int block_threads, int vec_bytes, int unroll,
-                uint32_t memset_byte, int num_sms)
+                uint32_t memset_byte, int num_sms, int engine)
 {
+    if (engine < 0 || engine > 2)
+        return TB_EINVAL;
     if (!p || !dst || n_src < 0 || n_src > TB_MAX_SRCS || num_bytes % 4 != 0 || num_subexec < 0 ||
         ctas_per_subexec < 0 || block_threads < 0 || block_threads > 512 || block_threads % 32 != 0 ||
         unroll < 0 || unroll > 4 || unroll == 3 || num_sms < 1 ||
@@ -311,6 +479,18 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     }
     p->vec_bytes = vb;
 
+    // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
+    // and works in 16-byte units; when it applies it is the default (it keeps
+    // more bytes in flight per SM than per-thread vector loads can).
+    const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
+    if (engine == 2 && !bulk_ok)
+        return TB_ENOTSUP;
+    p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0)) ? 2 : 1;
+    if (p->engine == 2) {
+        vb = 16;
+        p->vec_bytes = 16;
+    }
+
     if (vb > 4) {
         const uintptr_t mis = (uintptr_t)dst & (uintptr_t)(vb - 1);
         const uint64_t head = mis ? ((uint64_t)vb - mis) / 4 : 0;
@@ -323,7 +503,12 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
     // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
     // sub-executor); never fewer CTAs than sub-executors.
-    const int per_sm = reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
+    if (p->engine == 2) {
+        p->block_threads = kBulkThreads;
+        pick_bulk(n_src, &p->smem_bytes);
+    }
+    const int per_sm = p->engine == 2 ? bulk_ctas_per_sm(n_src)
+                                      : reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
     const int64_t full = (int64_t)num_sms * per_sm;
     const int64_t S = num_subexec > 0 ? num_subexec : full;
     const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, full);
@@ -345,10 +530,17 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.nvec = p.nvec;
     a.nsub = (uint32_t)p.num_subexec;
     a.memset_word = p.memset_word;
+    a.status = p.status;
     const unsigned grid = (unsigned)p.grid;
     if (p.n == 0)
         return cudaSuccess;
-    if (p.n_src > 8) {
+    if (p.engine == 2) {
+        size_t smem = 0;
+        BulkKernel k = pick_bulk(p.n_src, &smem);
+        if (!k || !bulk_kernel_setup(p.n_src))
+            return cudaErrorInvalidValue;
+        k<<<grid, kBulkThreads, smem, stream>>>(a);
+    } else if (p.n_src > 8) {
         if (p.vec_bytes == 16)
             k_reduce_many<16><<<grid, p.block_threads, 0, stream>>>(a, p.n_src);
         else

@@ -59,6 +59,7 @@ class Options(ct.Structure):
         ("vec_bytes", _i32),
         ("unroll", _i32),
         ("time_kernels", _i32),
+        ("reduce_engine", _i32),
     ]
 
 
@@ -83,6 +84,7 @@ class Result(ct.Structure):
         ("ctas", _i32),
         ("block_threads", _i32),
         ("gated", _i32),
+        ("engine", _i32),
         ("validated", _i32),
         ("total_ms", ct.c_double),
         ("mean_ms", ct.c_double),
@@ -94,6 +96,21 @@ class Result(ct.Structure):
         ("mismatch_index", _i64),
         ("mismatch_expected", _u32),
         ("mismatch_actual", _u32),
+    ]
+
+
+class LaunchInfo(ct.Structure):
+    _fields_ = [
+        ("engine", _i32),
+        ("vec_bytes", _i32),
+        ("unroll", _i32),
+        ("block_threads", _i32),
+        ("grid", _i32),
+        ("num_subexec", _i32),
+        ("head_elems", _u64),
+        ("body_vectors", _u64),
+        ("tail_elems", _u64),
+        ("smem_bytes", _u64),
     ]
 
 
@@ -152,6 +169,7 @@ _sig("tb_upload_sources", ct.c_int, _vp, _P(_vp), _P(_vp), ct.c_int, _u64)
 _sig("tb_prepare_sources", ct.c_int, _vp, _P(_vp), ct.c_int, _u64, _u64)
 _sig("tb_prep_h2d_bytes", _u64, _vp)
 _sig("tb_reduce_copy", ct.c_int, _vp, _P(_vp), ct.c_int, _vp, _u64, ct.c_int, _vp)
+_sig("tb_reduce_plan", ct.c_int, _vp, _P(_vp), ct.c_int, _vp, _u64, ct.c_int, _P(LaunchInfo))
 _sig("tb_run_transfer_ex", ct.c_int, _vp, _P(Transfer), _P(Result))
 _sig("tb_run_transfer", ct.c_int, _vp, _P(_vp), ct.c_int, _vp, _u64, ct.c_int, ct.c_int, _u64,
      _P(Result))
@@ -337,6 +355,13 @@ class Context:
     def reduce_copy(self, srcs, dst, num_bytes: int, num_subexec: int = 0, stream=None):
         self._ok(lib.tb_reduce_copy(self._h, _ptr_array(srcs), len(srcs), addr(dst), num_bytes,
                                     num_subexec, stream_handle(stream)), "tb_reduce_copy")
+
+    def reduce_plan(self, srcs, dst, num_bytes: int, num_subexec: int = 0) -> dict:
+        """The launch tb_reduce_copy would make (tb_reduce_plan), as a dict."""
+        info = LaunchInfo()
+        self._ok(lib.tb_reduce_plan(self._h, _ptr_array(srcs), len(srcs), addr(dst), num_bytes,
+                                    num_subexec, ct.byref(info)), "tb_reduce_plan")
+        return {name: getattr(info, name) for name, _ in LaunchInfo._fields_}
 
     def run_transfer(self, srcs, dst, num_bytes: int, num_subexec: int = 0, iters: int = 1,
                      rotate_bytes: int | None = None, expected=None) -> dict:

@@ -121,6 +121,12 @@ typedef struct {
     /* 1 = bracket every batched-copy kernel with CUDA events so that
        tb_last_batch_kernel_ms can report its device time.  Default 0. */
     int32_t time_kernels;
+    /* Reduce-copy engine: 1 = vector loads and stores by every thread;
+       2 = bulk copies (cp.async.bulk) through shared-memory stages with the
+       adds done in shared memory (1 to 4 sources sharing a 16-byte
+       alignment, else TB_ENOTSUP); 0 = the library's choice: 2 where it
+       applies (and vec_bytes is 0), else 1.  Default 0. */
+    int32_t reduce_engine;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -131,7 +137,7 @@ void tb_options_default(tb_options *opt);
      TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
      TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
-     TB_TIME_KERNELS.
+     TB_TIME_KERNELS, TB_REDUCE_ENGINE.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);
@@ -259,6 +265,25 @@ uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
 int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int nSrc, void *dst,
                    uint64_t numBytes, int numSubExec, tb_stream stream);
 
+/* The launch tb_reduce_copy makes for given arguments. */
+typedef struct {
+    int32_t engine;           /* 1 = vector loads, 2 = bulk copies via shared memory */
+    int32_t vec_bytes;        /* bytes per vector access: 32, 16 or 4 */
+    int32_t unroll;           /* vectors per source in flight per thread (engine 1) */
+    int32_t block_threads;    /* threads per CTA */
+    int32_t grid;             /* CTAs */
+    int32_t num_subexec;      /* sub-executors */
+    uint64_t head_elems;      /* scalar elements before the vector body */
+    uint64_t body_vectors;    /* vectors of vec_bytes in the body */
+    uint64_t tail_elems;      /* scalar elements after it */
+    uint64_t smem_bytes;      /* dynamic shared memory per CTA */
+} tb_launch_info;
+
+/* Describes, without launching, the launch tb_reduce_copy would make for
+   these arguments (same checks and errors). */
+int tb_reduce_plan(tb_ctx *ctx, const void *const *srcs, int nSrc, const void *dst,
+                   uint64_t numBytes, int numSubExec, tb_launch_info *out);
+
 typedef struct {
     uint64_t K;               /* slices per source */
     uint64_t slice_stride;    /* bytes between slices */
@@ -269,6 +294,7 @@ typedef struct {
     int32_t  ctas;            /* CTAs per launch */
     int32_t  block_threads;   /* threads per CTA */
     int32_t  gated;           /* 1 if the iterations ran behind the gate */
+    int32_t  engine;          /* reduce-copy engine used (see tb_launch_info) */
     int32_t  validated;       /* 1 if dst was compared with expected bytes */
     double   total_ms;        /* device time of all timed iterations */
     double   mean_ms, median_ms, min_ms, max_ms;

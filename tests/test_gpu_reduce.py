@@ -125,6 +125,49 @@ def test_reduce_parity_kernel_shapes(tb, vec, unroll, threads, nsrc):
         reduce_and_compare(tb, c, srcs, num_subexec=7)
 
 
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4])
+@pytest.mark.parametrize("n,offs,subexec", [
+    (5, 0, 0), (2048, 0, 1), (2048 * 7 + 3, 4, 3), (1000003, 20, 0), (262144 * 3 + 17, 16, 32),
+    (65536, 12, 1000)])
+def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
+    """The bulk engine (shared-memory stages filled and drained by bulk
+    copies) against the oracle: heads, ragged tails, tile edges and
+    sub-executor splits."""
+    g = np.random.default_rng(nsrc * 1000 + n % 1000 + offs)
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    with tb.Context(0, tb.options(reduce_engine=2)) as c:
+        reduce_and_compare(tb, c, srcs, byte_offsets=[offs] * nsrc, dst_offset=offs,
+                           num_subexec=subexec)
+
+
+def test_reduce_plan_engine_choice(tb, ctx):
+    d = dev_bytes(1 << 20)
+    p = d.data_ptr()
+    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, 4096)
+    assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
+    info = ctx.reduce_plan([p] * 5, p + 65536, 4096)
+    assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
+    info = ctx.reduce_plan([p + 4, p + 8], p + 65536, 4096)
+    assert info["engine"] == 1 and info["vec_bytes"] == 4        # no common alignment
+    info = ctx.reduce_plan([p + 4, p + 4100], p + 65540, 4096)
+    assert info["engine"] == 2 and info["head_elems"] == 3       # head to 16 bytes
+    assert info["head_elems"] + 4 * info["body_vectors"] + info["tail_elems"] == 1024
+    with tb.Context(0, tb.options(vec_bytes=32)) as c:
+        info = c.reduce_plan([p], p + 65536, 4096)
+        assert info["engine"] == 1 and info["vec_bytes"] == 32
+
+
+def test_bulk_engine_limits(tb):
+    d = dev_bytes(1 << 16)
+    with tb.Context(0, tb.options(reduce_engine=2)) as c:
+        with pytest.raises(tb.TBError) as e:
+            c.reduce_copy([d.data_ptr()] * 5, d.data_ptr(), 256)           # 5 sources
+        assert e.value.code == tb.TB_ENOTSUP
+        with pytest.raises(tb.TBError) as e:
+            c.reduce_copy([d.data_ptr() + 4], d.data_ptr() + 8192, 256)   # no common 16 B
+        assert e.value.code == tb.TB_ENOTSUP
+
+
 @pytest.mark.parametrize("byte", [0x00, 0xA5])
 def test_zero_sources_is_memset(tb, byte):
     with tb.Context(0, tb.options(memset_byte=byte)) as c:
@@ -353,14 +396,16 @@ def test_reduce_copy_host_end_to_end(tb, ctx):
 # ---------------------------------------------------------------------------
 # Full-size workloads, in the launch configuration the bench times
 # ---------------------------------------------------------------------------
-def test_three_source_256mib_all_subexecutors(tb):
+@pytest.mark.parametrize("engine", [0, 1, 2])
+def test_three_source_256mib_all_subexecutors(tb, engine):
     """3 x 256 MiB, src_k = PrepSrcValue(k, i), K = 1; sub-executor counts
-    1, 4, 16, 32 and auto.  dst = 6 * PrepSrcValue(0, i) exactly."""
+    1, 4, 16, 32 and auto, with each reduce engine.  dst = 6 *
+    PrepSrcValue(0, i) exactly."""
     nb = 256 * MiB
     n = nb // 4
     refs = [oracle.prepare_reference(n, k) for k in range(3)]
     exp = oracle.dst_reference(refs)
-    with tb.Context(0) as c:
+    with tb.Context(0, tb.options(reduce_engine=engine)) as c:
         srcs = [dev_bytes(nb) for _ in range(3)]
         for k, s in enumerate(srcs):
             c.fill_source(s, nb, tb.default_pattern(), k)
