@@ -21,7 +21,8 @@ Default line (rank 0 prints one JSON object):
 benchmark) on the same metric.  Under torchrun every rank runs its own
 replica on its own GPU (no data exchange); timings are the max over ranks.
 ``--study`` prints extra lines (single 4 MiB transfer, the fillCompress
-sweep with rotation on and off, cold and warm) instead of the default line.
+sweep with rotation on and off, cold and warm, and the batch split into its
+long and short copies) instead of the default line.
 """
 from __future__ import annotations
 
@@ -490,6 +491,36 @@ def study(args, tb, torch, local):
                 row[f"{tag}_K"] = plan.K
                 del src, dst
             print(json.dumps(row), flush=True)
+    del flush
+    study_batch_phases(tb, torch, local)
+
+
+def study_batch_phases(tb, torch, local):
+    """Kernel time of the 47,540 batch and of its parts: the 20 long copies
+    alone, the 47,520 short copies alone, and one 1 GiB copy (median of 10
+    launches after 3, kernel-only events)."""
+    import statistics as st
+    from copy_reduce_dst_gb300 import workloads
+    layout = workloads.batch_head_sliced()
+    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    long_ = desc[:, 2] > 16384
+    one = desc[:1].copy()
+    one[0] = (src.data_ptr(), dst.data_ptr(), GiB)
+    with tb.Context(local, ctx_options(tb, time_kernels=1)) as ctx:
+        for name, d in (("all 47,540", desc), ("20 long copies", desc[long_]),
+                        ("47,520 short copies", desc[~long_]), ("one 1 GiB copy", one)):
+            for _ in range(3):
+                ctx.batch_copy(d)
+            ms = []
+            for _ in range(10):
+                ctx.batch_copy(d)
+                ms.append(ctx.last_batch_kernel_ms())
+            k = st.median(ms)
+            moved = 2 * int(d[:, 2].sum())
+            print(json.dumps({"study": "batch phases", "part": name, "kernel_us": round(k * 1e3, 1),
+                              "gbps": round(moved / (k / 1e3) / 1e9, 1)}), flush=True)
 
 
 # ---------------------------------------------------------------------------
