@@ -119,7 +119,8 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem *p)
 }
 
 struct BatchArgs {
-    const WorkItem *shorts;      // n_short copies, longest first
+    uint32_t *claim;             // work counter of the short copies (starts at 0)
+    const WorkItem *shorts;      // n_short copies
     const WorkItem *longs;       // n_long copies
     const uint64_t *prefix;      // stream offset of each long copy
     const uint32_t *chunk_desc;  // long copy holding each chunk's first byte
@@ -283,24 +284,25 @@ __device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
     }
 }
 
+// Short copies claimed per atomic: a warp takes kClaim items at a time.
+constexpr uint32_t kClaim = 2;
+
 // Persistent grid of one wave.
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
 //   owns chunks b, b + G, ... (the same number for every CTA, the grid
 //   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned
 //   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
 //   the leftover edges.
-//   Short copies (longest first in memory) go to warps 1.. (all warps when
-//   there are no long copies), dealt in boustrophedon order: round r goes up
-//   the warp list when r is even and down when it is odd, which keeps every
-//   warp's byte total close to the mean.  Odd warps walk their rounds from
-//   the smallest item up, so small latency-bound copies overlap large ones.
-//   Each warp fetches its next item before copying the current one.
+//   Short copies: every warp (warp 0 once its pipeline has drained) claims
+//   kClaim items at a time from a counter in global memory, and claims the
+//   next ones before copying the current ones, so the claim's latency
+//   overlaps the copy; whichever warp is free takes the next items, which
+//   balances the work without any ordering on the host.
 __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const bool has_long = a.chunks > 0;
-    if (has_long) {
+    if (a.chunks > 0) {
         if (threadIdx.x == 0) {
             for (int s = 0; s < kStages; ++s)
                 mbar_init(smem_u32(smem) + 8 * s);
@@ -310,43 +312,32 @@ __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
         if (warp == 0) {
             if (lane == 0)
                 bulk_pipeline(a, smem_u32(smem), smem_u32(smem + kBarBytes));
-            return;
+            __syncwarp();
+        } else {
+            long_edges(a, threadIdx.x - 32, blockDim.x - 32);
         }
-        long_edges(a, threadIdx.x - 32, blockDim.x - 32);
     }
 
-    const uint32_t w0 = has_long ? 1u : 0u;
-    const uint32_t warps_per_cta = (blockDim.x >> 5) - w0;
-    const uint64_t W = (uint64_t)gridDim.x * warps_per_cta;
-    const uint64_t wid = (uint64_t)blockIdx.x * warps_per_cta + (warp - w0);
-    const uint64_t n_short = a.n_short;
-    const uint64_t R = (n_short + W - 1) / W;
-    const bool reverse = wid & 1u;
-    // The k-th item this warp copies (k in [0, R)), or n_short if none.
-    auto item_at = [&](uint64_t k) {
-        const uint64_t r = reverse ? (R - 1 - k) : k;
-        return r * W + ((r & 1) ? (W - 1 - wid) : wid);
-    };
-    uint64_t k = 0;
-    while (k < R && item_at(k) >= n_short)
-        ++k;
-    if (k >= R)
-        return;
-    WorkItem cur = load_item(a.shorts + item_at(k));
-    for (;;) {
-        uint64_t kn = k + 1;
-        while (kn < R && item_at(kn) >= n_short)
-            ++kn;
-        const bool more = kn < R;
-        WorkItem nxt = cur;
-        if (more)
-            nxt = load_item(a.shorts + item_at(kn));
-        copy_range(reinterpret_cast<uint8_t *>(cur.dst), reinterpret_cast<const uint8_t *>(cur.src),
-                   cur.len, lane, 32u);
-        if (!more)
-            break;
-        cur = nxt;
-        k = kn;
+    const uint32_t n_short = a.n_short;
+    uint32_t base = 0;
+    if (lane == 0)
+        base = atomicAdd(a.claim, kClaim);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    while (base < n_short) {
+        uint32_t next = 0;
+        if (lane == 0)
+            next = atomicAdd(a.claim, kClaim);
+        WorkItem it[kClaim];
+#pragma unroll
+        for (uint32_t q = 0; q < kClaim; ++q)
+            if (base + q < n_short)
+                it[q] = load_item(a.shorts + base + q);
+#pragma unroll
+        for (uint32_t q = 0; q < kClaim; ++q)
+            if (base + q < n_short)
+                copy_range(reinterpret_cast<uint8_t *>(it[q].dst),
+                           reinterpret_cast<const uint8_t *>(it[q].src), it[q].len, lane, 32u);
+        base = __shfl_sync(0xffffffffu, next, 0);
     }
 }
 
@@ -385,9 +376,10 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
         return cudaSuccess;
     if (!batch_kernel_setup())
         return cudaErrorInvalidValue;
-    const char *base = static_cast<const char *>(dev);
+    char *base = static_cast<char *>(const_cast<void *>(dev));
     BatchArgs a;
-    a.shorts = reinterpret_cast<const WorkItem *>(base);
+    a.claim = reinterpret_cast<uint32_t *>(base);
+    a.shorts = reinterpret_cast<const WorkItem *>(base + kBatchHeader);
     a.longs = a.shorts + plan.n_short;
     a.prefix = reinterpret_cast<const uint64_t *>(base + plan.prefix_offset);
     a.chunk_desc = reinterpret_cast<const uint32_t *>(base + plan.chunk_offset);

@@ -1,5 +1,6 @@
-// Source-pattern fill kernels ("TransferBench data validation", "Expected
-// source pattern") and the timing gate of libtb.
+// Small kernels of libtb: the source-pattern fills ("TransferBench data
+// validation", "Expected source pattern"), the device-side compare of
+// validation (its validateDirect option), and the timing gate.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -124,7 +125,71 @@ __global__ void k_gate(const volatile uint32_t *flag, volatile uint32_t *status,
 }
 
 
+// Device-side compare: the smallest byte index where a and b differ goes to
+// *first (which starts at UINT64_MAX).  16-byte vectors when both pointers
+// share their address modulo 16 (after a byte head), bytes otherwise.  A CTA
+// stops early once a smaller index than its next position is known.
+__device__ __forceinline__ uint32_t first_diff_byte(uint4 x, uint4 y)
+{
+    const uint32_t w[4] = {x.x ^ y.x, x.y ^ y.y, x.z ^ y.z, x.w ^ y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (w[i])
+            return 4 * i + (__ffs(w[i]) - 1) / 8;
+    return 16;
+}
+
+__global__ void k_compare(const uint8_t *a, const uint8_t *b, uint64_t n,
+                          unsigned long long *first)
+{
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t head = (16u - ((uintptr_t)a & 15u)) & 15u;
+    if (head > n)
+        head = n;
+    const bool vec = (((uintptr_t)a ^ (uintptr_t)b) & 15u) == 0;
+    if (!vec)
+        head = n;
+    for (uint64_t i = tid; i < head; i += stride)
+        if (a[i] != b[i])
+            atomicMin(first, (unsigned long long)i);
+    if (!vec)
+        return;
+    const uint4 *va = reinterpret_cast<const uint4 *>(a + head);
+    const uint4 *vb = reinterpret_cast<const uint4 *>(b + head);
+    const uint64_t nv = (n - head) / 16;
+    for (uint64_t v = tid, it = 0; v < nv; v += stride, ++it) {
+        // Every 64 steps: stop once a difference before this position is known.
+        if ((it & 63u) == 0 &&
+            *reinterpret_cast<volatile unsigned long long *>(first) < head + v * 16)
+            break;
+        const uint4 x = __ldcs(va + v), y = __ldcs(vb + v);
+        const uint32_t d = first_diff_byte(x, y);
+        if (d < 16)
+            atomicMin(first, (unsigned long long)(head + v * 16 + d));
+    }
+    const uint64_t t0 = head + nv * 16;
+    for (uint64_t i = t0 + tid; i < n; i += stride)
+        if (a[i] != b[i])
+            atomicMin(first, (unsigned long long)i);
+}
+
 }  // namespace
+
+cudaError_t launch_compare(const void *a, const void *b, uint64_t n, unsigned long long *first,
+                           int num_sms, cudaStream_t stream)
+{
+    if (cudaMemsetAsync(first, 0xFF, sizeof(*first), stream) != cudaSuccess)
+        return cudaGetLastError();
+    if (n == 0)
+        return cudaSuccess;
+    const int threads = 512;
+    const uint64_t want = (n / 16 + threads - 1) / threads + 1;
+    const unsigned grid = (unsigned)std::min<uint64_t>(want, (uint64_t)num_sms * 4);
+    k_compare<<<grid, threads, 0, stream>>>(static_cast<const uint8_t *>(a),
+                                             static_cast<const uint8_t *>(b), n, first);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fill_source(float *dst, uint64_t n, const tb_pattern &pat, int buffer_idx,
                                int num_sms, cudaStream_t stream)

@@ -74,13 +74,16 @@ struct tb_ctx {
     void *slot_status = nullptr;      // host-mapped status words, one per slot
     uint32_t next_slot = 0;
     int batch_grid = 0;               // one wave of batch-kernel CTAs
-    std::vector<uint32_t> bucket;     // counting-sort buckets
+    std::vector<WorkItem> longs;      // long copies of the run being packed
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
 
     Pipeline pipe;                    // staged host <-> device transfers
+    cudaStream_t ce = nullptr;        // copy-engine stream of routed batch copies
+    cudaEvent_t ce_fork = nullptr, ce_join = nullptr;
 
     void *val_stage = nullptr;        // pinned validation staging
+    unsigned long long *first_diff = nullptr;  // device word of the device-side compare
     uint64_t prep_h2d = 0;
     std::string err;
 };
@@ -350,6 +353,39 @@ int validate_impl(tb_ctx *ctx, const void *dev, const void *expected, uint64_t n
     return TB_OK;
 }
 
+// Device-side compare of two device ranges on ctx's stream (synchronous).
+int validate_device_impl(tb_ctx *ctx, const void *dev, const void *expected_dev, uint64_t num_bytes,
+                         uint32_t elem, tb_mismatch *out)
+{
+    if (out) {
+        out->index = -1;
+        out->expected = out->actual = 0;
+    }
+    if (!ctx->first_diff)
+        TB_CUDA(ctx, cudaMalloc(&ctx->first_diff, sizeof(unsigned long long)));
+    TB_CUDA(ctx, tb::launch_compare(dev, expected_dev, num_bytes, ctx->first_diff, ctx->num_sms,
+                                    ctx->stream));
+    unsigned long long first = 0;
+    TB_CUDA(ctx, cudaMemcpyAsync(&first, ctx->first_diff, sizeof first, cudaMemcpyDeviceToHost,
+                                 ctx->stream));
+    TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    if (first == ~0ull)
+        return TB_OK;
+    const uint64_t idx = first / elem;
+    if (out) {
+        uint32_t act = 0, exp = 0;
+        TB_CUDA(ctx, cudaMemcpy(&act, static_cast<const char *>(dev) + idx * elem, elem,
+                                cudaMemcpyDeviceToHost));
+        TB_CUDA(ctx, cudaMemcpy(&exp, static_cast<const char *>(expected_dev) + idx * elem, elem,
+                                cudaMemcpyDeviceToHost));
+        out->index = (int64_t)idx;
+        out->expected = exp;
+        out->actual = act;
+    }
+    return fail(ctx, TB_EVALIDATE, "destination differs from expected at element %llu",
+                (unsigned long long)idx);
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -397,6 +433,7 @@ void tb_options_default(tb_options *o)
     o->unroll = 0;
     o->time_kernels = 0;
     o->reduce_engine = 0;
+    o->ce_min_bytes = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -463,6 +500,7 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_UNROLL", &o->unroll, &bad);
     env_i32("TB_TIME_KERNELS", &o->time_kernels, &bad);
     env_i32("TB_REDUCE_ENGINE", &o->reduce_engine, &bad);
+    env_u64("TB_CE_MIN_BYTES", &o->ce_min_bytes, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -605,6 +643,13 @@ void tb_destroy(tb_ctx *ctx)
     }
     for (cudaEvent_t e : ctx->events)
         cudaEventDestroy(e);
+    if (ctx->ce) {
+        cudaStreamSynchronize(ctx->ce);
+        cudaStreamDestroy(ctx->ce);
+    }
+    for (cudaEvent_t e : {ctx->ce_fork, ctx->ce_join})
+        if (e)
+            cudaEventDestroy(e);
     Pipeline &pl = ctx->pipe;
     for (cudaStream_t s : {pl.h2d, pl.cmp, pl.d2h})
         if (s) {
@@ -624,6 +669,8 @@ void tb_destroy(tb_ctx *ctx)
         cudaFreeHost(ctx->slot_status);
     if (ctx->val_stage)
         cudaFreeHost(ctx->val_stage);
+    if (ctx->first_diff)
+        cudaFree(ctx->first_diff);
     delete ctx;
 }
 
@@ -883,7 +930,13 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     }
     ctx->iter_ms.assign(iters, 0.0f);
     cudaStream_t st = ctx->stream;
-    const bool per_iter_validate = o.always_validate && t->expected;
+    const bool has_expected = t->expected || t->expected_device;
+    const bool per_iter_validate = o.always_validate && has_expected;
+    auto check = [&](tb_mismatch *mm) {
+        return t->expected_device
+                   ? validate_device_impl(ctx, dst, t->expected_device, t->num_bytes, 4, mm)
+                   : validate_impl(ctx, dst, t->expected, t->num_bytes, 4, mm);
+    };
     const bool gated = o.use_gate && !per_iter_validate && o.warmup + iters <= kMaxGatedLaunches &&
                        !profiler_attached();
 
@@ -908,7 +961,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
             TB_CUDA(ctx, cudaEventRecord(ctx->events[it + 1], st));
         if (per_iter_validate && it >= 0) {
             tb_mismatch mm;
-            first_err = validate_impl(ctx, dst, t->expected, t->num_bytes, 4, &mm);
+            first_err = check(&mm);
             if (first_err != TB_OK) {
                 out->mismatch_index = mm.index;
                 out->mismatch_expected = mm.expected;
@@ -962,10 +1015,10 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
         out->validated = 1;
         return first_err;
     }
-    if (t->expected) {
+    if (has_expected) {
         out->validated = 1;
         tb_mismatch mm;
-        rc = validate_impl(ctx, dst, t->expected, t->num_bytes, 4, &mm);
+        rc = check(&mm);
         if (rc != TB_OK) {
             out->mismatch_index = mm.index;
             out->mismatch_expected = mm.expected;
@@ -988,6 +1041,7 @@ int tb_run_transfer(tb_ctx *ctx, void *const *srcs, int n_src, void *dst, uint64
     t.iters = iters;
     t.rotate_bytes = rotate_bytes;
     t.expected = nullptr;
+    t.expected_device = nullptr;
     return tb_run_transfer_ex(ctx, &t, out);
 }
 
@@ -999,60 +1053,88 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         return fail(ctx, TB_EINVAL, "batch_copy: null descriptor array");
     const tb_options &o = ctx->opt;
     const uint64_t small = o.small_max_bytes;
-    tb::BatchCounts all;
-    size_t bad = 0;
-    ctx->bucket.resize(tb::bucket_count(small));
-    if (tb::count_batch(desc, n, small, &all, &bad, ctx->bucket.data()) != TB_OK)
-        return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range", bad);
-    tb_batch_stats st{};
-    st.descs = all.descs;
-    st.bytes = all.bytes;
+    const uint64_t ce_min = o.ce_min_bytes;
     ctx->last_slots.clear();
-    if (all.descs == 0) {
-        ctx->last_batch = st;
-        return TB_OK;
-    }
+    tb_batch_stats st{};
     DeviceScope scope(ctx->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // One launch per run of at most slot_items non-empty descriptors (one
-    // run for every batch that fits a slot).
-    size_t begin = 0;
-    while (begin < n) {
-        size_t end = begin;
-        uint64_t taken = 0;
-        while (end < n && (taken < o.slot_items || desc[end].len == 0)) {
-            taken += desc[end].len != 0;
-            ++end;
-        }
-        tb::BatchCounts c = all;
-        if (begin != 0 || end != n)
-            tb::count_batch(desc + begin, end - begin, small, &c, nullptr, ctx->bucket.data());
-        const int grid = tb::batch_grid(c, ctx->batch_grid);
+    // A batch that fits one slot is checked and packed in a single pass
+    // straight into the slot's pinned staging.  A larger one is checked as a
+    // whole first, so that no launch happens for a batch that is rejected.
+    const bool one_slot = n <= o.slot_items;
+    size_t bad = 0;
+    if (!one_slot) {
+        tb::BatchCounts all;
+        if (tb::count_batch(desc, n, small, &all, &bad, ce_min) != TB_OK)
+            return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range",
+                        bad);
+    }
+    if (ctx->longs.size() < std::min<size_t>(n, o.slot_items))
+        ctx->longs.resize(std::min<size_t>(n, o.slot_items));
 
+    bool forked = false;
+    size_t begin = 0;
+    do {
+        // The next run of at most slot_items descriptors.
+        const size_t end = std::min(n, begin + (size_t)o.slot_items);
         Slot &slot = ctx->slots[ctx->next_slot];
-        ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
         int rc = wait_slot(ctx, slot);
         if (rc != TB_OK)
             return rc;
-        tb::BatchPlan plan;
-        tb::pack_batch(desc + begin, end - begin, small, c, grid, slot.host, ctx->bucket.data(),
-                       &plan);
-        TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
-                                     cudaMemcpyHostToDevice, s));
-        if (slot.t0)
-            TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-        TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev));
-        if (slot.t1)
-            TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
-        TB_CUDA(ctx, cudaEventRecord(slot.done, s));
-        ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
-        slot.pending = true;
-        st.launches += 1;
-        st.warp_items += plan.n_short;
-        st.cta_items += plan.chunks;
-        st.upload_bytes += plan.upload_bytes;
+        tb::BatchCounts c;
+        if (tb::gather_batch(desc + begin, end - begin, small, ce_min, slot.host, ctx->longs.data(),
+                             &c, &bad) != TB_OK)
+            return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range",
+                        begin + bad);
+        st.descs += c.descs;
+        st.bytes += c.bytes;
+        st.ce_copies += c.n_ce;
+
+        // Copies routed to the copy engines run on a stream forked from the
+        // caller's, alongside the kernel, and are joined back at the end.
+        if (c.n_ce) {
+            if (!ctx->ce) {
+                TB_CUDA(ctx, cudaStreamCreateWithFlags(&ctx->ce, cudaStreamNonBlocking));
+                TB_CUDA(ctx, cudaEventCreateWithFlags(&ctx->ce_fork, cudaEventDisableTiming));
+                TB_CUDA(ctx, cudaEventCreateWithFlags(&ctx->ce_join, cudaEventDisableTiming));
+            }
+            if (!forked) {
+                TB_CUDA(ctx, cudaEventRecord(ctx->ce_fork, s));
+                TB_CUDA(ctx, cudaStreamWaitEvent(ctx->ce, ctx->ce_fork, 0));
+                forked = true;
+            }
+            for (size_t i = begin; i < end; ++i)
+                if (desc[i].len && desc[i].len >= ce_min)
+                    TB_CUDA(ctx, cudaMemcpyAsync(reinterpret_cast<void *>(desc[i].dst),
+                                                 reinterpret_cast<const void *>(desc[i].src),
+                                                 desc[i].len, cudaMemcpyDeviceToDevice, ctx->ce));
+        }
+        if (c.n_short + c.n_long > 0) {
+            tb::BatchPlan plan;
+            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid), slot.host,
+                             &plan);
+            ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
+            TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
+                                         cudaMemcpyHostToDevice, s));
+            if (slot.t0)
+                TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
+            TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev));
+            if (slot.t1)
+                TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
+            TB_CUDA(ctx, cudaEventRecord(slot.done, s));
+            ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
+            slot.pending = true;
+            st.launches += 1;
+            st.warp_items += plan.n_short;
+            st.cta_items += plan.chunks;
+            st.upload_bytes += plan.upload_bytes;
+        }
         begin = end;
+    } while (begin < n);
+    if (forked) {
+        TB_CUDA(ctx, cudaEventRecord(ctx->ce_join, ctx->ce));
+        TB_CUDA(ctx, cudaStreamWaitEvent(s, ctx->ce_join, 0));
     }
     ctx->last_batch = st;
     return TB_OK;
@@ -1109,6 +1191,19 @@ int tb_last_batch_stats(const tb_ctx *ctx, tb_batch_stats *out)
         return TB_EINVAL;
     *out = ctx->last_batch;
     return TB_OK;
+}
+
+int tb_validate_device(tb_ctx *ctx, const void *dst_device, const void *expected_device,
+                       uint64_t num_bytes, uint32_t elem_size, tb_mismatch *out)
+{
+    if (!ctx)
+        return TB_EINVAL;
+    if ((num_bytes > 0 && (!dst_device || !expected_device)) ||
+        (elem_size != 1 && elem_size != 2 && elem_size != 4) || num_bytes % elem_size != 0)
+        return fail(ctx, TB_EINVAL, "validate_device: bad arguments");
+    DeviceScope scope(ctx->device);
+    TB_CUDA(ctx, cudaDeviceSynchronize());
+    return validate_device_impl(ctx, dst_device, expected_device, num_bytes, elem_size, out);
 }
 
 int tb_validate(tb_ctx *ctx, const void *dst_device, const void *expected_host, uint64_t num_bytes,

@@ -58,6 +58,11 @@ int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll);
 cudaError_t launch_fill_source(float *dst, uint64_t n, const tb_pattern &pat, int buffer_idx,
                                int num_sms, cudaStream_t stream);
 
+// Device-side compare of n bytes: *first (device memory) becomes the
+// smallest differing byte index, or stays UINT64_MAX.
+cudaError_t launch_compare(const void *a, const void *b, uint64_t n, unsigned long long *first,
+                           int num_sms, cudaStream_t stream);
+
 // ---------------------------------------------------------------------------
 // Gate kernel: waits, with a %globaltimer deadline, until *flag != 0.
 // Writes *status = 1 when released, 2 when the deadline passed first.
@@ -80,6 +85,7 @@ static_assert(sizeof(WorkItem) == 24, "WorkItem is packed as three 64-bit words"
 constexpr int kBatchThreads = 256;
 constexpr uint64_t kChunkBytes = 65536;  // target size of a long-copy chunk
 constexpr uint32_t kMaxChunks = 16384;   // chunks of one launch at most
+constexpr size_t kBatchHeader = 16;      // claim counter of the short copies
 
 // Descriptor counts of a batch (descriptors with len == 0 are skipped).
 struct BatchCounts {
@@ -88,6 +94,8 @@ struct BatchCounts {
     uint64_t n_long;      // len > small_max: CTA phase
     uint64_t long_bytes;  // sum of the long lengths
     uint64_t bytes;       // sum of all lengths
+    uint64_t n_ce;        // len >= ce_min: left to the copy engines
+    uint64_t ce_bytes;
 };
 
 // One packed launch (see tb_pack.cpp for the buffer layout).
@@ -112,21 +120,22 @@ __host__ __device__ inline uint64_t chunk_start(uint64_t total, uint64_t chunks,
     return raw & ~(uint64_t)63;
 }
 
-unsigned bucket_shift(uint64_t small_max);
-size_t bucket_count(uint64_t small_max);
 // Bytes a packed launch of at most `descs` non-empty descriptors needs.
 size_t batch_buffer_bytes(uint64_t descs);
 // Checks and counts descriptors; TB_EINVAL (index in *bad) for a null or
-// wrapping range.  With `bucket` (bucket_count(small_max) words) it also
-// counts the short copies per length bucket, which pack_batch needs.
+// wrapping range.  Descriptors with len >= ce_min (when ce_min > 0) are
+// counted apart: the caller sends them to the copy engines.
 int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCounts *c,
-                size_t *bad, uint32_t *bucket);
+                size_t *bad, uint64_t ce_min = 0);
+// One pass: checks and counts like count_batch, appends the short copies to
+// buf (after the header) and the long ones to `longs` (room for n).
+int gather_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, uint64_t ce_min,
+                 void *buf, WorkItem *longs, BatchCounts *c, size_t *bad);
 // CTAs for a batch: one full wave at most, fewer for small batches.
 int batch_grid(const BatchCounts &c, int full_grid);
-// Packs the descriptors into buf; c and bucket come from count_batch over
-// exactly these descriptors.
-void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const BatchCounts &c,
-                int grid, void *buf, uint32_t *bucket, BatchPlan *out);
+// Completes a buffer gather_batch filled: header, long copies, prefix and
+// chunk table; fills *out.
+void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out);
 
 // Launches k_batch over a packed buffer (device copy at `dev`).  status
 // (nullable, device-visible) is set to 1 if a bounded wait inside the kernel

@@ -2,15 +2,21 @@
 // array into the work list one k_batch launch reads.
 //
 // Layout of a packed launch (one device buffer):
-//   WorkItem shorts[n_short]     copies of at most small_max bytes, longest
-//                                first (one warp each)
-//   WorkItem longs[n_long]       the longer copies, in descriptor order
-//   uint64_t prefix[n_long + 1]  offset of each long copy in the stream of
-//                                all long-copy bytes; prefix[n_long] = total
-//   uint32_t chunk_desc[C + 1]   the long copy holding chunk c's first byte
+//   uint32_t claim; (16-byte header)  work counter of the short copies,
+//                                      uploaded as 0 with every launch
+//   WorkItem shorts[n_short]          copies of at most small_max bytes, in
+//                                      descriptor order (warps claim them)
+//   WorkItem longs[n_long]            the longer copies, in descriptor order
+//   uint64_t prefix[n_long + 1]       offset of each long copy in the stream
+//                                      of all long-copy bytes; last = total
+//   uint32_t chunk_desc[C + 1]        the long copy holding chunk c's first byte
 // The long-copy stream is cut into C = grid * m chunks of equal size (cuts
 // on 64-byte stream offsets); CTA b copies chunks b, b + grid, ... so every
 // CTA gets exactly m chunks and the grid sweeps the stream front to back.
+//
+// Packing is one pass over the descriptors (check, count, append) plus a
+// pass over the long copies; nothing is sorted, because the kernel balances
+// the short copies itself by claiming them from the counter.
 
 #include <algorithm>
 #include <cstring>
@@ -19,53 +25,79 @@
 
 namespace tb {
 
-unsigned bucket_shift(uint64_t small_max)
-{
-    unsigned shift = 6;
-    while ((small_max >> shift) > 4096)
-        ++shift;
-    return shift;
-}
-
-size_t bucket_count(uint64_t small_max)
-{
-    return (size_t)(small_max >> bucket_shift(small_max)) + 1;
-}
-
 size_t batch_buffer_bytes(uint64_t descs)
 {
-    return (size_t)descs * (sizeof(WorkItem) + sizeof(uint64_t)) + sizeof(uint64_t) +
-           ((size_t)kMaxChunks + 1) * sizeof(uint32_t);
+    return kBatchHeader + (size_t)descs * (sizeof(WorkItem) + sizeof(uint64_t)) +
+           sizeof(uint64_t) + ((size_t)kMaxChunks + 1) * sizeof(uint32_t);
+}
+
+static inline bool bad_range(uint64_t src, uint64_t dst, uint64_t len)
+{
+    return src == 0 || dst == 0 || src + len < src || dst + len < dst;
 }
 
 int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCounts *c,
-                size_t *bad, uint32_t *bucket)
+                size_t *bad, uint64_t ce_min)
 {
-    *c = BatchCounts{};
-    const unsigned shift = bucket_shift(small_max);
-    const size_t nb = bucket_count(small_max);
-    if (bucket)
-        std::fill(bucket, bucket + nb, 0u);
+    const tb_copy_desc *__restrict__ d = desc;
+    const uint64_t ce = ce_min ? ce_min : UINT64_MAX;
+    uint64_t descs = 0, bytes = 0, n_short = 0, n_long = 0, long_bytes = 0, n_ce = 0, ce_bytes = 0;
     for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
+        const uint64_t src = d[i].src, dst = d[i].dst, len = d[i].len;
+        if (len == 0)
             continue;
-        if (d.src == 0 || d.dst == 0 || d.src + d.len < d.src || d.dst + d.len < d.dst) {
+        if (bad_range(src, dst, len)) {
             if (bad)
                 *bad = i;
             return TB_EINVAL;
         }
-        ++c->descs;
-        c->bytes += d.len;
-        if (d.len <= small_max) {
-            ++c->n_short;
-            if (bucket)
-                ++bucket[nb - 1 - (size_t)(d.len >> shift)];
+        ++descs;
+        bytes += len;
+        if (len >= ce) {
+            ++n_ce;
+            ce_bytes += len;
+        } else if (len <= small_max) {
+            ++n_short;
         } else {
-            ++c->n_long;
-            c->long_bytes += d.len;
+            ++n_long;
+            long_bytes += len;
         }
     }
+    *c = BatchCounts{descs, n_short, n_long, long_bytes, bytes, n_ce, ce_bytes};
+    return TB_OK;
+}
+
+int gather_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, uint64_t ce_min,
+                 void *buf, WorkItem *longs, BatchCounts *c, size_t *bad)
+{
+    const tb_copy_desc *__restrict__ d = desc;
+    WorkItem *__restrict__ shorts =
+        reinterpret_cast<WorkItem *>(static_cast<char *>(buf) + kBatchHeader);
+    WorkItem *__restrict__ lg = longs;
+    const uint64_t ce = ce_min ? ce_min : UINT64_MAX;
+    uint64_t descs = 0, bytes = 0, ns = 0, nl = 0, long_bytes = 0, n_ce = 0, ce_bytes = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const uint64_t src = d[i].src, dst = d[i].dst, len = d[i].len;
+        if (len == 0)
+            continue;
+        if (bad_range(src, dst, len)) {
+            if (bad)
+                *bad = i;
+            return TB_EINVAL;
+        }
+        ++descs;
+        bytes += len;
+        if (len >= ce) {
+            ++n_ce;
+            ce_bytes += len;
+        } else if (len <= small_max) {
+            shorts[ns++] = WorkItem{src, dst, len};
+        } else {
+            lg[nl++] = WorkItem{src, dst, len};
+            long_bytes += len;
+        }
+    }
+    *c = BatchCounts{descs, ns, nl, long_bytes, bytes, n_ce, ce_bytes};
     return TB_OK;
 }
 
@@ -78,63 +110,53 @@ int batch_grid(const BatchCounts &c, int full_grid)
     return (int)std::min<uint64_t>(std::min<uint64_t>((uint64_t)full_grid, kMaxChunks), want);
 }
 
-void pack_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, const BatchCounts &c,
-                int grid, void *buf, uint32_t *bucket, BatchPlan *out)
+void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out)
 {
-    const unsigned shift = bucket_shift(small_max);
-    const size_t nb = bucket_count(small_max);
-
-    // Chunks: about kChunkBytes each, a whole number per CTA.
-    uint64_t m = (c.long_bytes + (uint64_t)grid * kChunkBytes / 2) / ((uint64_t)grid * kChunkBytes);
-    m = std::max<uint64_t>(1, std::min<uint64_t>(m, kMaxChunks / (uint64_t)grid));
-    const uint64_t chunks = c.n_long ? (uint64_t)grid * m : 0;
-
-    WorkItem *shorts = static_cast<WorkItem *>(buf);
-    WorkItem *longs = shorts + c.n_short;
-    uint64_t *prefix = reinterpret_cast<uint64_t *>(longs + c.n_long);
+    char *base = static_cast<char *>(buf);
+    std::memset(base, 0, kBatchHeader);  // the claim counter starts at 0
+    WorkItem *lg = reinterpret_cast<WorkItem *>(base + kBatchHeader) + c.n_short;
+    uint64_t *prefix = reinterpret_cast<uint64_t *>(lg + c.n_long);
     uint32_t *chunk_desc = reinterpret_cast<uint32_t *>(prefix + c.n_long + 1);
 
-    // Bucket counts (from count_batch) -> starts; short copies longest first.
-    uint32_t run = 0;
-    for (size_t k = 0; k < nb; ++k) {
-        const uint32_t cnt = bucket[k];
-        bucket[k] = run;
-        run += cnt;
-    }
-    // Place every copy.
-    uint32_t nl = 0;
+    // Chunks: about kChunkBytes each, a whole number per CTA.
+    const uint64_t G = (uint64_t)grid;
+    uint64_t m = (c.long_bytes + G * kChunkBytes / 2) / (G * kChunkBytes);
+    m = std::max<uint64_t>(1, std::min<uint64_t>(m, kMaxChunks / G));
+    const uint64_t chunks = c.n_long ? G * m : 0;
+
     uint64_t pos = 0;
-    for (size_t i = 0; i < n; ++i) {
-        const tb_copy_desc &d = desc[i];
-        if (d.len == 0)
-            continue;
-        if (d.len <= small_max) {
-            uint32_t &p = bucket[nb - 1 - (size_t)(d.len >> shift)];
-            shorts[p++] = WorkItem{d.src, d.dst, d.len};
-        } else {
-            prefix[nl] = pos;
-            longs[nl++] = WorkItem{d.src, d.dst, d.len};
-            pos += d.len;
-        }
+    for (uint64_t k = 0; k < c.n_long; ++k) {
+        lg[k] = longs[k];
+        prefix[k] = pos;
+        pos += longs[k].len;
     }
-    prefix[nl] = pos;
-    // Chunk -> first long copy it touches.
+    prefix[c.n_long] = pos;
+    // Chunk -> first long copy it touches.  Chunk starts are chunk_start()
+    // walked incrementally: raw_k = q k + floor(r k / chunks).
     uint32_t dcur = 0;
+    const uint64_t q = chunks ? pos / chunks : 0, r = chunks ? pos % chunks : 0;
+    uint64_t raw = 0, rem = 0;
     for (uint64_t k = 0; k < chunks; ++k) {
-        const uint64_t s0 = chunk_start(pos, chunks, k);
-        while (dcur + 1 < nl && prefix[dcur + 1] <= s0)
+        const uint64_t s0 = raw & ~(uint64_t)63;
+        while (dcur + 1 < c.n_long && prefix[dcur + 1] <= s0)
             ++dcur;
         chunk_desc[k] = dcur;
+        raw += q;
+        rem += r;
+        if (rem >= chunks) {
+            rem -= chunks;
+            raw += 1;
+        }
     }
-    chunk_desc[chunks] = nl;
+    chunk_desc[chunks] = (uint32_t)c.n_long;
 
     out->n_short = (uint32_t)c.n_short;
-    out->n_long = nl;
+    out->n_long = (uint32_t)c.n_long;
     out->grid = (uint32_t)grid;
     out->chunks = (uint32_t)chunks;
     out->long_bytes = pos;
-    out->prefix_offset = (size_t)((const char *)prefix - (const char *)buf);
-    out->chunk_offset = (size_t)((const char *)chunk_desc - (const char *)buf);
+    out->prefix_offset = (size_t)((const char *)prefix - base);
+    out->chunk_offset = (size_t)((const char *)chunk_desc - base);
     out->upload_bytes = out->chunk_offset + ((size_t)chunks + 1) * sizeof(uint32_t);
 }
 

@@ -33,16 +33,17 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxGrid = 2048;         // CTAs of one launch at most
 // Bytes of one packed launch of TB_NOALLOC_MAX_ITEMS descriptors.
 constexpr size_t kScratchBytes =
-    TB_NOALLOC_MAX_ITEMS * (sizeof(WorkItem) + sizeof(uint64_t)) + sizeof(uint64_t) +
-    ((size_t)tb::kMaxChunks + 1) * sizeof(uint32_t);
+    tb::kBatchHeader + TB_NOALLOC_MAX_ITEMS * (sizeof(WorkItem) + sizeof(uint64_t)) +
+    sizeof(uint64_t) + ((size_t)tb::kMaxChunks + 1) * sizeof(uint32_t);
 constexpr size_t kScratchItems = (kScratchBytes + sizeof(WorkItem) - 1) / sizeof(WorkItem);
 
 // The scratch: the packed launch of the batch in flight.
 static __device__ __align__(256) WorkItem g_scratch_items[kScratchItems];
 
-// Host-side packing area (static storage, no heap) and its lock.
+// Host-side packing area and long-copy list (static storage, no heap), and
+// their lock.
 WorkItem g_host_items[kScratchItems];
-uint32_t g_bucket[(kSmallMax >> 6) + 1];
+WorkItem g_longs[TB_NOALLOC_MAX_ITEMS];
 std::mutex g_lock;
 
 // Per-device set-up: the scratch array's device address and the grid size.
@@ -74,7 +75,7 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
         return TB_EINVAL;
     std::lock_guard<std::mutex> hold(g_lock);
     tb::BatchCounts c;
-    if (tb::count_batch(desc, n, kSmallMax, &c, nullptr, g_bucket) != TB_OK)
+    if (tb::count_batch(desc, n, kSmallMax, &c, nullptr) != TB_OK)
         return TB_EINVAL;
     if (c.descs > TB_NOALLOC_MAX_ITEMS)
         return TB_ENOTSUP;
@@ -84,11 +85,12 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
     int rc = setup_current_device(&device);
     if (rc != TB_OK)
         return rc;
-    static_assert(sizeof(g_bucket) / sizeof(g_bucket[0]) >= (kSmallMax >> 6) + 1, "bucket area");
 
+    // Packing writes the whole launch, including a zero for the work
+    // counter the kernel claims short copies from.
+    tb::gather_batch(desc, n, kSmallMax, 0, g_host_items, g_longs, &c, nullptr);
     tb::BatchPlan plan;
-    tb::pack_batch(desc, n, kSmallMax, c, tb::batch_grid(c, g_dev_grid[device]), g_host_items,
-                   g_bucket, &plan);
+    tb::finish_batch(c, g_longs, tb::batch_grid(c, g_dev_grid[device]), g_host_items, &plan);
     // The copy from pageable host memory returns once the bytes are staged,
     // so the host area is free again when this call returns.
     cudaStream_t s = static_cast<cudaStream_t>(stream);

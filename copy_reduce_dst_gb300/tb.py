@@ -60,6 +60,7 @@ class Options(ct.Structure):
         ("unroll", _i32),
         ("time_kernels", _i32),
         ("reduce_engine", _i32),
+        ("ce_min_bytes", _u64),
     ]
 
 
@@ -124,6 +125,7 @@ class Transfer(ct.Structure):
         ("iters", _i32),
         ("rotate_bytes", _u64),
         ("expected", _vp),
+        ("expected_device", _vp),
     ]
 
 
@@ -139,6 +141,7 @@ class BatchStats(ct.Structure):
         ("launches", _u64),
         ("bytes", _u64),
         ("upload_bytes", _u64),
+        ("ce_copies", _u64),
     ]
 
 
@@ -180,6 +183,7 @@ _sig("tb_last_batch_stats", ct.c_int, _vp, _P(BatchStats))
 _sig("tb_last_batch_kernel_ms", ct.c_int, _vp, _P(ct.c_double))
 _sig("tb_copy_each", ct.c_int, _vp, _P(CopyDesc), ct.c_size_t, _vp)
 _sig("tb_validate", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
+_sig("tb_validate_device", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
 _sig("tb_batch_copy_noalloc", ct.c_int, _P(CopyDesc), ct.c_size_t, _vp)
 
 TB_NOALLOC_MAX_ITEMS = 65536
@@ -364,7 +368,8 @@ class Context:
         return {name: getattr(info, name) for name, _ in LaunchInfo._fields_}
 
     def run_transfer(self, srcs, dst, num_bytes: int, num_subexec: int = 0, iters: int = 1,
-                     rotate_bytes: int | None = None, expected=None) -> dict:
+                     rotate_bytes: int | None = None, expected=None,
+                     expected_device=None) -> dict:
         """tb_run_transfer_ex; returns the tb_result fields as a dict.
 
         ``expected`` (host bytes, e.g. a numpy array) turns on validation; a
@@ -376,7 +381,8 @@ class Context:
         arr = _ptr_array(srcs)
         t = Transfer(srcs=ct.cast(arr, ct.POINTER(_vp)), n_src=len(srcs), dst=addr(dst),
                      num_bytes=num_bytes, num_subexec=num_subexec, iters=iters,
-                     rotate_bytes=rotate_bytes, expected=addr(expected) if expected is not None else 0)
+                     rotate_bytes=rotate_bytes, expected=addr(expected) if expected is not None else 0,
+                     expected_device=addr(expected_device))
         r = Result()
         code = lib.tb_run_transfer_ex(self._h, ct.byref(t), ct.byref(r))
         res = {name: getattr(r, name) for name, _ in Result._fields_ if name != "iter_ms"}
@@ -432,6 +438,16 @@ class Context:
         return {name: getattr(s, name) for name, _ in BatchStats._fields_}
 
     # -- validation --------------------------------------------------------
+    def validate_device(self, dst_device, expected_device, num_bytes: int, elem_size: int = 4):
+        """tb_validate_device: None when equal, else (index, expected_bits, actual_bits)."""
+        m = Mismatch()
+        code = lib.tb_validate_device(self._h, addr(dst_device), addr(expected_device), num_bytes,
+                                      elem_size, ct.byref(m))
+        if code == TB_EVALIDATE:
+            return (m.index, m.expected, m.actual)
+        self._ok(code, "tb_validate_device")
+        return None
+
     def validate(self, dst_device, expected_host, num_bytes: int, elem_size: int = 4):
         """Returns None when equal, else (index, expected_bits, actual_bits)."""
         m = Mismatch()

@@ -36,7 +36,7 @@
  *   - Nothing falls back to a different copy method on failure: an error is
  *     returned instead, so a benchmark never silently measures something else.
  *   - Synchronous calls (tb_upload_sources, tb_prepare_sources,
- *     tb_run_transfer*, tb_validate) first wait until all work already queued
+ *     tb_run_transfer*, tb_validate*) first wait until all work already queued
  *     on the device has finished, so they see the results of earlier
  *     asynchronous calls on any stream.
  *   - A context is not thread-safe; use one context per host thread.
@@ -127,6 +127,12 @@ typedef struct {
        alignment, else TB_ENOTSUP); 0 = the library's choice: 2 where it
        applies (and vec_bytes is 0), else 1.  Default 0. */
     int32_t reduce_engine;
+    /* Batched copy: descriptors of at least this many bytes go to the copy
+       engines (one cudaMemcpyAsync each, on an internal stream forked from
+       the caller's and joined back) while the kernel copies the rest, as the
+       Mooncake RFC does for copies over 1 MiB.  0 = everything in the
+       kernel.  Default 0. */
+    uint64_t ce_min_bytes;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -137,7 +143,7 @@ void tb_options_default(tb_options *opt);
      TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
      TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
-     TB_TIME_KERNELS, TB_REDUCE_ENGINE.
+     TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);
@@ -316,6 +322,9 @@ typedef struct {
     const void *expected;     /* NULL, or host bytes dst must equal (validation
                                  after the loop, or after every iteration when
                                  always_validate is set) */
+    const void *expected_device; /* NULL, or device bytes dst must equal,
+                                 compared on the GPU (tb_validate_device);
+                                 used instead of `expected` when set */
 } tb_transfer;
 
 /* TransferBench's timed iteration loop for one transfer, synchronous on an
@@ -364,10 +373,11 @@ typedef struct {
    `stream` (ordered after the caller's earlier work on it).  The descriptor
    array is read and packed before return, so the caller may reuse it at
    once.  The bytes of all descriptors longer than small_max_bytes form one
-   stream cut into equal shares, one per CTA; then descriptors of at most
-   small_max_bytes go to one warp each, longest first.  Destinations must not
-   overlap one another or any source of the batch (the order of copies is
-   unspecified).  TB_EINVAL for a null
+   stream cut into equal chunks, the same number for every CTA, moved with
+   bulk copies through shared memory; descriptors of at most small_max_bytes
+   go to one warp each, claimed by free warps from a counter in the packed
+   work list.  Destinations must not overlap one another or any source of
+   the batch (the order of copies is unspecified).  TB_EINVAL for a null
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
    slot came free within wait_timeout_ns, or when the previous batch that
    used the chosen slot stopped early because a bounded wait inside the
@@ -381,6 +391,7 @@ typedef struct {
     uint64_t launches;     /* kernel launches (slots) used */
     uint64_t bytes;        /* sum of len */
     uint64_t upload_bytes; /* packed work-item bytes copied host-to-device */
+    uint64_t ce_copies;    /* descriptors sent to the copy engines (ce_min_bytes) */
 } tb_batch_stats;
 
 /* Statistics of the last tb_batch_copy on ctx. */
@@ -438,6 +449,15 @@ typedef struct {
    the first difference otherwise.  out may be NULL. */
 int tb_validate(tb_ctx *ctx, const void *dstDevice, const void *expectedHost,
                 uint64_t numBytes, uint32_t elemSize, tb_mismatch *out);
+
+/* The validateDirect option of "TransferBench data validation" (which the
+   page gives for AMD only, with NVIDIA falling back to a host copy): compares
+   numBytes of dstDevice with expectedDevice on the GPU, without copying
+   either to the host, and reports the first differing element (elemSize
+   1, 2 or 4 bytes).  Synchronous; first waits for work already queued on
+   the device.  TB_OK when equal, TB_EVALIDATE with *out filled otherwise. */
+int tb_validate_device(tb_ctx *ctx, const void *dstDevice, const void *expectedDevice,
+                       uint64_t numBytes, uint32_t elemSize, tb_mismatch *out);
 
 #ifdef __cplusplus
 }

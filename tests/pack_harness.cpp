@@ -1,16 +1,24 @@
 // Test harness: exposes the batched copy's host packer to the CPU tests.
+#include <vector>
+
 #include "tb_internal.h"
 
-extern "C" int harness_pack(const tb_copy_desc *desc, size_t n, uint64_t small_max, int full_grid,
-                            void *buf, uint32_t *bucket, uint64_t *out)
+extern "C" int harness_pack(const tb_copy_desc *desc, size_t n, uint64_t small_max, uint64_t ce_min,
+                            int full_grid, void *buf, uint64_t *out)
 {
-    tb::BatchCounts c;
+    tb::BatchCounts c, c2;
     size_t bad = 0;
-    if (tb::count_batch(desc, n, small_max, &c, &bad, bucket) != TB_OK)
+    if (tb::count_batch(desc, n, small_max, &c2, &bad, ce_min) != TB_OK)
         return -1;
+    std::vector<tb::WorkItem> longs(n + 1);
+    if (tb::gather_batch(desc, n, small_max, ce_min, buf, longs.data(), &c, &bad) != TB_OK)
+        return -2;
+    if (c.descs != c2.descs || c.n_short != c2.n_short || c.n_long != c2.n_long ||
+        c.long_bytes != c2.long_bytes || c.n_ce != c2.n_ce)
+        return -3;
     const int grid = tb::batch_grid(c, full_grid);
     tb::BatchPlan plan;
-    tb::pack_batch(desc, n, small_max, c, grid, buf, bucket, &plan);
+    tb::finish_batch(c, longs.data(), grid, buf, &plan);
     out[0] = plan.n_short;
     out[1] = plan.n_long;
     out[2] = plan.grid;
@@ -20,7 +28,19 @@ extern "C" int harness_pack(const tb_copy_desc *desc, size_t n, uint64_t small_m
     out[6] = plan.chunk_offset;
     out[7] = plan.upload_bytes;
     out[8] = tb::batch_buffer_bytes(c.descs);
+    out[9] = c.n_ce;
     return 0;
+}
+
+extern "C" int harness_bad(const tb_copy_desc *desc, size_t n, uint64_t *bad_out)
+{
+    tb::BatchCounts c;
+    size_t bad = 0;
+    std::vector<tb::WorkItem> longs(n + 1);
+    std::vector<char> buf(tb::batch_buffer_bytes(n));
+    const int rc = tb::gather_batch(desc, n, 16384, 0, buf.data(), longs.data(), &c, &bad);
+    *bad_out = bad;
+    return rc;
 }
 
 extern "C" uint64_t harness_chunk_start(uint64_t total, uint64_t chunks, uint64_t c)

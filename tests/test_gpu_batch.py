@@ -99,6 +99,26 @@ def test_size_bins(tb, small):
         run_layout(tb, c, layout, 6, src_shift=1)
 
 
+@pytest.mark.parametrize("ce_min", [1, 16384, 1 << 20])
+def test_copy_engine_routing(tb, ce_min):
+    """Descriptors of at least ce_min_bytes go to the copy engines on a
+    forked stream, the rest to the kernel; the result is the same."""
+    import torch
+    with tb.Context(0, tb.options(ce_min_bytes=ce_min)) as c:
+        layout = workloads.random_batch(77, 500, 2 << 20, 1024 * MiB, align=1)
+        st = torch.cuda.Stream()
+        stats = run_layout(tb, c, layout, 78, stream=st)
+        routed = int(((layout.lens >= ce_min) & (layout.lens > 0)).sum())
+        assert stats["ce_copies"] == routed and routed > 0
+        assert stats["warp_items"] + routed <= stats["descs"]
+
+
+def test_copy_engine_routing_head_sliced(tb):
+    with tb.Context(0, tb.options(ce_min_bytes=1 << 20)) as c:
+        stats = run_layout(tb, c, workloads.batch_head_sliced(), 104)
+        assert stats["ce_copies"] == 20 and stats["warp_items"] == 47520
+
+
 def test_user_stream_ordering(tb, ctx):
     """The copy runs after earlier work on the caller's stream: a fill queued
     just before on the same stream is what gets copied."""

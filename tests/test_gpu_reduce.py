@@ -248,6 +248,42 @@ def test_fill_rejects_bad_patterns(tb, ctx):
         ctx.fill_source(d, 62, tb.default_pattern(), 0)
 
 
+@pytest.mark.parametrize("nsrc", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("engine", [1, 2])
+def test_multi_source_fill_compress(tb, nsrc, engine):
+    """Sources k = 0..N-1 of the fillCompress pattern (every mode, 2B0
+    included), written by the library's fill kernel and summed on the GPU,
+    against the oracle's patterns and dstReference.  Masks that zero a
+    float's exponent byte make tiny and subnormal values, so the sums test
+    the left-to-right order and the absence of flush-to-zero."""
+    if engine == 2 and nsrc > 4:
+        pytest.skip("the bulk engine takes 1 to 4 sources")
+    n = 16 * 40000 + 9
+    pct = (20, 20, 20, 20, 20)
+    refs = [oracle.fill_compress(n, pct, 0xC0FFEE, k) for k in range(nsrc)]
+    sub = sum(int(np.count_nonzero((r != 0) & (np.abs(r) < np.float32(1.1754944e-38))))
+              for r in refs)
+    assert sub > 1000                                   # subnormal inputs present
+    exp = oracle.dst_reference(refs)
+    with tb.Context(0, tb.options(reduce_engine=engine)) as c:
+        srcs = [dev_bytes(4 * n) for _ in range(nsrc)]
+        for k, d in enumerate(srcs):
+            c.fill_source(d, 4 * n, tb.compress_pattern(pct, 0xC0FFEE), k)
+        dst = dev_bytes(4 * n)
+        c.reduce_copy(srcs, dst, 4 * n)
+        got = to_host(dst).view(np.float32)
+        assert oracle.first_mismatch(got, exp) == -1
+        # with rotation: 4 slices each, validated after every iteration
+        plan = tb.rotation_plan(4 * n, 4 * 4 * n)
+        with tb.Context(0, tb.options(reduce_engine=engine, always_validate=1)) as cv:
+            rot = [dev_bytes(plan.alloc_bytes) for _ in range(nsrc)]
+            for k, d in enumerate(rot):
+                cv.fill_source(d, 4 * n, tb.compress_pattern(pct, 0xC0FFEE), k)
+            cv.prepare_sources(rot, 4 * n, 4 * 4 * n)
+            r = cv.run_transfer(rot, dst, 4 * n, iters=6, rotate_bytes=4 * 4 * n, expected=exp)
+            assert r["K"] == 4 and r["mismatch_index"] == -1 and r["engine"] == engine
+
+
 # ---------------------------------------------------------------------------
 # Rotation, timed loop and validation (tb_run_transfer)
 # ---------------------------------------------------------------------------
@@ -336,6 +372,53 @@ def test_validation_reports_first_mismatch(tb, always):
         assert c.validate(dst, wrong, nb) == (12345, int(r["mismatch_expected"]),
                                               int(r["mismatch_actual"]))
         assert c.validate(dst, oracle.prepare_reference(n, 0), nb) is None
+
+
+@pytest.mark.parametrize("da,db", [(0, 0), (4, 4), (3, 3), (0, 5), (7, 1)])
+def test_validate_device_first_mismatch(tb, ctx, da, db):
+    """validateDirect on the GPU: the first differing byte, wherever it sits
+    (byte head, vector body, tail), for co-aligned and misaligned buffers."""
+    g = np.random.default_rng(da * 16 + db)
+    n = 3 * (1 << 20) + 13
+    data = g.integers(0, 256, n, dtype=np.uint8)
+    a = dev_bytes(n + 16)
+    b = dev_bytes(n + 16)
+    a[da:da + n].copy_(to_dev(data))
+    b[db:db + n].copy_(to_dev(data))
+    pa, pb = a.data_ptr() + da, b.data_ptr() + db
+    assert ctx.validate_device(pa, pb, n, 1) is None
+    for pos in (0, 1, 15, 16, 4097, n // 2, n - 1):
+        for extra in (None, pos + 1000):
+            bad = data.copy()
+            bad[pos] ^= 0x5A
+            if extra is not None and extra < n:
+                bad[extra] ^= 0x01
+            b[db:db + n].copy_(to_dev(bad))
+            got = ctx.validate_device(pa, pb, n, 1)
+            assert got is not None and got[0] == pos
+            assert got[1] == bad[pos] and got[2] == data[pos]
+    b[db:db + n].copy_(to_dev(data))
+    assert ctx.validate_device(pa, pb, n - n % 4, 4) is None
+
+
+def test_run_transfer_validates_on_the_device(tb):
+    nb = 64 * MiB
+    n = nb // 4
+    refs = [oracle.prepare_reference(n, k) for k in range(3)]
+    exp_dev = to_dev(oracle.dst_reference(refs))
+    with tb.Context(0, tb.options(always_validate=1)) as c:
+        srcs = [dev_bytes(nb) for _ in range(3)]
+        for k, s in enumerate(srcs):
+            c.fill_source(s, nb, tb.default_pattern(), k)
+        dst = dev_bytes(nb)
+        r = c.run_transfer(srcs, dst, nb, iters=5, rotate_bytes=0, expected_device=exp_dev)
+        assert r["validated"] == 1 and r["mismatch_index"] == -1 and r["iters"] == 5
+        wrong = oracle.dst_reference(refs)
+        wrong[777777] = 0.5
+        with pytest.raises(tb.TBError) as e:
+            c.run_transfer(srcs, dst, nb, iters=5, rotate_bytes=0, expected_device=to_dev(wrong))
+        assert e.value.code == tb.TB_EVALIDATE and e.value.result["mismatch_index"] == 777777
+        assert e.value.result["iters"] == 1
 
 
 def test_gate_deadline_returns_timeout(tb):

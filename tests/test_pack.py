@@ -1,7 +1,8 @@
 """CPU tests of the batched copy's host packer (tb_pack.cpp), built with g++
-against a small harness: every long copy is covered exactly once by its
-pieces, CTA shares are equal, the per-CTA table is consistent, and short
-copies come longest first."""
+against a small harness: the one-pass gather agrees with the counting pass,
+short copies keep descriptor order, long copies are listed with their
+stream offsets, every CTA gets the same number of equal chunks, and each
+chunk's table entry names the long copy that holds its first byte."""
 import ctypes as ct
 import os
 import subprocess
@@ -23,28 +24,30 @@ def harness(tmp_path_factory):
     subprocess.run(cmd, check=True)
     lib = ct.CDLL(out)
     lib.harness_pack.restype = ct.c_int
-    lib.harness_pack.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_uint64, ct.c_int, ct.c_void_p,
+    lib.harness_pack.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_uint64, ct.c_uint64, ct.c_int,
                                  ct.c_void_p, ct.c_void_p]
+    lib.harness_bad.restype = ct.c_int
+    lib.harness_bad.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_void_p]
     return lib
 
 
-def pack(lib, desc, small_max=16384, full_grid=608):
+def pack(lib, desc, small_max=16384, full_grid=608, ce_min=0):
     desc = np.ascontiguousarray(desc, dtype=np.uint64).reshape(-1, 3)
     n = desc.shape[0]
-    cap = n * 32 + 8 + (16384 + 1) * 4
-    buf = np.zeros(cap, dtype=np.uint8)
-    bucket = np.zeros(8192, dtype=np.uint32)
-    out = np.zeros(9, dtype=np.uint64)
-    rc = lib.harness_pack(desc.ctypes.data if n else None, n, small_max, full_grid,
-                          buf.ctypes.data, bucket.ctypes.data, out.ctypes.data)
+    cap = 16 + n * 32 + 8 + (16384 + 1) * 4
+    buf = np.full(cap, 0xEE, dtype=np.uint8)
+    out = np.zeros(10, dtype=np.uint64)
+    rc = lib.harness_pack(desc.ctypes.data if n else None, n, small_max, ce_min, full_grid,
+                          buf.ctypes.data, out.ctypes.data)
     assert rc == 0
-    n_short, n_long, grid, chunks, total, poff, coff, upload, bound = (int(x) for x in out)
+    n_short, n_long, grid, chunks, total, poff, coff, upload, bound, n_ce = (int(x) for x in out)
     assert upload <= bound <= cap
-    items = buf[: (n_short + n_long) * 24].view(np.uint64).reshape(-1, 3)
+    assert np.all(buf[:16] == 0)                       # the claim counter starts at 0
+    items = buf[16: 16 + (n_short + n_long) * 24].view(np.uint64).reshape(-1, 3)
     prefix = buf[poff: poff + (n_long + 1) * 8].view(np.uint64)
     cdesc = buf[coff: coff + (chunks + 1) * 4].view(np.uint32)
     return dict(shorts=items[:n_short], longs=items[n_short:], prefix=prefix, chunk_desc=cdesc,
-                grid=grid, chunks=chunks, total=total)
+                grid=grid, chunks=chunks, total=total, n_ce=n_ce)
 
 
 def chunk_bytes(lib, p, c):
@@ -99,15 +102,30 @@ def test_packer_invariants(harness, seed, n, long_frac, small, grid):
     else:
         assert p["chunks"] == 0
 
-    # short copies: the same multiset, longest first by bucket
-    shorts = p["shorts"]
-    want = sorted(map(tuple, desc[(lens > 0) & ~is_long].tolist()))
-    assert sorted(map(tuple, shorts.tolist())) == want
-    shift = 6
-    while (small >> shift) > 4096:
-        shift += 1
-    keys = (shorts[:, 2] >> np.uint64(shift)).astype(np.int64)
-    assert np.all(np.diff(keys) <= 0)
+    # short copies: exactly the short descriptors, in descriptor order
+    assert np.array_equal(p["shorts"], desc[(lens > 0) & ~is_long])
+
+
+@pytest.mark.parametrize("ce_min", [1, 4096, 1 << 20])
+def test_packer_copy_engine_split(harness, ce_min):
+    g = np.random.default_rng(ce_min)
+    desc = random_desc(g, 2000, 0.2, 16384)
+    p = pack(harness, desc, ce_min=ce_min)
+    lens = desc[:, 2]
+    ce = (lens >= ce_min) & (lens > 0)
+    assert p["n_ce"] == ce.sum()
+    assert np.array_equal(p["shorts"], desc[(lens > 0) & ~ce & (lens <= 16384)])
+    assert np.array_equal(p["longs"], desc[~ce & (lens > 16384)])
+
+
+def test_packer_reports_bad_descriptor(harness):
+    desc = np.array([[1, 2, 3], [4, 5, 0], [0, 8, 9], [10, 11, 12]], dtype=np.uint64)
+    bad = np.zeros(1, np.uint64)
+    assert harness.harness_bad(desc.ctypes.data, 4, bad.ctypes.data) != 0 and bad[0] == 2
+    desc[2] = [2**64 - 4, 8, 9]                          # wraps
+    assert harness.harness_bad(desc.ctypes.data, 4, bad.ctypes.data) != 0 and bad[0] == 2
+    desc[2] = [7, 8, 0]                                  # len 0: skipped, even with null ends
+    assert harness.harness_bad(desc.ctypes.data, 4, bad.ctypes.data) == 0
 
 
 def test_packer_batch_47540(harness):
