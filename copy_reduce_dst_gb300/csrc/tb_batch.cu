@@ -17,12 +17,12 @@ using namespace dev;
 // ---------------------------------------------------------------------------
 // K2: batched copy.  copy_range copies len bytes with `size` cooperating
 // threads (a warp or a CTA), any alignment:
-//   - head bytes until dst is 16-byte aligned, one byte per thread;
+//   - head bytes until dst is 16-byte aligned, a byte per thread;
 //   - body in 16-byte vectors: direct when src is then 16-byte aligned too,
 //     otherwise every output vector is funnel-shifted out of the two aligned
 //     source vectors that hold its bytes (both contain bytes of the range,
 //     so no load leaves the source's aligned 16-byte words);
-//   - tail bytes, one byte per thread.
+//   - tail bytes, a byte per thread.
 // ---------------------------------------------------------------------------
 constexpr int kCopyUnroll = 4;
 
@@ -63,8 +63,8 @@ __device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, uin
     uint64_t h = (16u - ((uintptr_t)dst & 15u)) & 15u;
     if (h > len)
         h = len;
-    if (rank < h)
-        dst[rank] = src[rank];
+    for (uint64_t b = rank; b < h; b += size)
+        dst[b] = src[b];
     dst += h;
     src += h;
     len -= h;
@@ -105,8 +105,8 @@ __device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, uin
     }
 
     const uint64_t done = nv << 4;
-    if (rank < len - done)
-        dst[done + rank] = src[done + rank];
+    for (uint64_t b = done + rank; b < len; b += size)
+        dst[b] = src[b];
 }
 
 __device__ __forceinline__ WorkItem load_item(const WorkItem *p)
@@ -284,8 +284,11 @@ __device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
     }
 }
 
-// Short copies claimed per atomic: a warp takes kClaim items at a time.
+// Short copies claimed per atomic: a warp takes kClaim items at a time and
+// copies them side by side, 32 / kClaim lanes each, so their loads are in
+// flight together.
 constexpr uint32_t kClaim = 2;
+constexpr uint32_t kLanesPerItem = 32 / kClaim;
 
 // Persistent grid of one wave.
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
@@ -294,10 +297,11 @@ constexpr uint32_t kClaim = 2;
 //   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
 //   the leftover edges.
 //   Short copies: every warp (warp 0 once its pipeline has drained) claims
-//   kClaim items at a time from a counter in global memory, and claims the
-//   next ones before copying the current ones, so the claim's latency
-//   overlaps the copy; whichever warp is free takes the next items, which
-//   balances the work without any ordering on the host.
+//   kClaim items at a time from a counter in global memory and copies them
+//   side by side, 32 / kClaim lanes each; it claims the next ones before
+//   copying, so the claim's latency overlaps the copy.  Whichever warp is
+//   free takes the next items, which balances the work without any ordering
+//   on the host.
 __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -323,20 +327,17 @@ __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
     if (lane == 0)
         base = atomicAdd(a.claim, kClaim);
     base = __shfl_sync(0xffffffffu, base, 0);
+    const uint32_t group = lane / kLanesPerItem, rank = lane % kLanesPerItem;
     while (base < n_short) {
         uint32_t next = 0;
         if (lane == 0)
             next = atomicAdd(a.claim, kClaim);
-        WorkItem it[kClaim];
-#pragma unroll
-        for (uint32_t q = 0; q < kClaim; ++q)
-            if (base + q < n_short)
-                it[q] = load_item(a.shorts + base + q);
-#pragma unroll
-        for (uint32_t q = 0; q < kClaim; ++q)
-            if (base + q < n_short)
-                copy_range(reinterpret_cast<uint8_t *>(it[q].dst),
-                           reinterpret_cast<const uint8_t *>(it[q].src), it[q].len, lane, 32u);
+        const uint32_t i = base + group;
+        if (i < n_short) {
+            const WorkItem w = load_item(a.shorts + i);
+            copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
+                       w.len, rank, kLanesPerItem);
+        }
         base = __shfl_sync(0xffffffffu, next, 0);
     }
 }
