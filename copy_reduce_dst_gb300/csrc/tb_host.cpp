@@ -1,7 +1,9 @@
 // Host runtime of libtb: options, contexts, the rotation allocator's plan and
-// slice fill, TransferBench's timed iteration loop, the descriptor-slot ring
-// of the batched copy, and validation.  Every GPU step is one of the kernels
-// in tb_kernels.cu; this file only plans, enqueues and times them.
+// slice fill, TransferBench's timed iteration loop, the end-to-end transfer
+// from host memory, the descriptor-slot ring of the batched copy, and
+// validation.  Every GPU step is one of the kernels in tb_reduce.cu,
+// tb_batch.cu and tb_fill.cu (or a CUDA copy where the API says so); this
+// file only plans, enqueues and times them.
 
 #include <cuda_runtime.h>
 #include <stdarg.h>
@@ -12,7 +14,6 @@
 
 #include <algorithm>
 #include <chrono>
-#include <mutex>
 #include <string>
 #include <thread>
 #include <vector>

@@ -1,5 +1,6 @@
-// Internal interface between the host runtime (tb_host.cpp) and the kernels
-// (tb_kernels.cu) of libtb.  Not installed; the public ABI is include/tb.h.
+// Internal interface between the host side of libtb (tb_host.cpp,
+// tb_pack.cpp, tb_static.cu) and its kernels (tb_reduce.cu, tb_batch.cu,
+// tb_fill.cu).  Not installed; the public ABI is include/tb.h.
 #pragma once
 
 #include <cuda_runtime.h>
