@@ -463,7 +463,7 @@ def study(args, tb, torch, local):
         r = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
         print(json.dumps({"study": "single transfer 4 MiB, K=64", "gbps": r["gbps"],
                           "mean_ms": r["mean_ms"], "K": r["K"],
-                          "alloc_bytes": r["alloc_bytes"], "gated": r["gated"]}), flush=True)
+                          "alloc_bytes": r["alloc_bytes"], "graphed": r["graphed"]}), flush=True)
         del src
         pct = (40, 20, 0, 20, 20)
         for mib in (8, 16, 32, 64, 128, 256, 512):

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libtb.so")
 
 SOURCES = ["tb_reduce.cu", "tb_batch.cu", "tb_fill.cu", "tb_host.cpp", "tb_pack.cpp",
-           "tb_static.cu"]
+           "tb_occupancy.cpp", "tb_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-ftz=false",
               "-Xcompiler", "-fPIC,-O2,-Wall,-Wextra", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -342,32 +342,11 @@ __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
     }
 }
 
-int g_batch_ctas_per_sm = 0;
-
 }  // namespace
-
-
-static bool batch_kernel_setup()
-{
-    static bool done = false;
-    if (!done)
-        done = cudaFuncSetAttribute(k_batch, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kBatchSmem) == cudaSuccess;
-    return done;
-}
 
 int batch_ctas_per_sm()
 {
-    if (g_batch_ctas_per_sm == 0) {
-        int blocks = 0;
-        if (!batch_kernel_setup() ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_batch, kBatchThreads,
-                                                          kBatchSmem) != cudaSuccess ||
-            blocks < 1)
-            blocks = 1;
-        g_batch_ctas_per_sm = blocks;
-    }
-    return g_batch_ctas_per_sm;
+    return resident_ctas((const void *)k_batch, kBatchThreads, kBatchSmem);
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
@@ -375,7 +354,7 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
-    if (!batch_kernel_setup())
+    if (batch_ctas_per_sm() < 1)
         return cudaErrorInvalidValue;
     char *base = static_cast<char *>(const_cast<void *>(dev));
     BatchArgs a;

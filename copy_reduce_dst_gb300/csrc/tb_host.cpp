@@ -14,6 +14,7 @@
 
 #include <algorithm>
 #include <chrono>
+#include <functional>
 #include <string>
 #include <thread>
 #include <vector>
@@ -307,6 +308,49 @@ int pipeline_events(tb_ctx *ctx, uint64_t n)
     return TB_OK;
 }
 
+// Captures the iteration loop of tb_run_transfer (warm-up launches, an
+// external event record, the timed launches, a second external event
+// record) on ctx->stream, launches the graph and waits for it.  Only the
+// span of the timed launches is recorded: an event node between every two
+// launches costs more GPU time than the graph saves.  set_iteration(it)
+// points the plan's sources at the slice iteration `it` reads.
+int run_graphed(tb_ctx *ctx, tb::ReducePlan &plan, int iters,
+                const std::function<void(int64_t)> &set_iteration)
+{
+    cudaStream_t st = ctx->stream;
+    TB_CUDA(ctx, cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    cudaError_t err = cudaSuccess;
+    for (int64_t it = -(int64_t)ctx->opt.warmup; it < iters && err == cudaSuccess; ++it) {
+        set_iteration(it);
+        if (it == 0)
+            err = cudaEventRecordWithFlags(ctx->events[0], st, cudaEventRecordExternal);
+        if (err == cudaSuccess)
+            err = tb::launch_reduce(plan, st);
+        if (err == cudaSuccess && it == iters - 1)
+            err = cudaEventRecordWithFlags(ctx->events[iters], st, cudaEventRecordExternal);
+    }
+    cudaGraph_t graph = nullptr;
+    const cudaError_t end = cudaStreamEndCapture(st, &graph);
+    if (err != cudaSuccess || end != cudaSuccess) {
+        if (graph)
+            cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return cuda_fail(ctx, err != cudaSuccess ? err : end, "capturing the iteration graph");
+    }
+    cudaGraphExec_t exec = nullptr;
+    err = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (err != cudaSuccess)
+        return cuda_fail(ctx, err, "cudaGraphInstantiate");
+    err = cudaGraphLaunch(exec, st);
+    if (err == cudaSuccess)
+        err = cudaStreamSynchronize(st);
+    cudaGraphExecDestroy(exec);
+    if (err != cudaSuccess)
+        return cuda_fail(ctx, err, "iteration graph");
+    return TB_OK;
+}
+
 double median_of(std::vector<float> v)
 {
     if (v.empty())
@@ -435,6 +479,7 @@ void tb_options_default(tb_options *o)
     o->time_kernels = 0;
     o->reduce_engine = 0;
     o->ce_min_bytes = 0;
+    o->use_graph = 1;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -502,6 +547,7 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_TIME_KERNELS", &o->time_kernels, &bad);
     env_i32("TB_REDUCE_ENGINE", &o->reduce_engine, &bad);
     env_u64("TB_CE_MIN_BYTES", &o->ce_min_bytes, &bad);
+    env_i32("TB_USE_GRAPH", &o->use_graph, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -590,7 +636,10 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     ctx->gate_status_dev = ctx->gate_flag_dev + 1;
     ctx->reduce_status_dev = ctx->gate_flag_dev + 2;
 
-    ctx->batch_grid = ctx->num_sms * tb::batch_ctas_per_sm();
+    const int batch_per_sm = tb::batch_ctas_per_sm();
+    if (batch_per_sm < 1)
+        return bail(TB_ECUDA);
+    ctx->batch_grid = ctx->num_sms * batch_per_sm;
     ctx->slots.resize(o.num_slots);
     const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items);
     void *status_dev = nullptr;
@@ -938,8 +987,19 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
                    ? validate_device_impl(ctx, dst, t->expected_device, t->num_bytes, 4, mm)
                    : validate_impl(ctx, dst, t->expected, t->num_bytes, 4, mm);
     };
-    const bool gated = o.use_gate && !per_iter_validate && o.warmup + iters <= kMaxGatedLaunches &&
-                       !profiler_attached();
+    // Graph: the whole loop (warm-up and timed iterations, the per-iteration
+    // event records as external event nodes) captured and launched as one
+    // CUDA graph - no host launch gaps and less launch work on the GPU per
+    // iteration.  Per-iteration validation needs the host between
+    // iterations, so it keeps the stream loop.
+    const bool graphed = o.use_graph && !per_iter_validate;
+    if (graphed) {
+        int rc2 = run_graphed(ctx, plan, iters, at_iteration);
+        if (rc2 != TB_OK)
+            return rc2;
+    }
+    const bool gated = !graphed && o.use_gate && !per_iter_validate &&
+                       o.warmup + iters <= kMaxGatedLaunches && !profiler_attached();
 
     if (gated) {
         ctx->gate_flag[0] = 0;
@@ -947,7 +1007,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
         TB_CUDA(ctx, tb::launch_gate(ctx->gate_flag_dev, ctx->gate_status_dev, o.wait_timeout_ns, st));
     }
     int first_err = TB_OK;
-    for (int64_t it = -(int64_t)o.warmup; it < iters; ++it) {
+    for (int64_t it = graphed ? iters : -(int64_t)o.warmup; it < iters; ++it) {
         at_iteration(it);
         if (it == 0 || (per_iter_validate && it > 0))
             TB_CUDA(ctx, cudaEventRecord(ctx->events[it], st));
@@ -985,11 +1045,20 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
 
     const int done = first_err != TB_OK ? out->iters : iters;
     double total = 0.0;
-    for (int i = 0; i < done; ++i) {
+    if (graphed) {
+        // One span for all timed iterations; each iteration gets the mean.
         float ms = 0.0f;
-        TB_CUDA(ctx, cudaEventElapsedTime(&ms, ctx->events[i], ctx->events[i + 1]));
-        ctx->iter_ms[i] = ms;
-        total += ms;
+        TB_CUDA(ctx, cudaEventElapsedTime(&ms, ctx->events[0], ctx->events[iters]));
+        total = ms;
+        for (int i = 0; i < done; ++i)
+            ctx->iter_ms[i] = (float)(total / done);
+    } else {
+        for (int i = 0; i < done; ++i) {
+            float ms = 0.0f;
+            TB_CUDA(ctx, cudaEventElapsedTime(&ms, ctx->events[i], ctx->events[i + 1]));
+            ctx->iter_ms[i] = ms;
+            total += ms;
+        }
     }
     out->K = K;
     out->slice_stride = stride;
@@ -1000,6 +1069,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     out->ctas = plan.grid;
     out->block_threads = plan.block_threads;
     out->gated = gated ? 1 : 0;
+    out->graphed = graphed ? 1 : 0;
     out->engine = plan.engine;
     out->total_ms = total;
     if (done > 0) {

@@ -138,6 +138,12 @@ int batch_grid(const BatchCounts &c, int full_grid);
 // chunk table; fills *out.
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out);
 
+// CTAs of `kernel` resident per SM at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device; raises the kernel's shared
+// memory limit there first when it needs more than 48 KiB.  Cached per
+// (device, kernel, threads, smem); 0 when a CUDA call fails.
+int resident_ctas(const void *kernel, int threads, size_t smem);
+
 // Launches k_batch over a packed buffer (device copy at `dev`).  status
 // (nullable, device-visible) is set to 1 if a bounded wait inside the kernel
 // expired.

@@ -199,6 +199,7 @@ constexpr int kRStages = 3;
 constexpr uint32_t kTile = 8192;
 constexpr uint32_t kTileVecs = kTile / 16;
 constexpr int kBulkThreads = 256;
+constexpr uint64_t kBulkMinBytes = 32ull << 20;  // auto engine: bulk from 32 MiB per source
 
 template <int N>
 constexpr size_t bulk_smem_bytes()
@@ -324,19 +325,6 @@ BulkKernel pick_bulk(int n_src, size_t *smem)
     }
 }
 
-// Shared memory above 48 KiB must be allowed per kernel before its launch.
-bool bulk_kernel_setup(int n_src)
-{
-    static bool done[5] = {};
-    size_t smem = 0;
-    BulkKernel k = pick_bulk(n_src, &smem);
-    if (!k)
-        return false;
-    if (!done[n_src])
-        done[n_src] = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem) == cudaSuccess;
-    return done[n_src];
-}
 
 using ReduceKernel = void (*)(const ReduceArgs);
 
@@ -406,23 +394,14 @@ static int bulk_ctas_per_sm(int n_src)
 {
     size_t smem = 0;
     BulkKernel k = pick_bulk(n_src, &smem);
-    int blocks = 0;
-    if (!k || !bulk_kernel_setup(n_src) ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kBulkThreads, smem) != cudaSuccess ||
-        blocks < 1)
-        blocks = 1;
-    return blocks;
+    return k ? resident_ctas((const void *)k, kBulkThreads, smem) : 0;
 }
 
 int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll)
 {
     void *fn = n_src <= 8 ? (void *)pick_reduce(n_src, vec_bytes, unroll)
                           : (vec_bytes == 16 ? (void *)k_reduce_many<16> : (void *)k_reduce_many<4>);
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, block_threads, 0) != cudaSuccess ||
-        blocks < 1)
-        blocks = 1;
-    return blocks;
+    return resident_ctas(fn, block_threads, 0);
 }
 
 int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
@@ -480,12 +459,17 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     p->vec_bytes = vb;
 
     // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
-    // and works in 16-byte units; when it applies it is the default (it keeps
-    // more bytes in flight per SM than per-thread vector loads can).
+    // and works in 16-byte units.  It is the default from kBulkMinBytes per
+    // source up, where it keeps more bytes in flight per SM than per-thread
+    // vector loads; below that, its per-tile pipeline latency costs more
+    // than it saves and the vector form is faster.
     const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
-    p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0)) ? 2 : 1;
+    p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
+                                 num_bytes >= kBulkMinBytes))
+                    ? 2
+                    : 1;
     if (p->engine == 2) {
         vb = 16;
         p->vec_bytes = 16;
@@ -509,6 +493,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     }
     const int per_sm = p->engine == 2 ? bulk_ctas_per_sm(n_src)
                                       : reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
+    if (per_sm < 1)
+        return TB_ECUDA;
     const int64_t full = (int64_t)num_sms * per_sm;
     const int64_t S = num_subexec > 0 ? num_subexec : full;
     const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, full);
@@ -537,7 +523,7 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     if (p.engine == 2) {
         size_t smem = 0;
         BulkKernel k = pick_bulk(p.n_src, &smem);
-        if (!k || !bulk_kernel_setup(p.n_src))
+        if (!k || resident_ctas((const void *)k, kBulkThreads, smem) < 1)
             return cudaErrorInvalidValue;
         k<<<grid, kBulkThreads, smem, stream>>>(a);
     } else if (p.n_src > 8) {

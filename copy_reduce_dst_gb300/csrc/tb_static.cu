@@ -62,7 +62,10 @@ int setup_current_device(int *device)
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
         return TB_ECUDA;
-    g_dev_grid[*device] = std::min(kMaxGrid, sms * tb::batch_ctas_per_sm());
+    const int per_sm = tb::batch_ctas_per_sm();
+    if (per_sm < 1)
+        return TB_ECUDA;
+    g_dev_grid[*device] = std::min(kMaxGrid, sms * per_sm);
     g_dev_items[*device] = static_cast<WorkItem *>(ptr);
     return TB_OK;
 }

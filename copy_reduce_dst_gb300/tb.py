@@ -61,6 +61,7 @@ class Options(ct.Structure):
         ("time_kernels", _i32),
         ("reduce_engine", _i32),
         ("ce_min_bytes", _u64),
+        ("use_graph", _i32),
     ]
 
 
@@ -85,6 +86,7 @@ class Result(ct.Structure):
         ("ctas", _i32),
         ("block_threads", _i32),
         ("gated", _i32),
+        ("graphed", _i32),
         ("engine", _i32),
         ("validated", _i32),
         ("total_ms", ct.c_double),

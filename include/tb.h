@@ -125,7 +125,9 @@ typedef struct {
        2 = bulk copies (cp.async.bulk) through shared-memory stages with the
        adds done in shared memory (1 to 4 sources sharing a 16-byte
        alignment, else TB_ENOTSUP); 0 = the library's choice: 2 where it
-       applies (and vec_bytes is 0), else 1.  Default 0. */
+       applies, vec_bytes is 0 and each source has at least 32 MiB (below
+       that the per-tile pipeline latency outweighs its gain), else 1.
+       Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy
        engines (one cudaMemcpyAsync each, on an internal stream forked from
@@ -133,6 +135,15 @@ typedef struct {
        Mooncake RFC does for copies over 1 MiB.  0 = everything in the
        kernel.  Default 0. */
     uint64_t ce_min_bytes;
+    /* 1 = tb_run_transfer captures its whole iteration loop (warm-up and
+       timed launches) into one CUDA graph and launches that: no host gaps
+       between iterations and less launch work per iteration on the GPU.
+       Only the span of the timed iterations is recorded (an event between
+       every two launches costs more than the graph saves), so every
+       iteration reports the mean; use 0 for per-iteration events.  Not used
+       with always_validate, which needs the host between iterations.
+       Default 1. */
+    int32_t use_graph;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -143,7 +154,7 @@ void tb_options_default(tb_options *opt);
      TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
      TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
-     TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES.
+     TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);
@@ -300,6 +311,7 @@ typedef struct {
     int32_t  ctas;            /* CTAs per launch */
     int32_t  block_threads;   /* threads per CTA */
     int32_t  gated;           /* 1 if the iterations ran behind the gate */
+    int32_t  graphed;         /* 1 if the iterations ran as one CUDA graph */
     int32_t  engine;          /* reduce-copy engine used (see tb_launch_info) */
     int32_t  validated;       /* 1 if dst was compared with expected bytes */
     double   total_ms;        /* device time of all timed iterations */
@@ -331,8 +343,10 @@ typedef struct {
    internal stream: for it = -warmup .. iters-1, iteration it reads slice
    tb_slice_for_iteration(it, K) of every source (the slice offset is a kernel
    argument, so rotation costs no host-to-device traffic and sits outside
-   the timed region) and writes dst + byte_offset.  Each timed iteration is
-   bracketed by CUDA events.  Sources must already hold their slices
+   the timed region) and writes dst + byte_offset.  The loop runs as one
+   CUDA graph timed by events around the timed iterations (use_graph), or as
+   stream launches, behind the gate (use_gate) or not, with CUDA events
+   between every two iterations.  Sources must already hold their slices
    (tb_fill_source or tb_upload_sources, then tb_prepare_sources).  On a
    validation failure returns TB_EVALIDATE with the mismatch in *out. */
 int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out);

@@ -143,15 +143,18 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
 def test_reduce_plan_engine_choice(tb, ctx):
     d = dev_bytes(1 << 20)
     p = d.data_ptr()
-    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, 4096)
+    big = 32 << 20
+    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
+    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, big - 256)
+    assert info["engine"] == 1                                    # small: vector loads
     info = ctx.reduce_plan([p] * 5, p + 65536, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
     info = ctx.reduce_plan([p + 4, p + 8], p + 65536, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 4        # no common alignment
-    info = ctx.reduce_plan([p + 4, p + 4100], p + 65540, 4096)
+    info = ctx.reduce_plan([p + 4, p + 4100], p + 65540, big)
     assert info["engine"] == 2 and info["head_elems"] == 3       # head to 16 bytes
-    assert info["head_elems"] + 4 * info["body_vectors"] + info["tail_elems"] == 1024
+    assert info["head_elems"] + 4 * info["body_vectors"] + info["tail_elems"] == big // 4
     with tb.Context(0, tb.options(vec_bytes=32)) as c:
         info = c.reduce_plan([p], p + 65536, 4096)
         assert info["engine"] == 1 and info["vec_bytes"] == 32
@@ -312,16 +315,19 @@ def test_single_transfer_mechanism(tb):
             assert r["K"] == 64 and r["alloc_bytes"] == 268435456 and r["prep_h2d_bytes"] == nb
             assert r["iters"] == 10 and r["validated"] == 1 and r["mismatch_index"] == -1
             assert len(r["iter_ms"]) == 10 and all(t > 0 for t in r["iter_ms"])
-            assert r["gated"] == (0 if always else 1)
+            assert r["graphed"] == (0 if always else 1) and r["gated"] == 0
+            assert abs(sum(r["iter_ms"]) - r["total_ms"]) < 1e-3 * r["total_ms"] + 1e-6
 
 
+@pytest.mark.parametrize("graph", [1, 0])
 @pytest.mark.parametrize("iters,warmup,K", [(5, 3, 8), (1, 3, 8), (8, 0, 8), (3, 5, 4), (7, 2, 1)])
-def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K):
+def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K, graph):
     """Slices filled with different patterns: after the loop dst holds the
-    last iteration's slice, (iters - 1) % K."""
+    last iteration's slice, (iters - 1) % K - whether the loop runs as one
+    CUDA graph or as stream launches."""
     nb = 64 * 1024
     n = nb // 4
-    with tb.Context(0, tb.options(warmup=warmup)) as c:
+    with tb.Context(0, tb.options(warmup=warmup, use_graph=graph)) as c:
         plan = tb.rotation_plan(nb, K * nb)
         assert plan.K == K
         src = dev_bytes(plan.alloc_bytes)
@@ -331,7 +337,8 @@ def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K):
         last = oracle.slice_for_iteration(iters - 1, K)
         expect = oracle.prepare_reference(n, last)
         r = c.run_transfer([src], dst, nb, iters=iters, rotate_bytes=K * nb, expected=expect)
-        assert r["mismatch_index"] == -1
+        assert r["mismatch_index"] == -1 and r["graphed"] == graph
+        assert len(r["iter_ms"]) == iters and all(t > 0 for t in r["iter_ms"])
 
 
 def test_byte_offset(tb):
@@ -426,7 +433,7 @@ def test_gate_deadline_returns_timeout(tb):
     it returns on its own; the call reports TB_ETIMEOUT and the context stays
     usable."""
     nb = 1 * MiB
-    with tb.Context(0, tb.options(wait_timeout_ns=1000, warmup=3)) as c:
+    with tb.Context(0, tb.options(wait_timeout_ns=1000, warmup=3, use_graph=0)) as c:
         src = dev_bytes(nb)
         c.fill_source(src, nb, tb.default_pattern(), 0)
         dst = dev_bytes(nb)
@@ -435,13 +442,13 @@ def test_gate_deadline_returns_timeout(tb):
         assert e.value.code == tb.TB_ETIMEOUT
         ref = oracle.prepare_reference(nb // 4, 0)
         assert c.validate(dst, ref, nb) is None
-        c2 = tb.options(use_gate=0)
+        c2 = tb.options(use_gate=0, use_graph=0)
     with tb.Context(0, c2) as c:
         src = dev_bytes(nb)
         c.fill_source(src, nb, tb.default_pattern(), 0)
         dst = dev_bytes(nb)
         r = c.run_transfer([src], dst, nb, iters=4, rotate_bytes=0, expected=ref)
-        assert r["gated"] == 0
+        assert r["gated"] == 0 and r["graphed"] == 0
 
 
 @pytest.mark.parametrize("n", [1, 1000003, (96 << 20) // 4 + 5])
