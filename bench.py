@@ -446,14 +446,17 @@ def reference_arm(args):
 # ---------------------------------------------------------------------------
 def study(args, tb, torch, local):
     """Single 4 MiB transfer (K = 64) and the fillCompress sweep with rotation
-    on and off.  Warm = total device time of 20 back-to-back iterations after
-    3 warm-ups (per-iteration events telescope, so their ~1 us resolution
-    does not bias the sum); cold = mean of 10 single iterations, each after
-    writing a 512 MiB buffer (> L2).  Each figure is the median of 3 reps."""
+    on and off.  Like-for-like cold / warm, both with CUDA events around every
+    launch: cold = mean of 10 single iterations, each after writing a 512 MiB
+    buffer (> L2); warm = 20 back-to-back iterations after 3 warm-ups (their
+    events telescope, so the ~1 us event resolution does not bias the sum).
+    warm_graph = the same 20 iterations as one CUDA graph (no launch gaps).
+    Each figure is the median of 3 reps."""
     import statistics as st
     flush = torch.empty(512 * MiB, dtype=torch.uint8, device="cuda")
     with tb.Context(local, ctx_options(tb)) as ctx, \
-            tb.Context(local, ctx_options(tb, warmup=0)) as cold_ctx:
+            tb.Context(local, ctx_options(tb, use_graph=0)) as ev_ctx, \
+            tb.Context(local, ctx_options(tb, warmup=0, use_graph=0)) as cold_ctx:
         nb = 4 * MiB
         plan = tb.rotation_plan(nb, 256 * MiB)
         src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
@@ -461,9 +464,12 @@ def study(args, tb, torch, local):
         ctx.prepare_sources([src], nb, 256 * MiB)
         dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
         r = ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
-        print(json.dumps({"study": "single transfer 4 MiB, K=64", "gbps": r["gbps"],
-                          "mean_ms": r["mean_ms"], "K": r["K"],
-                          "alloc_bytes": r["alloc_bytes"], "graphed": r["graphed"]}), flush=True)
+        re = ev_ctx.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
+        print(json.dumps({"study": "single transfer 4 MiB, K=64", "gbps_graph": round(r["gbps"], 1),
+                          "us_per_iteration_graph": round(r["mean_ms"] * 1e3, 2),
+                          "gbps_events": round(re["gbps"], 1),
+                          "us_per_iteration_events": round(re["mean_ms"] * 1e3, 2),
+                          "K": r["K"], "alloc_bytes": r["alloc_bytes"]}), flush=True)
         del src
         pct = (40, 20, 0, 20, 20)
         for mib in (8, 16, 32, 64, 128, 256, 512):
@@ -475,7 +481,7 @@ def study(args, tb, torch, local):
                 ctx.fill_source(src, nb, tb.compress_pattern(pct, 0x5EED), 0)
                 ctx.prepare_sources([src], nb, rot)
                 dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
-                cold, warm = [], []
+                cold, warm, graph = [], [], []
                 for rep in range(3):
                     c = []
                     for _ in range(10):
@@ -483,110 +489,21 @@ def study(args, tb, torch, local):
                         c.append(cold_ctx.run_transfer([src], dst, nb, iters=1,
                                                        rotate_bytes=rot)["total_ms"])
                     cold.append(2 * nb / (st.mean(c) / 1e3) / 1e9)
-                    warm.append(ctx.run_transfer([src], dst, nb, iters=20, rotate_bytes=rot)["gbps"])
+                    warm.append(ev_ctx.run_transfer([src], dst, nb, iters=20, rotate_bytes=rot)["gbps"])
+                    graph.append(ctx.run_transfer([src], dst, nb, iters=20, rotate_bytes=rot)["gbps"])
                 tag = "on" if rot else "off"
+                row[f"{tag}_K"] = plan.K
                 row[f"{tag}_cold_gbps"] = round(st.median(cold), 1)
                 row[f"{tag}_warm_gbps"] = round(st.median(warm), 1)
                 row[f"{tag}_w_over_c"] = round(st.median(warm) / st.median(cold), 3)
-                row[f"{tag}_K"] = plan.K
+                row[f"{tag}_warm_graph_gbps"] = round(st.median(graph), 1)
                 del src, dst
+            row["off_over_on_warm_graph"] = round(row["off_warm_graph_gbps"] / row["on_warm_graph_gbps"], 3)
             print(json.dumps(row), flush=True)
     del flush
     study_batch_phases(tb, torch, local)
     study_batch_routing(tb, torch, local)
     study_interference(tb, torch, local)
-
-
-def study_batch_routing(tb, torch, local):
-    """The 47,540 batch with its copies of at least 1 MiB (the 20 long ones)
-    sent to the copy engines instead of the kernel: device time per call of
-    10 back-to-back calls after 3 (upload + kernel + copy engines; the host
-    packs the next call while the GPU works), median of 3 reps."""
-    import statistics as st
-    from copy_reduce_dst_gb300 import workloads
-    layout = workloads.batch_head_sliced()
-    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
-    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
-    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
-    stream = torch.cuda.current_stream()
-    for ce in (0, 1 << 20):
-        with tb.Context(local, ctx_options(tb, ce_min_bytes=ce)) as ctx:
-            ms = []
-            for rep in range(4):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize()
-                e0.record(stream)
-                for _ in range(10):
-                    ctx.batch_copy(desc, stream)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                if rep >= 1:
-                    ms.append(e0.elapsed_time(e1) / 10)
-            print(json.dumps({"study": "batch routing", "ce_min_bytes": ce,
-                              "device_ms": round(st.median(ms), 4),
-                              "gbps": round(2 * layout.total_bytes / (st.median(ms) / 1e3) / 1e9, 1)}),
-                  flush=True)
-
-
-def study_interference(tb, torch, local):
-    """bf16 GEMM throughput (8192^3 torch.matmul on one stream) while the
-    47,540 batch is copied on another stream at several rates (a batch every
-    `gap` ms; 0 = back to back), the Mooncake RFC's interference measurement."""
-    from copy_reduce_dst_gb300 import workloads
-    n = 8192
-    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
-    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
-    layout = workloads.batch_head_sliced()
-    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
-    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
-    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
-    gemm_s = torch.cuda.Stream()
-    copy_s = torch.cuda.Stream()
-    flops = 2 * n ** 3
-
-    def run(gap_ms, seconds=1.5):
-        with tb.Context(local, ctx_options(tb)) as ctx:
-            torch.cuda.synchronize()
-            with torch.cuda.stream(gemm_s):
-                for _ in range(3):
-                    torch.matmul(a, b)
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(gemm_s)
-            with torch.cuda.stream(gemm_s):
-                for _ in range(int(seconds * 1900e12 / flops)):
-                    torch.matmul(a, b)
-            e1.record(gemm_s)
-            batches = 0
-            t0 = time.perf_counter()
-            while not e1.query():
-                if gap_ms is not None:
-                    ctx.batch_copy(desc, copy_s)
-                    batches += 1
-                    if gap_ms > 0:
-                        time.sleep(gap_ms / 1e3)
-                    else:
-                        copy_s.synchronize()
-                else:
-                    time.sleep(0.01)
-            wall = time.perf_counter() - t0
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1)
-            iters = int(seconds * 1900e12 / flops)
-            return iters * flops / (ms / 1e3) / 1e12, 2 * layout.total_bytes * batches / wall / 1e9
-
-    alone, _ = run(None)
-    print(json.dumps({"study": "interference", "copy_gap_ms": None, "gemm_tflops": round(alone, 1),
-                      "copy_gbps": 0.0}), flush=True)
-    for gap in (20, 5, 1, 0):
-        tf, gbps = run(gap)
-        print(json.dumps({"study": "interference", "copy_gap_ms": gap, "gemm_tflops": round(tf, 1),
-                          "copy_gbps": round(gbps, 1),
-                          "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
-                          "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
-              flush=True)
 
 
 def study_batch_phases(tb, torch, local):
