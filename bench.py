@@ -6,7 +6,8 @@ Default line (rank 0 prints one JSON object):
             src_k = PrepSrcValue(k, i), SRC_ROTATE_BYTES = 256 MiB (K = 1);
   step      one reduce-copy launch over the whole transfer (1 GiB moved:
             3 x 256 MiB read + 256 MiB written); inputs (1 GiB) exceed the
-            129 MB L2, so no flush is needed between steps;
+            129 MB L2, so no flush is needed between steps; the K timed
+            steps are captured into one CUDA graph and replayed once;
   value     HBM GB/s counting read + write bytes, summed over ranks;
   e2e       the same transfer through tb_reduce_copy_host from pinned host
             buffers: host-to-device sources, the kernel, device-to-host dst;
@@ -232,11 +233,23 @@ def run_reduce(args, tb, torch, ranks, local):
         off = tb.slice_for_iteration(step, plan.K) * plan.slice_stride
         return [s.data_ptr() + off for s in srcs]
 
-    def step(i):
-        ctx.reduce_copy(srcs_at(i), dst, nb, subexec, stream)
+    def step(i, s=stream):
+        ctx.reduce_copy(srcs_at(i), dst, nb, subexec, s)
 
     for i in range(-args.warmup, 0):
         step(i)
+    # The K timed steps are captured into one CUDA graph (each step one
+    # reduce-copy launch over the whole transfer, its rotated slice baked in)
+    # and replayed once in the timed region: no launch gaps between steps.
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    gstream = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=gstream):
+        for i in range(args.steps):
+            step(i, gstream)
+    with torch.cuda.stream(gstream):
+        graph.replay()
+    torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.wait_first()
     # Untimed soak so the clock samples cover a steady load, then the timed loop.
@@ -252,13 +265,14 @@ def run_reduce(args, tb, torch, ranks, local):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
+    with torch.cuda.stream(gstream):
+        ev0.record(gstream)
+        graph.replay()
+        ev1.record(gstream)
     torch.cuda.synchronize()
     ranks.barrier()
     clocks = sampler.stop()
+    del graph
     ms = ev0.elapsed_time(ev1)
     units, worst_s = combine(ranks, bytes_per_step * args.steps, ms / 1e3)
     value = units / worst_s / 1e9
@@ -506,6 +520,98 @@ def study(args, tb, torch, local):
     study_interference(tb, torch, local)
 
 
+def study_batch_routing(tb, torch, local):
+    """The 47,540 batch with its copies of at least 1 MiB (the 20 long ones)
+    sent to the copy engines instead of the kernel: device time per call of
+    10 back-to-back calls after 3 (upload + kernel + copy engines; the host
+    packs the next call while the GPU works), median of 3 reps."""
+    import statistics as st
+    from copy_reduce_dst_gb300 import workloads
+    layout = workloads.batch_head_sliced()
+    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    stream = torch.cuda.current_stream()
+    for ce in (0, 1 << 20):
+        with tb.Context(local, ctx_options(tb, ce_min_bytes=ce)) as ctx:
+            ms = []
+            for rep in range(4):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(10):
+                    ctx.batch_copy(desc, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if rep >= 1:
+                    ms.append(e0.elapsed_time(e1) / 10)
+            print(json.dumps({"study": "batch routing", "ce_min_bytes": ce,
+                              "device_ms": round(st.median(ms), 4),
+                              "gbps": round(2 * layout.total_bytes / (st.median(ms) / 1e3) / 1e9, 1)}),
+                  flush=True)
+
+
+def study_interference(tb, torch, local):
+    """bf16 GEMM throughput (8192^3 torch.matmul on one stream) while the
+    47,540 batch is copied on another stream at several rates (a batch every
+    `gap` ms; 0 = back to back), the Mooncake RFC's interference measurement."""
+    from copy_reduce_dst_gb300 import workloads
+    n = 8192
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    layout = workloads.batch_head_sliced()
+    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    gemm_s = torch.cuda.Stream()
+    copy_s = torch.cuda.Stream()
+    flops = 2 * n ** 3
+
+    def run(gap_ms, seconds=1.5):
+        with tb.Context(local, ctx_options(tb)) as ctx:
+            torch.cuda.synchronize()
+            with torch.cuda.stream(gemm_s):
+                for _ in range(3):
+                    torch.matmul(a, b)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(gemm_s)
+            with torch.cuda.stream(gemm_s):
+                for _ in range(int(seconds * 1900e12 / flops)):
+                    torch.matmul(a, b)
+            e1.record(gemm_s)
+            batches = 0
+            t0 = time.perf_counter()
+            while not e1.query():
+                if gap_ms is not None:
+                    ctx.batch_copy(desc, copy_s)
+                    batches += 1
+                    if gap_ms > 0:
+                        time.sleep(gap_ms / 1e3)
+                    else:
+                        copy_s.synchronize()
+                else:
+                    time.sleep(0.01)
+            wall = time.perf_counter() - t0
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            iters = int(seconds * 1900e12 / flops)
+            return iters * flops / (ms / 1e3) / 1e12, 2 * layout.total_bytes * batches / wall / 1e9
+
+    alone, _ = run(None)
+    print(json.dumps({"study": "interference", "copy_gap_ms": None, "gemm_tflops": round(alone, 1),
+                      "copy_gbps": 0.0}), flush=True)
+    for gap in (20, 5, 1, 0):
+        tf, gbps = run(gap)
+        print(json.dumps({"study": "interference", "copy_gap_ms": gap, "gemm_tflops": round(tf, 1),
+                          "copy_gbps": round(gbps, 1),
+                          "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
+                          "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
+              flush=True)
+
+
 def study_batch_phases(tb, torch, local):
     """Kernel time of the 47,540 batch and of its parts: the 20 long copies
     alone, the 47,520 short copies alone, and one 1 GiB copy (median of 10
@@ -625,7 +731,8 @@ def main():
             "config": {"workload": WORKLOAD, "num_subexec": red["subexec"],
                        "num_subexec_choice": "best of the sweep 1, 4, 16, 32",
                        "step": "one reduce-copy launch over 3 x 256 MiB -> 256 MiB "
-                               "(1,073,741,824 B moved)",
+                               "(1,073,741,824 B moved); the K timed steps run as one CUDA "
+                               "graph replay",
                        "l2": "inputs larger than L2 (1 GiB per step vs 129 MB), no flush",
                        "parallelism": f"replicas x{world} (no data exchange)",
                        "subexec_sweep": red["subexec_sweep"],
