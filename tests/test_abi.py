@@ -98,6 +98,25 @@ def test_options_defaults(tb):
     assert o.rotate_bytes == 256 << 20 and o.warmup == 3 and o.use_gate == 1
     assert o.small_max_bytes == 16384 and o.slot_items == 65536 and o.num_slots == 4
     assert o.always_validate == 0 and o.memset_byte == 0 and o.byte_offset == 0
+    assert o.use_graph == 1 and o.reduce_engine == 0 and o.ce_min_bytes == 0
+    assert o.time_kernels == 0 and o.vec_bytes == 0 and o.unroll == 0
+
+
+def test_options_struct_matches_header(tb):
+    # every tb_options field of include/tb.h, in order, is in the binding
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct {\n    /* SRC_ROTATE_BYTES"):text.index("} tb_options;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"^\s*(?:u?int\d+_t)\s+(\w+);", body, flags=re.M)
+    assert fields == [name for name, _ in tb.Options._fields_]
+
+
+def test_options_env_new_fields(tb, monkeypatch):
+    monkeypatch.setenv("TB_USE_GRAPH", "0")
+    monkeypatch.setenv("TB_REDUCE_ENGINE", "2")
+    monkeypatch.setenv("TB_CE_MIN_BYTES", "1MiB")
+    o = tb.options_from_env()
+    assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
 
 
 def test_options_from_env(tb, monkeypatch):
