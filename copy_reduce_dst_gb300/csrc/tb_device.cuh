@@ -80,6 +80,21 @@ __device__ __forceinline__ void vadd(Vec<VB> &acc, const Vec<VB> &x)
 }
 
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream be scheduled once every CTA of this one has issued it;
+// wait_prerequisite returns once the kernel this one was launched behind
+// has completed and its memory operations are visible.  Both do nothing
+// for a launch without the programmatic attribute.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prerequisite()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_ns()
 {
     uint64_t t;

@@ -255,6 +255,7 @@ int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src,
                              o.block_threads, o.vec_bytes, o.unroll, o.memset_byte, ctx->num_sms,
                              o.reduce_engine);
     p->status = ctx->reduce_status_dev;
+    p->pdl = o.use_pdl ? 1 : 0;
     if (rc == TB_EINVAL)
         return fail(ctx, rc,
                     "reduce-copy arguments rejected (nSrc in [0,%d], numBytes %% 4 == 0, "
@@ -480,6 +481,7 @@ void tb_options_default(tb_options *o)
     o->reduce_engine = 0;
     o->ce_min_bytes = 0;
     o->use_graph = 1;
+    o->use_pdl = 1;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -548,6 +550,7 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_REDUCE_ENGINE", &o->reduce_engine, &bad);
     env_u64("TB_CE_MIN_BYTES", &o->ce_min_bytes, &bad);
     env_i32("TB_USE_GRAPH", &o->use_graph, &bad);
+    env_i32("TB_USE_PDL", &o->use_pdl, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 

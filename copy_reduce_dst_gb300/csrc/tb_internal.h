@@ -36,6 +36,7 @@ struct ReducePlan {
     size_t smem_bytes;     // dynamic shared memory of the launch
     uint32_t memset_word;  // 0-source fill, the memset byte repeated
     uint32_t *status;      // nullable, device-visible: 1 if a bounded wait expired
+    int pdl;               // 1 = launch with programmatic dependent launch
 };
 
 // Picks engine, vector width, head/tail, sub-executor split, grid and unroll

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(512) k_reduce(const ReduceArgs a)
     const uint32_t tid = threadIdx.x;
     const uint32_t bd = blockDim.x;
     const SubRange sr = sub_range(a.nvec, a.nsub);
+    pdl_launch_dependents();
+    pdl_wait_prerequisite();
 
     const char *s[N > 0 ? N : 1];
 #pragma unroll
@@ -147,6 +149,8 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
     const uint32_t tid = threadIdx.x;
     const uint32_t bd = blockDim.x;
     const SubRange sr = sub_range(a.nvec, a.nsub);
+    pdl_launch_dependents();
+    pdl_wait_prerequisite();
     const uint64_t vend = sr.vend;
     const uint64_t tile = (uint64_t)bd * 2;
     const uint64_t step = (uint64_t)sr.nparts * tile;
@@ -219,6 +223,8 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
     const uint32_t bars = smem_u32(smem);
     const uint32_t stages = smem_u32(smem + 128);
     const uint64_t sbase = (uint64_t)(a.head) * 4;
+    pdl_launch_dependents();
+    pdl_wait_prerequisite();
 
     // Tile j of this CTA: first body vector and vector count.
     auto tile = [&](uint64_t j, uint64_t &v0, uint32_t &nv) {
@@ -517,25 +523,30 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.nsub = (uint32_t)p.num_subexec;
     a.memset_word = p.memset_word;
     a.status = p.status;
-    const unsigned grid = (unsigned)p.grid;
     if (p.n == 0)
         return cudaSuccess;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.block_threads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
     if (p.engine == 2) {
         size_t smem = 0;
         BulkKernel k = pick_bulk(p.n_src, &smem);
         if (!k || resident_ctas((const void *)k, kBulkThreads, smem) < 1)
             return cudaErrorInvalidValue;
-        k<<<grid, kBulkThreads, smem, stream>>>(a);
-    } else if (p.n_src > 8) {
-        if (p.vec_bytes == 16)
-            k_reduce_many<16><<<grid, p.block_threads, 0, stream>>>(a, p.n_src);
-        else
-            k_reduce_many<4><<<grid, p.block_threads, 0, stream>>>(a, p.n_src);
-    } else {
-        ReduceKernel k = pick_reduce(p.n_src, p.vec_bytes, p.unroll);
-        k<<<grid, p.block_threads, 0, stream>>>(a);
+        cfg.blockDim = dim3(kBulkThreads);
+        cfg.dynamicSmemBytes = smem;
+        return cudaLaunchKernelEx(&cfg, k, a);
     }
-    return cudaGetLastError();
+    if (p.n_src > 8)
+        return cudaLaunchKernelEx(&cfg, p.vec_bytes == 16 ? k_reduce_many<16> : k_reduce_many<4>, a,
+                                  p.n_src);
+    return cudaLaunchKernelEx(&cfg, pick_reduce(p.n_src, p.vec_bytes, p.unroll), a);
 }
 
 }  // namespace tb

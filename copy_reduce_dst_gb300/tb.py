@@ -62,6 +62,7 @@ class Options(ct.Structure):
         ("reduce_engine", _i32),
         ("ce_min_bytes", _u64),
         ("use_graph", _i32),
+        ("use_pdl", _i32),
     ]
 
 

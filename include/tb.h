@@ -144,6 +144,13 @@ typedef struct {
        with always_validate, which needs the host between iterations.
        Default 1. */
     int32_t use_graph;
+    /* 1 = reduce-copy kernels are launched with programmatic dependent
+       launch: a launch may be scheduled while the previous kernel on its
+       stream drains, and every CTA waits for that kernel to complete and its
+       writes to be visible before it touches memory, so the results are
+       those of serialised launches with less idle time between them.
+       Default 1. */
+    int32_t use_pdl;
 } tb_options;
 
 /* Fills *opt with the defaults above. */

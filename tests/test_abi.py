@@ -98,7 +98,7 @@ def test_options_defaults(tb):
     assert o.rotate_bytes == 256 << 20 and o.warmup == 3 and o.use_gate == 1
     assert o.small_max_bytes == 16384 and o.slot_items == 65536 and o.num_slots == 4
     assert o.always_validate == 0 and o.memset_byte == 0 and o.byte_offset == 0
-    assert o.use_graph == 1 and o.reduce_engine == 0 and o.ce_min_bytes == 0
+    assert o.use_graph == 1 and o.reduce_engine == 0 and o.ce_min_bytes == 0 and o.use_pdl == 1
     assert o.time_kernels == 0 and o.vec_bytes == 0 and o.unroll == 0
 
 
@@ -115,8 +115,10 @@ def test_options_env_new_fields(tb, monkeypatch):
     monkeypatch.setenv("TB_USE_GRAPH", "0")
     monkeypatch.setenv("TB_REDUCE_ENGINE", "2")
     monkeypatch.setenv("TB_CE_MIN_BYTES", "1MiB")
+    monkeypatch.setenv("TB_USE_PDL", "0")
     o = tb.options_from_env()
     assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
+    assert o.use_pdl == 0
 
 
 def test_options_from_env(tb, monkeypatch):

@@ -319,6 +319,72 @@ def test_single_transfer_mechanism(tb):
             assert abs(sum(r["iter_ms"]) - r["total_ms"]) < 1e-3 * r["total_ms"] + 1e-6
 
 
+@pytest.mark.parametrize("pdl", [1, 0])
+@pytest.mark.parametrize("engine,nsrc", [(1, 2), (2, 2), (2, 4), (1, 10)])
+def test_back_to_back_launches_read_previous_output(tb, engine, nsrc, pdl):
+    """A chain of launches on one stream with no host synchronisation, each
+    reading what the launch before it wrote (x_{j+1} = x_j + c_1 + ...).
+    With programmatic dependent launch a kernel is scheduled while its
+    predecessor drains; its CTAs must still see every byte the predecessor
+    wrote, so the chain ends bit-exact with the oracle's."""
+    import torch
+    n = (24 << 20) // 4 + 7                     # 24 MiB + a ragged tail
+    g = np.random.default_rng(300 + 10 * engine + nsrc)
+    x0 = finite_floats(g, n, max_exp=120)
+    consts = [finite_floats(g, n, max_exp=120) for _ in range(nsrc - 1)]
+    with tb.Context(0, tb.options(reduce_engine=engine, use_pdl=pdl)) as c:
+        bufs = [to_dev(x0), dev_bytes(4 * n)]
+        cd = [to_dev(k) for k in consts]
+        st = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        steps = 9
+        for j in range(steps):
+            cur, nxt = bufs[j % 2], bufs[(j + 1) % 2]
+            c.reduce_copy([cur.data_ptr()] + [k.data_ptr() for k in cd], nxt.data_ptr(), 4 * n,
+                          0, st)
+        st.synchronize()
+        got = to_host(bufs[steps % 2]).view(np.float32)
+    exp = x0
+    for _ in range(steps):
+        exp = oracle.dst_reference([exp] + consts)
+    mm = oracle.first_mismatch(got.view(np.uint32), exp.view(np.uint32))
+    assert mm == -1, f"first mismatch at element {mm}"
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_captured_chain_reads_previous_output(tb, engine):
+    """The same chain captured into one CUDA graph through the caller's
+    stream (as the bench's timed loop is): consecutive kernel nodes get
+    programmatic edges, and the result is still the serial one."""
+    import torch
+    n = (16 << 20) // 4 + 3
+    g = np.random.default_rng(400 + engine)
+    x0 = finite_floats(g, n, max_exp=120)
+    c1 = finite_floats(g, n, max_exp=120)
+    with tb.Context(0, tb.options(reduce_engine=engine)) as c:
+        bufs = [to_dev(x0), dev_bytes(4 * n)]
+        cd = to_dev(c1)
+        st = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        steps = 6
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            for j in range(steps):
+                c.reduce_copy([bufs[j % 2].data_ptr(), cd.data_ptr()],
+                              bufs[(j + 1) % 2].data_ptr(), 4 * n, 0, st)
+        bufs[0].copy_(to_dev(x0))             # capture does not run the kernels
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got = to_host(bufs[steps % 2]).view(np.float32)
+        del graph
+    exp = x0
+    for _ in range(steps):
+        exp = oracle.dst_reference([exp, c1])
+    mm = oracle.first_mismatch(got.view(np.uint32), exp.view(np.uint32))
+    assert mm == -1, f"first mismatch at element {mm}"
+
+
 @pytest.mark.parametrize("graph", [1, 0])
 @pytest.mark.parametrize("iters,warmup,K", [(5, 3, 8), (1, 3, 8), (8, 0, 8), (3, 5, 4), (7, 2, 1)])
 def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K, graph):
