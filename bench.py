@@ -523,6 +523,7 @@ def study(args, tb, torch, local):
             row["off_over_on_warm_graph"] = round(row["off_warm_graph_gbps"] / row["on_warm_graph_gbps"], 3)
             print(json.dumps(row), flush=True)
     del flush
+    study_batch_configs(tb, torch, local)
     study_batch_phases(tb, torch, local)
     study_batch_routing(tb, torch, local)
     study_interference(tb, torch, local)
@@ -618,6 +619,67 @@ def study_interference(tb, torch, local):
                           "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
                           "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
               flush=True)
+
+
+def study_batch_configs(tb, torch, local):
+    """The three batch workloads side by side: 3840 x 2112 B pages into a
+    1 GiB pool, 7200 copies of 512 B-16 KiB, and the 47,540-descriptor batch.
+    kernel_us = kernel-only events (median of 20); device_us = events around
+    30 back-to-back calls (work-list upload + kernel); wall_us = one call
+    with packing, upload, kernel and stream sync (median of 20); each_ms =
+    one cudaMemcpyAsync per copy, wall-timed the same way (best of 2)."""
+    import statistics as st
+    from copy_reduce_dst_gb300 import workloads
+    for layout in (workloads.batch_index_pages(), workloads.batch_block_pages(),
+                   workloads.batch_head_sliced()):
+        src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+        dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+        desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+        stream = torch.cuda.Stream()
+        moved = 2 * int(layout.total_bytes)
+        with tb.Context(local, ctx_options(tb, time_kernels=1)) as kctx, \
+                tb.Context(local, ctx_options(tb)) as ctx:
+            for _ in range(3):
+                kctx.batch_copy(desc, stream)
+            kern = []
+            for _ in range(20):
+                kctx.batch_copy(desc, stream)
+                kern.append(kctx.last_batch_kernel_ms())
+            for _ in range(3):
+                ctx.batch_copy(desc, stream)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            a.record(stream)
+            for _ in range(30):
+                ctx.batch_copy(desc, stream)
+            b.record(stream)
+            b.synchronize()
+            dev_ms = a.elapsed_time(b) / 30
+            walls = []
+            for _ in range(20):
+                t0 = time.perf_counter()
+                ctx.batch_copy(desc, stream)
+                stream.synchronize()
+                walls.append(time.perf_counter() - t0)
+            each = []
+            for _ in range(2):
+                t0 = time.perf_counter()
+                ctx.copy_each(desc, stream)
+                stream.synchronize()
+                each.append(time.perf_counter() - t0)
+        k_ms = st.median(kern)
+        wall = st.median(walls)
+        print(json.dumps({
+            "study": "batch configs", "workload": layout.name, "descriptors": layout.n,
+            "bytes_copied": int(layout.total_bytes),
+            "kernel_us": round(k_ms * 1e3, 2), "kernel_gbps": round(moved / (k_ms / 1e3) / 1e9, 1),
+            "device_us": round(dev_ms * 1e3, 2), "device_gbps": round(moved / (dev_ms / 1e3) / 1e9, 1),
+            "wall_us": round(wall * 1e6, 1), "copies_per_s_wall": round(layout.n / wall, 1),
+            "copies_per_s_device": round(layout.n / (dev_ms / 1e3), 1),
+            "each_ms": round(min(each) * 1e3, 3),
+            "speedup_vs_memcpy_each": round(min(each) / wall, 1)}), flush=True)
+        del src, dst
 
 
 def study_batch_phases(tb, torch, local):

@@ -16,15 +16,25 @@ using namespace dev;
 
 // ---------------------------------------------------------------------------
 // K2: batched copy.  copy_range copies len bytes with `size` cooperating
-// threads (a warp or a CTA), any alignment:
-//   - head bytes until dst is 16-byte aligned, a byte per thread;
-//   - body in 16-byte vectors: direct when src is then 16-byte aligned too,
-//     otherwise every output vector is funnel-shifted out of the two aligned
-//     source vectors that hold its bytes (both contain bytes of the range,
-//     so no load leaves the source's aligned 16-byte words);
-//   - tail bytes, a byte per thread.
+// threads (a warp or part of one, or a CTA), any alignment:
+//   - src and dst equal modulo 32: head bytes until dst is 32-byte aligned,
+//     then 32-byte vectors (the 256-bit global access of sm_100-class GPUs);
+//   - else: head bytes until dst is 16-byte aligned, then 16-byte vectors,
+//     direct when src is then 16-byte aligned too, otherwise every output
+//     vector is funnel-shifted out of the two aligned source vectors that
+//     hold its bytes (both contain bytes of the range, so no load leaves the
+//     source's aligned 16-byte words);
+//   - tail bytes; head and tail go a byte per thread.
+// The body goes in rounds: each thread issues all its loads of a round,
+// predicated on the range, before its stores, so a range of up to
+// size * 32 * kWideUnroll bytes (32-byte path) costs one memory round trip.
+// The unrolls are the largest that compile without spilling at the kernel's
+// 64 registers (four 256-thread CTAs per SM); spilling variants (4 or 8
+// wide vectors) measured 1.3-1.7x slower on the short copies.
 // ---------------------------------------------------------------------------
-constexpr int kCopyUnroll = 4;
+constexpr int kWideUnroll = 2;    // 32-byte vectors per thread and round
+constexpr int kNarrowUnroll = 2;  // 16-byte vectors per thread and round
+constexpr int kShiftUnroll = 1;   // funnel-shifted 16-byte vectors per thread and round
 
 __device__ __forceinline__ uint4 ld16(const uint4 *p)
 {
@@ -39,6 +49,13 @@ __device__ __forceinline__ void st16(uint4 *p, const uint4 &v)
 {
     asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w));
+}
+
+__device__ __forceinline__ void st32(void *p, const Vec<32> &v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+                 "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+                 "r"(v.w[7]));
 }
 
 // Bytes sh .. sh+15 of the 32-byte concatenation lo|hi (little-endian).
@@ -57,56 +74,77 @@ __device__ __forceinline__ uint4 shift_pair(const uint4 &lo, const uint4 &hi, ui
     return r;
 }
 
+__device__ __forceinline__ void copy_bytes(uint8_t *dst, const uint8_t *src, uint64_t len,
+                                           uint32_t rank, uint32_t size)
+{
+    for (uint64_t b = rank; b < len; b += size)
+        dst[b] = src[b];
+}
+
 __device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, uint64_t len,
                                            uint32_t rank, uint32_t size)
 {
-    uint64_t h = (16u - ((uintptr_t)dst & 15u)) & 15u;
+    const uint32_t align = ((((uintptr_t)src ^ (uintptr_t)dst) & 31u) == 0) ? 32u : 16u;
+    uint64_t h = (align - ((uintptr_t)dst & (align - 1))) & (align - 1);
     if (h > len)
         h = len;
-    for (uint64_t b = rank; b < h; b += size)
-        dst[b] = src[b];
+    copy_bytes(dst, src, h, rank, size);
     dst += h;
     src += h;
     len -= h;
 
-    const uint64_t nv = len >> 4;
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    const uint32_t sh = (uint32_t)((uintptr_t)src & 15u);
-    uint64_t v = rank;
-    if (sh == 0) {
-        const uint4 *s = reinterpret_cast<const uint4 *>(src);
-        for (; v + (kCopyUnroll - 1) * (uint64_t)size < nv; v += kCopyUnroll * (uint64_t)size) {
-            uint4 r[kCopyUnroll];
+    uint64_t done;
+    if (align == 32) {
+        const uint64_t nv = len >> 5;
+        for (uint64_t v = rank; v < nv; v += kWideUnroll * (uint64_t)size) {
+            Vec<32> r[kWideUnroll];
 #pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u)
-                r[u] = ld16(s + v + u * size);
+            for (int u = 0; u < kWideUnroll; ++u)
+                if (v + u * (uint64_t)size < nv)
+                    vload<32>(r[u], src + (v + u * (uint64_t)size) * 32);
 #pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u)
-                st16(d + v + u * size, r[u]);
+            for (int u = 0; u < kWideUnroll; ++u)
+                if (v + u * (uint64_t)size < nv)
+                    st32(dst + (v + u * (uint64_t)size) * 32, r[u]);
         }
-        for (; v < nv; v += size)
-            st16(d + v, ld16(s + v));
+        done = nv << 5;
     } else {
-        const uint4 *s = reinterpret_cast<const uint4 *>(src - sh);
-        const uint32_t q = sh >> 2, rbits = (sh & 3u) * 8u;
-        for (; v + (kCopyUnroll - 1) * (uint64_t)size < nv; v += kCopyUnroll * (uint64_t)size) {
-            uint4 lo[kCopyUnroll], hi[kCopyUnroll];
+        const uint64_t nv = len >> 4;
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        const uint32_t sh = (uint32_t)((uintptr_t)src & 15u);
+        if (sh == 0) {
+            const uint4 *s = reinterpret_cast<const uint4 *>(src);
+            for (uint64_t v = rank; v < nv; v += kNarrowUnroll * (uint64_t)size) {
+                uint4 r[kNarrowUnroll];
 #pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u) {
-                lo[u] = ld16(s + v + u * size);
-                hi[u] = ld16(s + v + u * size + 1);
+                for (int u = 0; u < kNarrowUnroll; ++u)
+                    if (v + u * (uint64_t)size < nv)
+                        r[u] = ld16(s + v + u * size);
+#pragma unroll
+                for (int u = 0; u < kNarrowUnroll; ++u)
+                    if (v + u * (uint64_t)size < nv)
+                        st16(d + v + u * size, r[u]);
             }
+        } else {
+            const uint4 *s = reinterpret_cast<const uint4 *>(src - sh);
+            const uint32_t q = sh >> 2, rbits = (sh & 3u) * 8u;
+            for (uint64_t v = rank; v < nv; v += kShiftUnroll * (uint64_t)size) {
+                uint4 lo[kShiftUnroll], hi[kShiftUnroll];
 #pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u)
-                st16(d + v + u * size, shift_pair(lo[u], hi[u], q, rbits));
+                for (int u = 0; u < kShiftUnroll; ++u)
+                    if (v + u * (uint64_t)size < nv) {
+                        lo[u] = ld16(s + v + u * size);
+                        hi[u] = ld16(s + v + u * size + 1);
+                    }
+#pragma unroll
+                for (int u = 0; u < kShiftUnroll; ++u)
+                    if (v + u * (uint64_t)size < nv)
+                        st16(d + v + u * size, shift_pair(lo[u], hi[u], q, rbits));
+            }
         }
-        for (; v < nv; v += size)
-            st16(d + v, shift_pair(ld16(s + v), ld16(s + v + 1), q, rbits));
+        done = nv << 4;
     }
-
-    const uint64_t done = nv << 4;
-    for (uint64_t b = done + rank; b < len; b += size)
-        dst[b] = src[b];
+    copy_bytes(dst + done, src + done, len - done, rank, size);
 }
 
 __device__ __forceinline__ WorkItem load_item(const WorkItem *p)
@@ -128,6 +166,7 @@ struct BatchArgs {
     uint64_t long_bytes;
     uint32_t n_short;
     uint32_t chunks;
+    uint32_t claim_items;        // short copies a warp takes at a time: 1 or 2
 };
 
 // ---------------------------------------------------------------------------
@@ -284,11 +323,39 @@ __device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
     }
 }
 
-// Short copies claimed per atomic: a warp takes kClaim items at a time and
-// copies them side by side, 32 / kClaim lanes each, so their loads are in
-// flight together.
-constexpr uint32_t kClaim = 2;
-constexpr uint32_t kLanesPerItem = 32 / kClaim;
+// Short copies.  A warp takes C items at a time (C = 1 or 2) and copies them
+// side by side, 32 / C lanes each, so their loads are in flight together.
+// Its first C items are fixed by its index among the warps that start on
+// short copies (no atomic); the items past those first rounds are claimed
+// from the counter, each warp claiming its next items before copying the
+// current ones so that the claim's latency overlaps the copy.
+template <uint32_t C>
+__device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first, uint32_t dyn_base,
+                                             bool dynamic, uint32_t lane)
+{
+    constexpr uint32_t kLanes = 32 / C;
+    const uint32_t n_short = a.n_short;
+    const uint32_t group = lane / kLanes, rank = lane % kLanes;
+    uint32_t base = first;
+    if (base >= n_short && dynamic) {
+        uint32_t c = 0;
+        if (lane == 0)
+            c = dyn_base + atomicAdd(a.claim, C);
+        base = __shfl_sync(0xffffffffu, c, 0);
+    }
+    while (base < n_short) {
+        uint32_t next = n_short;
+        if (dynamic && lane == 0)
+            next = dyn_base + atomicAdd(a.claim, C);
+        const uint32_t i = base + group;
+        if (i < n_short) {
+            const WorkItem w = load_item(a.shorts + i);
+            copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
+                       w.len, rank, kLanes);
+        }
+        base = __shfl_sync(0xffffffffu, next, 0);
+    }
+}
 
 // Persistent grid of one wave.
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
@@ -296,12 +363,11 @@ constexpr uint32_t kLanesPerItem = 32 / kClaim;
 //   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned
 //   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
 //   the leftover edges.
-//   Short copies: every warp (warp 0 once its pipeline has drained) claims
-//   kClaim items at a time from a counter in global memory and copies them
-//   side by side, 32 / kClaim lanes each; it claims the next ones before
-//   copying, so the claim's latency overlaps the copy.  Whichever warp is
-//   free takes the next items, which balances the work without any ordering
-//   on the host.
+//   Short copies (short_copies): the warps free at the start (all of them,
+//   or warps 1.. when there are long chunks) take a first claim_items items
+//   each by warp index; the rest are claimed from a counter in global memory
+//   by whichever warp is free, warp 0 joining once its pipeline has
+//   drained, which balances the work without any ordering on the host.
 __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -322,24 +388,20 @@ __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
         }
     }
 
-    const uint32_t n_short = a.n_short;
-    uint32_t base = 0;
-    if (lane == 0)
-        base = atomicAdd(a.claim, kClaim);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const uint32_t group = lane / kLanesPerItem, rank = lane % kLanesPerItem;
-    while (base < n_short) {
-        uint32_t next = 0;
-        if (lane == 0)
-            next = atomicAdd(a.claim, kClaim);
-        const uint32_t i = base + group;
-        if (i < n_short) {
-            const WorkItem w = load_item(a.shorts + i);
-            copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
-                       w.len, rank, kLanesPerItem);
-        }
-        base = __shfl_sync(0xffffffffu, next, 0);
-    }
+    // Warps that start on short copies, and this warp's index among them.
+    const uint32_t wpc = blockDim.x >> 5;
+    const bool busy0 = a.chunks > 0;  // warp 0 runs the bulk pipeline first
+    const uint32_t starters = gridDim.x * (busy0 ? wpc - 1 : wpc);
+    const bool starter = !(busy0 && warp == 0);
+    const uint32_t sidx = blockIdx.x * (busy0 ? wpc - 1 : wpc) + (busy0 ? warp - 1 : warp);
+    const uint32_t C = a.claim_items;
+    const uint32_t fixed = starters * C;  // items taken by index
+    const bool dynamic = fixed < a.n_short;
+    const uint32_t first = starter ? sidx * C : a.n_short;
+    if (C == 1)
+        short_copies<1>(a, first, fixed, dynamic, lane);
+    else
+        short_copies<2>(a, first, fixed, dynamic, lane);
 }
 
 }  // namespace
@@ -367,6 +429,7 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.long_bytes = plan.long_bytes;
     a.n_short = plan.n_short;
     a.chunks = plan.chunks;
+    a.claim_items = batch_claim_items(plan);
     // Short copies only: no shared memory needed.
     const size_t smem = plan.chunks ? kBatchSmem : 0;
     k_batch<<<plan.grid, kBatchThreads, smem, stream>>>(a);

@@ -138,6 +138,10 @@ int batch_grid(const BatchCounts &c, int full_grid);
 // Completes a buffer gather_batch filled: header, long copies, prefix and
 // chunk table; fills *out.
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out);
+// Short copies a warp of the launch takes at a time: 1 (a whole warp per
+// copy) when the warps that start on short copies cover every short copy
+// in two rounds, else 2 (half a warp per copy, more copies in flight).
+uint32_t batch_claim_items(const BatchPlan &plan);
 
 // CTAs of `kernel` resident per SM at `threads` threads and `smem` bytes of
 // dynamic shared memory on the current device; raises the kernel's shared

@@ -160,4 +160,11 @@ void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *b
     out->upload_bytes = out->chunk_offset + ((size_t)chunks + 1) * sizeof(uint32_t);
 }
 
+uint32_t batch_claim_items(const BatchPlan &plan)
+{
+    const uint64_t warps = kBatchThreads / 32;
+    const uint64_t starters = (uint64_t)plan.grid * (plan.chunks ? warps - 1 : warps);
+    return (uint64_t)plan.n_short <= 2 * starters ? 1u : 2u;
+}
+
 }  // namespace tb

@@ -29,6 +29,7 @@ extern "C" int harness_pack(const tb_copy_desc *desc, size_t n, uint64_t small_m
     out[7] = plan.upload_bytes;
     out[8] = tb::batch_buffer_bytes(c.descs);
     out[9] = c.n_ce;
+    out[10] = tb::batch_claim_items(plan);
     return 0;
 }
 

@@ -68,6 +68,15 @@ def test_misalignment_pairs(tb, ctx, ss, ds):
     run_layout(tb, ctx, layout, 7, src_shift=ss, dst_shift=ds)
 
 
+@pytest.mark.parametrize("ss,ds", [(0, 0), (5, 5), (16, 16), (31, 31), (16, 0), (0, 16), (8, 24)])
+def test_thirty_two_byte_classes(tb, ctx, ss, ds):
+    # offsets on 32-byte boundaries, shifted: src and dst equal modulo 32 take
+    # the 32-byte path after a head of up to 31 bytes; equal modulo 16 only,
+    # the 16-byte path
+    layout = workloads.random_batch(100 + ss + ds, 3000, 9000, 64 * MiB, align=32)
+    run_layout(tb, ctx, layout, 9, src_shift=ss, dst_shift=ds)
+
+
 def test_lengths_one_byte_to_three_mib(tb, ctx):
     # Mooncake RFC "Correctness": lengths from 1 B to 3 MiB, unaligned ranges
     g = np.random.default_rng(11)

@@ -36,18 +36,18 @@ def pack(lib, desc, small_max=16384, full_grid=608, ce_min=0):
     n = desc.shape[0]
     cap = 16 + n * 32 + 8 + (16384 + 1) * 4
     buf = np.full(cap, 0xEE, dtype=np.uint8)
-    out = np.zeros(10, dtype=np.uint64)
+    out = np.zeros(11, dtype=np.uint64)
     rc = lib.harness_pack(desc.ctypes.data if n else None, n, small_max, ce_min, full_grid,
                           buf.ctypes.data, out.ctypes.data)
     assert rc == 0
-    n_short, n_long, grid, chunks, total, poff, coff, upload, bound, n_ce = (int(x) for x in out)
+    n_short, n_long, grid, chunks, total, poff, coff, upload, bound, n_ce, claim = (int(x) for x in out)
     assert upload <= bound <= cap
     assert np.all(buf[:16] == 0)                       # the claim counter starts at 0
     items = buf[16: 16 + (n_short + n_long) * 24].view(np.uint64).reshape(-1, 3)
     prefix = buf[poff: poff + (n_long + 1) * 8].view(np.uint64)
     cdesc = buf[coff: coff + (chunks + 1) * 4].view(np.uint32)
     return dict(shorts=items[:n_short], longs=items[n_short:], prefix=prefix, chunk_desc=cdesc,
-                grid=grid, chunks=chunks, total=total, n_ce=n_ce)
+                grid=grid, chunks=chunks, total=total, n_ce=n_ce, claim=claim)
 
 
 def chunk_bytes(lib, p, c):
@@ -135,3 +135,31 @@ def test_packer_batch_47540(harness):
     p = pack(harness, desc)
     assert p["grid"] == 608 and p["shorts"].shape[0] == 47520 and p["longs"].shape[0] == 20
     assert p["total"] == 288 << 20 and p["chunks"] == 608 * 8
+
+
+def short_assignment(n_short, grid, chunks, claim, warps=8):
+    """Which warp copies which short copy, following the kernel's rule: the
+    warps free at the start take `claim` copies each by index, the rest go
+    out through the counter in claim-sized runs.  Returns the copies of the
+    fixed round and of the counter round, for a coverage check."""
+    starters = grid * (warps - 1 if chunks else warps)
+    fixed = [i for w in range(starters) for i in range(w * claim, w * claim + claim) if i < n_short]
+    counted = list(range(starters * claim, n_short))
+    return fixed, counted
+
+
+@pytest.mark.parametrize("n,long_n,expect_claim", [
+    (3840, 0, 1), (7200, 0, 1), (47520, 20, 2), (100, 0, 1), (9728, 0, 1), (9729, 0, 2),
+    (8512, 20, 1), (8513, 20, 2)])
+def test_claim_items_and_coverage(harness, n, long_n, expect_claim):
+    """One copy per warp while the warps that start on short copies cover the
+    batch in two rounds, else two per warp; the fixed first round and the
+    counter together name every short copy exactly once."""
+    lens = np.full(n + long_n, 2112, dtype=np.uint64)
+    lens[n:] = 8 << 20
+    desc = np.stack([np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(24),
+                     np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(25), lens], axis=1)
+    p = pack(harness, desc)
+    assert p["claim"] == expect_claim
+    fixed, counted = short_assignment(n, p["grid"], p["chunks"], p["claim"])
+    assert sorted(fixed + counted) == list(range(n))
