@@ -160,6 +160,23 @@ def test_reduce_plan_engine_choice(tb, ctx):
         assert info["engine"] == 1 and info["vec_bytes"] == 32
 
 
+def test_vector_grid_follows_the_work(tb, ctx):
+    """The vector form launches one CTA per round of work (block_threads x
+    unroll vectors), at least one per SM and at most one full wave; the bulk
+    form and fixed sub-executor counts keep their grids."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d = dev_bytes(64 << 20)
+    p = d.data_ptr()
+    for nb in (4096, 4 << 20, 16 << 20, 24 << 20):
+        info = ctx.reduce_plan([p], p + (32 << 20), nb)
+        assert info["engine"] == 1
+        rounds = -(-info["body_vectors"] // (info["block_threads"] * info["unroll"]))
+        assert info["grid"] >= sms and (info["grid"] == sms or info["grid"] <= rounds)
+    assert ctx.reduce_plan([p], p + (32 << 20), 4 << 20)["grid"] == sms
+    assert ctx.reduce_plan([p], p + (32 << 20), 4 << 20, 1000)["grid"] == 1000
+
+
 def test_bulk_engine_limits(tb):
     d = dev_bytes(1 << 16)
     with tb.Context(0, tb.options(reduce_engine=2)) as c:
