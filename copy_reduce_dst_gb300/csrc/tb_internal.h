@@ -37,6 +37,7 @@ struct ReducePlan {
     uint32_t memset_word;  // 0-source fill, the memset byte repeated
     uint32_t *status;      // nullable, device-visible: 1 if a bounded wait expired
     int pdl;               // 1 = launch with programmatic dependent launch
+    int stages;            // bulk form: shared-memory pipeline stages
 };
 
 // Picks engine, vector width, head/tail, sub-executor split, grid and unroll

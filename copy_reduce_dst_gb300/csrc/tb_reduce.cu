@@ -32,6 +32,7 @@ struct ReduceArgs {
     uint32_t nsub;         // sub-executors; never more than the grid's CTAs
     uint32_t memset_word;
     uint32_t *status;      // nullable: set to 1 if a bounded wait expired
+    uint32_t stages;       // bulk form: pipeline stages (2 .. kRMaxStages)
 };
 
 // The CTAs of a launch are dealt to the sub-executors as evenly as integers
@@ -199,7 +200,9 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
 // with a bulk copy and refills the previous stage.  With one source the
 // tiles go straight from the load to the store (a bit copy).
 // ---------------------------------------------------------------------------
-constexpr int kRStages = 3;
+constexpr uint32_t kRStages = 3;      // stages of a CTA that shares its SM
+constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
+constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
 constexpr uint64_t kBulkMinBytes = 32ull << 20;  // auto engine: bulk from 32 MiB per source
 
@@ -215,11 +218,23 @@ __host__ __device__ constexpr uint32_t bulk_tile()
 }
 
 template <int N>
-constexpr size_t bulk_smem_bytes()
+constexpr size_t bulk_smem_bytes(uint32_t stages)
 {
-    return 128 + (size_t)kRStages * N * bulk_tile<N>();
+    return 128 + (size_t)stages * N * bulk_tile<N>();
 }
 
+// Most stages whose shared memory one CTA can hold (a CTA alone on its SM).
+template <int N>
+constexpr uint32_t bulk_max_stages()
+{
+    const size_t fit = (kSmemOptIn - 128) / ((size_t)N * bulk_tile<N>());
+    return (uint32_t)(fit < kRMaxStages ? fit : kRMaxStages);
+}
+
+// The pipeline runs a.stages stages (kRStages when CTAs share an SM, up to
+// bulk_max_stages when each CTA has an SM to itself, so one CTA keeps more
+// bytes in flight).  Stage and phase advance incrementally: tile j uses
+// stage j mod stages, on that stage's mbarrier phase floor(j / stages).
 template <int N>
 __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a)
 {
@@ -227,6 +242,7 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
     constexpr uint32_t kTile = bulk_tile<N>();
     constexpr uint32_t kTileVecs = kTile / 16;
     const uint32_t tid = threadIdx.x;
+    const uint32_t nst = a.stages;
     const SubRange sr = sub_range(a.nvec, a.nsub);
     const uint64_t span = sr.vend > sr.vbeg ? sr.vend - sr.vbeg : 0;
     const uint64_t ntiles = (span + kTileVecs - 1) / kTileVecs;
@@ -243,11 +259,10 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
         const uint64_t left = sr.vend - v0;
         nv = (uint32_t)(left < kTileVecs ? left : kTileVecs);
     };
-    auto issue = [&](uint64_t j) {
+    auto issue = [&](uint64_t j, uint32_t s) {
         uint64_t v0;
         uint32_t nv;
         tile(j, v0, nv);
-        const uint32_t s = (uint32_t)(j % kRStages);
         const uint32_t bar = bars + 8 * s;
         mbar_expect_tx(bar, N * nv * 16);
 #pragma unroll
@@ -257,17 +272,17 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
     };
 
     if (mine > 0) {
+        uint64_t issued = 0;  // tiles whose loads thread 0 has issued
         if (tid == 0) {
-            for (int s = 0; s < kRStages; ++s)
+            for (uint32_t s = 0; s < nst; ++s)
                 mbar_init(bars + 8 * s);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            for (uint64_t j = 0; j < mine && j < (uint64_t)kRStages; ++j)
-                issue(j);
+            for (; issued < mine && issued < (uint64_t)nst; ++issued)
+                issue(issued, (uint32_t)issued);
         }
         __syncthreads();
+        uint32_t s = 0, parity = 0, prev = nst - 1;
         for (uint64_t j = 0; j < mine; ++j) {
-            const uint32_t s = (uint32_t)(j % kRStages);
-            const uint32_t parity = (uint32_t)((j / kRStages) & 1);
             uint64_t v0;
             uint32_t nv;
             tile(j, v0, nv);
@@ -301,10 +316,16 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
                 if (tid == 0) {
                     if (a.status)
                         *reinterpret_cast<volatile uint32_t *>(a.status) = 1u;
-                    // Let the loads already issued land (each wait bounded again).
-                    for (uint64_t m = j; m < mine && m < j + kRStages; ++m)
-                        mbar_wait_bounded(bars + 8 * (uint32_t)(m % kRStages),
-                                          (uint32_t)((m / kRStages) & 1));
+                    // Let the loads already issued land (tiles j .. issued-1,
+                    // each wait bounded again).
+                    uint32_t ms = s, mp = parity;
+                    for (uint64_t m = j; m < issued; ++m) {
+                        mbar_wait_bounded(bars + 8 * ms, mp);
+                        if (++ms == nst) {
+                            ms = 0;
+                            mp ^= 1u;
+                        }
+                    }
                     bulk_wait_all();
                 }
                 return;
@@ -312,10 +333,17 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
             if (tid == 0) {
                 bulk_store(reinterpret_cast<uint64_t>(a.dst) + sbase + v0 * 16,
                            stages + s * N * kTile, nv * 16);
-                if (j >= 1 && j - 1 + kRStages < mine) {
+                // Refill the previous tile's stage once its store has read it.
+                if (j >= 1 && issued < mine) {
                     bulk_wait_read_all_but_newest();
-                    issue(j - 1 + kRStages);
+                    issue(issued, prev);
+                    ++issued;
                 }
+            }
+            prev = s;
+            if (++s == nst) {
+                s = 0;
+                parity ^= 1u;
             }
         }
         if (tid == 0)
@@ -331,14 +359,25 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
 
 using BulkKernel = void (*)(const ReduceArgs);
 
-BulkKernel pick_bulk(int n_src, size_t *smem)
+BulkKernel pick_bulk(int n_src, uint32_t stages, size_t *smem)
 {
     switch (n_src) {
-    case 1: *smem = bulk_smem_bytes<1>(); return k_reduce_bulk<1>;
-    case 2: *smem = bulk_smem_bytes<2>(); return k_reduce_bulk<2>;
-    case 3: *smem = bulk_smem_bytes<3>(); return k_reduce_bulk<3>;
-    case 4: *smem = bulk_smem_bytes<4>(); return k_reduce_bulk<4>;
+    case 1: *smem = bulk_smem_bytes<1>(stages); return k_reduce_bulk<1>;
+    case 2: *smem = bulk_smem_bytes<2>(stages); return k_reduce_bulk<2>;
+    case 3: *smem = bulk_smem_bytes<3>(stages); return k_reduce_bulk<3>;
+    case 4: *smem = bulk_smem_bytes<4>(stages); return k_reduce_bulk<4>;
     default: *smem = 0; return nullptr;
+    }
+}
+
+uint32_t bulk_deep_stages(int n_src)
+{
+    switch (n_src) {
+    case 1: return bulk_max_stages<1>();
+    case 2: return bulk_max_stages<2>();
+    case 3: return bulk_max_stages<3>();
+    case 4: return bulk_max_stages<4>();
+    default: return kRStages;
     }
 }
 
@@ -410,7 +449,7 @@ int default_unroll(int n_src, int vb)
 static int bulk_ctas_per_sm(int n_src)
 {
     size_t smem = 0;
-    BulkKernel k = pick_bulk(n_src, &smem);
+    BulkKernel k = pick_bulk(n_src, kRStages, &smem);
     return k ? resident_ctas((const void *)k, kBulkThreads, smem) : 0;
 }
 
@@ -475,16 +514,27 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     }
     p->vec_bytes = vb;
 
+    // A fixed sub-executor split of at most one CTA per SM (TransferBench's
+    // one block per sub-executor): every CTA has an SM to itself.
+    const bool alone = ctas_per_subexec > 0 && num_subexec > 0 &&
+                       (int64_t)num_subexec * ctas_per_subexec <= (int64_t)num_sms;
+
     // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
     // and works in 16-byte units.  It is the default from kBulkMinBytes per
     // source up, where it keeps more bytes in flight per SM than per-thread
     // vector loads; below that, its per-tile pipeline latency costs more
-    // than it saves and the vector form is faster.
+    // than it saves and the vector form is faster.  A CTA alone on its SM
+    // with 2 or 3 sources is limited by the bulk form's per-tile adds and
+    // barrier instead, and the vector form with 32-byte vectors, two per
+    // source in flight, streams more (per CTA: 77 against 60 GB/s for 2
+    // sources, 74 against 61 for 3).  One source (a relay, 103 against 89)
+    // and 4 sources (one vector per source fits: 52 against 68) stay bulk.
     const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
+    const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 3;
     p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
-                                 num_bytes >= kBulkMinBytes))
+                                 num_bytes >= kBulkMinBytes && !vector_alone))
                     ? 2
                     : 1;
     if (p->engine == 2) {
@@ -499,7 +549,12 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     }
     p->nvec = (p->n - p->head) / ((uint64_t)vb / 4);
     p->block_threads = block_threads ? block_threads : 512;
-    p->unroll = vb == 4 ? 4 : std::min(unroll ? unroll : default_unroll(n_src, vb), max_unroll(n_src, vb));
+    // Unroll: the largest that keeps two 512-thread CTAs per SM, or the
+    // largest without spills when each CTA has an SM (and its registers) alone.
+    p->unroll = vb == 4 ? 4
+                        : std::min(unroll ? unroll : (alone ? max_unroll(n_src, vb)
+                                                            : default_unroll(n_src, vb)),
+                                   max_unroll(n_src, vb));
 
     // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
     // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
@@ -509,10 +564,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // bound by launch and memory latency, and CTAs without a full round add
     // launch work without adding bytes in flight (4 MiB: 152 CTAs 2.5 us
     // against 304 CTAs 2.9 us per iteration).
-    if (p->engine == 2) {
+    if (p->engine == 2)
         p->block_threads = kBulkThreads;
-        pick_bulk(n_src, &p->smem_bytes);
-    }
     const int per_sm = p->engine == 2 ? bulk_ctas_per_sm(n_src)
                                       : reduce_ctas_per_sm(n_src, vb, p->block_threads, p->unroll);
     if (per_sm < 1)
@@ -530,6 +583,20 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         return TB_EINVAL;
     p->num_subexec = (int)S;
     p->grid = (int)G;
+    // Bulk form: three stages while CTAs share SMs; a grid of at most one CTA
+    // per SM gives every CTA all the stages one CTA's shared memory holds, so
+    // a lone CTA keeps several times more bytes in flight.
+    if (p->engine == 2) {
+        p->stages = kRStages;
+        if (G <= (int64_t)num_sms) {
+            const uint32_t deep = bulk_deep_stages(n_src);
+            size_t smem = 0;
+            BulkKernel k = pick_bulk(n_src, deep, &smem);
+            if (k && resident_ctas((const void *)k, kBulkThreads, smem) >= 1)
+                p->stages = (int)deep;
+        }
+        pick_bulk(n_src, (uint32_t)p->stages, &p->smem_bytes);
+    }
     return TB_OK;
 }
 
@@ -545,6 +612,7 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.nsub = (uint32_t)p.num_subexec;
     a.memset_word = p.memset_word;
     a.status = p.status;
+    a.stages = (uint32_t)(p.stages > 0 ? p.stages : (int)kRStages);
     if (p.n == 0)
         return cudaSuccess;
     cudaLaunchAttribute attr[1];
@@ -558,8 +626,9 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     cfg.numAttrs = p.pdl ? 1 : 0;
     if (p.engine == 2) {
         size_t smem = 0;
-        BulkKernel k = pick_bulk(p.n_src, &smem);
-        if (!k || resident_ctas((const void *)k, kBulkThreads, smem) < 1)
+        BulkKernel k = pick_bulk(p.n_src, a.stages, &smem);
+        if (!k || a.stages < 2 || a.stages > kRMaxStages ||
+            resident_ctas((const void *)k, kBulkThreads, smem) < 1)
             return cudaErrorInvalidValue;
         cfg.blockDim = dim3(kBulkThreads);
         cfg.dynamicSmemBytes = smem;

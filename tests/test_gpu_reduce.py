@@ -140,6 +140,29 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
                            num_subexec=subexec)
 
 
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4])
+@pytest.mark.parametrize("subexec", [1, 4, 32, 152])
+def test_bulk_deep_pipeline(tb, nsrc, subexec):
+    """One CTA per sub-executor and no more CTAs than SMs: each CTA runs the
+    bulk pipeline with every stage its shared memory holds (7 to 14 instead
+    of 3).  Enough tiles per CTA that the stage ring wraps many times, a head
+    and a ragged tail; bit-exact against the oracle."""
+    import torch
+    if subexec > torch.cuda.get_device_properties(0).multi_processor_count:
+        pytest.skip("fewer SMs than sub-executors")
+    n = 786432 * 2 + 5
+    g = np.random.default_rng(50 + nsrc * 7 + subexec)
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    with tb.Context(0, tb.options(reduce_engine=2, ctas_per_subexec=1)) as c:
+        d = dev_bytes(4 * n + 64)
+        info = c.reduce_plan([d.data_ptr() + 4] * nsrc, d.data_ptr() + 4, 4 * n, subexec)
+        tile = 32768 if nsrc == 1 else 8192
+        stages = (info["smem_bytes"] - 128) // (nsrc * tile)
+        assert info["grid"] == subexec and stages > 3
+        reduce_and_compare(tb, c, srcs, byte_offsets=[4] * nsrc, dst_offset=4,
+                           num_subexec=subexec)
+
+
 def test_reduce_plan_engine_choice(tb, ctx):
     d = dev_bytes(1 << 20)
     p = d.data_ptr()
@@ -158,6 +181,27 @@ def test_reduce_plan_engine_choice(tb, ctx):
     with tb.Context(0, tb.options(vec_bytes=32)) as c:
         info = c.reduce_plan([p], p + 65536, 4096)
         assert info["engine"] == 1 and info["vec_bytes"] == 32
+
+
+def test_engine_choice_one_cta_per_subexecutor(tb):
+    """With one CTA per sub-executor and no more CTAs than SMs, large
+    transfers of 2 or 3 sources take the vector form with two 32-byte
+    vectors per source in flight; 1 and 4 sources keep the bulk form with
+    its deep pipeline."""
+    d = dev_bytes(1 << 20)
+    p = d.data_ptr()
+    big = 64 << 20
+    with tb.Context(0, tb.options(ctas_per_subexec=1)) as c:
+        for n, engine in ((1, 2), (2, 1), (3, 1), (4, 2)):
+            info = c.reduce_plan([p] * n, p, big, 32)
+            assert info["engine"] == engine and info["grid"] == 32
+            if engine == 1:
+                assert info["vec_bytes"] == 32 and info["unroll"] == 2
+            else:
+                assert info["smem_bytes"] > 128 + 3 * n * (32768 if n == 1 else 8192)
+        assert c.reduce_plan([p] * 3, p, big, 1000)["engine"] == 2    # CTAs share SMs
+    with tb.Context(0) as c:
+        assert c.reduce_plan([p] * 3, p, big, 32)["engine"] == 2      # one wave shared
 
 
 def test_vector_grid_follows_the_work(tb, ctx):
