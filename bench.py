@@ -523,6 +523,7 @@ def study(args, tb, torch, local):
             row["off_over_on_warm_graph"] = round(row["off_warm_graph_gbps"] / row["on_warm_graph_gbps"], 3)
             print(json.dumps(row), flush=True)
     del flush
+    study_validation(tb, torch, local)
     study_batch_configs(tb, torch, local)
     study_batch_phases(tb, torch, local)
     study_batch_routing(tb, torch, local)
@@ -619,6 +620,53 @@ def study_interference(tb, torch, local):
                           "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
                           "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
               flush=True)
+
+
+def study_validation(tb, torch, local):
+    """Validation of a 256 MiB destination (the bench line's dst): on the
+    device (tb_validate_device, a compare kernel reading dst and an expected
+    copy in HBM, first difference by atomicMin) against the host path
+    (tb_validate: device-to-host copy in chunks and memcmp).  Wall time of
+    each synchronous call, median of 5 after 2; and the 3-source transfer
+    with validation after every iteration on the device."""
+    import statistics as st
+    nb = 256 * MiB
+    n = nb // 4
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        srcs = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(3)]
+        for k, s_ in enumerate(srcs):
+            ctx.fill_source(s_, nb, tb.default_pattern(), k)
+        dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        ctx.reduce_copy(srcs, dst, nb)
+        exp_dev = dst.clone()
+        exp_host = exp_dev.cpu().numpy()
+        torch.cuda.synchronize()
+        out = {"study": "validation", "MiB": 256}
+        for name, fn in (("device", lambda: ctx.validate_device(dst, exp_dev, nb)),
+                         ("host", lambda: ctx.validate(dst, exp_host, nb))):
+            for _ in range(2):
+                assert fn() is None
+            t = []
+            for _ in range(5):
+                t0 = time.perf_counter()
+                assert fn() is None
+                t.append(time.perf_counter() - t0)
+            ms = st.median(t) * 1e3
+            out[name + "_ms"] = round(ms, 3)
+            read = 2 * nb if name == "device" else nb
+            out[name + "_gbps_read"] = round(read / (ms / 1e3) / 1e9, 1)
+        with tb.Context(local, ctx_options(tb, always_validate=1)) as vctx:
+            walls = {}
+            for name, c, kw in (("end", ctx, {}), ("every_iteration", vctx,
+                                                   {"expected_device": exp_dev})):
+                c.run_transfer(srcs, dst, nb, 0, iters=10, rotate_bytes=0, **kw)
+                t0 = time.perf_counter()
+                c.run_transfer(srcs, dst, nb, 0, iters=10, rotate_bytes=0, **kw)
+                walls[name] = (time.perf_counter() - t0) * 1e3 / (10 + 3)
+            out["transfer_wall_ms_per_launch_no_validation"] = round(walls["end"], 4)
+            out["transfer_wall_ms_per_launch_validating_each"] = round(walls["every_iteration"], 4)
+        print(json.dumps(out), flush=True)
+        del srcs, dst, exp_dev
 
 
 def study_batch_configs(tb, torch, local):
