@@ -35,6 +35,7 @@ struct Slot {
     void *dev = nullptr;       // device copy of one packed launch
     void *host = nullptr;      // pinned staging of it
     cudaEvent_t done = nullptr;
+    cudaEvent_t uploaded = nullptr;  // the work list is on the device (upload stream)
     bool pending = false;      // `done` recorded and maybe not reached yet
     cudaEvent_t t0 = nullptr;  // kernel timing (time_kernels only)
     cudaEvent_t t1 = nullptr;
@@ -81,6 +82,7 @@ struct tb_ctx {
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
 
     Pipeline pipe;                    // staged host <-> device transfers
+    cudaStream_t up = nullptr;        // upload stream of batch work lists
     cudaStream_t ce = nullptr;        // copy-engine stream of routed batch copies
     cudaEvent_t ce_fork = nullptr, ce_join = nullptr;
 
@@ -620,7 +622,8 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
         return bail(TB_ECUDA);
     if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return bail(TB_ECUDA);
-    if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess)
+    if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ctx->up, cudaStreamNonBlocking) != cudaSuccess)
         return bail(TB_ECUDA);
 
     void *gate = nullptr;
@@ -660,7 +663,8 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
             return bail(TB_ENOMEM);
         if (cudaHostAlloc(&s.host, slot_bytes, cudaHostAllocDefault) != cudaSuccess)
             return bail(TB_ENOMEM);
-        if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess)
+        if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.uploaded, cudaEventDisableTiming) != cudaSuccess)
             return bail(TB_ECUDA);
         if (o.time_kernels &&
             (cudaEventCreate(&s.t0) != cudaSuccess || cudaEventCreate(&s.t1) != cudaSuccess))
@@ -681,6 +685,8 @@ void tb_destroy(tb_ctx *ctx)
                 cudaEventSynchronize(s.done);
             cudaEventDestroy(s.done);
         }
+        if (s.uploaded)
+            cudaEventDestroy(s.uploaded);
         if (s.t0)
             cudaEventDestroy(s.t0);
         if (s.t1)
@@ -693,6 +699,10 @@ void tb_destroy(tb_ctx *ctx)
     if (ctx->stream) {
         cudaStreamSynchronize(ctx->stream);
         cudaStreamDestroy(ctx->stream);
+    }
+    if (ctx->up) {
+        cudaStreamSynchronize(ctx->up);
+        cudaStreamDestroy(ctx->up);
     }
     for (cudaEvent_t e : ctx->events)
         cudaEventDestroy(e);
@@ -1132,6 +1142,14 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     tb_batch_stats st{};
     DeviceScope scope(ctx->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Work lists go up on the internal upload stream, so that a call's upload
+    // overlaps the kernel of the call before it; the kernel waits for it on
+    // the caller's stream.  The slot is free by then: wait_slot has seen its
+    // previous kernel finish.  While the caller's stream is being captured
+    // into a graph, the upload stays on that stream.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    TB_CUDA(ctx, cudaStreamIsCapturing(s, &capture));
+    const bool side_upload = capture == cudaStreamCaptureStatusNone;
 
     // A batch that fits one slot is checked and packed in a single pass
     // straight into the slot's pinned staging.  A larger one is checked as a
@@ -1189,8 +1207,15 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid), slot.host,
                              &plan);
             ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
-            TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
-                                         cudaMemcpyHostToDevice, s));
+            if (side_upload) {
+                TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
+                                             cudaMemcpyHostToDevice, ctx->up));
+                TB_CUDA(ctx, cudaEventRecord(slot.uploaded, ctx->up));
+                TB_CUDA(ctx, cudaStreamWaitEvent(s, slot.uploaded, 0));
+            } else {
+                TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
+                                             cudaMemcpyHostToDevice, s));
+            }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
             TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev));

@@ -393,11 +393,13 @@ typedef struct {
    alignment, with one kernel launch per descriptor slot, asynchronously on
    `stream` (ordered after the caller's earlier work on it).  The descriptor
    array is read and packed before return, so the caller may reuse it at
-   once.  The bytes of all descriptors longer than small_max_bytes form one
-   stream cut into equal chunks, the same number for every CTA, moved with
-   bulk copies through shared memory; descriptors of at most small_max_bytes
-   go to one warp each, claimed by free warps from a counter in the packed
-   work list.  Destinations must not overlap one another or any source of
+   once.  The packed work list goes to the device on an internal stream,
+   overlapping earlier work, and the kernel waits for it on `stream`.  The bytes of all descriptors longer than
+   small_max_bytes form one stream cut into equal chunks, the same number
+   for every CTA, moved with bulk copies through shared memory; descriptors
+   of at most small_max_bytes go to a warp or half a warp each, the first
+   round fixed by warp index and the rest claimed by free warps from a
+   counter in the packed work list.  Destinations must not overlap one another or any source of
    the batch (the order of copies is unspecified).  TB_EINVAL for a null
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
    slot came free within wait_timeout_ns, or when the previous batch that
