@@ -273,7 +273,8 @@ __device__ bool bulk_pipeline(const BatchArgs &a, uint32_t bars, uint32_t stages
         ++issued;
     }
     bool ok = true;
-    for (uint32_t i = 0; i < issued; ++i) {
+    uint32_t i = 0;
+    for (; i < issued; ++i) {
         const uint32_t s = i % kStages;
         if (!mbar_wait_bounded(bars + 8 * s, (uses >> s) & 1u)) {
             ok = false;
@@ -294,9 +295,12 @@ __device__ bool bulk_pipeline(const BatchArgs &a, uint32_t bars, uint32_t stages
     if (!ok) {
         if (a.status)
             *reinterpret_cast<volatile uint32_t *>(a.status) = 1u;
-        // Let the loads still in flight land (each wait bounded again).
-        for (uint32_t k = 0; k < kStages; ++k)
+        // Let the loads still in flight land: blocks i .. issued-1, at most
+        // one per stage, each on its stage's pending phase (waits bounded).
+        for (uint32_t m = i; m < issued; ++m) {
+            const uint32_t k = m % kStages;
             mbar_wait_bounded(bars + 8 * k, (uses >> k) & 1u);
+        }
     }
     bulk_wait_all();
     return ok;
