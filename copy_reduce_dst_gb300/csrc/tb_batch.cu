@@ -167,6 +167,7 @@ struct BatchArgs {
     uint32_t n_short;
     uint32_t chunks;
     uint32_t claim_items;        // short copies a warp takes at a time: 1 or 2
+    uint64_t wait_ns;            // limit of each wait for a block's load
 };
 
 // ---------------------------------------------------------------------------
@@ -276,7 +277,7 @@ __device__ bool bulk_pipeline(const BatchArgs &a, uint32_t bars, uint32_t stages
     uint32_t i = 0;
     for (; i < issued; ++i) {
         const uint32_t s = i % kStages;
-        if (!mbar_wait_bounded(bars + 8 * s, (uses >> s) & 1u)) {
+        if (!mbar_wait_bounded(bars + 8 * s, (uses >> s) & 1u, a.wait_ns)) {
             ok = false;
             break;
         }
@@ -416,7 +417,7 @@ int batch_ctas_per_sm()
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
-                         uint32_t *status)
+                         uint32_t *status, uint64_t wait_ns)
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
@@ -434,6 +435,7 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.n_short = plan.n_short;
     a.chunks = plan.chunks;
     a.claim_items = batch_claim_items(plan);
+    a.wait_ns = wait_ns;
     // Short copies only: no shared memory needed.
     const size_t smem = plan.chunks ? kBatchSmem : 0;
     k_batch<<<plan.grid, kBatchThreads, smem, stream>>>(a);

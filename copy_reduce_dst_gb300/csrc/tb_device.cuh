@@ -131,14 +131,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Waits for the phase of the given parity, for at most kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+// Non-blocking probe of the phase of the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity, for at most limit_ns; a limit of
+// 0 does not wait at all (one non-blocking probe).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs)
+{
+    if (limit_ns == 0)
+        return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs)
+        if (global_ns() - t0 > limit_ns)
             return false;
     return true;
 }

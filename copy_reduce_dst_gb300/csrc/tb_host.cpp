@@ -258,6 +258,7 @@ int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src,
                              o.reduce_engine);
     p->status = ctx->reduce_status_dev;
     p->pdl = o.use_pdl ? 1 : 0;
+    p->wait_ns = o.kernel_wait_ns;
     if (rc == TB_EINVAL)
         return fail(ctx, rc,
                     "reduce-copy arguments rejected (nSrc in [0,%d], numBytes %% 4 == 0, "
@@ -484,6 +485,7 @@ void tb_options_default(tb_options *o)
     o->ce_min_bytes = 0;
     o->use_graph = 1;
     o->use_pdl = 1;
+    o->kernel_wait_ns = 2000000000ull;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -553,6 +555,7 @@ int tb_options_from_env(tb_options *o)
     env_u64("TB_CE_MIN_BYTES", &o->ce_min_bytes, &bad);
     env_i32("TB_USE_GRAPH", &o->use_graph, &bad);
     env_i32("TB_USE_PDL", &o->use_pdl, &bad);
+    env_u64("TB_KERNEL_WAIT_NS", &o->kernel_wait_ns, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -1218,7 +1221,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-            TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev));
+            TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev, o.kernel_wait_ns));
             if (slot.t1)
                 TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
             TB_CUDA(ctx, cudaEventRecord(slot.done, s));

@@ -38,6 +38,7 @@ struct ReducePlan {
     uint32_t *status;      // nullable, device-visible: 1 if a bounded wait expired
     int pdl;               // 1 = launch with programmatic dependent launch
     int stages;            // bulk form: shared-memory pipeline stages
+    uint64_t wait_ns = 2000000000ull;  // bulk form: limit of each wait for a tile's loads
 };
 
 // Picks engine, vector width, head/tail, sub-executor split, grid and unroll
@@ -152,9 +153,10 @@ int resident_ctas(const void *kernel, int threads, size_t smem);
 
 // Launches k_batch over a packed buffer (device copy at `dev`).  status
 // (nullable, device-visible) is set to 1 if a bounded wait inside the kernel
-// expired.
+// expired; wait_ns limits each wait of its bulk pipeline for a block's load
+// (0: one non-blocking probe).
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
-                         uint32_t *status = nullptr);
+                         uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull);
 
 // CTAs resident per SM for the batch kernel.
 int batch_ctas_per_sm();

@@ -33,6 +33,7 @@ struct ReduceArgs {
     uint32_t memset_word;
     uint32_t *status;      // nullable: set to 1 if a bounded wait expired
     uint32_t stages;       // bulk form: pipeline stages (2 .. kRMaxStages)
+    uint64_t wait_ns;      // bulk form: limit of each wait for a tile's loads
 };
 
 // The CTAs of a launch are dealt to the sub-executors as evenly as integers
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
             tile(j, v0, nv);
             bool expired = false;
             if (N > 1 || tid == 0) {
-                expired = !mbar_wait_bounded(bars + 8 * s, parity);
+                expired = !mbar_wait_bounded(bars + 8 * s, parity, a.wait_ns);
                 if (N > 1 && !expired) {
                     const uint32_t out = stages + s * N * kTile;
                     for (uint32_t v = tid; v < nv; v += kBulkThreads) {
@@ -613,6 +614,7 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.memset_word = p.memset_word;
     a.status = p.status;
     a.stages = (uint32_t)(p.stages > 0 ? p.stages : (int)kRStages);
+    a.wait_ns = p.wait_ns;
     if (p.n == 0)
         return cudaSuccess;
     cudaLaunchAttribute attr[1];

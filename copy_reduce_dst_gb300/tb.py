@@ -63,6 +63,7 @@ class Options(ct.Structure):
         ("ce_min_bytes", _u64),
         ("use_graph", _i32),
         ("use_pdl", _i32),
+        ("kernel_wait_ns", _u64),
     ]
 
 

@@ -151,6 +151,15 @@ typedef struct {
        those of serialised launches with less idle time between them.
        Default 1. */
     int32_t use_pdl;
+    /* Limit, in nanoseconds, of each wait inside the kernels' shared-memory
+       pipelines (bulk reduce-copy, batched copy) for a load to land.  A wait
+       that runs out makes the kernel record the failure in a status word,
+       wait (up to 2 s each) for the loads it has already issued, and stop;
+       the call that reads the status returns TB_ETIMEOUT (tb_run_transfer;
+       for batches, the next call that reuses the slot, or
+       tb_last_batch_kernel_ms).  0 = never wait: a load that has not landed
+       at the first check counts as expired.  Default 2e9. */
+    uint64_t kernel_wait_ns;
 } tb_options;
 
 /* Fills *opt with the defaults above. */

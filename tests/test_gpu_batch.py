@@ -181,6 +181,30 @@ def test_slot_wait_deadline(tb):
         st.synchronize()
 
 
+def test_pipeline_wait_expiry_is_reported(tb):
+    """kernel_wait_ns = 0: the bulk pipeline of the long copies cannot meet
+    its first wait; the kernel records it in the slot's status word and
+    stops its pipeline after the issued loads land.  The failure comes back
+    as TB_ETIMEOUT from tb_last_batch_kernel_ms and from the next call that
+    reuses the slot; a context with the default limit then copies the same
+    batch bit-exactly."""
+    import torch
+    with tb.Context(0, tb.options(kernel_wait_ns=0, time_kernels=1, num_slots=1)) as c:
+        layout = workloads.random_batch(61, 40, 4 * MiB, 256 * MiB, align=64, min_len=1 * MiB)
+        src = torch.zeros(256 * MiB, dtype=torch.uint8, device="cuda")
+        dst = torch.zeros(256 * MiB, dtype=torch.uint8, device="cuda")
+        desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+        c.batch_copy(desc)
+        with pytest.raises(tb.TBError) as e:
+            c.last_batch_kernel_ms()
+        assert e.value.code == tb.TB_ETIMEOUT
+        with pytest.raises(tb.TBError) as e:
+            c.batch_copy(desc)                   # the slot reports it once
+        assert e.value.code == tb.TB_ETIMEOUT
+    with tb.Context(0) as c:
+        run_layout(tb, c, layout, 62)
+
+
 # ---------------------------------------------------------------------------
 # Full-size layouts, in the launch configuration the bench times
 # ---------------------------------------------------------------------------

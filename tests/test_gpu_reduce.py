@@ -578,6 +578,30 @@ def test_gate_deadline_returns_timeout(tb):
         assert r["gated"] == 0 and r["graphed"] == 0
 
 
+@pytest.mark.parametrize("nsrc,graph", [(3, 1), (3, 0), (1, 1)])
+def test_pipeline_wait_expiry_is_reported(tb, nsrc, graph):
+    """kernel_wait_ns = 0: the bulk pipeline's wait for the first tile's loads
+    cannot be met (they were issued a few instructions earlier), so the
+    kernel records the failure, lets the loads it issued land and stops.
+    tb_run_transfer reports TB_ETIMEOUT; the context and the device stay
+    usable, and a normal transfer afterwards is bit-exact."""
+    nb = 64 * MiB
+    n = nb // 4
+    srcs = [dev_bytes(nb) for _ in range(nsrc)]
+    dst = dev_bytes(nb, fill=0)
+    with tb.Context(0, tb.options(reduce_engine=2, kernel_wait_ns=0, use_graph=graph)) as c:
+        for k, s_ in enumerate(srcs):
+            c.fill_source(s_, nb, tb.default_pattern(), k)
+        with pytest.raises(tb.TBError) as e:
+            c.run_transfer(srcs, dst, nb, iters=2, rotate_bytes=0)
+        assert e.value.code == tb.TB_ETIMEOUT
+        assert "expired" in str(e.value)
+    with tb.Context(0, tb.options(reduce_engine=2)) as c:
+        expect = oracle.dst_reference([oracle.prepare_reference(n, k) for k in range(nsrc)])
+        r = c.run_transfer(srcs, dst, nb, iters=2, rotate_bytes=0, expected=expect)
+        assert r["mismatch_index"] == -1
+
+
 @pytest.mark.parametrize("n", [1, 1000003, (96 << 20) // 4 + 5])
 def test_reduce_copy_host_staged(tb, ctx, n):
     """Pageable host memory: the bytes are staged through device buffers in
