@@ -841,6 +841,11 @@ int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int n_src, void *dst, u
     if (!ctx)
         return TB_EINVAL;
     DeviceScope scope(ctx->device);
+    if (ctx->reduce_status[0] != 0u) {
+        ctx->reduce_status[0] = 0u;
+        return fail(ctx, TB_ETIMEOUT, "an earlier reduce-copy on this context stopped early: a "
+                                      "bounded wait inside the kernel expired");
+    }
     tb::ReducePlan p;
     int rc = plan_for(ctx, &p, srcs, n_src, dst, num_bytes, num_subexec);
     if (rc != TB_OK)

@@ -294,7 +294,10 @@ uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
    ranges (sub-executors), each served by its own CTAs and sized in
    proportion to them (equal when numSubExec divides the grid);
    numSubExec == 0 means one per CTA of the default grid.  The split does not
-   change the result.  dst must not overlap any source. */
+   change the result.  dst must not overlap any source.  TB_ETIMEOUT, with
+   nothing launched, when an earlier launch of this context stopped early
+   because a bounded wait inside the kernel expired (kernel_wait_ns); the
+   call after that one launches again. */
 int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int nSrc, void *dst,
                    uint64_t numBytes, int numSubExec, tb_stream stream);
 

@@ -602,6 +602,22 @@ def test_pipeline_wait_expiry_is_reported(tb, nsrc, graph):
         assert r["mismatch_index"] == -1
 
 
+def test_async_reduce_copy_reports_an_earlier_expiry(tb):
+    """tb_reduce_copy is asynchronous; an expired wait in one launch is
+    reported by the context's next tb_reduce_copy, which launches nothing."""
+    import torch
+    nb = 64 * MiB
+    srcs = [dev_bytes(nb, fill=0) for _ in range(3)]
+    dst = dev_bytes(nb, fill=0)
+    with tb.Context(0, tb.options(reduce_engine=2, kernel_wait_ns=0)) as c:
+        c.reduce_copy(srcs, dst, nb)
+        torch.cuda.synchronize()
+        with pytest.raises(tb.TBError) as e:
+            c.reduce_copy(srcs, dst, nb)
+        assert e.value.code == tb.TB_ETIMEOUT
+        torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("n", [1, 1000003, (96 << 20) // 4 + 5])
 def test_reduce_copy_host_staged(tb, ctx, n):
     """Pageable host memory: the bytes are staged through device buffers in
