@@ -111,14 +111,26 @@ def test_options_struct_matches_header(tb):
     assert fields == [name for name, _ in tb.Options._fields_]
 
 
+def test_every_option_has_an_environment_variable(tb):
+    # the header's list of variables covers every tb_options field
+    text = open(HEADER).read()
+    block = text[text.index("Overrides fields of *opt from the environment"):
+                 text.index("int tb_options_from_env")]
+    names = set(re.findall(r"\bTB_([A-Z_]+)\b", block))
+    renamed = {"rotate_bytes": "SRC_ROTATE_BYTES", "memset_byte": "MEMSET_CHAR"}
+    for field, _ in tb.Options._fields_:
+        assert renamed.get(field, field.upper()) in names, field
+
+
 def test_options_env_new_fields(tb, monkeypatch):
     monkeypatch.setenv("TB_USE_GRAPH", "0")
     monkeypatch.setenv("TB_REDUCE_ENGINE", "2")
     monkeypatch.setenv("TB_CE_MIN_BYTES", "1MiB")
     monkeypatch.setenv("TB_USE_PDL", "0")
+    monkeypatch.setenv("TB_KERNEL_WAIT_NS", "0")
     o = tb.options_from_env()
     assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
-    assert o.use_pdl == 0
+    assert o.use_pdl == 0 and o.kernel_wait_ns == 0
 
 
 def test_options_from_env(tb, monkeypatch):
