@@ -87,6 +87,8 @@ struct tb_ctx {
     cudaEvent_t ce_fork = nullptr, ce_join = nullptr;
 
     void *val_stage = nullptr;        // pinned validation staging
+    void *direct_expected = nullptr;  // device copy of `expected` (validate_direct)
+    uint64_t direct_bytes = 0;
     unsigned long long *first_diff = nullptr;  // device word of the device-side compare
     uint64_t prep_h2d = 0;
     std::string err;
@@ -486,6 +488,8 @@ void tb_options_default(tb_options *o)
     o->use_graph = 1;
     o->use_pdl = 1;
     o->kernel_wait_ns = 2000000000ull;
+    o->validate_direct = 0;
+    o->validate_source = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -556,6 +560,10 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_USE_GRAPH", &o->use_graph, &bad);
     env_i32("TB_USE_PDL", &o->use_pdl, &bad);
     env_u64("TB_KERNEL_WAIT_NS", &o->kernel_wait_ns, &bad);
+    if (!env_i32("TB_VALIDATE_DIRECT", &o->validate_direct, &bad))
+        env_i32("VALIDATE_DIRECT", &o->validate_direct, &bad);
+    if (!env_i32("TB_VALIDATE_SOURCE", &o->validate_source, &bad))
+        env_i32("VALIDATE_SOURCE", &o->validate_source, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -735,6 +743,8 @@ void tb_destroy(tb_ctx *ctx)
         cudaFreeHost(ctx->slot_status);
     if (ctx->val_stage)
         cudaFreeHost(ctx->val_stage);
+    if (ctx->direct_expected)
+        cudaFree(ctx->direct_expected);
     if (ctx->first_diff)
         cudaFree(ctx->first_diff);
     delete ctx;
@@ -795,6 +805,19 @@ int tb_upload_sources(tb_ctx *ctx, void *const *srcs, const void *const *host_sr
         ctx->prep_h2d += num_bytes;
     }
     TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    // validateSource: every device source against the host copy it came from.
+    if (ctx->opt.validate_source) {
+        for (int k = 0; k < n_src; ++k) {
+            const char *d = static_cast<const char *>(srcs[k]) + ctx->opt.byte_offset;
+            tb_mismatch mm;
+            const int rc = validate_impl(ctx, d, host_srcs[k], num_bytes, 4, &mm);
+            if (rc == TB_EVALIDATE)
+                return fail(ctx, rc, "source %d differs from its host copy at element %lld", k,
+                            (long long)mm.index);
+            if (rc != TB_OK)
+                return rc;
+        }
+    }
     return TB_OK;
 }
 
@@ -827,6 +850,21 @@ int tb_prepare_sources(tb_ctx *ctx, void *const *srcs, int n_src, uint64_t num_b
         }
     }
     TB_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    // validateSource: every filled slice against slice 0, on the device.
+    if (ctx->opt.validate_source) {
+        for (int k = 0; k < n_src; ++k) {
+            const char *base = static_cast<const char *>(srcs[k]) + ctx->opt.byte_offset;
+            for (uint64_t j = 1; j < K; ++j) {
+                tb_mismatch mm;
+                const int rc = validate_device_impl(ctx, base + j * stride, base, num_bytes, 4, &mm);
+                if (rc == TB_EVALIDATE)
+                    return fail(ctx, rc, "source %d slice %llu differs from slice 0 at element %lld",
+                                k, (unsigned long long)j, (long long)mm.index);
+                if (rc != TB_OK)
+                    return rc;
+            }
+        }
+    }
     return TB_OK;
 }
 
@@ -1003,10 +1041,25 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     cudaStream_t st = ctx->stream;
     const bool has_expected = t->expected || t->expected_device;
     const bool per_iter_validate = o.always_validate && has_expected;
+    // validateDirect: the host expected values go to the device once, before
+    // the loop, and every validation compares on the GPU.
+    const void *expected_dev = t->expected_device;
+    if (!expected_dev && t->expected && o.validate_direct) {
+        if (ctx->direct_bytes < t->num_bytes) {
+            if (ctx->direct_expected)
+                TB_CUDA(ctx, cudaFree(ctx->direct_expected));
+            ctx->direct_expected = nullptr;
+            ctx->direct_bytes = 0;
+            TB_CUDA(ctx, cudaMalloc(&ctx->direct_expected, t->num_bytes));
+            ctx->direct_bytes = t->num_bytes;
+        }
+        TB_CUDA(ctx, cudaMemcpy(ctx->direct_expected, t->expected, t->num_bytes,
+                                cudaMemcpyHostToDevice));
+        expected_dev = ctx->direct_expected;
+    }
     auto check = [&](tb_mismatch *mm) {
-        return t->expected_device
-                   ? validate_device_impl(ctx, dst, t->expected_device, t->num_bytes, 4, mm)
-                   : validate_impl(ctx, dst, t->expected, t->num_bytes, 4, mm);
+        return expected_dev ? validate_device_impl(ctx, dst, expected_dev, t->num_bytes, 4, mm)
+                            : validate_impl(ctx, dst, t->expected, t->num_bytes, 4, mm);
     };
     // Graph: the whole loop (warm-up and timed iterations, the per-iteration
     // event records as external event nodes) captured and launched as one

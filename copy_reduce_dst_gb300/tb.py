@@ -64,6 +64,8 @@ class Options(ct.Structure):
         ("use_graph", _i32),
         ("use_pdl", _i32),
         ("kernel_wait_ns", _u64),
+        ("validate_direct", _i32),
+        ("validate_source", _i32),
     ]
 
 

@@ -160,6 +160,18 @@ typedef struct {
        tb_last_batch_kernel_ms).  0 = never wait: a load that has not landed
        at the first check counts as expired.  Default 2e9. */
     uint64_t kernel_wait_ns;
+    /* TransferBench's validateDirect: 1 = tb_run_transfer compares dst with
+       the expected values on the GPU (the host `expected` copied once to a
+       context-owned device buffer before the loop) instead of copying dst
+       to the host for every validation.  Unused when the transfer gives
+       expected_device.  Default 0. */
+    int32_t validate_direct;
+    /* TransferBench's validateSource: 1 = check the sources right after they
+       are initialised: tb_upload_sources compares each device source with
+       its host copy, tb_prepare_sources every filled slice with slice 0;
+       a difference returns TB_EVALIDATE naming source, slice and element.
+       Default 0. */
+    int32_t validate_source;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -171,7 +183,8 @@ void tb_options_default(tb_options *opt);
      TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
-     TB_USE_PDL, TB_KERNEL_WAIT_NS.
+     TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
+     TB_VALIDATE_SOURCE (or VALIDATE_SOURCE).
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);

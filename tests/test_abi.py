@@ -100,6 +100,7 @@ def test_options_defaults(tb):
     assert o.always_validate == 0 and o.memset_byte == 0 and o.byte_offset == 0
     assert o.use_graph == 1 and o.reduce_engine == 0 and o.ce_min_bytes == 0 and o.use_pdl == 1
     assert o.time_kernels == 0 and o.vec_bytes == 0 and o.unroll == 0
+    assert o.kernel_wait_ns == 2_000_000_000 and o.validate_direct == 0 and o.validate_source == 0
 
 
 def test_options_struct_matches_header(tb):
@@ -131,6 +132,16 @@ def test_options_env_new_fields(tb, monkeypatch):
     o = tb.options_from_env()
     assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
     assert o.use_pdl == 0 and o.kernel_wait_ns == 0
+
+
+def test_validation_options_from_env(tb, monkeypatch):
+    # the pages' variable names, and the TB_ ones winning over them
+    monkeypatch.setenv("VALIDATE_DIRECT", "1")
+    monkeypatch.setenv("VALIDATE_SOURCE", "1")
+    o = tb.options_from_env()
+    assert o.validate_direct == 1 and o.validate_source == 1
+    monkeypatch.setenv("TB_VALIDATE_SOURCE", "0")
+    assert tb.options_from_env().validate_source == 0
 
 
 def test_options_from_env(tb, monkeypatch):

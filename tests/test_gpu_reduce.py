@@ -485,10 +485,13 @@ def test_byte_offset(tb):
 
 
 @pytest.mark.parametrize("always", [0, 1])
-def test_validation_reports_first_mismatch(tb, always):
+@pytest.mark.parametrize("direct", [0, 1])
+def test_validation_reports_first_mismatch(tb, always, direct):
+    """validateDirect = 1 compares on the GPU against a device copy of the
+    host expected values; the reported mismatch is the same either way."""
     nb = 256 * 1024
     n = nb // 4
-    with tb.Context(0, tb.options(always_validate=always)) as c:
+    with tb.Context(0, tb.options(always_validate=always, validate_direct=direct)) as c:
         src = dev_bytes(nb)
         c.fill_source(src, nb, tb.default_pattern(), 0)
         dst = dev_bytes(nb)
@@ -506,6 +509,27 @@ def test_validation_reports_first_mismatch(tb, always):
         assert c.validate(dst, wrong, nb) == (12345, int(r["mismatch_expected"]),
                                               int(r["mismatch_actual"]))
         assert c.validate(dst, oracle.prepare_reference(n, 0), nb) is None
+
+
+def test_validate_source_checks_uploads_and_slices(tb):
+    """validateSource = 1: tb_upload_sources compares every device source
+    with its host copy and tb_prepare_sources every one of the 64 slices of
+    a 4 MiB source with slice 0; both pass on correct data, and the transfer
+    afterwards validates."""
+    nb = 4 * MiB
+    n = nb // 4
+    plan = tb.rotation_plan(nb, 256 * MiB)
+    refs = [oracle.prepare_reference(n, k) for k in range(2)]
+    with tb.Context(0, tb.options(validate_source=1, byte_offset=12)) as c:
+        srcs = [dev_bytes(plan.alloc_bytes + 12) for _ in range(2)]
+        c.upload_sources(srcs, refs, nb)
+        c.prepare_sources(srcs, nb, 256 * MiB)
+        whole = to_host(srcs[1])[12:12 + 64 * plan.slice_stride].reshape(64, -1)
+        assert all(np.array_equal(whole[j][:nb], refs[1].view(np.uint8)) for j in (0, 37, 63))
+        dst = dev_bytes(nb + 12, fill=0)
+        r = c.run_transfer(srcs, dst, nb, iters=4, rotate_bytes=256 * MiB,
+                           expected=oracle.dst_reference(refs))
+        assert r["mismatch_index"] == -1 and r["K"] == 64
 
 
 @pytest.mark.parametrize("da,db", [(0, 0), (4, 4), (3, 3), (0, 5), (7, 1)])
