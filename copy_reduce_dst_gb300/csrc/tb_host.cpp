@@ -490,6 +490,7 @@ void tb_options_default(tb_options *o)
     o->kernel_wait_ns = 2000000000ull;
     o->validate_direct = 0;
     o->validate_source = 0;
+    o->check_overlap = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -564,6 +565,7 @@ int tb_options_from_env(tb_options *o)
         env_i32("VALIDATE_DIRECT", &o->validate_direct, &bad);
     if (!env_i32("TB_VALIDATE_SOURCE", &o->validate_source, &bad))
         env_i32("VALIDATE_SOURCE", &o->validate_source, &bad);
+    env_i32("TB_CHECK_OVERLAP", &o->check_overlap, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -1217,11 +1219,19 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     // whole first, so that no launch happens for a batch that is rejected.
     const bool one_slot = n <= o.slot_items;
     size_t bad = 0;
-    if (!one_slot) {
+    if (!one_slot || o.check_overlap) {
         tb::BatchCounts all;
         if (tb::count_batch(desc, n, small, &all, &bad, ce_min) != TB_OK)
             return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range",
                         bad);
+    }
+    if (o.check_overlap) {
+        size_t a = 0, b = 0;
+        if (tb::find_overlap(desc, n, &a, &b))
+            return fail(ctx, TB_EINVAL,
+                        "batch_copy: descriptors %zu and %zu overlap (a destination over another "
+                        "destination or over a source)",
+                        std::min(a, b), std::max(a, b));
     }
     if (ctx->longs.size() < std::min<size_t>(n, o.slot_items))
         ctx->longs.resize(std::min<size_t>(n, o.slot_items));

@@ -140,6 +140,11 @@ int batch_grid(const BatchCounts &c, int full_grid);
 // Completes a buffer gather_batch filled: header, long copies, prefix and
 // chunk table; fills *out.
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out);
+// Looks for two descriptors whose ranges make the batch's result depend on
+// the order of the copies: two overlapping destinations, or a destination
+// overlapping a source (its own included).  Sources may overlap one
+// another.  Returns true with their indices (in either order).
+bool find_overlap(const tb_copy_desc *desc, size_t n, size_t *first, size_t *second);
 // Short copies a warp of the launch takes at a time: 1 (a whole warp per
 // copy) when the warps that start on short copies cover every short copy
 // in two rounds, else 2 (half a warp per copy, more copies in flight).

@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "tb_internal.h"
 
@@ -158,6 +159,56 @@ void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *b
     out->prefix_offset = (size_t)((const char *)prefix - base);
     out->chunk_offset = (size_t)((const char *)chunk_desc - base);
     out->upload_bytes = out->chunk_offset + ((size_t)chunks + 1) * sizeof(uint32_t);
+}
+
+bool find_overlap(const tb_copy_desc *desc, size_t n, size_t *first, size_t *second)
+{
+    // Every non-empty range, sorted by start; one sweep keeps the furthest
+    // end among the destinations and among the sources seen so far.  A
+    // range that starts before such an end overlaps that range.
+    struct Range {
+        uint64_t begin, end;
+        size_t index;
+        bool dst;
+    };
+    std::vector<Range> r;
+    r.reserve(2 * n);
+    for (size_t i = 0; i < n; ++i) {
+        if (desc[i].len == 0)
+            continue;
+        r.push_back(Range{desc[i].dst, desc[i].dst + desc[i].len, i, true});
+        r.push_back(Range{desc[i].src, desc[i].src + desc[i].len, i, false});
+    }
+    std::sort(r.begin(), r.end(), [](const Range &a, const Range &b) { return a.begin < b.begin; });
+    uint64_t dst_end = 0, src_end = 0;
+    size_t dst_at = 0, src_at = 0;
+    bool any_dst = false, any_src = false;
+    for (const Range &x : r) {
+        if (any_dst && x.begin < dst_end) {  // overlaps an earlier destination
+            *first = dst_at;
+            *second = x.index;
+            return true;
+        }
+        if (x.dst && any_src && x.begin < src_end) {  // a destination over an earlier source
+            *first = src_at;
+            *second = x.index;
+            return true;
+        }
+        if (x.dst) {
+            if (!any_dst || x.end > dst_end) {
+                dst_end = x.end;
+                dst_at = x.index;
+            }
+            any_dst = true;
+        } else {
+            if (!any_src || x.end > src_end) {
+                src_end = x.end;
+                src_at = x.index;
+            }
+            any_src = true;
+        }
+    }
+    return false;
 }
 
 uint32_t batch_claim_items(const BatchPlan &plan)

@@ -66,6 +66,7 @@ class Options(ct.Structure):
         ("kernel_wait_ns", _u64),
         ("validate_direct", _i32),
         ("validate_source", _i32),
+        ("check_overlap", _i32),
     ]
 
 

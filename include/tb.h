@@ -172,6 +172,12 @@ typedef struct {
        a difference returns TB_EVALIDATE naming source, slice and element.
        Default 0. */
     int32_t validate_source;
+    /* 1 = tb_batch_copy first sorts the descriptors' ranges and rejects,
+       with TB_EINVAL naming two of them and nothing launched, a batch whose
+       result would depend on the order of its copies: two overlapping
+       destinations, or a destination overlapping a source.  O(n log n) on
+       the host; a debugging aid.  Default 0. */
+    int32_t check_overlap;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -184,7 +190,7 @@ void tb_options_default(tb_options *opt);
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
-     TB_VALIDATE_SOURCE (or VALIDATE_SOURCE).
+     TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);

@@ -44,6 +44,15 @@ extern "C" int harness_bad(const tb_copy_desc *desc, size_t n, uint64_t *bad_out
     return rc;
 }
 
+extern "C" int harness_overlap(const tb_copy_desc *desc, size_t n, uint64_t *pair)
+{
+    size_t a = 0, b = 0;
+    const bool found = tb::find_overlap(desc, n, &a, &b);
+    pair[0] = a;
+    pair[1] = b;
+    return found ? 1 : 0;
+}
+
 extern "C" uint64_t harness_chunk_start(uint64_t total, uint64_t chunks, uint64_t c)
 {
     return tb::chunk_start(total, chunks, c);

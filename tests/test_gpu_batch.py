@@ -159,6 +159,23 @@ def test_bad_descriptors(tb, ctx):
     ctx.batch_copy(np.zeros((0, 3), dtype=np.uint64))
 
 
+def test_check_overlap(tb):
+    """check_overlap = 1: a batch whose copies overlap is rejected before
+    any launch (the destination pool is untouched); a clean one copies."""
+    import torch
+    with tb.Context(0, tb.options(check_overlap=1)) as c:
+        run_layout(tb, c, workloads.random_batch(71, 2000, 5000, 64 * MiB, align=1), 72)
+        src = torch.arange(256, dtype=torch.uint8, device="cuda").repeat(4096)
+        dst = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+        s0, d0 = src.data_ptr(), dst.data_ptr()
+        for rows in ([[s0, d0, 4096], [s0 + 8192, d0 + 4000, 4096]],      # dst over dst
+                     [[s0, d0, 4096], [d0 + 100, d0 + 8192, 64]]):        # dst over a source
+            with pytest.raises(tb.TBError) as e:
+                c.batch_copy(np.array(rows, dtype=np.uint64))
+            assert e.value.code == tb.TB_EINVAL and "overlap" in str(e.value)
+        assert int(dst.count_nonzero().item()) == 0
+
+
 def test_slot_wait_deadline(tb):
     """With one slot, a second batch waits for the first launch; a 1 ns limit
     expires first and the call returns TB_ETIMEOUT instead of blocking."""

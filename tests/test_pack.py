@@ -28,6 +28,8 @@ def harness(tmp_path_factory):
                                  ct.c_void_p, ct.c_void_p]
     lib.harness_bad.restype = ct.c_int
     lib.harness_bad.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_void_p]
+    lib.harness_overlap.restype = ct.c_int
+    lib.harness_overlap.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_void_p]
     return lib
 
 
@@ -163,3 +165,41 @@ def test_claim_items_and_coverage(harness, n, long_n, expect_claim):
     assert p["claim"] == expect_claim
     fixed, counted = short_assignment(n, p["grid"], p["chunks"], p["claim"])
     assert sorted(fixed + counted) == list(range(n))
+
+
+def _conflict(d, i, j):
+    """Brute force: do descriptors i and j (i may equal j) make the result
+    order-dependent - a destination over the other's destination (i != j)
+    or over a source (its own included)?"""
+    def over(a0, alen, b0, blen):
+        return alen > 0 and blen > 0 and a0 < b0 + blen and b0 < a0 + alen
+    si, di, li = (int(x) for x in d[i])
+    sj, dj, lj = (int(x) for x in d[j])
+    return ((i != j and over(di, li, dj, lj)) or over(di, li, sj, lj) or over(dj, lj, si, li))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_overlap_check_against_brute_force(harness, seed):
+    g = np.random.default_rng(seed)
+    n = int(g.integers(1, 40))
+    span = int(g.integers(200, 20000))      # small address space: overlaps are common
+    d = np.stack([g.integers(1, span, n), g.integers(1, span, n),
+                  g.integers(0, 300, n)], axis=1).astype(np.uint64)
+    pair = np.zeros(2, dtype=np.uint64)
+    found = harness.harness_overlap(d.ctypes.data, n, pair.ctypes.data)
+    expect = any(_conflict(d, i, j) for i in range(n) for j in range(i, n))
+    assert bool(found) == expect
+    if found:
+        assert _conflict(d, int(min(pair)), int(max(pair)))
+
+
+def test_overlap_check_cases(harness):
+    def run(rows):
+        d = np.array(rows, dtype=np.uint64).reshape(-1, 3)
+        pair = np.zeros(2, dtype=np.uint64)
+        return harness.harness_overlap(d.ctypes.data, d.shape[0], pair.ctypes.data), sorted(pair)
+    assert run([[1000, 5000, 100], [1000, 5100, 100]])[0] == 0      # shared source, adjacent dst
+    assert run([[1000, 5000, 100], [3000, 5099, 10]]) == (1, [0, 1])  # dst over dst
+    assert run([[1000, 5000, 100], [5050, 9000, 10]]) == (1, [0, 1])  # dst over a source
+    assert run([[1000, 1050, 100]]) == (1, [0, 0])                    # its own source
+    assert run([[1000, 5000, 0], [1000, 5000, 100]])[0] == 0          # empty ranges ignored
