@@ -1,0 +1,54 @@
+"""CPU tests of bench.py's command line: the reference arm (the CPU oracle,
+timed on host cores) prints one JSON line with every key of the bench
+contract; the GPU arm refuses to run without a GPU instead of falling back
+to the CPU; fewer than 3 warm-up steps are rejected."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run(*args, timeout=300):
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1")
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=timeout, env=env)
+
+
+def test_reference_arm_prints_the_contract_line():
+    from oracle import _build
+    _build.build()
+    r = run("--impl", "reference", "--steps", "2", "--warmup", "3")
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_gpu_arm_refuses_to_run_without_a_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = run("--steps", "1", "--warmup", "3")
+    assert r.returncode != 0
+    assert "needs a CUDA GPU" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_warmup_below_three_is_rejected():
+    r = run("--impl", "reference", "--steps", "1", "--warmup", "2")
+    assert r.returncode != 0 and "warmup" in r.stderr
