@@ -128,6 +128,54 @@ def test_copy_engine_routing_head_sliced(tb):
         assert stats["ce_copies"] == 20 and stats["warp_items"] == 47520
 
 
+def test_two_contexts_on_two_threads(tb):
+    """Two host threads, each with its own context and stream, submit
+    batches (and reduce-copies) at the same time; every result is exact.
+    Contexts share only the library's per-device launch caches."""
+    import threading
+    import torch
+    layouts = [workloads.random_batch(80 + t, 3000, 40000, 128 * MiB, align=1) for t in range(2)]
+    pools = []
+    for t, lay in enumerate(layouts):
+        src_h = workloads.random_bytes(lay.src_pool_bytes, 90 + t)
+        pools.append((src_h, to_dev(src_h), torch.zeros(lay.dst_pool_bytes, dtype=torch.uint8,
+                                                        device="cuda")))
+    red = [(dev_bytes_f(1 << 22, 3.0), dev_bytes_f(1 << 22, 0.0)) for _ in range(2)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(t):
+        try:
+            with tb.Context(0) as c:
+                st = torch.cuda.Stream()
+                src_h, src_d, dst_d = pools[t]
+                desc = layouts[t].descriptors(src_d.data_ptr(), dst_d.data_ptr())
+                for _ in range(20):
+                    c.batch_copy(desc, st)
+                    c.reduce_copy([red[t][0], red[t][0]], red[t][1], 1 << 22, 0, st)
+                st.synchronize()
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t, lay in enumerate(layouts):
+        src_h, _, dst_d = pools[t]
+        exp = np.zeros(lay.dst_pool_bytes, dtype=np.uint8)
+        oracle.apply_batch(exp, src_h, lay.src_off, lay.dst_off, lay.lens)
+        assert oracle.first_mismatch(to_host(dst_d), exp) == -1
+        assert np.all(to_host(red[t][1]).view(np.float32) == 6.0)
+
+
+def dev_bytes_f(nbytes, value):
+    import torch
+    return torch.full((nbytes // 4,), value, dtype=torch.float32, device="cuda")
+
+
 def test_user_stream_ordering(tb, ctx):
     """The copy runs after earlier work on the caller's stream: a fill queued
     just before on the same stream is what gets copied."""
