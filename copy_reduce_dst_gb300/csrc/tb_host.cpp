@@ -33,7 +33,8 @@ constexpr int kMaxGatedLaunches = 256;
 
 struct Slot {
     void *dev = nullptr;       // device copy of one packed launch
-    void *host = nullptr;      // pinned staging of it
+    void *host = nullptr;      // pinned staging of it (mapped)
+    void *host_dev = nullptr;  // device address of the staging
     cudaEvent_t done = nullptr;
     cudaEvent_t uploaded = nullptr;  // the work list is on the device (upload stream)
     bool pending = false;      // `done` recorded and maybe not reached yet
@@ -674,8 +675,10 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     for (Slot &s : ctx->slots) {
         if (cudaMalloc(&s.dev, slot_bytes) != cudaSuccess)
             return bail(TB_ENOMEM);
-        if (cudaHostAlloc(&s.host, slot_bytes, cudaHostAllocDefault) != cudaSuccess)
+        if (cudaHostAlloc(&s.host, slot_bytes, cudaHostAllocMapped) != cudaSuccess)
             return bail(TB_ENOMEM);
+        if (cudaHostGetDevicePointer(&s.host_dev, s.host, 0) != cudaSuccess)
+            return bail(TB_ECUDA);
         if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&s.uploaded, cudaEventDisableTiming) != cudaSuccess)
             return bail(TB_ECUDA);
@@ -1278,7 +1281,15 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid), slot.host,
                              &plan);
             ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
-            if (side_upload) {
+            // A small batch of short copies all assigned by warp index reads
+            // its work list in place from the pinned staging: no upload and
+            // no cross-stream event, which is most of a small call's cost.
+            // The staging is not rewritten before the kernel has finished:
+            // wait_slot waits for it first.
+            const bool direct = side_upload && tb::batch_direct(plan);
+            if (direct) {
+                st.direct_launches += 1;
+            } else if (side_upload) {
                 TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
                                              cudaMemcpyHostToDevice, ctx->up));
                 TB_CUDA(ctx, cudaEventRecord(slot.uploaded, ctx->up));
@@ -1289,7 +1300,8 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-            TB_CUDA(ctx, tb::launch_batch(slot.dev, plan, s, slot.status_dev, o.kernel_wait_ns));
+            TB_CUDA(ctx, tb::launch_batch(direct ? slot.host_dev : slot.dev, plan, s,
+                                          slot.status_dev, o.kernel_wait_ns));
             if (slot.t1)
                 TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
             TB_CUDA(ctx, cudaEventRecord(slot.done, s));

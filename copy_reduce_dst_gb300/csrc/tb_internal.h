@@ -149,6 +149,13 @@ bool find_overlap(const tb_copy_desc *desc, size_t n, size_t *first, size_t *sec
 // copy) when the warps that start on short copies cover every short copy
 // in two rounds, else 2 (half a warp per copy, more copies in flight).
 uint32_t batch_claim_items(const BatchPlan &plan);
+// Work lists up to this size may be read by the kernel in place.
+constexpr size_t kDirectMaxBytes = 256 * 1024;
+// True when the launch can read its work list in place from pinned host
+// memory instead of a device copy: short copies only, every one of them in
+// the fixed first round (so the kernel never touches the claim counter),
+// and a work list of at most kDirectMaxBytes.
+bool batch_direct(const BatchPlan &plan);
 
 // CTAs of `kernel` resident per SM at `threads` threads and `smem` bytes of
 // dynamic shared memory on the current device; raises the kernel's shared

@@ -218,4 +218,12 @@ uint32_t batch_claim_items(const BatchPlan &plan)
     return (uint64_t)plan.n_short <= 2 * starters ? 1u : 2u;
 }
 
+bool batch_direct(const BatchPlan &plan)
+{
+    const uint64_t warps = kBatchThreads / 32;
+    const uint64_t fixed = (uint64_t)plan.grid * warps * batch_claim_items(plan);
+    return plan.chunks == 0 && plan.n_short > 0 && plan.upload_bytes <= kDirectMaxBytes &&
+           (uint64_t)plan.n_short <= fixed;
+}
+
 }  // namespace tb

@@ -149,6 +149,7 @@ class BatchStats(ct.Structure):
         ("bytes", _u64),
         ("upload_bytes", _u64),
         ("ce_copies", _u64),
+        ("direct_launches", _u64),
     ]
 
 

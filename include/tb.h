@@ -445,8 +445,11 @@ typedef struct {
     uint64_t cta_items;    /* pieces of long descriptors copied by whole CTAs */
     uint64_t launches;     /* kernel launches (slots) used */
     uint64_t bytes;        /* sum of len */
-    uint64_t upload_bytes; /* packed work-item bytes copied host-to-device */
+    uint64_t upload_bytes; /* bytes of the packed work lists the kernels read */
     uint64_t ce_copies;    /* descriptors sent to the copy engines (ce_min_bytes) */
+    uint64_t direct_launches; /* launches that read their work list in place from
+                                 pinned host memory (small batches of short copies
+                                 only: no upload, no event) */
 } tb_batch_stats;
 
 /* Statistics of the last tb_batch_copy on ctx. */

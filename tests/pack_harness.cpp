@@ -30,6 +30,7 @@ extern "C" int harness_pack(const tb_copy_desc *desc, size_t n, uint64_t small_m
     out[8] = tb::batch_buffer_bytes(c.descs);
     out[9] = c.n_ce;
     out[10] = tb::batch_claim_items(plan);
+    out[11] = tb::batch_direct(plan) ? 1 : 0;
     return 0;
 }
 

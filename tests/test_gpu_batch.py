@@ -59,6 +59,7 @@ def test_tiny_any_alignment(tb, ctx, seed):
     layout = workloads.random_batch(seed, 2000, 300, 4 * MiB, align=1)
     st = run_layout(tb, ctx, layout, seed)
     assert st["descs"] == int((layout.lens > 0).sum())
+    assert st["direct_launches"] == 1
 
 
 @pytest.mark.parametrize("ss,ds", [(0, 0), (1, 0), (0, 1), (3, 7), (15, 1), (4, 12), (8, 8)])
@@ -276,6 +277,7 @@ def test_pipeline_wait_expiry_is_reported(tb):
 def test_index_pages_full(tb, ctx):
     st = run_layout(tb, ctx, workloads.batch_index_pages(), 101)
     assert st["descs"] == 3840 and st["warp_items"] == 3840
+    assert st["direct_launches"] == 1        # work list read in place from pinned memory
 
 
 def test_block_pages_full(tb, ctx):
@@ -288,4 +290,4 @@ def test_head_sliced_full(tb, ctx):
     st = run_layout(tb, ctx, layout, 103)
     assert st["descs"] == 47540 and st["warp_items"] == 47520
     assert st["cta_items"] > 0                     # chunks of the 20 long copies
-    assert st["launches"] == 1
+    assert st["launches"] == 1 and st["direct_launches"] == 0

@@ -38,18 +38,20 @@ def pack(lib, desc, small_max=16384, full_grid=608, ce_min=0):
     n = desc.shape[0]
     cap = 16 + n * 32 + 8 + (16384 + 1) * 4
     buf = np.full(cap, 0xEE, dtype=np.uint8)
-    out = np.zeros(11, dtype=np.uint64)
+    out = np.zeros(12, dtype=np.uint64)
     rc = lib.harness_pack(desc.ctypes.data if n else None, n, small_max, ce_min, full_grid,
                           buf.ctypes.data, out.ctypes.data)
     assert rc == 0
-    n_short, n_long, grid, chunks, total, poff, coff, upload, bound, n_ce, claim = (int(x) for x in out)
+    (n_short, n_long, grid, chunks, total, poff, coff, upload, bound, n_ce, claim,
+     direct) = (int(x) for x in out)
     assert upload <= bound <= cap
     assert np.all(buf[:16] == 0)                       # the claim counter starts at 0
     items = buf[16: 16 + (n_short + n_long) * 24].view(np.uint64).reshape(-1, 3)
     prefix = buf[poff: poff + (n_long + 1) * 8].view(np.uint64)
     cdesc = buf[coff: coff + (chunks + 1) * 4].view(np.uint32)
     return dict(shorts=items[:n_short], longs=items[n_short:], prefix=prefix, chunk_desc=cdesc,
-                grid=grid, chunks=chunks, total=total, n_ce=n_ce, claim=claim)
+                grid=grid, chunks=chunks, total=total, n_ce=n_ce, claim=claim, direct=direct,
+                upload=upload)
 
 
 def chunk_bytes(lib, p, c):
@@ -203,3 +205,20 @@ def test_overlap_check_cases(harness):
     assert run([[1000, 5000, 100], [5050, 9000, 10]]) == (1, [0, 1])  # dst over a source
     assert run([[1000, 1050, 100]]) == (1, [0, 0])                    # its own source
     assert run([[1000, 5000, 0], [1000, 5000, 100]])[0] == 0          # empty ranges ignored
+
+
+@pytest.mark.parametrize("n,long_n,expect", [
+    (3840, 0, 1), (1, 0, 1), (4864, 0, 1), (4865, 0, 0), (7200, 0, 0), (3840, 1, 0), (0, 5, 0)])
+def test_direct_work_list(harness, n, long_n, expect):
+    """A launch reads its work list in place from pinned host memory only
+    when it has short copies alone, all of them in the fixed first round
+    (no counter), and a work list of at most 256 KiB."""
+    lens = np.full(n + long_n, 2112, dtype=np.uint64)
+    lens[n:] = 8 << 20
+    desc = np.stack([np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(24),
+                     np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(25), lens], axis=1)
+    p = pack(harness, desc)
+    assert p["direct"] == expect
+    if expect:
+        assert p["chunks"] == 0 and p["upload"] <= 256 * 1024
+        assert p["shorts"].shape[0] <= p["grid"] * 8 * p["claim"]
