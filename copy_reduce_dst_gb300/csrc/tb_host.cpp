@@ -695,12 +695,19 @@ void tb_destroy(tb_ctx *ctx)
     if (!ctx)
         return;
     DeviceScope scope(ctx->device);
+    // Quiesce first: the launches on slots, then every internal stream
+    // (an upload may be queued on `up` even when its launch failed), and
+    // only then free what they may still read or write.
+    for (Slot &s : ctx->slots)
+        if (s.done && s.pending)
+            cudaEventSynchronize(s.done);
+    for (cudaStream_t s : {ctx->stream, ctx->up, ctx->ce, ctx->pipe.h2d, ctx->pipe.cmp,
+                           ctx->pipe.d2h})
+        if (s)
+            cudaStreamSynchronize(s);
     for (Slot &s : ctx->slots) {
-        if (s.done) {
-            if (s.pending)
-                cudaEventSynchronize(s.done);
+        if (s.done)
             cudaEventDestroy(s.done);
-        }
         if (s.uploaded)
             cudaEventDestroy(s.uploaded);
         if (s.t0)
@@ -712,29 +719,18 @@ void tb_destroy(tb_ctx *ctx)
         if (s.host)
             cudaFreeHost(s.host);
     }
-    if (ctx->stream) {
-        cudaStreamSynchronize(ctx->stream);
-        cudaStreamDestroy(ctx->stream);
-    }
-    if (ctx->up) {
-        cudaStreamSynchronize(ctx->up);
-        cudaStreamDestroy(ctx->up);
-    }
+    for (cudaStream_t s : {ctx->stream, ctx->up, ctx->ce})
+        if (s)
+            cudaStreamDestroy(s);
     for (cudaEvent_t e : ctx->events)
         cudaEventDestroy(e);
-    if (ctx->ce) {
-        cudaStreamSynchronize(ctx->ce);
-        cudaStreamDestroy(ctx->ce);
-    }
     for (cudaEvent_t e : {ctx->ce_fork, ctx->ce_join})
         if (e)
             cudaEventDestroy(e);
     Pipeline &pl = ctx->pipe;
     for (cudaStream_t s : {pl.h2d, pl.cmp, pl.d2h})
-        if (s) {
-            cudaStreamSynchronize(s);
+        if (s)
             cudaStreamDestroy(s);
-        }
     for (cudaEvent_t e : {pl.begin, pl.end})
         if (e)
             cudaEventDestroy(e);
@@ -961,6 +957,18 @@ int tb_reduce_copy_host(tb_ctx *ctx, const void *const *host_srcs, int n_src, vo
     for (int k = 0; k < n_src; ++k)
         if (!dev_srcs[k])
             return fail(ctx, TB_EINVAL, "reduce_copy_host: null device source");
+    // Every chunk starts at a multiple of kStageChunk, so all chunks share
+    // the pointers' alignments: one plan checks the arguments of all of
+    // them before anything is queued.
+    if (num_bytes > 0) {
+        tb::ReducePlan probe;
+        const int prc = plan_for(ctx, &probe, const_cast<const void *const *>(dev_srcs), n_src,
+                                 dev_dst, std::min<uint64_t>(kStageChunk, num_bytes), num_subexec);
+        if (prc != TB_OK)
+            return prc;
+        if (num_bytes % 4 != 0)
+            return fail(ctx, TB_EINVAL, "reduce_copy_host: numBytes must be a multiple of 4");
+    }
     int rc = ensure_pipeline(ctx);
     if (rc != TB_OK)
         return rc;
@@ -1300,8 +1308,15 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
-            TB_CUDA(ctx, tb::launch_batch(direct ? slot.host_dev : slot.dev, plan, s,
-                                          slot.status_dev, o.kernel_wait_ns));
+            const cudaError_t le = tb::launch_batch(direct ? slot.host_dev : slot.dev, plan, s,
+                                                    slot.status_dev, o.kernel_wait_ns);
+            if (le != cudaSuccess) {
+                // The slot is not marked pending, so its staging may be
+                // rewritten next: let a queued upload finish reading it.
+                if (side_upload && !direct)
+                    cudaStreamSynchronize(ctx->up);
+                return cuda_fail(ctx, le, "launch of the batch kernel");
+            }
             if (slot.t1)
                 TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
             TB_CUDA(ctx, cudaEventRecord(slot.done, s));

@@ -660,6 +660,30 @@ def test_reduce_copy_host_staged(tb, ctx, n):
         ctx.reduce_copy_host(srcs, hd, 4 * n, [None] * 3, None, 0, st)
 
 
+def test_reduce_copy_host_rejects_before_queuing(tb, ctx):
+    """A staged call whose length is not whole float32 elements (here past
+    the first 32 MiB chunk) or whose device buffers are misaligned is
+    rejected before any copy is queued; the next call on the stream works."""
+    import torch
+    n = (40 << 20) // 4
+    srcs = [np.full(n, 1.5, np.float32) for _ in range(2)]
+    hd = np.zeros(n, np.float32)
+    ds = [dev_bytes(4 * n + 64) for _ in range(2)]
+    dd = dev_bytes(4 * n + 64, fill=0x7F)
+    st = torch.cuda.Stream()
+    with pytest.raises(tb.TBError) as e:
+        ctx.reduce_copy_host(srcs, hd, 4 * n - 2, ds, dd, 0, st)
+    assert e.value.code == tb.TB_EINVAL
+    with pytest.raises(tb.TBError) as e:
+        ctx.reduce_copy_host(srcs, hd, 4 * n, [d.data_ptr() + 2 for d in ds], dd, 0, st)
+    assert e.value.code == tb.TB_EINVAL
+    st.synchronize()
+    assert np.all(to_host(dd) == 0x7F) and np.all(hd == 0)    # nothing ran
+    ctx.reduce_copy_host(srcs, hd, 4 * n, ds, dd, 0, st)
+    st.synchronize()
+    assert np.all(hd == 3.0)
+
+
 def test_reduce_copy_host_end_to_end(tb, ctx):
     import torch
     g = np.random.default_rng(9)
