@@ -1094,19 +1094,24 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
         TB_CUDA(ctx, tb::launch_gate(ctx->gate_flag_dev, ctx->gate_status_dev, o.wait_timeout_ns, st));
     }
     int first_err = TB_OK;
+    // A failed call inside the loop releases the gate before returning, so
+    // the launches already queued behind it run and the stream drains.
+    auto abort_loop = [&](cudaError_t e, const char *what) {
+        if (gated)
+            __atomic_store_n(ctx->gate_flag, 1u, __ATOMIC_SEQ_CST);
+        cudaStreamSynchronize(st);
+        return cuda_fail(ctx, e, what);
+    };
     for (int64_t it = graphed ? iters : -(int64_t)o.warmup; it < iters; ++it) {
         at_iteration(it);
+        cudaError_t e = cudaSuccess;
         if (it == 0 || (per_iter_validate && it > 0))
-            TB_CUDA(ctx, cudaEventRecord(ctx->events[it], st));
-        cudaError_t e = tb::launch_reduce(plan, st);
-        if (e != cudaSuccess) {
-            if (gated)
-                __atomic_store_n(ctx->gate_flag, 1u, __ATOMIC_SEQ_CST);
-            cudaStreamSynchronize(st);
-            return cuda_fail(ctx, e, "reduce-copy launch");
-        }
-        if (it >= 0)
-            TB_CUDA(ctx, cudaEventRecord(ctx->events[it + 1], st));
+            if ((e = cudaEventRecord(ctx->events[it], st)) != cudaSuccess)
+                return abort_loop(e, "cudaEventRecord");
+        if ((e = tb::launch_reduce(plan, st)) != cudaSuccess)
+            return abort_loop(e, "reduce-copy launch");
+        if (it >= 0 && (e = cudaEventRecord(ctx->events[it + 1], st)) != cudaSuccess)
+            return abort_loop(e, "cudaEventRecord");
         if (per_iter_validate && it >= 0) {
             tb_mismatch mm;
             first_err = check(&mm);
