@@ -529,6 +529,8 @@ def study(args, tb, torch, local):
             print(json.dumps(row), flush=True)
     del flush
     study_validation(tb, torch, local)
+    study_tiny_batches(tb, torch, local)
+    study_small_copies_under_compute(tb, torch, local)
     study_batch_configs(tb, torch, local)
     study_batch_phases(tb, torch, local)
     study_batch_routing(tb, torch, local)
@@ -625,6 +627,93 @@ def study_interference(tb, torch, local):
                           "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
                           "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
               flush=True)
+
+
+def study_small_copies_under_compute(tb, torch, local):
+    """The 3840-page batch (3840 x 2112 B) copied while an 8192^3 bf16 GEMM
+    loop keeps every SM busy on another stream, against the same copies on
+    an idle GPU: tb_batch_copy, and one cudaMemcpyAsync per copy
+    (tb_copy_each).  The Mooncake RFC saw per-copy memcpy collapse to
+    0.03-0.04 GB/s under compute.  Wall time per batch (call + sync), median
+    of the batches that ran while the GEMM loop was in flight."""
+    import statistics as st
+    from copy_reduce_dst_gb300 import workloads
+    n = 8192
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    layout = workloads.batch_index_pages()
+    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    gemm_s = torch.cuda.Stream()
+    copy_s = torch.cuda.Stream()
+    hi_s = torch.cuda.Stream(priority=-1)      # the caller's high-priority stream
+    moved = 2 * layout.total_bytes
+    out = {"study": "small copies under compute", "workload": layout.name}
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        for name, fn, cs in (("batch", lambda: ctx.batch_copy(desc, copy_s), copy_s),
+                             ("batch_high_priority", lambda: ctx.batch_copy(desc, hi_s), hi_s),
+                             ("memcpy_each", lambda: ctx.copy_each(desc, copy_s), copy_s)):
+            for busy in (False, True):
+                torch.cuda.synchronize()
+                end = None
+                if busy:
+                    with torch.cuda.stream(gemm_s):
+                        for _ in range(3):
+                            torch.matmul(a, b)
+                    torch.cuda.synchronize()
+                    end = torch.cuda.Event()
+                    with torch.cuda.stream(gemm_s):
+                        for _ in range(1500):         # ~1 s of GEMM
+                            torch.matmul(a, b)
+                    end.record(gemm_s)
+                times = []
+                limit = 3 if name == "memcpy_each" else 50
+                while len(times) < limit and (end is None or not end.query()):
+                    t0 = time.perf_counter()
+                    fn()
+                    cs.synchronize()
+                    times.append(time.perf_counter() - t0)
+                torch.cuda.synchronize()
+                key = f"{name}_{'under_gemm' if busy else 'idle'}"
+                if times:
+                    w = st.median(times)
+                    out[key + "_ms"] = round(w * 1e3, 3)
+                    out[key + "_gbps"] = round(moved / w / 1e9, 2)
+                out[key + "_samples"] = len(times)
+    print(json.dumps(out), flush=True)
+    del a, b, src, dst
+
+
+def study_tiny_batches(tb, torch, local):
+    """Batches of 1 to 64 copies of 2112 B: wall time per call (call + sync,
+    median of 200) through tb_batch_copy (one kernel) and through one
+    cudaMemcpyAsync per copy - where a kernel launch stops paying off."""
+    import statistics as st
+    import numpy as np
+    pool = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    base = pool.data_ptr()
+    rows = []
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        for k in (1, 2, 4, 8, 16, 32, 64):
+            desc = np.array([[base + i * 4224, base + (32 << 20) + i * 4224, 2112]
+                             for i in range(k)], dtype=np.uint64)
+            row = {"copies": k}
+            for name, fn in (("batch_us", lambda: ctx.batch_copy(desc, s)),
+                             ("memcpy_each_us", lambda: ctx.copy_each(desc, s))):
+                for _ in range(20):
+                    fn()
+                s.synchronize()
+                t = []
+                for _ in range(200):
+                    t0 = time.perf_counter()
+                    fn()
+                    s.synchronize()
+                    t.append(time.perf_counter() - t0)
+                row[name] = round(st.median(t) * 1e6, 2)
+            rows.append(row)
+    print(json.dumps({"study": "tiny batches", "rows": rows}), flush=True)
 
 
 def study_validation(tb, torch, local):

@@ -198,6 +198,8 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "slot_items must be in [1024, 2^24]");
     if (o.num_slots < 1 || o.num_slots > 64)
         return fail(ctx, TB_EINVAL, "num_slots must be in [1, 64]");
+    if (o.batch_min_copies < 0)
+        return fail(ctx, TB_EINVAL, "batch_min_copies must be >= 0");
     if (o.wait_timeout_ns == 0)
         return fail(ctx, TB_EINVAL, "wait_timeout_ns must be > 0");
     if (o.vec_bytes != 0 && o.vec_bytes != 4 && o.vec_bytes != 16 && o.vec_bytes != 32)
@@ -492,6 +494,7 @@ void tb_options_default(tb_options *o)
     o->validate_direct = 0;
     o->validate_source = 0;
     o->check_overlap = 0;
+    o->batch_min_copies = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -567,6 +570,7 @@ int tb_options_from_env(tb_options *o)
     if (!env_i32("TB_VALIDATE_SOURCE", &o->validate_source, &bad))
         env_i32("VALIDATE_SOURCE", &o->validate_source, &bad);
     env_i32("TB_CHECK_OVERLAP", &o->check_overlap, &bad);
+    env_i32("TB_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -1240,6 +1244,32 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         if (tb::count_batch(desc, n, small, &all, &bad, ce_min) != TB_OK)
             return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range",
                         bad);
+    }
+    // Fewer copies than batch_min_copies: one cudaMemcpyAsync each, no kernel.
+    size_t nonempty = 0;
+    for (size_t i = 0; i < n && nonempty < (size_t)o.batch_min_copies; ++i)
+        nonempty += desc[i].len != 0;
+    if (nonempty < (size_t)o.batch_min_copies) {
+        tb::BatchCounts few;
+        if (tb::count_batch(desc, n, small, &few, &bad, 0) != TB_OK)
+            return fail(ctx, TB_EINVAL, "batch_copy: descriptor %zu has a null or wrapping range",
+                        bad);
+        if (o.check_overlap) {
+            size_t a = 0, b = 0;
+            if (tb::find_overlap(desc, n, &a, &b))
+                return fail(ctx, TB_EINVAL, "batch_copy: descriptors %zu and %zu overlap",
+                            std::min(a, b), std::max(a, b));
+        }
+        for (size_t i = 0; i < n; ++i)
+            if (desc[i].len)
+                TB_CUDA(ctx, cudaMemcpyAsync(reinterpret_cast<void *>(desc[i].dst),
+                                             reinterpret_cast<const void *>(desc[i].src),
+                                             desc[i].len, cudaMemcpyDeviceToDevice, s));
+        st.descs = few.descs;
+        st.bytes = few.bytes;
+        st.ce_copies = few.descs;
+        ctx->last_batch = st;
+        return TB_OK;
     }
     if (o.check_overlap) {
         size_t a = 0, b = 0;

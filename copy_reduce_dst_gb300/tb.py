@@ -67,6 +67,7 @@ class Options(ct.Structure):
         ("validate_direct", _i32),
         ("validate_source", _i32),
         ("check_overlap", _i32),
+        ("batch_min_copies", _i32),
     ]
 
 

@@ -178,6 +178,11 @@ typedef struct {
        destinations, or a destination overlapping a source.  O(n log n) on
        the host; a debugging aid.  Default 0. */
     int32_t check_overlap;
+    /* The Mooncake RFC's MC_HIP_BATCH_COPY_MIN: a batch with fewer non-empty
+       descriptors than this is copied with one cudaMemcpyAsync per
+       descriptor on `stream` instead of a kernel launch (counted in
+       tb_batch_stats.ce_copies).  0 = always the kernel.  Default 0. */
+    int32_t batch_min_copies;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -190,7 +195,8 @@ void tb_options_default(tb_options *opt);
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
-     TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP.
+     TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP, TB_BATCH_COPY_MIN
+     (batch_min_copies).
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);
@@ -426,7 +432,11 @@ typedef struct {
    `stream` (ordered after the caller's earlier work on it).  The descriptor
    array is read and packed before return, so the caller may reuse it at
    once.  The packed work list goes to the device on an internal stream,
-   overlapping earlier work, and the kernel waits for it on `stream`.  The bytes of all descriptors longer than
+   overlapping earlier work, and the kernel waits for it on `stream`; a small
+   batch of short copies only has its list read in place from pinned host
+   memory.  The kernel runs at the priority of `stream`: on a high-priority
+   stream its CTAs are scheduled ahead of waiting work of lower-priority
+   streams, such as a GEMM loop.  The bytes of all descriptors longer than
    small_max_bytes form one stream cut into equal chunks, the same number
    for every CTA, moved with bulk copies through shared memory; descriptors
    of at most small_max_bytes go to a warp or half a warp each, the first

@@ -118,7 +118,8 @@ def test_every_option_has_an_environment_variable(tb):
     block = text[text.index("Overrides fields of *opt from the environment"):
                  text.index("int tb_options_from_env")]
     names = set(re.findall(r"\bTB_([A-Z_]+)\b", block))
-    renamed = {"rotate_bytes": "SRC_ROTATE_BYTES", "memset_byte": "MEMSET_CHAR"}
+    renamed = {"rotate_bytes": "SRC_ROTATE_BYTES", "memset_byte": "MEMSET_CHAR",
+               "batch_min_copies": "BATCH_COPY_MIN"}
     for field, _ in tb.Options._fields_:
         assert renamed.get(field, field.upper()) in names, field
 

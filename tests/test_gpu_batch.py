@@ -208,6 +208,18 @@ def test_bad_descriptors(tb, ctx):
     ctx.batch_copy(np.zeros((0, 3), dtype=np.uint64))
 
 
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_batch_min_copies(tb, k):
+    """batch_min_copies = 3 (the RFC's MC_HIP_BATCH_COPY_MIN): batches of 1
+    or 2 copies go out as one cudaMemcpyAsync each, 3 or more as a kernel;
+    the bytes are the same."""
+    with tb.Context(0, tb.options(batch_min_copies=3)) as c:
+        layout = workloads.random_batch(200 + k, k, 70000, 8 * MiB, align=1, min_len=1)
+        st = run_layout(tb, c, layout, 210 + k)
+        assert st["descs"] == k
+        assert (st["launches"], st["ce_copies"]) == ((0, k) if k < 3 else (1, 0))
+
+
 def test_check_overlap(tb):
     """check_overlap = 1: a batch whose copies overlap is rejected before
     any launch (the destination pool is untouched); a clean one copies."""
