@@ -206,6 +206,7 @@ constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
 constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
 constexpr uint64_t kBulkMinBytes = 32ull << 20;  // auto engine: bulk from 32 MiB per source
+constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
 // Bytes per source of one tile.  With several sources the stages hold
 // N pieces each and 8 KiB keeps three CTAs (three pipelines) per SM; one
@@ -369,6 +370,11 @@ BulkKernel pick_bulk(int n_src, uint32_t stages, size_t *smem)
     case 4: *smem = bulk_smem_bytes<4>(stages); return k_reduce_bulk<4>;
     default: *smem = 0; return nullptr;
     }
+}
+
+uint32_t bulk_tile_bytes(int n_src)
+{
+    return n_src == 1 ? bulk_tile<1>() : bulk_tile<2>();
 }
 
 uint32_t bulk_deep_stages(int n_src)
@@ -577,8 +583,25 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         const uint64_t per_cta = (uint64_t)p->block_threads * (uint64_t)p->unroll;
         const uint64_t rounds = (p->nvec + per_cta - 1) / per_cta;
         wave = (int64_t)std::min<uint64_t>((uint64_t)full, std::max<uint64_t>((uint64_t)num_sms, rounds));
+    } else {
+        // Bulk form: many short-lived CTAs of about kBulkTilesPerCta tiles
+        // each rather than one resident wave with equal shares.  The CTA
+        // scheduler then hands the next CTA to whichever SM finishes first,
+        // so no SM ends the launch late (1 source, 2 GiB: 7.1 TB/s against
+        // 6.6 with one wave; 3 sources, 3 x 256 MiB: 7.18 against 7.11).
+        // Whole waves only: a partial last wave leaves SMs idle at the end
+        // (1 source, 64 MiB: 1.7 waves 6.7 TB/s, one wave 7.2).
+        const uint64_t tile_vecs = bulk_tile_bytes(n_src) / 16;
+        const uint64_t tiles = (p->nvec + tile_vecs - 1) / tile_vecs;
+        const uint64_t want = (tiles + kBulkTilesPerCta - 1) / kBulkTilesPerCta;
+        const uint64_t waves = std::max<uint64_t>(1, std::min<uint64_t>(want / (uint64_t)full, 4096));
+        wave = (int64_t)(waves * (uint64_t)full);
     }
-    const int64_t S = num_subexec > 0 ? num_subexec : wave;
+    // numSubExec = 0: the vector form gives each CTA its own range; the bulk
+    // form deals all tiles round robin over its whole grid (one range), so
+    // each wave of CTAs sweeps neighbouring tiles (3 sources, 3 x 256 MiB:
+    // 7.22 against 6.98 TB/s with a range per CTA).
+    const int64_t S = num_subexec > 0 ? num_subexec : (p->engine == 2 ? 1 : wave);
     const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, wave);
     if (G > (int64_t)INT32_MAX)
         return TB_EINVAL;

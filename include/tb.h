@@ -86,8 +86,10 @@ typedef struct {
     int32_t always_validate;
     /* MEMSET_CHAR: the byte a 0-source transfer writes.  Default 0. */
     uint32_t memset_byte;
-    /* Reduce-copy CTAs per sub-executor.  0 = one full wave of resident CTAs
-       dealt to the sub-executors as evenly as possible (at least one each);
+    /* Reduce-copy CTAs per sub-executor.  0 = the library's grid dealt to
+       the sub-executors as evenly as possible (at least one each): for the
+       vector form one wave of resident CTAs (fewer for a small transfer),
+       for the bulk form one CTA per ~4 tiles of work, at least one wave;
        1 gives TransferBench's one CTA per sub-executor.  Default 0. */
     int32_t ctas_per_subexec;
     /* Reduce-copy threads per CTA (multiple of 32, <= 512); 0 = 512. */
@@ -319,8 +321,9 @@ uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
    nSrc <= TB_MAX_SRCS.  The elements are split into numSubExec contiguous
    ranges (sub-executors), each served by its own CTAs and sized in
    proportion to them (equal when numSubExec divides the grid);
-   numSubExec == 0 means one per CTA of the default grid.  The split does not
-   change the result.  dst must not overlap any source.  TB_ETIMEOUT, with
+   numSubExec == 0 is the library's choice: one per CTA of the vector form's
+   grid, one for the whole grid of the bulk form.  The split does not change
+   the result.  dst must not overlap any source.  TB_ETIMEOUT, with
    nothing launched, when an earlier launch of this context stopped early
    because a bounded wait inside the kernel expired (kernel_wait_ns); the
    call after that one launches again. */
