@@ -89,6 +89,11 @@ static_assert(sizeof(WorkItem) == 24, "WorkItem is packed as three 64-bit words"
 constexpr int kBatchThreads = 256;
 constexpr uint64_t kChunkBytes = 65536;  // target size of a long-copy chunk
 constexpr uint32_t kMaxChunks = 16384;   // chunks of one launch at most
+// Waves of resident CTAs a batch launch may span.  Short-lived CTAs over
+// several waves let the CTA scheduler balance the SMs' finishing times
+// (47,540 batch: 141 us at 8 waves against 145 at one; one 2 GiB copy
+// 6.86 against 6.45 TB/s).
+constexpr uint64_t kBatchWaves = 8;
 constexpr size_t kBatchHeader = 16;      // claim counter of the short copies
 
 // Descriptor counts of a batch (descriptors with len == 0 are skipped).
@@ -135,7 +140,7 @@ int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCou
 // buf (after the header) and the long ones to `longs` (room for n).
 int gather_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, uint64_t ce_min,
                  void *buf, WorkItem *longs, BatchCounts *c, size_t *bad);
-// CTAs for a batch: one full wave at most, fewer for small batches.
+// CTAs for a batch: kBatchWaves full waves at most, fewer for small batches.
 int batch_grid(const BatchCounts &c, int full_grid);
 // Completes a buffer gather_batch filled: header, long copies, prefix and
 // chunk table; fills *out.

@@ -108,7 +108,8 @@ int batch_grid(const BatchCounts &c, int full_grid)
     const uint64_t for_short = (c.n_short + warps - 1) / warps;
     const uint64_t for_long = (c.long_bytes + kChunkBytes - 1) / kChunkBytes;
     const uint64_t want = std::max<uint64_t>(1, std::max(for_short, for_long));
-    return (int)std::min<uint64_t>(std::min<uint64_t>((uint64_t)full_grid, kMaxChunks), want);
+    return (int)std::min<uint64_t>(
+        std::min<uint64_t>((uint64_t)full_grid * kBatchWaves, kMaxChunks), want);
 }
 
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out)

@@ -33,6 +33,9 @@ def harness(tmp_path_factory):
     return lib
 
 
+WAVES = 8  # waves of resident CTAs a batch launch may span (kBatchWaves)
+
+
 def pack(lib, desc, small_max=16384, full_grid=608, ce_min=0):
     desc = np.ascontiguousarray(desc, dtype=np.uint64).reshape(-1, 3)
     n = desc.shape[0]
@@ -80,7 +83,7 @@ def test_packer_invariants(harness, seed, n, long_frac, small, grid):
     lens = desc[:, 2] if n else np.zeros(0, np.uint64)
     is_long = lens > small
     G = p["grid"]
-    assert 1 <= G <= grid
+    assert 1 <= G <= grid * WAVES
 
     # long copies in descriptor order, prefix = running stream offset
     assert np.array_equal(p["longs"], desc[is_long])
@@ -137,8 +140,8 @@ def test_packer_batch_47540(harness):
     lay = workloads.batch_head_sliced()
     desc = lay.descriptors(1 << 32, 1 << 36)
     p = pack(harness, desc)
-    assert p["grid"] == 608 and p["shorts"].shape[0] == 47520 and p["longs"].shape[0] == 20
-    assert p["total"] == 288 << 20 and p["chunks"] == 608 * 8
+    assert p["grid"] == 608 * WAVES and p["shorts"].shape[0] == 47520 and p["longs"].shape[0] == 20
+    assert p["total"] == 288 << 20 and p["chunks"] == 608 * WAVES
 
 
 def short_assignment(n_short, grid, chunks, claim, warps=8):
@@ -153,8 +156,8 @@ def short_assignment(n_short, grid, chunks, claim, warps=8):
 
 
 @pytest.mark.parametrize("n,long_n,expect_claim", [
-    (3840, 0, 1), (7200, 0, 1), (47520, 20, 2), (100, 0, 1), (9728, 0, 1), (9729, 0, 2),
-    (8512, 20, 1), (8513, 20, 2)])
+    (3840, 0, 1), (7200, 0, 1), (47520, 20, 1), (100, 0, 1), (77824, 0, 1), (77825, 0, 2),
+    (68096, 20, 1), (68097, 20, 2)])
 def test_claim_items_and_coverage(harness, n, long_n, expect_claim):
     """One copy per warp while the warps that start on short copies cover the
     batch in two rounds, else two per warp; the fixed first round and the
@@ -208,7 +211,8 @@ def test_overlap_check_cases(harness):
 
 
 @pytest.mark.parametrize("n,long_n,expect", [
-    (3840, 0, 1), (1, 0, 1), (4864, 0, 1), (4865, 0, 0), (7200, 0, 0), (3840, 1, 0), (0, 5, 0)])
+    (3840, 0, 1), (1, 0, 1), (7200, 0, 1), (10900, 0, 1), (11000, 0, 0), (3840, 1, 0),
+    (0, 5, 0)])
 def test_direct_work_list(harness, n, long_n, expect):
     """A launch reads its work list in place from pinned host memory only
     when it has short copies alone, all of them in the fixed first round
