@@ -267,7 +267,8 @@ int plan_for(tb_ctx *ctx, tb::ReducePlan *p, const void *const *srcs, int n_src,
     if (rc == TB_EINVAL)
         return fail(ctx, rc,
                     "reduce-copy arguments rejected (nSrc in [0,%d], numBytes %% 4 == 0, "
-                    "4-byte aligned non-null pointers, numSubExec >= 0)",
+                    "4-byte aligned non-null pointers, dst not overlapping a source, "
+                    "numSubExec >= 0)",
                     TB_MAX_SRCS);
     if (rc != TB_OK)
         return fail(ctx, rc,

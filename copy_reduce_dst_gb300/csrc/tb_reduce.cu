@@ -481,10 +481,17 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     if (n_src > 0 && !srcs)
         return TB_EINVAL;
     uintptr_t any = (uintptr_t)dst;
+    const uintptr_t d0 = (uintptr_t)dst, d1 = d0 + num_bytes;
+    if (d1 < d0)
+        return TB_EINVAL;
     for (int k = 0; k < n_src; ++k) {
         if (!srcs[k])
             return TB_EINVAL;
         any |= (uintptr_t)srcs[k];
+        // dst must not overlap a source: CTAs would read bytes others write.
+        const uintptr_t s0 = (uintptr_t)srcs[k], s1 = s0 + num_bytes;
+        if (s1 < s0 || (num_bytes > 0 && s0 < d1 && d0 < s1))
+            return TB_EINVAL;
     }
     if (any & 3u)
         return TB_EINVAL;

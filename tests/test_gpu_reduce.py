@@ -155,7 +155,8 @@ def test_bulk_deep_pipeline(tb, nsrc, subexec):
     srcs = [finite_floats(g, n) for _ in range(nsrc)]
     with tb.Context(0, tb.options(reduce_engine=2, ctas_per_subexec=1)) as c:
         d = dev_bytes(4 * n + 64)
-        info = c.reduce_plan([d.data_ptr() + 4] * nsrc, d.data_ptr() + 4, 4 * n, subexec)
+        far = d.data_ptr() + (1 << 36) + 4       # planning only: never accessed
+        info = c.reduce_plan([d.data_ptr() + 4] * nsrc, far, 4 * n, subexec)
         tile = 32768 if nsrc == 1 else 8192
         stages = (info["smem_bytes"] - 128) // (nsrc * tile)
         assert info["grid"] == subexec and stages > 3
@@ -164,22 +165,24 @@ def test_bulk_deep_pipeline(tb, nsrc, subexec):
 
 
 def test_reduce_plan_engine_choice(tb, ctx):
+    # planning only: the addresses are never accessed; dst lies far away
     d = dev_bytes(1 << 20)
     p = d.data_ptr()
+    far = p + (1 << 36)
     big = 32 << 20
-    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, big)
+    info = ctx.reduce_plan([p, p + 4096, p + 8192], far, big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
-    info = ctx.reduce_plan([p, p + 4096, p + 8192], p + 65536, big - 256)
+    info = ctx.reduce_plan([p, p + 4096, p + 8192], far, big - 256)
     assert info["engine"] == 1                                    # small: vector loads
-    info = ctx.reduce_plan([p] * 5, p + 65536, 4096)
+    info = ctx.reduce_plan([p] * 5, far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
-    info = ctx.reduce_plan([p + 4, p + 8], p + 65536, 4096)
+    info = ctx.reduce_plan([p + 4, p + 8], far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 4        # no common alignment
-    info = ctx.reduce_plan([p + 4, p + 4100], p + 65540, big)
+    info = ctx.reduce_plan([p + 4, p + 4100], far + 4, big)
     assert info["engine"] == 2 and info["head_elems"] == 3       # head to 16 bytes
     assert info["head_elems"] + 4 * info["body_vectors"] + info["tail_elems"] == big // 4
     with tb.Context(0, tb.options(vec_bytes=32)) as c:
-        info = c.reduce_plan([p], p + 65536, 4096)
+        info = c.reduce_plan([p], far, 4096)
         assert info["engine"] == 1 and info["vec_bytes"] == 32
 
 
@@ -190,18 +193,19 @@ def test_engine_choice_one_cta_per_subexecutor(tb):
     its deep pipeline."""
     d = dev_bytes(1 << 20)
     p = d.data_ptr()
+    far = p + (1 << 36)            # planning only: never accessed
     big = 64 << 20
     with tb.Context(0, tb.options(ctas_per_subexec=1)) as c:
         for n, engine in ((1, 2), (2, 1), (3, 1), (4, 2)):
-            info = c.reduce_plan([p] * n, p, big, 32)
+            info = c.reduce_plan([p] * n, far, big, 32)
             assert info["engine"] == engine and info["grid"] == 32
             if engine == 1:
                 assert info["vec_bytes"] == 32 and info["unroll"] == 2
             else:
                 assert info["smem_bytes"] > 128 + 3 * n * (32768 if n == 1 else 8192)
-        assert c.reduce_plan([p] * 3, p, big, 1000)["engine"] == 2    # CTAs share SMs
+        assert c.reduce_plan([p] * 3, far, big, 1000)["engine"] == 2  # CTAs share SMs
     with tb.Context(0) as c:
-        assert c.reduce_plan([p] * 3, p, big, 32)["engine"] == 2      # one wave shared
+        assert c.reduce_plan([p] * 3, far, big, 32)["engine"] == 2    # the grid shared
 
 
 def test_vector_grid_follows_the_work(tb, ctx):
@@ -225,7 +229,7 @@ def test_bulk_engine_limits(tb):
     d = dev_bytes(1 << 16)
     with tb.Context(0, tb.options(reduce_engine=2)) as c:
         with pytest.raises(tb.TBError) as e:
-            c.reduce_copy([d.data_ptr()] * 5, d.data_ptr(), 256)           # 5 sources
+            c.reduce_copy([d.data_ptr()] * 5, d.data_ptr() + 8192, 256)    # 5 sources
         assert e.value.code == tb.TB_ENOTSUP
         with pytest.raises(tb.TBError) as e:
             c.reduce_copy([d.data_ptr() + 4], d.data_ptr() + 8192, 256)   # no common 16 B
@@ -268,6 +272,11 @@ def test_bad_arguments(tb, ctx):
         ctx.reduce_copy([d.data_ptr()] * 17, d.data_ptr(), 8)          # too many sources
     with pytest.raises(tb.TBError):
         ctx.reduce_copy([0], d.data_ptr(), 8)                          # null source
+    for src_off, dst_off in ((0, 0), (16, 0), (0, 16), (0, 28)):         # dst overlaps a source
+        with pytest.raises(tb.TBError) as e:
+            ctx.reduce_copy([d.data_ptr() + 32, d.data_ptr() + src_off], d.data_ptr() + dst_off, 32)
+        assert e.value.code == tb.TB_EINVAL
+    ctx.reduce_copy([d.data_ptr(), d.data_ptr()], d.data_ptr() + 32, 32)  # sources may alias
 
 
 # ---------------------------------------------------------------------------
