@@ -1,0 +1,114 @@
+"""Seeded random cases over the option space, each compared with the oracle.
+
+Reduce-copy: 0-16 sources, 0-300,000 elements, byte offsets of any 4-byte
+class, engine, vector width, block size, unroll, sub-executor layout and
+programmatic launch drawn at random; a combination the library does not
+support must be refused with TB_ENOTSUP, everything else must be bit-exact
+with dstReference and leave the guard bytes around dst untouched.
+Batched copy: 0-3000 copies of 0 B - 256 KiB at any byte alignment, with the
+short/long threshold, slot size and count, copy-count and copy-engine
+routing drawn at random; the whole destination pool must equal the oracle's
+apply of the batch.  The seeds are fixed, so a failure names its case."""
+import numpy as np
+import pytest
+
+import oracle
+from copy_reduce_dst_gb300 import workloads
+from gpu_helpers import dev_bytes, finite_floats, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from copy_reduce_dst_gb300 import _build
+    _build.build()
+    from copy_reduce_dst_gb300 import tb as mod
+    return mod
+
+
+def _reduce_case(seed):
+    g = np.random.default_rng(1000 + seed)
+    n_src = int(g.choice([0, 1, 1, 2, 3, 3, 4, 5, 8, 9, 16]))
+    n = int(g.choice([0, 1, 3, 1000, int(g.integers(1, 300000))]))
+    common = int(g.choice([0, 4, 8, 16, 32, 48]))
+    offs = [common if g.random() < 0.8 else int(g.integers(0, 16)) * 4 for _ in range(n_src)]
+    dst_off = common if g.random() < 0.8 else int(g.integers(0, 16)) * 4
+    opts = dict(reduce_engine=int(g.choice([0, 0, 1, 2])),
+                vec_bytes=int(g.choice([0, 0, 4, 16, 32])),
+                block_threads=int(g.choice([0, 128, 256, 512])),
+                unroll=int(g.choice([0, 1, 2, 4])),
+                ctas_per_subexec=int(g.choice([0, 0, 1, 2])),
+                use_pdl=int(g.choice([0, 1])))
+    subexec = int(g.choice([0, 0, 1, 4, 7, 32, 200]))
+    return g, n_src, n, offs, dst_off, opts, subexec
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_reduce_fuzz(tb, seed):
+    g, n_src, n, offs, dst_off, opts, subexec = _reduce_case(seed)
+    srcs = [finite_floats(g, n) for _ in range(n_src)]
+    nbytes = 4 * n
+    pad = 256
+    bufs = []
+    for a, off in zip(srcs, offs):
+        b = dev_bytes(nbytes + off + pad, fill=0x5A)
+        if nbytes:
+            b[off:off + nbytes].copy_(to_dev(a))
+        bufs.append((b, off))
+    dst = dev_bytes(nbytes + dst_off + pad, fill=0xC3)
+    with tb.Context(0, tb.options(**opts)) as c:
+        try:
+            c.reduce_copy([b.data_ptr() + off for b, off in bufs], dst.data_ptr() + dst_off,
+                          nbytes, subexec)
+        except tb.TBError as e:
+            # only a combination the library cannot serve may be refused
+            assert e.code == tb.TB_ENOTSUP, (seed, opts, e)
+            assert opts["reduce_engine"] == 2 or opts["vec_bytes"] in (16, 32)
+            return
+    got = to_host(dst)
+    exp = oracle.dst_reference(srcs, n=n)
+    body = got[dst_off:dst_off + nbytes]
+    if nbytes:
+        mm = oracle.first_mismatch(body.view(np.uint32), exp.view(np.uint32))
+        assert mm == -1, f"seed {seed} {opts} subexec {subexec}: first mismatch at {mm}"
+    assert np.all(got[:dst_off] == 0xC3) and np.all(got[dst_off + nbytes:] == 0xC3)
+
+
+@pytest.mark.parametrize("seed", range(100))
+def test_batch_fuzz(tb, seed):
+    import torch
+    g = np.random.default_rng(5000 + seed)
+    n = int(g.choice([0, 1, 2, 17, int(g.integers(1, 3000))]))
+    long_frac = float(g.choice([0.0, 0.01, 0.2]))
+    lens = np.where(g.random(n) < long_frac, g.integers(16385, 1 << 18, n),
+                    g.integers(0, 16385, n)).astype(np.uint64)
+    pool = int(lens.sum()) * 2 + (4 << 20)
+    gen = workloads.rng(6000 + seed)
+    so = workloads.scatter_offsets(gen, lens, 0, pool, 1)
+    do = workloads.scatter_offsets(gen, lens, 0, pool, 1)
+    opts = dict(small_max_bytes=int(g.choice([64, 4096, 16384, 1 << 20])),
+                slot_items=int(g.choice([1024, 4096, 65536])),
+                num_slots=int(g.choice([1, 2, 4])),
+                batch_min_copies=int(g.choice([0, 0, 3])),
+                ce_min_bytes=int(g.choice([0, 0, 0, 1 << 17])))
+    src_h = workloads.random_bytes(pool, 7000 + seed)
+    dst_h = workloads.random_bytes(pool, 8000 + seed)
+    src_d, dst_d = to_dev(src_h), to_dev(dst_h)
+    desc = np.stack([np.uint64(src_d.data_ptr()) + so, np.uint64(dst_d.data_ptr()) + do, lens],
+                    axis=1) if n else np.zeros((0, 3), np.uint64)
+    with tb.Context(0, tb.options(**opts)) as c:
+        st = torch.cuda.Stream()
+        c.batch_copy(desc, st)
+        st.synchronize()
+        stats = c.last_batch_stats()
+    assert stats["descs"] == int((lens > 0).sum())
+    exp = dst_h.copy()
+    oracle.apply_batch(exp, src_h, so, do, lens)
+    mm = oracle.first_mismatch(to_host(dst_d), exp)
+    assert mm == -1, f"seed {seed} {opts} n {n}: first differing byte {mm}"
