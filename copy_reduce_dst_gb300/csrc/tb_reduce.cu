@@ -111,8 +111,8 @@ __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, const char *
             vstore<VB>(d + (v0 + u * stride) * VB, acc[u]);
 }
 
-template <int N, int VB, int U>
-__global__ void __launch_bounds__(512) k_reduce(const ReduceArgs a)
+template <int N, int VB, int U, int MAXT = 512>
+__global__ void __launch_bounds__(MAXT) k_reduce(const ReduceArgs a)
 {
     const uint32_t tid = threadIdx.x;
     const uint32_t bd = blockDim.x;
@@ -411,6 +411,22 @@ ReduceKernel pick_vec(int vb, int u)
     }
 }
 
+// 1024-thread forms for a CTA alone on its SM: 2 to 4 sources, 32-byte
+// vectors, two vectors per source in flight (one for 4 sources).  The
+// 3-source, two-vector form spills 80 bytes at 64 registers and still
+// measured fastest (131 against 110 GB/s per CTA with one vector).
+ReduceKernel pick_wide(int n_src, int u)
+{
+    switch (n_src) {
+    case 2: return u >= 2 ? k_reduce<2, 32, 2, 1024> : k_reduce<2, 32, 1, 1024>;
+    case 3: return u >= 2 ? k_reduce<3, 32, 2, 1024> : k_reduce<3, 32, 1, 1024>;
+    case 4: return k_reduce<4, 32, 1, 1024>;
+    default: return nullptr;
+    }
+}
+
+constexpr int kWideThreads = 1024;
+
 ReduceKernel pick_reduce(int n_src, int vb, int u)
 {
     switch (n_src) {
@@ -462,9 +478,10 @@ static int bulk_ctas_per_sm(int n_src)
 
 int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll)
 {
-    void *fn = n_src <= 8 ? (void *)pick_reduce(n_src, vec_bytes, unroll)
-                          : (vec_bytes == 16 ? (void *)k_reduce_many<16> : (void *)k_reduce_many<4>);
-    return resident_ctas(fn, block_threads, 0);
+    void *fn = block_threads > 512 ? (void *)pick_wide(n_src, unroll)
+               : n_src <= 8 ? (void *)pick_reduce(n_src, vec_bytes, unroll)
+                            : (vec_bytes == 16 ? (void *)k_reduce_many<16> : (void *)k_reduce_many<4>);
+    return fn ? resident_ctas(fn, block_threads, 0) : 0;
 }
 
 int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, uint64_t num_bytes,
@@ -538,15 +555,16 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // source up, where it keeps more bytes in flight per SM than per-thread
     // vector loads; below that, its per-tile pipeline latency costs more
     // than it saves and the vector form is faster.  A CTA alone on its SM
-    // with 2 or 3 sources is limited by the bulk form's per-tile adds and
-    // barrier instead, and the vector form with 32-byte vectors, two per
-    // source in flight, streams more (per CTA: 77 against 60 GB/s for 2
-    // sources, 74 against 61 for 3).  One source (a relay, 103 against 89)
-    // and 4 sources (one vector per source fits: 52 against 68) stay bulk.
+    // with 2 to 4 sources is limited by the bulk form's per-tile adds and
+    // barrier instead; the vector form in a 1024-thread CTA with 32-byte
+    // vectors (two per source in flight, one for 4 sources) streams about
+    // twice as much (per CTA: 122 against 60 GB/s for 2 sources, 131
+    // against 61 for 3, 130 against 65 for 4).  One source stays bulk (a
+    // relay: 105 against 101).
     const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
-    const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 3;
+    const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 4;
     p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
                                  num_bytes >= kBulkMinBytes && !vector_alone))
                     ? 2
@@ -569,6 +587,12 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
                         : std::min(unroll ? unroll : (alone ? max_unroll(n_src, vb)
                                                             : default_unroll(n_src, vb)),
                                    max_unroll(n_src, vb));
+    // A CTA alone on its SM with 2 to 4 sources and 32-byte vectors runs
+    // 1024 threads (pick_wide) unless the caller fixed the block size.
+    if (alone && p->engine == 1 && vb == 32 && n_src >= 2 && n_src <= 4 && block_threads == 0) {
+        p->block_threads = kWideThreads;
+        p->unroll = std::min(unroll ? unroll : 2, n_src <= 3 ? 2 : 1);
+    }
 
     // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
     // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
@@ -669,7 +693,11 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     if (p.n_src > 8)
         return cudaLaunchKernelEx(&cfg, p.vec_bytes == 16 ? k_reduce_many<16> : k_reduce_many<4>, a,
                                   p.n_src);
-    return cudaLaunchKernelEx(&cfg, pick_reduce(p.n_src, p.vec_bytes, p.unroll), a);
+    ReduceKernel k = p.block_threads > 512 ? pick_wide(p.n_src, p.unroll)
+                                           : pick_reduce(p.n_src, p.vec_bytes, p.unroll);
+    if (!k || (p.block_threads > 512 && resident_ctas((const void *)k, p.block_threads, 0) < 1))
+        return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 }  // namespace tb

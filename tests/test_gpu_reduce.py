@@ -164,6 +164,26 @@ def test_bulk_deep_pipeline(tb, nsrc, subexec):
                            num_subexec=subexec)
 
 
+@pytest.mark.parametrize("nsrc", [2, 3, 4])
+@pytest.mark.parametrize("subexec,n,off", [(1, 262144 * 5 + 7, 4), (5, 1000003, 20),
+                                           (32, 65536 * 3 + 1, 0), (152, 4099, 12)])
+def test_reduce_parity_wide_ctas(tb, nsrc, subexec, n, off):
+    """1024-thread CTAs (one CTA per sub-executor, no more than one per SM)
+    against the oracle: heads, ragged tails, several rounds per CTA."""
+    import torch
+    if subexec > torch.cuda.get_device_properties(0).multi_processor_count:
+        pytest.skip("fewer SMs than sub-executors")
+    g = np.random.default_rng(700 + nsrc * 10 + subexec)
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    with tb.Context(0, tb.options(ctas_per_subexec=1)) as c:
+        d = dev_bytes(64)
+        info = c.reduce_plan([d.data_ptr() + off] * nsrc, d.data_ptr() + off + (1 << 36), 4 * n,
+                             subexec)
+        assert info["block_threads"] == 1024 and info["grid"] == subexec
+        reduce_and_compare(tb, c, srcs, byte_offsets=[off] * nsrc, dst_offset=off,
+                           num_subexec=subexec)
+
+
 def test_reduce_plan_engine_choice(tb, ctx):
     # planning only: the addresses are never accessed; dst lies far away
     d = dev_bytes(1 << 20)
@@ -188,19 +208,20 @@ def test_reduce_plan_engine_choice(tb, ctx):
 
 def test_engine_choice_one_cta_per_subexecutor(tb):
     """With one CTA per sub-executor and no more CTAs than SMs, large
-    transfers of 2 or 3 sources take the vector form with two 32-byte
-    vectors per source in flight; 1 and 4 sources keep the bulk form with
-    its deep pipeline."""
+    transfers of 2 to 4 sources take the vector form in 1024-thread CTAs
+    with 32-byte vectors (two per source in flight, one for 4 sources); one
+    source keeps the bulk form with its deep pipeline."""
     d = dev_bytes(1 << 20)
     p = d.data_ptr()
     far = p + (1 << 36)            # planning only: never accessed
     big = 64 << 20
     with tb.Context(0, tb.options(ctas_per_subexec=1)) as c:
-        for n, engine in ((1, 2), (2, 1), (3, 1), (4, 2)):
+        for n, engine in ((1, 2), (2, 1), (3, 1), (4, 1)):
             info = c.reduce_plan([p] * n, far, big, 32)
             assert info["engine"] == engine and info["grid"] == 32
             if engine == 1:
-                assert info["vec_bytes"] == 32 and info["unroll"] == 2
+                assert info["vec_bytes"] == 32 and info["block_threads"] == 1024
+                assert info["unroll"] == (2 if n <= 3 else 1)
             else:
                 assert info["smem_bytes"] > 128 + 3 * n * (32768 if n == 1 else 8192)
         assert c.reduce_plan([p] * 3, far, big, 1000)["engine"] == 2  # CTAs share SMs
