@@ -594,14 +594,14 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         p->unroll = std::min(unroll ? unroll : 2, n_src <= 3 ? 2 : 1);
     }
 
-    // One full wave of resident CTAs, or S * ctas_per_subexec when the caller
-    // fixes the CTAs of each sub-executor (1 = TransferBench's one block per
-    // sub-executor); never fewer CTAs than sub-executors.  The vector form
-    // launches no more CTAs than its body has rounds of work (block_threads
-    // * unroll vectors each), but at least one per SM: a small transfer is
-    // bound by launch and memory latency, and CTAs without a full round add
-    // launch work without adding bytes in flight (4 MiB: 152 CTAs 2.5 us
-    // against 304 CTAs 2.9 us per iteration).
+    // Grid: S * ctas_per_subexec when the caller fixes the CTAs of each
+    // sub-executor (1 = TransferBench's one block per sub-executor), else
+    // the library's grid below, never fewer CTAs than sub-executors.  The
+    // vector form launches at most one wave and no more CTAs than its body
+    // has rounds of work (block_threads * unroll vectors each), but at least
+    // one per SM: a small transfer is bound by launch and memory latency,
+    // and CTAs without a full round add launch work without adding bytes in
+    // flight (4 MiB: 152 CTAs 2.5 us against 304 CTAs 2.9 us per iteration).
     if (p->engine == 2)
         p->block_threads = kBulkThreads;
     const int per_sm = p->engine == 2 ? bulk_ctas_per_sm(n_src)
@@ -628,11 +628,12 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         const uint64_t waves = std::max<uint64_t>(1, std::min<uint64_t>(want / (uint64_t)full, 4096));
         wave = (int64_t)(waves * (uint64_t)full);
     }
-    // numSubExec = 0: the vector form gives each CTA its own range; the bulk
-    // form deals all tiles round robin over its whole grid (one range), so
-    // each wave of CTAs sweeps neighbouring tiles (3 sources, 3 x 256 MiB:
-    // 7.22 against 6.98 TB/s with a range per CTA).
-    const int64_t S = num_subexec > 0 ? num_subexec : (p->engine == 2 ? 1 : wave);
+    // numSubExec = 0: one range per CTA, except that the bulk form on the
+    // library's grid deals all tiles round robin over the whole grid (one
+    // range), so each wave of CTAs sweeps neighbouring tiles (3 sources,
+    // 3 x 256 MiB: 7.22 against 6.98 TB/s with a range per CTA).
+    const int64_t S = num_subexec > 0 ? num_subexec
+                      : (p->engine == 2 && ctas_per_subexec == 0) ? 1 : wave;
     const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, wave);
     if (G > (int64_t)INT32_MAX)
         return TB_EINVAL;

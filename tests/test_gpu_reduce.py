@@ -184,6 +184,19 @@ def test_reduce_parity_wide_ctas(tb, nsrc, subexec, n, off):
                            num_subexec=subexec)
 
 
+def test_plan_fixed_ctas_with_automatic_subexecutors(tb):
+    """ctas_per_subexec fixed and numSubExec 0: one sub-executor per CTA of
+    the library's grid, for both forms (not a single CTA)."""
+    d = dev_bytes(64)
+    p = d.data_ptr()
+    far = p + (1 << 36)            # planning only: never accessed
+    for engine in (1, 2):
+        with tb.Context(0, tb.options(reduce_engine=engine, ctas_per_subexec=1)) as c:
+            info = c.reduce_plan([p] * 3, far, 256 << 20, 0)
+            assert info["engine"] == engine
+            assert info["grid"] == info["num_subexec"] and info["grid"] >= 152
+
+
 def test_reduce_plan_engine_choice(tb, ctx):
     # planning only: the addresses are never accessed; dst lies far away
     d = dev_bytes(1 << 20)
