@@ -323,9 +323,9 @@ uint64_t tb_prep_h2d_bytes(const tb_ctx *ctx);
    nSrc <= TB_MAX_SRCS.  The elements are split into numSubExec contiguous
    ranges (sub-executors), each served by its own CTAs and sized in
    proportion to them (equal when numSubExec divides the grid);
-   numSubExec == 0 is the library's choice: one per CTA of the vector form's
-   grid, one for the whole grid of the bulk form.  The split does not change
-   the result.  dst must not overlap any source (TB_EINVAL).  TB_ETIMEOUT, with
+   numSubExec == 0 is the library's choice: one per CTA, except one for the
+   whole grid of the bulk form when ctas_per_subexec is 0.  The split does
+   not change the result.  dst must not overlap any source (TB_EINVAL).  TB_ETIMEOUT, with
    nothing launched, when an earlier launch of this context stopped early
    because a bounded wait inside the kernel expired (kernel_wait_ns); the
    call after that one launches again. */
