@@ -362,7 +362,8 @@ __device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first,
     }
 }
 
-// Persistent grid of one wave.
+// A grid of up to kBatchWaves waves of resident CTAs (short-lived CTAs let
+// the scheduler balance the SMs' finishing times).
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
 //   owns chunks b, b + G, ... (the same number for every CTA, the grid
 //   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned

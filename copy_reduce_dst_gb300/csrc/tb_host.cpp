@@ -77,7 +77,7 @@ struct tb_ctx {
     std::vector<Slot> slots;
     void *slot_status = nullptr;      // host-mapped status words, one per slot
     uint32_t next_slot = 0;
-    int batch_grid = 0;               // one wave of batch-kernel CTAs
+    int batch_grid = 0;               // batch-kernel CTAs resident at once (one wave)
     std::vector<WorkItem> longs;      // long copies of the run being packed
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
