@@ -580,13 +580,23 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         p->head = std::min<uint64_t>(head, p->n);
     }
     p->nvec = (p->n - p->head) / ((uint64_t)vb / 4);
-    p->block_threads = block_threads ? block_threads : 512;
     // Unroll: the largest that keeps two 512-thread CTAs per SM, or the
     // largest without spills when each CTA has an SM (and its registers) alone.
     p->unroll = vb == 4 ? 4
                         : std::min(unroll ? unroll : (alone ? max_unroll(n_src, vb)
                                                             : default_unroll(n_src, vb)),
                                    max_unroll(n_src, vb));
+    // Block size: the caller's, else 512 or 256 threads, whichever keeps
+    // more threads resident per SM at this kernel's register use (ties: 512).
+    // Many sources need many registers: 4 to 6 sources fit one 512-thread
+    // CTA per SM but three 256-thread ones (6 sources, 128 MiB: 6.2 against
+    // 4.7-5.1 TB/s).
+    p->block_threads = block_threads;
+    if (block_threads == 0) {
+        const int r512 = reduce_ctas_per_sm(n_src, vb, 512, p->unroll);
+        const int r256 = reduce_ctas_per_sm(n_src, vb, 256, p->unroll);
+        p->block_threads = 256 * r256 > 512 * r512 ? 256 : 512;
+    }
     // A CTA alone on its SM with 2 to 4 sources and 32-byte vectors runs
     // 1024 threads (pick_wide) unless the caller fixed the block size.
     if (alone && p->engine == 1 && vb == 32 && n_src >= 2 && n_src <= 4 && block_threads == 0) {
@@ -610,10 +620,12 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         return TB_ECUDA;
     const int64_t full = (int64_t)num_sms * per_sm;
     int64_t wave = full;
+    bool whole_rounds = true;  // at least one full round of work per CTA
     if (p->engine == 1) {
         const uint64_t per_cta = (uint64_t)p->block_threads * (uint64_t)p->unroll;
         const uint64_t rounds = (p->nvec + per_cta - 1) / per_cta;
         wave = (int64_t)std::min<uint64_t>((uint64_t)full, std::max<uint64_t>((uint64_t)num_sms, rounds));
+        whole_rounds = rounds >= (uint64_t)wave;
     } else {
         // Bulk form: many short-lived CTAs of about kBulkTilesPerCta tiles
         // each rather than one resident wave with equal shares.  The CTA
@@ -628,12 +640,16 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         const uint64_t waves = std::max<uint64_t>(1, std::min<uint64_t>(want / (uint64_t)full, 4096));
         wave = (int64_t)(waves * (uint64_t)full);
     }
-    // numSubExec = 0: one range per CTA, except that the bulk form on the
-    // library's grid deals all tiles round robin over the whole grid (one
-    // range), so each wave of CTAs sweeps neighbouring tiles (3 sources,
-    // 3 x 256 MiB: 7.22 against 6.98 TB/s with a range per CTA).
+    // numSubExec = 0 on the library's grid: one range over the whole grid,
+    // its tiles dealt round robin, so each wave of CTAs sweeps neighbouring
+    // tiles (bulk, 3 sources, 3 x 256 MiB: 7.22 against 6.98 TB/s with a
+    // range per CTA; vector, 128 MiB: 2-11% faster for 1 to 12 sources) -
+    // as long as every CTA gets a whole round: a smaller vector transfer
+    // gives each CTA its own part of a round instead, so that all of them
+    // load (4 MiB: 152 CTAs busy, not 64).  With the CTAs per sub-executor
+    // fixed: one range per CTA.
     const int64_t S = num_subexec > 0 ? num_subexec
-                      : (p->engine == 2 && ctas_per_subexec == 0) ? 1 : wave;
+                      : (ctas_per_subexec == 0 && whole_rounds) ? 1 : wave;
     const int64_t G = ctas_per_subexec > 0 ? S * ctas_per_subexec : std::max<int64_t>(S, wave);
     if (G > (int64_t)INT32_MAX)
         return TB_EINVAL;

@@ -93,8 +93,9 @@ typedef struct {
        1 gives TransferBench's one CTA per sub-executor.  Default 0. */
     int32_t ctas_per_subexec;
     /* Reduce-copy threads per CTA (multiple of 32, <= 512); 0 = the
-       library's choice: 512, or 1024 for a CTA alone on its SM (one CTA
-       per sub-executor, no more CTAs than SMs) with 2 to 4 sources. */
+       library's choice: 512 or 256, whichever keeps more threads resident
+       per SM, or 1024 for a CTA alone on its SM (one CTA per sub-executor,
+       no more CTAs than SMs) with 2 to 4 sources. */
     int32_t block_threads;
     /* Batched copy: descriptors up to this many bytes are copied by one
        warp; the bytes of all longer ones are shared equally among the CTAs.
