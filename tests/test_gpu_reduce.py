@@ -255,8 +255,15 @@ def test_vector_grid_follows_the_work(tb, ctx):
         assert info["engine"] == 1
         rounds = -(-info["body_vectors"] // (info["block_threads"] * info["unroll"]))
         assert info["grid"] >= sms and (info["grid"] == sms or info["grid"] <= rounds)
-    assert ctx.reduce_plan([p], p + (32 << 20), 4 << 20)["grid"] == sms
+    small = ctx.reduce_plan([p], p + (32 << 20), 4 << 20)
+    assert small["grid"] == sms and small["num_subexec"] == sms    # every CTA takes a part
     assert ctx.reduce_plan([p], p + (32 << 20), 4 << 20, 1000)["grid"] == 1000
+    with tb.Context(0, tb.options(reduce_engine=1)) as c:
+        far = p + (1 << 36)                                          # planning only
+        big = c.reduce_plan([p] * 3, far, 128 << 20)
+        assert big["num_subexec"] == 1 and big["grid"] >= sms        # one range, whole rounds
+        five = c.reduce_plan([p] * 5, far, 128 << 20)
+        assert five["block_threads"] == 256                           # more threads resident
 
 
 def test_bulk_engine_limits(tb):
