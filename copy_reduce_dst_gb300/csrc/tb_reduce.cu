@@ -586,6 +586,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
                         : std::min(unroll ? unroll : (alone ? max_unroll(n_src, vb)
                                                             : default_unroll(n_src, vb)),
                                    max_unroll(n_src, vb));
+    if (n_src > 8)
+        p->unroll = 2;  // k_reduce_many keeps two vectors per thread in flight
     // Block size: the caller's, else 512 or 256 threads, whichever keeps
     // more threads resident per SM at this kernel's register use (ties: 512).
     // Many sources need many registers: 4 to 6 sources fit one 512-thread
