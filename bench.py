@@ -529,6 +529,7 @@ def study(args, tb, torch, local):
             print(json.dumps(row), flush=True)
     del flush
     study_validation(tb, torch, local)
+    study_host_paths(tb, torch, local)
     study_tiny_batches(tb, torch, local)
     study_small_copies_under_compute(tb, torch, local)
     study_batch_configs(tb, torch, local)
@@ -683,6 +684,40 @@ def study_small_copies_under_compute(tb, torch, local):
                 out[key + "_samples"] = len(times)
     print(json.dumps(out), flush=True)
     del a, b, src, dst
+
+
+def study_host_paths(tb, torch, local):
+    """tb_reduce_copy_host on the bench workload (3 x 256 MiB): pinned host
+    buffers (one kernel reads and writes them across the host link) against
+    pageable ones (staged through device buffers in 32 MiB chunks on three
+    streams); wall time per call with the stream synchronised, median of 5
+    after 1, GB/s counting read + write bytes as the bench line does."""
+    import statistics as st
+    nb = 256 * MiB
+    moved = 4 * nb
+    dsrc = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    ddst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    out = {"study": "host paths", "workload": "3 x 256 MiB reduce-copy from host memory"}
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        for kind in ("pinned", "pageable"):
+            hs = [torch.full((nb // 4,), float(k + 1), dtype=torch.float32) for k in range(3)]
+            hd = torch.empty(nb // 4, dtype=torch.float32)
+            if kind == "pinned":
+                hs = [h.pin_memory() for h in hs]
+                hd = hd.pin_memory()
+            t = []
+            for i in range(6):
+                t0 = time.perf_counter()
+                ctx.reduce_copy_host(hs, hd, nb, dsrc, ddst, 0, stream)
+                stream.synchronize()
+                if i:
+                    t.append(time.perf_counter() - t0)
+            assert float(hd[12345]) == 6.0
+            out[kind + "_ms"] = round(st.median(t) * 1e3, 2)
+            out[kind + "_gbps"] = round(moved / st.median(t) / 1e9, 1)
+            del hs, hd
+    print(json.dumps(out), flush=True)
 
 
 def study_tiny_batches(tb, torch, local):
