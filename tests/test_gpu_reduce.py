@@ -244,8 +244,10 @@ def test_engine_choice_one_cta_per_subexecutor(tb):
 
 def test_vector_grid_follows_the_work(tb, ctx):
     """The vector form launches one CTA per round of work (block_threads x
-    unroll vectors), at least one per SM and at most one full wave; the bulk
-    form and fixed sub-executor counts keep their grids."""
+    unroll vectors), at least one per SM and at most one full wave; a small
+    transfer gives every CTA its own range, a large one deals whole rounds
+    over one range; its block size keeps the most threads resident; fixed
+    sub-executor counts keep their grids."""
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     d = dev_bytes(64 << 20)
