@@ -30,7 +30,8 @@ using tb::WorkItem;
 
 constexpr uint64_t kSmallMax = 16384;  // one warp per copy up to this size
 constexpr int kMaxDevices = 64;
-constexpr int kMaxGrid = 2048;         // CTAs of one launch at most
+constexpr int kMaxGrid = 2048;         // CTAs of one wave at most (a launch spans up to
+                                       // kBatchWaves waves; nothing is sized by the grid)
 // Bytes of one packed launch of TB_NOALLOC_MAX_ITEMS descriptors.
 constexpr size_t kScratchBytes =
     tb::kBatchHeader + TB_NOALLOC_MAX_ITEMS * (sizeof(WorkItem) + sizeof(uint64_t)) +
