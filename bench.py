@@ -21,9 +21,15 @@ Default line (rank 0 prints one JSON object):
 ``--impl reference`` times the CPU oracle itself (the reference arm of this
 benchmark) on the same metric.  Under torchrun every rank runs its own
 replica on its own GPU (no data exchange); timings are the max over ranks.
-``--study`` prints extra lines (single 4 MiB transfer, the fillCompress
-sweep with rotation on and off, cold and warm, and the batch split into its
-long and short copies) instead of the default line.
+``--study`` prints extra lines instead of the default line: the single
+4 MiB transfer (graph with and without programmatic dependent launch,
+events per launch), the fillCompress sweep with rotation on and off (cold,
+warm, graphed), validation on the device against the host, end to end from
+pinned and pageable host memory, tiny batches against per-copy memcpy,
+small copies under a GEMM loop (normal and high-priority stream), the three
+batch workloads, the batch's long and short parts, copy-engine routing, and
+GEMM interference.  ``--profile reduce|batch|rotation`` runs one workload
+for an ncu capture (commands in ``profiles/``).
 """
 from __future__ import annotations
 
