@@ -28,8 +28,8 @@ warm, graphed), validation on the device against the host, end to end from
 pinned and pageable host memory, tiny batches against per-copy memcpy,
 small copies under a GEMM loop (normal and high-priority stream), the three
 batch workloads, the batch's long and short parts, copy-engine routing, and
-GEMM interference.  ``--profile reduce|batch|rotation`` runs one workload
-for an ncu capture (commands in ``profiles/``).
+GEMM interference.  ``--profile reduce|batch|batch-short|rotation`` runs
+one workload for an ncu capture (commands in ``profiles/``).
 """
 from __future__ import annotations
 
@@ -402,7 +402,7 @@ def run_batch(args, tb, torch, ranks, local):
                      "frac": round(algo / (kernel_ms / 1e3) / 1e9 / peak, 4),
                      "traffic": profiled_traffic("batch_head_sliced"),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
-                     "kernel": "k_batch"},
+                     "kernel": "k_batch<2, 4>"},
     }
 
 
@@ -933,6 +933,8 @@ def profile_target(kind, args, tb, torch, local):
         src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
         dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
         desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+        if kind == "batch-short":  # its 47,520 short copies alone
+            desc = desc[desc[:, 2] <= 16384]
         with tb.Context(local, ctx_options(tb)) as ctx:
             for _ in range(6):
                 ctx.batch_copy(desc, stream)
@@ -951,7 +953,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--study", action="store_true")
-    ap.add_argument("--profile", choices=["reduce", "batch", "rotation"])
+    ap.add_argument("--profile", choices=["reduce", "batch", "batch-short", "rotation"])
     ap.add_argument("--mib", type=int, default=16, help="--profile rotation: transfer MiB")
     ap.add_argument("--rotate-mib", type=int, default=256,
                     help="--profile rotation: SRC_ROTATE_BYTES in MiB (0 = off)")

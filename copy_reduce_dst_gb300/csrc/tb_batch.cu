@@ -1,7 +1,7 @@
 // K2, the batched descriptor copy of libtb (sm_103a): one launch over a
 // packed (src, dst, len) work list (Mooncake RFC #5041, "Design of #5040").
 // Long copies stream through a bulk (TMA) pipeline in shared memory; short
-// copies go to warps.
+// copies go to warps, through shared memory by asynchronous copies.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,9 +28,11 @@ using namespace dev;
 // The body goes in rounds: each thread issues all its loads of a round,
 // predicated on the range, before its stores, so a range of up to
 // size * 32 * kWideUnroll bytes (32-byte path) costs one memory round trip.
-// The unrolls are the largest that compile without spilling at the kernel's
-// 64 registers (four 256-thread CTAs per SM); spilling variants (4 or 8
-// wide vectors) measured 1.3-1.7x slower on the short copies.
+// The unrolls are the largest that compiled without spilling at 64
+// registers; spilling variants (4 or 8 wide vectors) measured 1.3-1.7x
+// slower on the short copies.  Short copies whose src and dst are equal
+// modulo 16 no longer come here: they go through the shared-memory pipe
+// below, which keeps more bytes in flight than a round of registers.
 // ---------------------------------------------------------------------------
 constexpr int kWideUnroll = 2;    // 32-byte vectors per thread and round
 constexpr int kNarrowUnroll = 2;  // 16-byte vectors per thread and round
@@ -166,7 +168,7 @@ struct BatchArgs {
     uint64_t long_bytes;
     uint32_t n_short;
     uint32_t chunks;
-    uint32_t claim_items;        // short copies a warp takes at a time: 1 or 2
+    uint32_t claim_items;        // short copies a warp takes by its index: 1 or 2
     uint64_t wait_ns;            // limit of each wait for a block's load
 };
 
@@ -328,53 +330,228 @@ __device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
     }
 }
 
-// Short copies.  A warp takes C items at a time (C = 1 or 2) and copies them
-// side by side, 32 / C lanes each, so their loads are in flight together.
-// Its first C items are fixed by its index among the warps that start on
-// short copies (no atomic); the items past those first rounds are claimed
-// from the counter, each warp claiming its next items before copying the
-// current ones so that the claim's latency overlaps the copy.
-template <uint32_t C>
-__device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first, uint32_t dyn_base,
-                                             bool dynamic, uint32_t lane)
+// Short copies through shared memory.  Each warp streams its copies as
+// pieces of up to 32 * U 16-byte units through a ring of S piece slots:
+// every lane issues asynchronous 16-byte global -> shared copies (cp.async,
+// no registers held) for its units of a piece and commits them as a group,
+// then waits for the oldest piece in the ring and stores that one from
+// shared memory.  A warp so keeps S - 1 pieces landing while it stores one,
+// and no register holds data in flight.  Each lane reads back only the
+// units it loaded, so no barrier is needed.  Measured on GB300 (47,520
+// short copies of 64 B - 16 KiB alone / the 47,540 batch with long copies):
+// register rounds 62.5 / 142.7 us; S = 2: U = 8 55.4, U = 4 57.0 /
+// U = 4 141.6, U = 8 143.7; S = 4: U = 4 54.5 / U = 2 141.0; S = 8: U = 2
+// 58.4 / U = 1 143.5; U = 16 (one CTA per SM) 71.1.  Short-only launches
+// take 8 KiB of slots per warp (three CTAs per SM), launches with long
+// copies 4 KiB beside the bulk stages (two per SM).
+constexpr int kShortUnits = 4;  // U of a launch of short copies only
+constexpr int kShortSlots = 4;  // S of a launch of short copies only
+constexpr int kMixedUnits = 2;  // U beside the long copies' bulk stages
+constexpr int kMixedSlots = 4;
+
+template <int U>
+__host__ __device__ constexpr uint32_t piece_bytes()
 {
-    constexpr uint32_t kLanes = 32 / C;
-    const uint32_t n_short = a.n_short;
-    const uint32_t group = lane / kLanes, rank = lane % kLanes;
-    uint32_t base = first;
-    if (base >= n_short && dynamic) {
-        uint32_t c = 0;
-        if (lane == 0)
-            c = dyn_base + atomicAdd(a.claim, C);
-        base = __shfl_sync(0xffffffffu, c, 0);
-    }
-    while (base < n_short) {
-        uint32_t next = n_short;
-        if (dynamic && lane == 0)
-            next = dyn_base + atomicAdd(a.claim, C);
-        const uint32_t i = base + group;
-        if (i < n_short) {
-            const WorkItem w = load_item(a.shorts + i);
-            copy_range(reinterpret_cast<uint8_t *>(w.dst), reinterpret_cast<const uint8_t *>(w.src),
-                       w.len, rank, kLanes);
-        }
-        base = __shfl_sync(0xffffffffu, next, 0);
-    }
+    return 32u * U * 16u;
 }
 
-// A grid of up to kBatchWaves waves of resident CTAs (short-lived CTAs let
-// the scheduler balance the SMs' finishing times).
+template <int U, int S>
+__host__ __device__ constexpr size_t warp_stage_bytes()
+{
+    return S * (size_t)piece_bytes<U>();
+}
+
+template <int U, int S>
+__host__ __device__ constexpr size_t short_smem_bytes()
+{
+    return (kBatchThreads / 32) * warp_stage_bytes<U, S>();
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void *g)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(g) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t smem)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem)
+                 : "memory");
+    return r;
+}
+
+// The ring: slot `cur` is free; the S - 1 pieces in flight are q[0]
+// (oldest, in slot cur + 1) .. q[S - 2] (newest, in slot cur - 1), slots
+// taken mod S.  It starts with S - 1 empty pieces (nv = 0), so every push
+// runs the same steps: load into slot cur, commit, wait until at most S - 1
+// groups are pending (the oldest piece has landed), store q[0], shift.
+// While fewer than S groups were ever committed the oldest entry is an
+// empty piece and the wait returns at once.
+template <int U, int S>
+struct ShortPipe {
+    struct Piece {
+        uint64_t dst;  // 16-byte aligned
+        uint32_t nv;   // 16-byte units, 0 = nothing
+    };
+    uint32_t base;  // this warp's S slots
+    uint32_t lane;
+    uint32_t cur;
+    Piece q[S - 1];
+
+    __device__ ShortPipe(uint32_t b, uint32_t l) : base(b), lane(l), cur(0)
+    {
+#pragma unroll
+        for (int j = 0; j < S - 1; ++j)
+            q[j] = Piece{0ull, 0u};
+    }
+    __device__ uint32_t unit(uint32_t slot, int u) const
+    {
+        return base + (((slot * U + (uint32_t)u) * 32u + lane) << 4);
+    }
+    __device__ void store(const Piece &p, uint32_t slot) const
+    {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t k = lane + 32u * u;
+            if (k < p.nv)
+                st16(reinterpret_cast<uint4 *>(p.dst) + k, lds16(unit(slot, u)));
+        }
+    }
+    // Loads a piece of nv <= 32 * U units (src and dst 16-byte aligned)
+    // into slot cur, then stores the oldest piece in flight.
+    __device__ void push(const uint8_t *src, uint64_t dst, uint32_t nv)
+    {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t k = lane + 32u * u;
+            if (k < nv)
+                cp_async16(unit(cur, u), src + 16ull * k);
+        }
+        cp_async_commit();
+        const uint32_t oldest = cur + 1 == S ? 0u : cur + 1;
+        cp_async_wait<S - 1>();
+        store(q[0], oldest);
+#pragma unroll
+        for (int j = 0; j + 1 < S - 1; ++j)
+            q[j] = q[j + 1];
+        q[S - 2] = Piece{dst, nv};
+        cur = oldest;
+    }
+    // Stores every piece still in flight, oldest first.
+    __device__ void flush()
+    {
+        cp_async_wait<0>();
+#pragma unroll
+        for (int j = 0; j < S - 1; ++j) {
+            const uint32_t slot = (cur + 1 + (uint32_t)j) % S;
+            store(q[j], slot);
+            q[j] = Piece{0ull, 0u};
+        }
+    }
+};
+
+// One short copy by a whole warp.  src and dst equal modulo 16: up to 15
+// head bytes (lanes 0..14) and 15 tail bytes (lanes 16..30) go a byte per
+// lane, loaded before the body's pieces are pushed and stored after, so
+// their latency overlaps the pipe's; the body goes through the pipe.  Any
+// other alignment: copy_range through registers.
+template <int U, int S>
+__device__ __forceinline__ void short_item(ShortPipe<U, S> &p, const WorkItem &w, uint32_t lane)
+{
+    const uint8_t *s = reinterpret_cast<const uint8_t *>(w.src);
+    uint8_t *d = reinterpret_cast<uint8_t *>(w.dst);
+    if (((w.src ^ w.dst) & 15u) != 0) {
+        copy_range(d, s, w.len, lane, 32);
+        return;
+    }
+    const uint64_t h = min((uint64_t)((16u - (w.dst & 15u)) & 15u), w.len);
+    const uint64_t body = (w.len - h) & ~(uint64_t)15;
+    const uint64_t t = w.len - h - body;
+    const bool edge = lane < h || (lane >= 16 && lane - 16 < t);
+    const uint64_t eoff = lane < 16 ? lane : h + body + (lane - 16);
+    uint8_t eb = 0;
+    if (edge)
+        eb = s[eoff];
+    for (uint64_t off = 0; off < body; off += piece_bytes<U>()) {
+        const uint32_t nv = (uint32_t)min((body - off) >> 4, (uint64_t)(32u * U));
+        p.push(s + h + off, w.dst + h + off, nv);
+    }
+    if (edge)
+        d[eoff] = eb;
+}
+
+// The short copies of one warp: up to claim_items items by its index
+// among the warps that start on short copies (first, first + stride, ...;
+// no atomic), then items claimed one at a time from the counter.  Lane 0 keeps one claim in
+// flight and the descriptor of the next item is loaded before the current
+// item is copied, so neither latency stalls the pipe.
+template <int U, int S>
+__device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first, uint32_t stride,
+                                             uint32_t dyn_base, bool dynamic, uint32_t lane,
+                                             uint32_t pipe_smem)
+{
+    const uint32_t n = a.n_short;
+    const uint64_t fixed_end = min(dyn_base, n);  // copies taken by index
+    uint32_t pending = n;  // lane 0: the claim in flight
+    if (dynamic && lane == 0)
+        pending = dyn_base + atomicAdd(a.claim, 1u);
+    auto after = [&](uint32_t i) -> uint32_t {
+        if ((uint64_t)i + stride < fixed_end)
+            return i + stride;
+        const uint32_t v = __shfl_sync(0xffffffffu, pending, 0);
+        if (dynamic && v < n && lane == 0)
+            pending = dyn_base + atomicAdd(a.claim, 1u);
+        return v;
+    };
+    uint32_t cur = first < n ? first : after(UINT32_MAX - 1);
+    if (cur >= n)
+        return;
+    ShortPipe<U, S> p(pipe_smem, lane);
+    WorkItem w = load_item(a.shorts + cur);
+    for (;;) {
+        const uint32_t nx = after(cur);
+        WorkItem wn{0, 0, 0};
+        if (nx < n)
+            wn = load_item(a.shorts + nx);
+        short_item(p, w, lane);
+        if (nx >= n)
+            break;
+        cur = nx;
+        w = wn;
+    }
+    p.flush();
+}
+
+// A grid of up to kBatchWaves waves of resident CTAs with long copies
+// (short-lived CTAs let the scheduler balance the SMs' finishing times),
+// kShortWaves with short copies only.  U: see ShortPipe.
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
 //   owns chunks b, b + G, ... (the same number for every CTA, the grid
 //   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned
 //   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
 //   the leftover edges.
-//   Short copies (short_copies): the warps free at the start (all of them,
-//   or warps 1.. when there are long chunks) take a first claim_items items
-//   each by warp index; the rest are claimed from a counter in global memory
-//   by whichever warp is free, warp 0 joining once its pipeline has
-//   drained, which balances the work without any ordering on the host.
-__global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
+//   Short copies (short_copies, each warp through its own shared-memory
+//   pipe): the warps free at the start (all of them, or warps 1.. when
+//   there are long chunks) take up to claim_items items each by warp
+//   index (warp w: w, w + starters); the rest are claimed one at a time
+//   from a counter in global memory by whichever warp is free, warp 0
+//   joining once its pipeline has drained, which balances the work without
+//   any ordering on the host.
+template <int U, int S>
+__global__ void __launch_bounds__(kBatchThreads, 3) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
@@ -403,18 +580,21 @@ __global__ void __launch_bounds__(kBatchThreads, 4) k_batch(const BatchArgs a)
     const uint32_t C = a.claim_items;
     const uint32_t fixed = starters * C;  // items taken by index
     const bool dynamic = fixed < a.n_short;
-    const uint32_t first = starter ? sidx * C : a.n_short;
-    if (C == 1)
-        short_copies<1>(a, first, fixed, dynamic, lane);
-    else
-        short_copies<2>(a, first, fixed, dynamic, lane);
+    const uint32_t first = starter ? sidx : a.n_short;
+    const uint32_t pipes = smem_u32(smem) + (busy0 ? (uint32_t)kBatchSmem : 0u);
+    short_copies<U, S>(a, first, starters, fixed, dynamic, lane,
+                       pipes + warp * (uint32_t)warp_stage_bytes<U, S>());
 }
 
 }  // namespace
 
-int batch_ctas_per_sm()
+int batch_ctas_per_sm(bool with_long)
 {
-    return resident_ctas((const void *)k_batch, kBatchThreads, kBatchSmem);
+    if (with_long)
+        return resident_ctas((const void *)k_batch<kMixedUnits, kMixedSlots>, kBatchThreads,
+                             kBatchSmem + short_smem_bytes<kMixedUnits, kMixedSlots>());
+    return resident_ctas((const void *)k_batch<kShortUnits, kShortSlots>, kBatchThreads,
+                         short_smem_bytes<kShortUnits, kShortSlots>());
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
@@ -422,7 +602,7 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
-    if (batch_ctas_per_sm() < 1)
+    if (batch_ctas_per_sm(plan.chunks > 0) < 1)
         return cudaErrorInvalidValue;
     char *base = static_cast<char *>(const_cast<void *>(dev));
     BatchArgs a;
@@ -437,9 +617,13 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.chunks = plan.chunks;
     a.claim_items = batch_claim_items(plan);
     a.wait_ns = wait_ns;
-    // Short copies only: no shared memory needed.
-    const size_t smem = plan.chunks ? kBatchSmem : 0;
-    k_batch<<<plan.grid, kBatchThreads, smem, stream>>>(a);
+    if (plan.chunks)
+        k_batch<kMixedUnits, kMixedSlots><<<plan.grid, kBatchThreads,
+                                            kBatchSmem + short_smem_bytes<kMixedUnits, kMixedSlots>(),
+                                            stream>>>(a);
+    else  // short copies only: no bulk stages
+        k_batch<kShortUnits, kShortSlots><<<plan.grid, kBatchThreads,
+                                            short_smem_bytes<kShortUnits, kShortSlots>(), stream>>>(a);
     return cudaGetLastError();
 }
 

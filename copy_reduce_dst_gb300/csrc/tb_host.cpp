@@ -77,7 +77,8 @@ struct tb_ctx {
     std::vector<Slot> slots;
     void *slot_status = nullptr;      // host-mapped status words, one per slot
     uint32_t next_slot = 0;
-    int batch_grid = 0;               // batch-kernel CTAs resident at once (one wave)
+    int batch_grid_long = 0;          // batch-kernel CTAs resident at once (one wave),
+    int batch_grid_short = 0;         // with long copies and with short copies only
     std::vector<WorkItem> longs;      // long copies of the run being packed
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
@@ -661,10 +662,12 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     ctx->gate_status_dev = ctx->gate_flag_dev + 1;
     ctx->reduce_status_dev = ctx->gate_flag_dev + 2;
 
-    const int batch_per_sm = tb::batch_ctas_per_sm();
-    if (batch_per_sm < 1)
+    const int long_per_sm = tb::batch_ctas_per_sm(true);
+    const int short_per_sm = tb::batch_ctas_per_sm(false);
+    if (long_per_sm < 1 || short_per_sm < 1)
         return bail(TB_ECUDA);
-    ctx->batch_grid = ctx->num_sms * batch_per_sm;
+    ctx->batch_grid_long = ctx->num_sms * long_per_sm;
+    ctx->batch_grid_short = ctx->num_sms * short_per_sm;
     ctx->slots.resize(o.num_slots);
     const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items);
     void *status_dev = nullptr;
@@ -1322,8 +1325,8 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         }
         if (c.n_short + c.n_long > 0) {
             tb::BatchPlan plan;
-            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid), slot.host,
-                             &plan);
+            const int full = c.n_long ? ctx->batch_grid_long : ctx->batch_grid_short;
+            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, full), slot.host, &plan);
             ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
             // A small batch of short copies all assigned by warp index reads
             // its work list in place from the pinned staging: no upload and

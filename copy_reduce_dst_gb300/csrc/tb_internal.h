@@ -94,6 +94,10 @@ constexpr uint32_t kMaxChunks = 16384;   // chunks of one launch at most
 // (47,540 batch: 141 us at 8 waves against 145 at one; one 2 GiB copy
 // 6.86 against 6.45 TB/s).
 constexpr uint64_t kBatchWaves = 8;
+// Waves of a launch of short copies only: fewer CTAs leave more of the
+// copies to the claim counter, which balances them (47,520 short copies:
+// 55.4 us at 4 waves, 61.0 at 8, 57.3 at 2, 58.5 at 1).
+constexpr uint64_t kShortWaves = 4;
 constexpr size_t kBatchHeader = 16;      // claim counter of the short copies
 
 // Descriptor counts of a batch (descriptors with len == 0 are skipped).
@@ -150,9 +154,10 @@ void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *b
 // overlapping a source (its own included).  Sources may overlap one
 // another.  Returns true with their indices (in either order).
 bool find_overlap(const tb_copy_desc *desc, size_t n, size_t *first, size_t *second);
-// Short copies a warp of the launch takes at a time: 1 (a whole warp per
-// copy) when the warps that start on short copies cover every short copy
-// in two rounds, else 2 (half a warp per copy, more copies in flight).
+// Short copies each warp that starts on short copies takes by its index
+// (no atomic; warp w of `starters` takes copies w, w + starters, ...)
+// before it claims more one at a time from the counter: 1 when those warps
+// outnumber the short copies, else 2.
 uint32_t batch_claim_items(const BatchPlan &plan);
 // Work lists up to this size may be read by the kernel in place.
 constexpr size_t kDirectMaxBytes = 256 * 1024;
@@ -175,7 +180,8 @@ int resident_ctas(const void *kernel, int threads, size_t smem);
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
                          uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull);
 
-// CTAs resident per SM for the batch kernel.
-int batch_ctas_per_sm();
+// CTAs resident per SM for the batch kernel of a launch with long copies
+// (with_long) or of one with short copies only.
+int batch_ctas_per_sm(bool with_long);
 
 }  // namespace tb

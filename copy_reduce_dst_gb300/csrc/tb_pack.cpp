@@ -107,9 +107,15 @@ int batch_grid(const BatchCounts &c, int full_grid)
     const uint64_t warps = kBatchThreads / 32;
     const uint64_t for_short = (c.n_short + warps - 1) / warps;
     const uint64_t for_long = (c.long_bytes + kChunkBytes - 1) / kChunkBytes;
-    const uint64_t want = std::max<uint64_t>(1, std::max(for_short, for_long));
-    return (int)std::min<uint64_t>(
-        std::min<uint64_t>((uint64_t)full_grid * kBatchWaves, kMaxChunks), want);
+    uint64_t want = std::max<uint64_t>(1, std::max(for_short, for_long));
+    if (c.n_long == 0 && want > (uint64_t)full_grid) {
+        // Short copies only, more than one wave's warps: whole waves, the
+        // warps taking the copies past the first one each (a partial wave
+        // would run after the first one has finished).
+        want = (uint64_t)full_grid * std::min<uint64_t>(kShortWaves, want / (uint64_t)full_grid);
+    }
+    const uint64_t waves = c.n_long ? kBatchWaves : kShortWaves;
+    return (int)std::min<uint64_t>(std::min<uint64_t>((uint64_t)full_grid * waves, kMaxChunks), want);
 }
 
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out)
@@ -216,7 +222,7 @@ uint32_t batch_claim_items(const BatchPlan &plan)
 {
     const uint64_t warps = kBatchThreads / 32;
     const uint64_t starters = (uint64_t)plan.grid * (plan.chunks ? warps - 1 : warps);
-    return (uint64_t)plan.n_short <= 2 * starters ? 1u : 2u;
+    return (uint64_t)plan.n_short <= starters ? 1u : 2u;
 }
 
 bool batch_direct(const BatchPlan &plan)

@@ -47,9 +47,11 @@ WorkItem g_host_items[kScratchItems];
 WorkItem g_longs[TB_NOALLOC_MAX_ITEMS];
 std::mutex g_lock;
 
-// Per-device set-up: the scratch array's device address and the grid size.
+// Per-device set-up: the scratch array's device address and the full grid
+// of a launch with long copies and of one with short copies only.
 WorkItem *g_dev_items[kMaxDevices];
-int g_dev_grid[kMaxDevices];
+int g_dev_grid_long[kMaxDevices];
+int g_dev_grid_short[kMaxDevices];
 
 int setup_current_device(int *device)
 {
@@ -63,10 +65,12 @@ int setup_current_device(int *device)
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
         return TB_ECUDA;
-    const int per_sm = tb::batch_ctas_per_sm();
-    if (per_sm < 1)
+    const int long_per_sm = tb::batch_ctas_per_sm(true);
+    const int short_per_sm = tb::batch_ctas_per_sm(false);
+    if (long_per_sm < 1 || short_per_sm < 1)
         return TB_ECUDA;
-    g_dev_grid[*device] = std::min(kMaxGrid, sms * per_sm);
+    g_dev_grid_long[*device] = std::min(kMaxGrid, sms * long_per_sm);
+    g_dev_grid_short[*device] = std::min(kMaxGrid, sms * short_per_sm);
     g_dev_items[*device] = static_cast<WorkItem *>(ptr);
     return TB_OK;
 }
@@ -94,7 +98,8 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
     // counter the kernel claims short copies from.
     tb::gather_batch(desc, n, kSmallMax, 0, g_host_items, g_longs, &c, nullptr);
     tb::BatchPlan plan;
-    tb::finish_batch(c, g_longs, tb::batch_grid(c, g_dev_grid[device]), g_host_items, &plan);
+    const int full = c.n_long ? g_dev_grid_long[device] : g_dev_grid_short[device];
+    tb::finish_batch(c, g_longs, tb::batch_grid(c, full), g_host_items, &plan);
     // The copy from pageable host memory returns once the bytes are staged,
     // so the host area is free again when this call returns.
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -33,7 +33,8 @@ def harness(tmp_path_factory):
     return lib
 
 
-WAVES = 8  # waves of resident CTAs a batch launch may span (kBatchWaves)
+WAVES = 8        # waves of resident CTAs a launch with long copies may span (kBatchWaves)
+SHORT_WAVES = 4  # the same for a launch of short copies only (kShortWaves)
 
 
 def pack(lib, desc, small_max=16384, full_grid=608, ce_min=0):
@@ -83,7 +84,7 @@ def test_packer_invariants(harness, seed, n, long_frac, small, grid):
     lens = desc[:, 2] if n else np.zeros(0, np.uint64)
     is_long = lens > small
     G = p["grid"]
-    assert 1 <= G <= grid * WAVES
+    assert 1 <= G <= grid * (WAVES if is_long.any() else SHORT_WAVES)
 
     # long copies in descriptor order, prefix = running stream offset
     assert np.array_equal(p["longs"], desc[is_long])
@@ -142,32 +143,41 @@ def test_packer_batch_47540(harness):
     p = pack(harness, desc)
     assert p["grid"] == 608 * WAVES and p["shorts"].shape[0] == 47520 and p["longs"].shape[0] == 20
     assert p["total"] == 288 << 20 and p["chunks"] == 608 * WAVES
+    # its short copies alone: a launch of short copies only, fewer waves
+    short = desc[desc[:, 2] <= 16384]
+    q = pack(harness, short)
+    assert q["grid"] == 608 * SHORT_WAVES and q["chunks"] == 0 and q["claim"] == 2
 
 
 def short_assignment(n_short, grid, chunks, claim, warps=8):
     """Which warp copies which short copy, following the kernel's rule: the
-    warps free at the start take `claim` copies each by index, the rest go
-    out through the counter in claim-sized runs.  Returns the copies of the
-    fixed round and of the counter round, for a coverage check."""
+    warps free at the start take up to `claim` copies each by index (warp
+    w: w, w + starters, ...), the rest go out through the counter.  Returns
+    the copies of the fixed round and of the counter round, for a coverage
+    check."""
     starters = grid * (warps - 1 if chunks else warps)
-    fixed = [i for w in range(starters) for i in range(w * claim, w * claim + claim) if i < n_short]
+    fixed = [i for w in range(starters) for i in range(w, starters * claim, starters)
+             if i < n_short]
     counted = list(range(starters * claim, n_short))
     return fixed, counted
 
 
-@pytest.mark.parametrize("n,long_n,expect_claim", [
-    (3840, 0, 1), (7200, 0, 1), (47520, 20, 1), (100, 0, 1), (77824, 0, 1), (77825, 0, 2),
-    (68096, 20, 1), (68097, 20, 2)])
-def test_claim_items_and_coverage(harness, n, long_n, expect_claim):
-    """One copy per warp while the warps that start on short copies cover the
-    batch in two rounds, else two per warp; the fixed first round and the
-    counter together name every short copy exactly once."""
+@pytest.mark.parametrize("n,long_n,expect_grid,expect_claim", [
+    (3840, 0, 480, 1), (4864, 0, 608, 1), (4865, 0, 608, 2), (7200, 0, 608, 2),
+    (100, 0, 13, 1), (38912, 0, 2432, 2), (47520, 0, 2432, 2), (47520, 20, 4864, 2),
+    (1000, 20, 2560, 1)])
+def test_grid_claim_items_and_coverage(harness, n, long_n, expect_grid, expect_claim):
+    """Short copies only: one warp per copy while a wave's warps suffice,
+    else whole waves (at most four) with the copies past the first round
+    taken by the warps again.  One copy per starting warp while those warps
+    outnumber the short copies, else two; the fixed round and the counter
+    together name every short copy exactly once."""
     lens = np.full(n + long_n, 2112, dtype=np.uint64)
     lens[n:] = 8 << 20
     desc = np.stack([np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(24),
                      np.arange(1, n + long_n + 1, dtype=np.uint64) << np.uint64(25), lens], axis=1)
     p = pack(harness, desc)
-    assert p["claim"] == expect_claim
+    assert p["grid"] == expect_grid and p["claim"] == expect_claim
     fixed, counted = short_assignment(n, p["grid"], p["chunks"], p["claim"])
     assert sorted(fixed + counted) == list(range(n))
 
