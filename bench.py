@@ -490,11 +490,14 @@ def study(args, tb, torch, local):
         ctx.prepare_sources([src], nb, 256 * MiB)
         dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
 
-        def med(c):
-            runs = [c.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB)
+        def med(c, iters=10):
+            runs = [c.run_transfer([src], dst, nb, iters=iters, rotate_bytes=256 * MiB)
                     for _ in range(5)]
             return sorted(runs, key=lambda r: r["gbps"])[2]
         r, re, rs = med(ctx), med(ev_ctx), med(serial_ctx)
+        # One full rotation (64 iterations): the event timer's ~2 us steps
+        # blur a 10-iteration span, not a 64-iteration one.
+        r64, rs64 = med(ctx, 64), med(serial_ctx, 64)
         print(json.dumps({"study": "single transfer 4 MiB, K=64 (median of 5 runs of 10)",
                           "gbps_graph": round(r["gbps"], 1),
                           "us_per_iteration_graph": round(r["mean_ms"] * 1e3, 2),
@@ -502,6 +505,10 @@ def study(args, tb, torch, local):
                           "us_per_iteration_graph_no_pdl": round(rs["mean_ms"] * 1e3, 2),
                           "gbps_events": round(re["gbps"], 1),
                           "us_per_iteration_events": round(re["mean_ms"] * 1e3, 2),
+                          "gbps_graph_64": round(r64["gbps"], 1),
+                          "us_per_iteration_graph_64": round(r64["mean_ms"] * 1e3, 3),
+                          "gbps_graph_no_pdl_64": round(rs64["gbps"], 1),
+                          "us_per_iteration_graph_no_pdl_64": round(rs64["mean_ms"] * 1e3, 3),
                           "K": r["K"], "alloc_bytes": r["alloc_bytes"]}), flush=True)
         del src
         pct = (40, 20, 0, 20, 20)

@@ -333,6 +333,8 @@ int run_graphed(tb_ctx *ctx, tb::ReducePlan &plan, int iters,
     cudaError_t err = cudaSuccess;
     for (int64_t it = -(int64_t)ctx->opt.warmup; it < iters && err == cudaSuccess; ++it) {
         set_iteration(it);
+        // Every launch but the first follows one of this transfer.
+        plan.early = it > -(int64_t)ctx->opt.warmup;
         if (it == 0)
             err = cudaEventRecordWithFlags(ctx->events[0], st, cudaEventRecordExternal);
         if (err == cudaSuccess)
@@ -1112,6 +1114,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     };
     for (int64_t it = graphed ? iters : -(int64_t)o.warmup; it < iters; ++it) {
         at_iteration(it);
+        plan.early = it > -(int64_t)o.warmup;
         cudaError_t e = cudaSuccess;
         if (it == 0 || (per_iter_validate && it > 0))
             if ((e = cudaEventRecord(ctx->events[it], st)) != cudaSuccess)

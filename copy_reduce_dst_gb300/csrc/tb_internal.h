@@ -39,6 +39,11 @@ struct ReducePlan {
     int pdl;               // 1 = launch with programmatic dependent launch
     int stages;            // bulk form: shared-memory pipeline stages
     uint64_t wait_ns = 2000000000ull;  // bulk form: limit of each wait for a tile's loads
+    // 1 = the launch may start reading its sources before the launch ahead
+    // of it on the stream has finished: only for a launch that follows
+    // another of the same transfer, which reads the same (unmodified)
+    // sources and writes only dst.
+    int early = 0;
 };
 
 // Picks engine, vector width, head/tail, sub-executor split, grid and unroll

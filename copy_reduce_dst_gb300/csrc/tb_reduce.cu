@@ -34,7 +34,31 @@ struct ReduceArgs {
     uint32_t *status;      // nullable: set to 1 if a bounded wait expired
     uint32_t stages;       // bulk form: pipeline stages (2 .. kRMaxStages)
     uint64_t wait_ns;      // bulk form: limit of each wait for a tile's loads
+    uint32_t early;        // 1: read sources before the launch ahead has finished
 };
+
+// Tiles of its own that a CTA of the vector form prefetches into L2 before
+// waiting for the launch ahead.
+constexpr uint32_t kEarlyTiles = 1;
+
+// Prefetches a CTA's first kEarlyTiles tiles of every source into L2 (bulk
+// prefetches; thread j * N + k takes tile j of source k).  Used before
+// waiting for the launch ahead, whose writes never touch the sources.
+template <int N, int VB>
+__device__ __forceinline__ void prefetch_tiles(const ReduceArgs &a, uint64_t t0, uint64_t tile,
+                                               uint64_t step, uint64_t vend)
+{
+    const uint32_t k = threadIdx.x % N, j = threadIdx.x / N;
+    if (j >= kEarlyTiles)
+        return;
+    const uint64_t t = t0 + j * step;
+    if (t >= vend)
+        return;
+    const uint64_t nv = min(tile, vend - t);
+    const uint64_t p = reinterpret_cast<uint64_t>(a.src[k]) + (a.head + t * (VB / 4)) * 4;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(nv * VB))
+                 : "memory");
+}
 
 // The CTAs of a launch are dealt to the sub-executors as evenly as integers
 // allow (sub-executor s gets CTAs [s*G/S, (s+1)*G/S)), and each sub-executor
@@ -118,6 +142,13 @@ __global__ void __launch_bounds__(MAXT) k_reduce(const ReduceArgs a)
     const uint32_t bd = blockDim.x;
     const SubRange sr = sub_range(a.nvec, a.nsub);
     pdl_launch_dependents();
+    if constexpr (N > 0 && VB >= 16) {
+        // Early launch: this CTA's first tiles of every source go to L2
+        // while the launch ahead finishes.
+        if (a.early)
+            prefetch_tiles<N, VB>(a, sr.vbeg + (uint64_t)sr.part * bd * U, (uint64_t)bd * U,
+                                  (uint64_t)sr.nparts * bd * U, sr.vend);
+    }
     pdl_wait_prerequisite();
 
     const char *s[N > 0 ? N : 1];
@@ -253,7 +284,10 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
     const uint32_t stages = smem_u32(smem + 128);
     const uint64_t sbase = (uint64_t)(a.head) * 4;
     pdl_launch_dependents();
-    pdl_wait_prerequisite();
+    // An early launch issues its first tiles' loads before waiting for the
+    // launch ahead (they read only sources); its first store comes after.
+    if (!a.early)
+        pdl_wait_prerequisite();
 
     // Tile j of this CTA: first body vector and vector count.
     auto tile = [&](uint64_t j, uint64_t &v0, uint32_t &nv) {
@@ -282,6 +316,8 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
             for (; issued < mine && issued < (uint64_t)nst; ++issued)
                 issue(issued, (uint32_t)issued);
         }
+        if (a.early)
+            pdl_wait_prerequisite();
         __syncthreads();
         uint32_t s = 0, parity = 0, prev = nst - 1;
         for (uint64_t j = 0; j < mine; ++j) {
@@ -352,6 +388,8 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
             bulk_wait_all();
     }
 
+    if (a.early)
+        pdl_wait_prerequisite();  // (returns at once if this thread waited already)
     if (blockIdx.x == 0 && tid < a.head)
         reduce_one<N>(a, tid);
     const uint64_t tail0 = a.head + a.nvec * 4;
@@ -688,6 +726,7 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     a.status = p.status;
     a.stages = (uint32_t)(p.stages > 0 ? p.stages : (int)kRStages);
     a.wait_ns = p.wait_ns;
+    a.early = p.early ? 1u : 0u;
     if (p.n == 0)
         return cudaSuccess;
     cudaLaunchAttribute attr[1];
