@@ -78,6 +78,42 @@ def test_thirty_two_byte_classes(tb, ctx, ss, ds):
     run_layout(tb, ctx, layout, 9, src_shift=ss, dst_shift=ds)
 
 
+@pytest.mark.parametrize("shift", [0, 1, 8, 15])
+def test_ring_piece_boundaries(tb, ctx, shift):
+    # Short copies whose src and dst agree modulo 16 go through each warp's
+    # ring of shared-memory slots in pieces of 1-2 KiB: lengths at and
+    # around every multiple of 1 KiB up to the 16 KiB short limit, with
+    # heads and tails of 0-15 bytes (the shift moves src and dst alike).
+    base = [1024 * k + d for k in range(17) for d in (-17, -16, -1, 0, 1, 15, 16, 17)]
+    lens = np.array([x for x in base if 0 < x <= 16384] * 4, dtype=np.uint64)
+    gen = workloads.rng(40 + shift)
+    so = workloads.scatter_offsets(gen, lens, 0, 64 * MiB, 16)
+    do = workloads.scatter_offsets(gen, lens, 0, 64 * MiB, 16)
+    layout = workloads.BatchLayout("piece boundaries", so, do, lens, 64 * MiB, 64 * MiB)
+    st = run_layout(tb, ctx, layout, 41 + shift, src_shift=shift, dst_shift=shift)
+    assert st["warp_items"] == lens.size
+
+
+@pytest.mark.parametrize("waves", [1, 2, 4, 5])
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_short_counts_around_whole_waves(tb, ctx, waves, delta):
+    # A launch of short copies only takes one copy per warp while a wave of
+    # warps suffices, else whole waves whose warps take a second copy by
+    # index (warp w: w, w + starters) before claiming from the counter.
+    # Counts at and next to multiples of one copy per warp of a wave (three
+    # 256-thread CTAs per SM on GB300) cross each of those rules.
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = sms * 3 * 8 * waves + delta
+    lens = np.full(n, 2112, dtype=np.uint64)
+    gen = workloads.rng(50 + waves)
+    so = workloads.scatter_offsets(gen, lens, 0, 256 * MiB, 64)
+    do = workloads.scatter_offsets(gen, lens, 0, 256 * MiB, 64)
+    layout = workloads.BatchLayout("around waves", so, do, lens, 256 * MiB, 256 * MiB)
+    st = run_layout(tb, ctx, layout, 60 + waves * 3 + delta)
+    assert st["descs"] == n and st["launches"] == 1
+
+
 def test_lengths_one_byte_to_three_mib(tb, ctx):
     # Mooncake RFC "Correctness": lengths from 1 B to 3 MiB, unaligned ranges
     g = np.random.default_rng(11)

@@ -136,6 +136,21 @@ def test_fill_pattern_repeats_the_vector():
     pat = np.array([1.5, -2.0, 3.25], np.float32)
     got = oracle.fill_pattern(100, pat)
     assert np.array_equal(got, np.resize(pat, 100))
+    # written out by hand: the vector, again, then its start
+    assert got[:7].tolist() == [1.5, -2.0, 3.25, 1.5, -2.0, 3.25, 1.5]
+
+
+def test_fill_pattern_edges():
+    # one value: a constant buffer; a vector longer than the buffer: its
+    # first n values; n = 0: nothing; values kept bit for bit (-0, subnormal)
+    assert oracle.fill_pattern(5, [7.0]).tolist() == [7.0] * 5
+    assert oracle.fill_pattern(2, [4.0, 5.0, 6.0]).tolist() == [4.0, 5.0]
+    assert oracle.fill_pattern(0, [1.0]).size == 0
+    odd = np.array([-0.0, np.float32(1e-45), np.inf], np.float32)
+    got = oracle.fill_pattern(6, odd)
+    assert np.array_equal(got.view(np.uint32), np.tile(odd.view(np.uint32), 2))
+    with pytest.raises(ValueError):
+        oracle.fill_pattern(4, [])
 
 
 def test_splitmix64_known_answers(golden):
