@@ -495,9 +495,9 @@ __device__ __forceinline__ void short_item(ShortPipe<U, S> &p, const WorkItem &w
 
 // The short copies of one warp: up to claim_items items by its index
 // among the warps that start on short copies (first, first + stride, ...;
-// no atomic), then items claimed one at a time from the counter.  Lane 0 keeps one claim in
-// flight and the descriptor of the next item is loaded before the current
-// item is copied, so neither latency stalls the pipe.
+// no atomic), then items claimed one at a time from the counter.  Lane 0
+// keeps one claim in flight and the descriptor of the next item is loaded
+// before the current item is copied, so neither latency stalls the pipe.
 template <int U, int S>
 __device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first, uint32_t stride,
                                              uint32_t dyn_base, bool dynamic, uint32_t lane,
