@@ -445,10 +445,13 @@ typedef struct {
    streams, such as a GEMM loop.  The bytes of all descriptors longer than
    small_max_bytes form one stream cut into equal chunks, the same number
    for every CTA, moved with bulk copies through shared memory; descriptors
-   of at most small_max_bytes go to a warp or half a warp each, the first
-   round fixed by warp index and the rest claimed by free warps from a
-   counter in the packed work list.  Destinations must not overlap one another or any source of
-   the batch (the order of copies is unspecified).  TB_EINVAL for a null
+   of at most small_max_bytes go to a warp each, streamed through that
+   warp's ring of shared-memory slots by asynchronous 16-byte copies, the
+   first ones fixed by warp index and the rest claimed one at a time by free
+   warps from a counter in the packed work list.  Addresses may also be
+   pinned host memory mapped into the device's address space.  Destinations
+   must not overlap one another or any source of the batch (the order of
+   copies is unspecified).  TB_EINVAL for a null
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
    slot came free within wait_timeout_ns, or when the previous batch that
    used the chosen slot stopped early because a bounded wait inside the

@@ -114,6 +114,37 @@ def test_short_counts_around_whole_waves(tb, ctx, waves, delta):
     assert st["descs"] == n and st["launches"] == 1
 
 
+@pytest.mark.parametrize("host_side", ["src", "dst"])
+def test_pinned_host_pool(tb, ctx, host_side):
+    # One pool in page-locked host memory (mapped into the device's address
+    # space): the short copies' asynchronous copies and the long copies'
+    # bulk copies cross the host link, byte-exact.
+    import torch
+    g = np.random.default_rng(31)
+    lens = np.concatenate([g.integers(1, 16385, 400), g.integers(16385, 1 << 20, 6)]).astype(np.uint64)
+    gen = workloads.rng(32)
+    pool = 32 * MiB
+    so = workloads.scatter_offsets(gen, lens, 0, pool, 1)
+    do = workloads.scatter_offsets(gen, lens, 0, pool, 1)
+    src_h = workloads.random_bytes(pool, 33)
+    dst_h = workloads.random_bytes(pool, 34)
+    if host_side == "src":
+        src = torch.from_numpy(src_h.copy()).pin_memory()
+        dst = to_dev(dst_h)
+    else:
+        src = to_dev(src_h)
+        dst = torch.from_numpy(dst_h.copy()).pin_memory()
+    desc = np.stack([np.uint64(src.data_ptr()) + so, np.uint64(dst.data_ptr()) + do, lens], axis=1)
+    ctx.batch_copy(desc)
+    torch.cuda.synchronize()
+    got = dst.numpy() if host_side == "dst" else to_host(dst)
+    exp = dst_h.copy()
+    oracle.apply_batch(exp, src_h, so, do, lens)
+    assert oracle.first_mismatch(got, exp) == -1
+    st = ctx.last_batch_stats()
+    assert st["warp_items"] == 400 and st["cta_items"] > 0
+
+
 def test_lengths_one_byte_to_three_mib(tb, ctx):
     # Mooncake RFC "Correctness": lengths from 1 B to 3 MiB, unaligned ranges
     g = np.random.default_rng(11)
