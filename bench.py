@@ -425,11 +425,41 @@ def oracle_sample(budget_s: float, n: int = 4 * MiB):
     return 4 * 4 * n * reps / el / 1e9, reps, el
 
 
+def host_cpu() -> dict:
+    """The host the oracle ran on: CPU model (or Arm implementer / part
+    numbers where the kernel reports no model name), architecture, logical
+    CPUs and the current / maximum clock of CPU 0 where sysfs reports them."""
+    import platform
+    info = {"arch": platform.machine(), "logical_cpus": os.cpu_count()}
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k and v and k not in fields:
+                    fields[k] = v
+    except OSError:
+        pass
+    if "model name" in fields:
+        info["model"] = fields["model name"]
+    elif "CPU part" in fields:
+        info["model"] = f"Arm implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    for key, name in (("mhz", "scaling_cur_freq"), ("max_mhz", "cpuinfo_max_freq")):
+        try:
+            with open(f"/sys/devices/system/cpu/cpu0/cpufreq/{name}") as f:
+                info[key] = round(int(f.read().strip()) / 1000)
+        except (OSError, ValueError):
+            pass
+    return info
+
+
 def cpu_baseline(budget_s: float):
     gbps, reps, el = oracle_sample(budget_s)
     return {"value": round(gbps, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"dstReference[3] over 3 x 4,194,304 float32 default-pattern sources "
-                      f"(64 MiB moved per call), {reps} calls in {el:.1f} s, single thread"}
+                      f"(64 MiB moved per call), {reps} calls in {el:.1f} s, single thread",
+            "host": host_cpu()}
 
 
 def reference_arm(args):
@@ -458,7 +488,7 @@ def reference_arm(args):
                    "parallelism": "none (CPU, 1 thread)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"dstReference[3] over 3 x 4,194,304 float32 per step, "
-                                   f"{args.steps} steps"},
+                                   f"{args.steps} steps", "host": host_cpu()},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -35,6 +35,7 @@ def test_reference_arm_prints_the_contract_line():
     assert "workload" in d["config"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["host"]["logical_cpus"] >= 1 and cb["host"]["arch"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
 
