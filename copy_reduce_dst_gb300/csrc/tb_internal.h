@@ -161,8 +161,8 @@ void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *b
 bool find_overlap(const tb_copy_desc *desc, size_t n, size_t *first, size_t *second);
 // Short copies each warp that starts on short copies takes by its index
 // (no atomic; warp w of `starters` takes copies w, w + starters, ...)
-// before it claims more one at a time from the counter: 1 when those warps
-// outnumber the short copies, else 2.
+// before it claims more, a few at a time, from the counter: 1 when those
+// warps outnumber the short copies, else 2.
 uint32_t batch_claim_items(const BatchPlan &plan);
 // Work lists up to this size may be read by the kernel in place.
 constexpr size_t kDirectMaxBytes = 256 * 1024;

@@ -447,7 +447,7 @@ typedef struct {
    for every CTA, moved with bulk copies through shared memory; descriptors
    of at most small_max_bytes go to a warp each, streamed through that
    warp's ring of shared-memory slots by asynchronous 16-byte copies, the
-   first ones fixed by warp index and the rest claimed one at a time by free
+   first ones fixed by warp index and the rest claimed four at a time by free
    warps from a counter in the packed work list.  Addresses may also be
    pinned host memory mapped into the device's address space.  Destinations
    must not overlap one another or any source of the batch (the order of
