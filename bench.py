@@ -441,10 +441,15 @@ def host_cpu() -> dict:
                     fields[k] = v
     except OSError:
         pass
+    # Arm Ltd. (implementer 0x41) core part numbers
+    arm_parts = {"0xd0c": "Neoverse N1", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2",
+                 "0xd4f": "Neoverse V2"}
     if "model name" in fields:
         info["model"] = fields["model name"]
     elif "CPU part" in fields:
-        info["model"] = f"Arm implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+        impl, part = fields.get("CPU implementer", "?"), fields["CPU part"]
+        named = arm_parts.get(part) if impl == "0x41" else None
+        info["model"] = named or f"Arm implementer {impl} part {part}"
     for key, name in (("mhz", "scaling_cur_freq"), ("max_mhz", "cpuinfo_max_freq")):
         try:
             with open(f"/sys/devices/system/cpu/cpu0/cpufreq/{name}") as f:
