@@ -154,7 +154,9 @@ typedef struct {
        stream drains, and every CTA waits for that kernel to complete and its
        writes to be visible before it touches memory, so the results are
        those of serialised launches with less idle time between them.
-       Default 1. */
+       Inside tb_run_transfer, where the launch before is one of the same
+       transfer (same sources, writing only dst), a launch starts reading
+       its sources before that wait; only its writes wait.  Default 1. */
     int32_t use_pdl;
     /* Limit, in nanoseconds, of each wait inside the kernels' shared-memory
        pipelines (bulk reduce-copy, batched copy) for a load to land.  A wait
@@ -398,8 +400,10 @@ typedef struct {
    CUDA graph timed by events around the timed iterations (use_graph), or as
    stream launches, behind the gate (use_gate) or not, with CUDA events
    between every two iterations.  Sources must already hold their slices
-   (tb_fill_source or tb_upload_sources, then tb_prepare_sources).  On a
-   validation failure returns TB_EVALIDATE with the mismatch in *out. */
+   (tb_fill_source or tb_upload_sources, then tb_prepare_sources), and
+   nothing else may write them during the call: every launch after the
+   first starts reading its sources while the launch before it finishes.
+   On a validation failure returns TB_EVALIDATE with the mismatch in *out. */
 int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out);
 
 /* tb_run_transfer_ex without expected bytes. */
