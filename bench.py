@@ -28,8 +28,8 @@ warm, graphed), validation on the device against the host, end to end from
 pinned and pageable host memory, tiny batches against per-copy memcpy,
 small copies under a GEMM loop (normal and high-priority stream), the three
 batch workloads, the batch's long and short parts, copy-engine routing, and
-GEMM interference.  ``--profile reduce|batch|batch-short|rotation`` runs
-one workload for an ncu capture (commands in ``profiles/``).
+GEMM interference.  ``--profile reduce|batch|batch-short|batch-small|
+rotation`` runs one workload for an ncu capture (commands in ``profiles/``).
 """
 from __future__ import annotations
 
@@ -969,6 +969,26 @@ def profile_target(kind, args, tb, torch, local):
             r = ctx.run_transfer([src], dst, nb, iters=4, rotate_bytes=rot)
             torch.cuda.nvtx.range_pop()
             print(json.dumps({"K": r["K"], "iter_ms": r["iter_ms"]}), flush=True)
+    elif kind == "batch-small":
+        # The 3840-page and 7200-page batches, 5 calls each; kernel times
+        # from the library's events.
+        from copy_reduce_dst_gb300 import workloads
+        with tb.Context(local, ctx_options(tb, time_kernels=1)) as ctx:
+            for name, lay in (("3840 index pages", workloads.batch_index_pages()),
+                              ("7200 block pages", workloads.batch_block_pages())):
+                src = torch.zeros(lay.src_pool_bytes, dtype=torch.uint8, device="cuda")
+                dst = torch.zeros(lay.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+                desc = lay.descriptors(src.data_ptr(), dst.data_ptr())
+                ms = []
+                for _ in range(5):
+                    ctx.batch_copy(desc)
+                    ms.append(round(ctx.last_batch_kernel_ms() * 1e3, 2))
+                print(json.dumps({"batch": name, "event_us": ms,
+                                  "direct": ctx.last_batch_stats()["direct_launches"]}),
+                      flush=True)
+                del src, dst
+        print("profile target batch-small: 10 launches done", flush=True)
+        return 0
     else:
         from copy_reduce_dst_gb300 import workloads
         layout = workloads.batch_head_sliced()
@@ -995,7 +1015,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--study", action="store_true")
-    ap.add_argument("--profile", choices=["reduce", "batch", "batch-short", "rotation"])
+    ap.add_argument("--profile", choices=["reduce", "batch", "batch-short", "batch-small",
+                                          "rotation"])
     ap.add_argument("--mib", type=int, default=16, help="--profile rotation: transfer MiB")
     ap.add_argument("--rotate-mib", type=int, default=256,
                     help="--profile rotation: SRC_ROTATE_BYTES in MiB (0 = off)")
