@@ -139,6 +139,8 @@ __device__ __forceinline__ uint32_t first_diff_byte(uint4 x, uint4 y)
     return 16;
 }
 
+constexpr uint32_t kCompareUnroll = 4;
+
 __global__ void k_compare(const uint8_t *a, const uint8_t *b, uint64_t n,
                           unsigned long long *first)
 {
@@ -158,15 +160,27 @@ __global__ void k_compare(const uint8_t *a, const uint8_t *b, uint64_t n,
     const uint4 *va = reinterpret_cast<const uint4 *>(a + head);
     const uint4 *vb = reinterpret_cast<const uint4 *>(b + head);
     const uint64_t nv = (n - head) / 16;
-    for (uint64_t v = tid, it = 0; v < nv; v += stride, ++it) {
-        // Every 64 steps: stop once a difference before this position is known.
-        if ((it & 63u) == 0 &&
+    // kCompareUnroll vector pairs per thread and step, all loads issued
+    // before the first compare.
+    for (uint64_t v = tid, it = 0; v < nv; v += kCompareUnroll * stride, ++it) {
+        // Every 64 vectors: stop once a difference before this position is known.
+        if ((it & (64u / kCompareUnroll - 1u)) == 0 &&
             *reinterpret_cast<volatile unsigned long long *>(first) < head + v * 16)
             break;
-        const uint4 x = __ldcs(va + v), y = __ldcs(vb + v);
-        const uint32_t d = first_diff_byte(x, y);
-        if (d < 16)
-            atomicMin(first, (unsigned long long)(head + v * 16 + d));
+        uint4 x[kCompareUnroll], y[kCompareUnroll];
+#pragma unroll
+        for (int u = 0; u < kCompareUnroll; ++u)
+            if (v + u * stride < nv) {
+                x[u] = __ldcs(va + v + u * stride);
+                y[u] = __ldcs(vb + v + u * stride);
+            }
+#pragma unroll
+        for (int u = 0; u < kCompareUnroll; ++u)
+            if (v + u * stride < nv) {
+                const uint32_t d = first_diff_byte(x[u], y[u]);
+                if (d < 16)
+                    atomicMin(first, (unsigned long long)(head + (v + u * stride) * 16 + d));
+            }
     }
     const uint64_t t0 = head + nv * 16;
     for (uint64_t i = t0 + tid; i < n; i += stride)
