@@ -909,20 +909,32 @@ def study_batch_configs(tb, torch, local):
 
 def study_batch_phases(tb, torch, local):
     """Kernel time of the 47,540 batch and of its parts: the 20 long copies
-    alone, the 47,520 short copies alone, and one 1 GiB copy (median of 10
-    launches after 3, kernel-only events)."""
+    alone, the 47,520 short copies alone, the same short copies laid out
+    back to back in both pools, their bytes as one contiguous copy, and one
+    1 GiB copy (median of 10 launches after 3, kernel-only events)."""
     import statistics as st
+    import numpy as np
     from copy_reduce_dst_gb300 import workloads
     layout = workloads.batch_head_sliced()
     src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
     dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
     desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
     long_ = desc[:, 2] > 16384
+    short = desc[~long_]
+    lens = short[:, 2]
+    packed = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.uint64)
+    back_to_back = np.stack([np.uint64(src.data_ptr()) + packed,
+                             np.uint64(dst.data_ptr()) + packed, lens], axis=1)
+    same_bytes = desc[:1].copy()
+    same_bytes[0] = (src.data_ptr(), dst.data_ptr(), int(lens.sum()))
     one = desc[:1].copy()
     one[0] = (src.data_ptr(), dst.data_ptr(), GiB)
     with tb.Context(local, ctx_options(tb, time_kernels=1)) as ctx:
         for name, d in (("all 47,540", desc), ("20 long copies", desc[long_]),
-                        ("47,520 short copies", desc[~long_]), ("one 1 GiB copy", one)):
+                        ("47,520 short copies", short),
+                        ("47,520 short copies laid out back to back", back_to_back),
+                        ("their bytes as one contiguous copy", same_bytes),
+                        ("one 1 GiB copy", one)):
             for _ in range(3):
                 ctx.batch_copy(d)
             ms = []
