@@ -908,10 +908,11 @@ def study_batch_configs(tb, torch, local):
 
 
 def study_batch_phases(tb, torch, local):
-    """Kernel time of the 47,540 batch and of its parts: the 20 long copies
-    alone, the 47,520 short copies alone, the same short copies laid out
-    back to back in both pools, their bytes as one contiguous copy, and one
-    1 GiB copy (median of 10 launches after 3, kernel-only events)."""
+    """Kernel time of the 47,540 batch, of its bytes as one contiguous copy,
+    and of its parts: the 20 long copies alone, the 47,520 short copies
+    alone, the same short copies laid out back to back in both pools, their
+    bytes as one contiguous copy, and one 1 GiB copy (median of 10 launches
+    after 3, kernel-only events)."""
     import statistics as st
     import numpy as np
     from copy_reduce_dst_gb300 import workloads
@@ -927,10 +928,13 @@ def study_batch_phases(tb, torch, local):
                              np.uint64(dst.data_ptr()) + packed, lens], axis=1)
     same_bytes = desc[:1].copy()
     same_bytes[0] = (src.data_ptr(), dst.data_ptr(), int(lens.sum()))
+    all_bytes = desc[:1].copy()
+    all_bytes[0] = (src.data_ptr(), dst.data_ptr(), int(desc[:, 2].sum()))
     one = desc[:1].copy()
     one[0] = (src.data_ptr(), dst.data_ptr(), GiB)
     with tb.Context(local, ctx_options(tb, time_kernels=1)) as ctx:
-        for name, d in (("all 47,540", desc), ("20 long copies", desc[long_]),
+        for name, d in (("all 47,540", desc), ("all their bytes as one contiguous copy", all_bytes),
+                        ("20 long copies", desc[long_]),
                         ("47,520 short copies", short),
                         ("47,520 short copies laid out back to back", back_to_back),
                         ("their bytes as one contiguous copy", same_bytes),
