@@ -13,9 +13,10 @@ header, no table.  Each wrapper names the passage it restates:
 * Mooncake RFC #5041, "Design of #5040": a (src, dst, len) descriptor array
   applied as plain memcpys.
 
-Parity status: ``fill_compress`` is parity unpinned against the pages (they
-name its zeroing modes without defining them); everything else is pinned by
-the ``-m "not gpu"`` tests.
+Parity status: every function is pinned by the ``-m "not gpu"`` tests.  The
+pages name ``fill_compress``'s zeroing modes without defining them, so it
+follows a stated reading, pinned by hand-worked words in
+``tests/golden/fill_compress.txt``.
 """
 import ctypes as _ct
 
@@ -88,7 +89,8 @@ def splitmix64_stream(seed: int, count: int) -> _np.ndarray:
 
 
 def fill_compress(n: int, pct, seed: int, buffer_idx: int = 0) -> _np.ndarray:
-    """fillCompress: random floats with per-64-byte-line zeroing (parity unpinned)."""
+    """fillCompress: random floats with per-64-byte-line zeroing (the stated reading,
+    pinned by tests/golden/fill_compress.txt)."""
     p = _np.ascontiguousarray(pct, dtype=_np.uint32)
     if p.size != 5:
         raise ValueError("fillCompress takes five percentages")

@@ -23,9 +23,12 @@
  * no reassociation, subnormals kept), so each float add below is one IEEE-754
  * binary32 round-to-nearest-even addition.
  *
- * Parity status: fillCompress (orc_fill_compress) is "parity unpinned" against
- * the pages - they name the 1B0/2B0/4B0/32B0 modes without defining them; its
- * tests pin only the structural reading and the SplitMix64 generator.
+ * Parity status: the pages name fillCompress's 1B0/2B0/4B0/32B0 modes without
+ * defining them, so orc_fill_compress follows a stated reading (below).  That
+ * reading is pinned by hand-worked words (tests/golden/fill_compress.txt,
+ * derived with integer arithmetic from the published SplitMix64 vector), which
+ * fix its draw order, float mapping, each zero mask, the mode boundary, the
+ * partial last line and the per-buffer seed.
  */
 #include <stdint.h>
 #include <stddef.h>

@@ -225,6 +225,111 @@ def test_fill_compress_zero_masks_by_mode():
         assert np.mean(rows[:, ~zero] != 0) > 0.9
 
 
+def _golden_compress_cases(golden):
+    rows = golden("fill_compress.txt")
+    cases = {}
+    for r in rows:
+        if r[0] == "case":
+            name, seed, k, n = r[1], int(r[2]), int(r[3]), int(r[4])
+            pct = tuple(int(x) for x in r[5:10])
+            modes = [int(x) for x in r[10:]]
+            cases[name] = dict(seed=seed, k=k, n=n, pct=pct, modes=modes, words={})
+        elif r[0] == "word":
+            cases[r[1]]["words"][int(r[2])] = int(r[3], 16)
+    return rows, cases
+
+
+def test_fill_compress_golden_draws_are_the_published_vector(golden):
+    # The golden file's stream for seed 1234567 starts with the published
+    # SplitMix64 known-answer vector, so its words rest on that vector and
+    # not on the oracle's generator.
+    rows, _ = _golden_compress_cases(golden)
+    draws = {int(r[2]): int(r[3]) for r in rows if r[0] == "draw"}
+    kat = [r for r in golden("splitmix64.txt") if r[0] != "counts"]
+    for seed, idx, val in kat:
+        assert seed == "1234567" and draws[int(idx)] == int(val)
+    for i, v in draws.items():
+        row = next(r for r in rows if r[0] == "draw" and int(r[2]) == i)
+        assert int(row[4]) == v % 100 and int(row[5]) == v >> 40
+
+
+def test_fill_compress_hand_worked_golden(golden):
+    # "Expected source pattern", fillCompress row, under the reading stated in
+    # the oracle: every word of tests/golden/fill_compress.txt (mode draw,
+    # float mapping, each zero mask, a partial last line, seed + k).
+    _, cases = _golden_compress_cases(golden)
+    assert len(cases) == 8
+    seen_modes = set()
+    for name, c in cases.items():
+        got = oracle.fill_compress(c["n"], c["pct"], c["seed"], c["k"]).view(np.uint32)
+        want = np.array([c["words"][i] for i in range(c["n"])], dtype=np.uint32)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, f"{name}: word {bad[0]} {got[bad[0]]:08X} != {want[bad[0]]:08X}"
+        seen_modes.update(c["modes"][: (c["n"] + 15) // 16])
+    assert seen_modes == {0, 1, 2, 3, 4}
+
+
+# Slips a restatement of fillCompress could plausibly make, planted one at a
+# time into a copy of oracle.c: (what it gets wrong, text replaced, replacement).
+_MODE_BLOCK = ("        uint64_t r = orc_splitmix64_next(&state) % 100u;\n"
+               "        int mode = 0;\n"
+               "        while (mode < 4 && r >= cum[mode])\n"
+               "            ++mode;\n")
+_FLOAT_LOOP_END = ("            vals[j] = (float)(int32_t)(d >> 40) * 0x1p-23f - 1.0f;\n"
+                   "        }\n")
+_SLIPS = [
+    ("mode drawn after the floats", _MODE_BLOCK + "\n        float vals[16];\n",
+     "        float vals[16];\n"),
+    ("shift by 41", "(d >> 40)", "(d >> 41)"),
+    ("low 24 bits", "(d >> 40)", "(d & 0xFFFFFFu)"),
+    ("no -1 offset", "* 0x1p-23f - 1.0f", "* 0x1p-23f"),
+    ("seed xor k", "seed + (uint64_t)bufferIdx", "seed ^ (uint64_t)bufferIdx"),
+    ("k ignored", "seed + (uint64_t)bufferIdx", "seed"),
+    ("mode boundary <=", "r >= cum[mode]", "r > cum[mode]"),
+    ("even chunks zeroed", "(b / chunk) % 2u == 1u", "(b / chunk) % 2u == 0u"),
+    ("big-endian bytes", "bytes[b] = 0;", "bytes[63u - b] = 0;"),
+    ("32B0 as 16-byte chunks", "{ 0u, 1u, 2u, 4u, 32u }", "{ 0u, 1u, 2u, 4u, 16u }"),
+    ("2B0 as 4B0", "{ 0u, 1u, 2u, 4u, 32u }", "{ 0u, 1u, 4u, 4u, 32u }"),
+    ("partial line dropped", "uint64_t nLines = (n + 15u) / 16u;", "uint64_t nLines = n / 16u;"),
+]
+
+
+def test_fill_compress_golden_catches_planted_slips(golden, tmp_path):
+    # Mutation check of the pin above: each slip, compiled into its own copy
+    # of the oracle on the CPU, must change at least one golden word.
+    import ctypes
+    import subprocess
+    from oracle import _build
+    src = open(_build.SRC).read()
+    _, cases = _golden_compress_cases(golden)
+    for i, (what, old, new) in enumerate(_SLIPS):
+        if what == "mode drawn after the floats":
+            assert old in src and _FLOAT_LOOP_END in src, what
+            mutated = src.replace(old, new).replace(_FLOAT_LOOP_END, _FLOAT_LOOP_END + _MODE_BLOCK)
+        else:
+            assert old in src, what
+            mutated = src.replace(old, new)
+        c_file = tmp_path / f"slip{i}.c"
+        so_file = tmp_path / f"slip{i}.so"
+        c_file.write_text(mutated)
+        flags = [f for f in _build.CFLAGS if f != "-Werror"]
+        subprocess.run(["gcc", *flags, str(c_file), "-o", str(so_file)], check=True)
+        lib = ctypes.CDLL(str(so_file))
+        lib.orc_fill_compress.restype = ctypes.c_int
+        lib.orc_fill_compress.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                                          ctypes.c_uint64, ctypes.c_int64]
+        caught = False
+        for c in cases.values():
+            out = np.full(c["n"], 0xA5A5A5A5, dtype=np.uint32)
+            pct = np.array(c["pct"], dtype=np.uint32)
+            lib.orc_fill_compress(out.ctypes.data, c["n"], pct.ctypes.data, c["seed"], c["k"])
+            want = np.array([c["words"][j] for j in range(c["n"])], dtype=np.uint32)
+            if not np.array_equal(out, want):
+                caught = True
+                break
+        assert caught, f"the golden words do not catch: {what}"
+
+
 def test_fill_compress_rejects_bad_percentages():
     with pytest.raises(ValueError):
         oracle.fill_compress(16, (50, 20, 0, 20, 20), 1)
