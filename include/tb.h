@@ -483,8 +483,8 @@ int tb_last_batch_stats(const tb_ctx *ctx, tb_batch_stats *out);
    TB_ENOTSUP unless the context was created with time_kernels = 1. */
 int tb_last_batch_kernel_ms(tb_ctx *ctx, double *ms);
 
-/* The per-copy baseline the Mooncake RFC measures against ("Every request is
-   one hipMemcpyAsync"): one cudaMemcpyAsync (device to device) per
+/* The per-copy baseline of the HipTransport RFC (section "Motivation": each
+   request there costs one memcpy call): one cudaMemcpyAsync (device to device) per
    descriptor with len > 0, in array order, on `stream`.  Same arguments and
    checks as tb_batch_copy; provided so the two can be timed side by side. */
 int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stream);
@@ -500,17 +500,33 @@ int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stre
    Same copy semantics and scheduling as tb_batch_copy with default options
    (copies up to 16 KiB go to one warp each), on the current CUDA device,
    asynchronously on `stream`; no context is needed.
-   The packed work items live in a fixed __device__ array of about 1.6 MiB
-   that every GPU loading this library holds until the process exits.  The first call on a
-   device looks up that array's device address (with that device current);
-   make that first call before any stream capture.  Every call on a device
-   shares the one array and leaves the last batch's items in it: calls whose
-   work overlaps on the GPU (different streams, no ordering between them)
-   race; calls on one stream run in order.  Host-side packing is serialized
-   by a lock.  Returns TB_EINVAL for a null or wrapping range, TB_ENOTSUP
-   when the batch has more than TB_NOALLOC_MAX_ITEMS descriptors with
-   len > 0 (nothing is copied then), TB_ECUDA when a CUDA call fails.  It calls no cudaMalloc,
-   cudaFree or other allocating routine. */
+   Memory: the packed work items live in a fixed __device__ array of
+   2,162,736 bytes (about 2.06 MiB: room for the work items, stream prefix
+   and chunk table of TB_NOALLOC_MAX_ITEMS descriptors) that every GPU
+   loading this library holds until the process exits.  The status words
+   below sit in one 4 KiB page of the library's static host memory.
+   Set-up: the first call on a device that has something to copy looks up
+   that array's device address (with that device current), reads the wait
+   limit of the long copies' bulk pipeline (environment variable
+   TB_KERNEL_WAIT_NS, else 2 s) and, on the first device only, page-locks
+   and maps the status page (cudaHostRegister of the library's own page);
+   make that first call before any stream capture.
+   Sharing: every call on a device uses the one array and leaves the last
+   batch's items in it: calls whose work overlaps on the GPU (different
+   streams, no ordering between them) race; calls on one stream run in
+   order.  Host-side packing is serialized by a lock.
+   Expired waits: when a bounded wait inside a kernel runs out, that kernel
+   stops its long copies early and sets the device's status word.  The
+   first call on the device that starts after that kernel has finished
+   returns TB_ETIMEOUT, clears the word and enqueues nothing.  To learn
+   whether a given batch completed, synchronize its stream and then call
+   with n == 0, which copies nothing and only reports (and clears) the word.
+   Errors: TB_EINVAL for a null or wrapping range; TB_ENOTSUP when the batch
+   has more than TB_NOALLOC_MAX_ITEMS descriptors with len > 0, or when
+   `stream` is capturing work into a graph (the work list is copied from a
+   host array that the next call rewrites); TB_ETIMEOUT as above; TB_ECUDA
+   when a CUDA call fails.  Nothing is copied after an error.  It calls no
+   cudaMalloc, cudaFree or other allocating routine. */
 int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stream stream);
 
 /* ----------------------------------------------------------------------- */
