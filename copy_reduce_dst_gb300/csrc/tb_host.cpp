@@ -325,20 +325,18 @@ int pipeline_events(tb_ctx *ctx, uint64_t n)
 // span of the timed launches is recorded: an event node between every two
 // launches costs more GPU time than the graph saves.  set_iteration(it)
 // points the plan's sources at the slice iteration `it` reads.
-int run_graphed(tb_ctx *ctx, tb::ReducePlan &plan, int iters,
-                const std::function<void(int64_t)> &set_iteration)
+int run_graphed(tb_ctx *ctx, int iters, const std::function<void(int64_t)> &set_iteration,
+                const std::function<cudaError_t(cudaStream_t)> &issue)
 {
     cudaStream_t st = ctx->stream;
     TB_CUDA(ctx, cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
     cudaError_t err = cudaSuccess;
     for (int64_t it = -(int64_t)ctx->opt.warmup; it < iters && err == cudaSuccess; ++it) {
         set_iteration(it);
-        // Every launch but the first follows one of this transfer.
-        plan.early = it > -(int64_t)ctx->opt.warmup;
         if (it == 0)
             err = cudaEventRecordWithFlags(ctx->events[0], st, cudaEventRecordExternal);
         if (err == cudaSuccess)
-            err = tb::launch_reduce(plan, st);
+            err = issue(st);
         if (err == cudaSuccess && it == iters - 1)
             err = cudaEventRecordWithFlags(ctx->events[iters], st, cudaEventRecordExternal);
     }
@@ -1026,6 +1024,12 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     if (!t || !out || t->iters < 1 || t->n_src < 0 || t->n_src > TB_MAX_SRCS || !t->dst ||
         (t->n_src > 0 && !t->srcs))
         return fail(ctx, TB_EINVAL, "run_transfer: bad arguments");
+    if (t->executor != TB_EXEC_GPU && t->executor != TB_EXEC_DMA)
+        return fail(ctx, TB_EINVAL, "run_transfer: unknown executor %d", (int)t->executor);
+    // The DMA executor copies one source to dst with the copy engines.
+    const bool dma = t->executor == TB_EXEC_DMA;
+    if (dma && t->n_src != 1)
+        return fail(ctx, TB_ENOTSUP, "run_transfer: the DMA executor takes exactly one source");
     memset(out, 0, sizeof *out);
     out->mismatch_index = -1;
     const tb_options &o = ctx->opt;
@@ -1052,6 +1056,15 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
         const uint64_t off = tb_slice_for_iteration(it, K) * stride;
         for (int k = 0; k < t->n_src; ++k)
             plan.src[k] = reinterpret_cast<const float *>(static_cast<const char *>(base[k]) + off);
+        // Every launch but the first follows one of this transfer.
+        plan.early = it > -(int64_t)o.warmup;
+    };
+    // One iteration: the reduce-copy kernel, or on the DMA executor one
+    // device-to-device copy of the iteration's slice (rotated inline).
+    auto issue = [&](cudaStream_t s) -> cudaError_t {
+        if (dma)
+            return cudaMemcpyAsync(dst, plan.src[0], t->num_bytes, cudaMemcpyDeviceToDevice, s);
+        return tb::launch_reduce(plan, s);
     };
 
     const int iters = t->iters;
@@ -1091,7 +1104,7 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     // iterations, so it keeps the stream loop.
     const bool graphed = o.use_graph && !per_iter_validate;
     if (graphed) {
-        int rc2 = run_graphed(ctx, plan, iters, at_iteration);
+        int rc2 = run_graphed(ctx, iters, at_iteration, issue);
         if (rc2 != TB_OK)
             return rc2;
     }
@@ -1114,13 +1127,12 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     };
     for (int64_t it = graphed ? iters : -(int64_t)o.warmup; it < iters; ++it) {
         at_iteration(it);
-        plan.early = it > -(int64_t)o.warmup;
         cudaError_t e = cudaSuccess;
         if (it == 0 || (per_iter_validate && it > 0))
             if ((e = cudaEventRecord(ctx->events[it], st)) != cudaSuccess)
                 return abort_loop(e, "cudaEventRecord");
-        if ((e = tb::launch_reduce(plan, st)) != cudaSuccess)
-            return abort_loop(e, "reduce-copy launch");
+        if ((e = issue(st)) != cudaSuccess)
+            return abort_loop(e, dma ? "DMA copy" : "reduce-copy launch");
         if (it >= 0 && (e = cudaEventRecord(ctx->events[it + 1], st)) != cudaSuccess)
             return abort_loop(e, "cudaEventRecord");
         if (per_iter_validate && it >= 0) {
@@ -1168,12 +1180,13 @@ int tb_run_transfer_ex(tb_ctx *ctx, const tb_transfer *t, tb_result *out)
     out->alloc_bytes = alloc;
     out->prep_h2d_bytes = ctx->prep_h2d;
     out->iters = done;
-    out->num_subexec = plan.num_subexec;
-    out->ctas = plan.grid;
-    out->block_threads = plan.block_threads;
+    out->num_subexec = dma ? 1 : plan.num_subexec;
+    out->ctas = dma ? 0 : plan.grid;
+    out->block_threads = dma ? 0 : plan.block_threads;
     out->gated = gated ? 1 : 0;
     out->graphed = graphed ? 1 : 0;
-    out->engine = plan.engine;
+    out->engine = dma ? 0 : plan.engine;
+    out->executor = t->executor;
     out->total_ms = total;
     if (done > 0) {
         std::vector<float> v(ctx->iter_ms.begin(), ctx->iter_ms.begin() + done);
@@ -1216,6 +1229,7 @@ int tb_run_transfer(tb_ctx *ctx, void *const *srcs, int n_src, void *dst, uint64
     t.rotate_bytes = rotate_bytes;
     t.expected = nullptr;
     t.expected_device = nullptr;
+    t.executor = TB_EXEC_GPU;
     return tb_run_transfer_ex(ctx, &t, out);
 }
 

@@ -105,6 +105,7 @@ class Result(ct.Structure):
         ("mismatch_index", _i64),
         ("mismatch_expected", _u32),
         ("mismatch_actual", _u32),
+        ("executor", _i32),
     ]
 
 
@@ -134,6 +135,7 @@ class Transfer(ct.Structure):
         ("rotate_bytes", _u64),
         ("expected", _vp),
         ("expected_device", _vp),
+        ("executor", _i32),
     ]
 
 
@@ -196,6 +198,8 @@ _sig("tb_validate_device", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
 _sig("tb_batch_copy_noalloc", ct.c_int, _P(CopyDesc), ct.c_size_t, _vp)
 
 TB_NOALLOC_MAX_ITEMS = 65536
+TB_EXEC_GPU = 0
+TB_EXEC_DMA = 1
 
 
 class TBError(RuntimeError):
@@ -378,12 +382,14 @@ class Context:
 
     def run_transfer(self, srcs, dst, num_bytes: int, num_subexec: int = 0, iters: int = 1,
                      rotate_bytes: int | None = None, expected=None,
-                     expected_device=None) -> dict:
+                     expected_device=None, executor: int = 0) -> dict:
         """tb_run_transfer_ex; returns the tb_result fields as a dict.
 
         ``expected`` (host bytes, e.g. a numpy array) turns on validation; a
         mismatch raises TBError with code TB_EVALIDATE after filling the
         result, which is attached to the exception as ``.result``.
+        ``executor``: TB_EXEC_GPU (the reduce-copy kernel) or TB_EXEC_DMA (one
+        copy-engine copy per iteration, one source).
         """
         if rotate_bytes is None:
             rotate_bytes = self.get_options().rotate_bytes
@@ -391,7 +397,7 @@ class Context:
         t = Transfer(srcs=ct.cast(arr, ct.POINTER(_vp)), n_src=len(srcs), dst=addr(dst),
                      num_bytes=num_bytes, num_subexec=num_subexec, iters=iters,
                      rotate_bytes=rotate_bytes, expected=addr(expected) if expected is not None else 0,
-                     expected_device=addr(expected_device))
+                     expected_device=addr(expected_device), executor=executor)
         r = Result()
         code = lib.tb_run_transfer_ex(self._h, ct.byref(t), ct.byref(r))
         res = {name: getattr(r, name) for name, _ in Result._fields_ if name != "iter_ms"}

@@ -361,11 +361,11 @@ typedef struct {
     uint64_t prep_h2d_bytes;  /* the context's prep-H2D counter */
     int32_t  iters;           /* timed iterations run */
     int32_t  num_subexec;     /* sub-executors used */
-    int32_t  ctas;            /* CTAs per launch */
+    int32_t  ctas;            /* CTAs per launch (0 on the DMA executor) */
     int32_t  block_threads;   /* threads per CTA */
     int32_t  gated;           /* 1 if the iterations ran behind the gate */
     int32_t  graphed;         /* 1 if the iterations ran as one CUDA graph */
-    int32_t  engine;          /* reduce-copy engine used (see tb_launch_info) */
+    int32_t  engine;          /* reduce-copy engine used (see tb_launch_info); 0 on DMA */
     int32_t  validated;       /* 1 if dst was compared with expected bytes */
     double   total_ms;        /* device time of all timed iterations */
     double   mean_ms, median_ms, min_ms, max_ms;
@@ -374,6 +374,7 @@ typedef struct {
                                  valid until the next tb_run_transfer) */
     int64_t  mismatch_index;  /* first bad element when validation failed, else -1 */
     uint32_t mismatch_expected, mismatch_actual;  /* its bits */
+    int32_t  executor;        /* TB_EXEC_* the iterations ran on */
 } tb_result;
 
 typedef struct {
@@ -390,13 +391,27 @@ typedef struct {
     const void *expected_device; /* NULL, or device bytes dst must equal,
                                  compared on the GPU (tb_validate_device);
                                  used instead of `expected` when set */
+    int32_t executor;         /* TB_EXEC_GPU (0) or TB_EXEC_DMA (1), below */
 } tb_transfer;
+
+/* Executors of a transfer (TransferBench PR #365, section "Technical
+   Details": rotation applies to the GFX and DMA executors; the DMA one reads
+   its source directly and rotates inline).
+     TB_EXEC_GPU  the reduce-copy kernel (tb_reduce_copy's launch).
+     TB_EXEC_DMA  the copy engines: iteration it is one cudaMemcpyAsync,
+                  device to device, of numBytes from slice
+                  tb_slice_for_iteration(it, K) of the one source to dst.
+                  Exactly one source (TB_ENOTSUP otherwise); numSubExec,
+                  the reduce-copy options and use_pdl do not apply. */
+#define TB_EXEC_GPU 0
+#define TB_EXEC_DMA 1
 
 /* TransferBench's timed iteration loop for one transfer, synchronous on an
    internal stream: for it = -warmup .. iters-1, iteration it reads slice
    tb_slice_for_iteration(it, K) of every source (the slice offset is a kernel
-   argument, so rotation costs no host-to-device traffic and sits outside
-   the timed region) and writes dst + byte_offset.  The loop runs as one
+   argument, or the copy's source address on the DMA executor, so rotation
+   costs no host-to-device traffic and sits outside the timed region) and
+   writes dst + byte_offset.  The loop runs as one
    CUDA graph timed by events around the timed iterations (use_graph), or as
    stream launches, behind the gate (use_gate) or not, with CUDA events
    between every two iterations.  Sources must already hold their slices

@@ -112,6 +112,20 @@ def test_options_struct_matches_header(tb):
     assert fields == [name for name, _ in tb.Options._fields_]
 
 
+@pytest.mark.parametrize("name,cls", [("tb_transfer", "Transfer"), ("tb_result", "Result")])
+def test_transfer_and_result_structs_match_header(tb, name, cls):
+    # every field of the header's struct, in order, is in the binding
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    end = text.index("} " + name + ";")
+    body = text[text.rindex("typedef struct {", 0, end):end]
+    fields = []
+    for decl in body.split(";")[:-1]:
+        decl = decl.split("{")[-1].strip()
+        for part in decl.split(","):
+            fields.append(re.findall(r"(\w+)\s*$", part.strip())[0])
+    assert fields == [f for f, _ in getattr(tb, cls)._fields_]
+
+
 def test_every_option_has_an_environment_variable(tb):
     # the header's list of variables covers every tb_options field
     text = open(HEADER).read()

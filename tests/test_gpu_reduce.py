@@ -518,6 +518,61 @@ def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K, graph):
         assert len(r["iter_ms"]) == iters and all(t > 0 for t in r["iter_ms"])
 
 
+@pytest.mark.parametrize("graph,gate", [(1, 0), (0, 1), (0, 0)])
+@pytest.mark.parametrize("iters,warmup,K", [(10, 3, 4), (7, 2, 5), (1, 0, 3)])
+def test_dma_executor_reads_slice_i_mod_k(tb, iters, warmup, K, graph, gate):
+    """The DMA (copy-engine) executor of PR #365's "Technical Details" rotates
+    inline: slices filled with different patterns, dst ends as the slice of
+    the last iteration, (iters - 1) % K, in graph and stream loops."""
+    nb = 64 * 1024 + 12
+    n = nb // 4
+    with tb.Context(0, tb.options(warmup=warmup, use_graph=graph, use_gate=gate)) as c:
+        plan = tb.rotation_plan(nb, K * nb)
+        assert plan.K == K
+        src = dev_bytes(plan.alloc_bytes)
+        for j in range(K):
+            c.fill_source(src.data_ptr() + j * plan.slice_stride, nb, tb.default_pattern(), j)
+        dst = dev_bytes(nb + 64, fill=0x5A)
+        expect = oracle.prepare_reference(n, oracle.slice_for_iteration(iters - 1, K))
+        r = c.run_transfer([src], dst, nb, iters=iters, rotate_bytes=K * nb, expected=expect,
+                           executor=tb.TB_EXEC_DMA)
+        assert r["mismatch_index"] == -1 and r["validated"] == 1
+        assert r["executor"] == tb.TB_EXEC_DMA and r["ctas"] == 0 and r["engine"] == 0
+        assert r["graphed"] == graph and len(r["iter_ms"]) == iters
+        assert np.all(to_host(dst, 64, nb) == 0x5A)
+
+
+def test_dma_executor_single_transfer_4mib(tb):
+    """The 4 MiB single transfer (K = 64 at 256 MiB of rotation, a
+    268,435,456 B allocation) on the copy engines: dst == src0 bit for bit,
+    checked on the device and against the oracle's PrepSrcValue."""
+    nb = 4 * MiB
+    with tb.Context(0) as c:
+        plan = tb.rotation_plan(nb, 256 * MiB)
+        assert plan.K == 64 and plan.alloc_bytes == 268435456
+        src = dev_bytes(plan.alloc_bytes)
+        c.fill_source(src, nb, tb.default_pattern(), 0)
+        c.prepare_sources([src], nb, 256 * MiB)
+        dst = dev_bytes(nb, fill=0)
+        r = c.run_transfer([src], dst, nb, iters=10, rotate_bytes=256 * MiB,
+                           expected_device=src, executor=tb.TB_EXEC_DMA)
+        assert r["K"] == 64 and r["validated"] == 1 and r["gbps"] > 0
+        assert np.array_equal(to_host(dst).view(np.float32), oracle.prepare_reference(nb // 4, 0))
+
+
+def test_dma_executor_rejects_other_source_counts(tb):
+    with tb.Context(0) as c:
+        a, b, d = dev_bytes(4096), dev_bytes(4096), dev_bytes(4096, fill=3)
+        for srcs in ([], [a, b]):
+            with pytest.raises(tb.TBError) as e:
+                c.run_transfer(srcs, d, 4096, iters=1, rotate_bytes=0, executor=tb.TB_EXEC_DMA)
+            assert e.value.code == tb.TB_ENOTSUP
+        with pytest.raises(tb.TBError) as e:
+            c.run_transfer([a], d, 4096, iters=1, rotate_bytes=0, executor=7)
+        assert e.value.code == tb.TB_EINVAL
+        assert np.all(to_host(d) == 3)
+
+
 def test_byte_offset(tb):
     nb = 1 * MiB + 64
     n = nb // 4
