@@ -338,8 +338,8 @@ def run_reduce(args, tb, torch, ranks, local):
 def run_batch(args, tb, torch, ranks, local):
     from copy_reduce_dst_gb300 import workloads
     layout = workloads.batch_head_sliced()
-    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
-    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    src = device_random_bytes(torch, layout.src_pool_bytes, 41)
+    dst = device_random_bytes(torch, layout.dst_pool_bytes, 42)
     desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
     stream = torch.cuda.current_stream()
     ctx = tb.Context(local, ctx_options(tb, time_kernels=1))
@@ -382,11 +382,13 @@ def run_batch(args, tb, torch, ranks, local):
         each.append(time.perf_counter() - t0)
     each_ms = min(each) * 1e3
     ctx.close()
+    del src, dst
+    torch.cuda.empty_cache()
     peak, peak_kind = read_peaks()
     algo = payload + stats["upload_bytes"]  # the kernel also reads each work item once
     units, worst = combine(ranks, n * args.steps, wall_total)
     return {
-        "workload": layout.name + " (uint8, two 2 GiB pools, seeded layout)",
+        "workload": layout.name + " (uint8 random from seed, two 2 GiB pools, seeded layout)",
         "descriptors": n, "bytes_copied": layout.total_bytes,
         "copies_per_s": round(units / worst, 1),
         "gbps_rw_device": round(payload / (dev_ms / 1e3) / 1e9, 1),
@@ -404,6 +406,261 @@ def run_batch(args, tb, torch, ranks, local):
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
                      "kernel": "k_batch<2, 4>"},
     }
+
+
+def device_random_bytes(torch, n: int, seed: int):
+    """A seeded uniform uint8 pool written on the device (input preparation,
+    outside every timed region)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+
+
+# ---------------------------------------------------------------------------
+# The other workloads, bounded to a few seconds each, on the default line
+# ---------------------------------------------------------------------------
+def run_single_transfer(tb, torch, local):
+    """The single 4 MiB transfer: 1 source of 1,048,576 float32 =
+    PrepSrcValue(0, i), uploaded from the host into slice 0 (prep H2D 4 MiB),
+    slices 1..63 filled on the device; SRC_ROTATE_BYTES 256 MiB, so K = 64 and
+    a 268,435,456 B allocation; 3 warm-up + 10 timed iterations, dst validated
+    against src0 on the device.  Median of 5 runs, on the reduce-copy kernel
+    (one CUDA graph) and on the copy engines (DMA executor); a full rotation
+    of 64 iterations beside it."""
+    nb, rot = 4 * MiB, 256 * MiB
+    plan = tb.rotation_plan(nb, rot)
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
+        ctx.fill_source(src, nb, tb.default_pattern(), 0)
+        host = src[:nb].cpu().pin_memory()
+        src.zero_()
+        ctx.upload_sources([src], [host], nb)
+        ctx.prepare_sources([src], nb, rot)
+        dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+
+        def med(iters, executor):
+            runs = [ctx.run_transfer([src], dst, nb, iters=iters, rotate_bytes=rot,
+                                     expected_device=src, executor=executor) for _ in range(5)]
+            return sorted(runs, key=lambda r: r["gbps"])[2]
+        k1, k1_64 = med(10, tb.TB_EXEC_GPU), med(64, tb.TB_EXEC_GPU)
+        dma = med(10, tb.TB_EXEC_DMA)
+        out = {"workload": "1 source, 1,048,576 float32 = PrepSrcValue(0, i), SRC_ROTATE_BYTES "
+                           "256 MiB, 3 warm-up + 10 timed iterations, dst == src0",
+               "K": k1["K"], "alloc_bytes": k1["alloc_bytes"],
+               "prep_h2d_bytes": k1["prep_h2d_bytes"], "validated": bool(k1["validated"]),
+               "gbps": round(k1["gbps"], 1), "us_per_iteration": round(k1["mean_ms"] * 1e3, 3),
+               "graphed": bool(k1["graphed"]), "ctas": k1["ctas"],
+               "gbps_64_iterations": round(k1_64["gbps"], 1),
+               "us_per_iteration_64": round(k1_64["mean_ms"] * 1e3, 3),
+               "dma_gbps": round(dma["gbps"], 1),
+               "dma_us_per_iteration": round(dma["mean_ms"] * 1e3, 3),
+               "dma_validated": bool(dma["validated"])}
+        del src, dst, host
+    return out
+
+
+def run_dma_large(tb, torch, local):
+    """The copy-engine (DMA) executor beside the reduce-copy kernel on one
+    256 MiB source (K = 1): 3 warm-up + 20 timed iterations, median of 3."""
+    nb = 256 * MiB
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        src = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        ctx.fill_source(src, nb, tb.default_pattern(), 0)
+        dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        res = {}
+        for name, ex in (("kernel", tb.TB_EXEC_GPU), ("dma", tb.TB_EXEC_DMA)):
+            runs = [ctx.run_transfer([src], dst, nb, iters=20, rotate_bytes=256 * MiB,
+                                     expected_device=src, executor=ex) for _ in range(3)]
+            r = sorted(runs, key=lambda r: r["gbps"])[1]
+            res[name + "_gbps"] = round(r["gbps"], 1)
+            res[name + "_us_per_iteration"] = round(r["mean_ms"] * 1e3, 2)
+        del src, dst
+    res["workload"] = "1 source of 256 MiB (67,108,864 float32), K = 1, 20 iterations, dst == src0"
+    return res
+
+
+def run_rotation_sweep(tb, torch, local):
+    """fillCompress sweep: 1 source, 8-512 MiB, 40% random / 20% 1B0 / 0% 2B0 /
+    20% 4B0 / 20% 32B0 per 64-byte line (seed 0x5EED), rotation at 256 MiB
+    and off.  cold = mean of 5 single iterations each after writing a 512 MiB
+    buffer (> L2); warm = 20 iterations after 3 warm-ups with events around
+    every launch; warm_graph = the same 20 as one CUDA graph; median of 3."""
+    import statistics as st
+    flush = torch.empty(512 * MiB, dtype=torch.uint8, device="cuda")
+    pct = (40, 20, 0, 20, 20)
+    rows = []
+    with tb.Context(local, ctx_options(tb)) as ctx, \
+            tb.Context(local, ctx_options(tb, use_graph=0)) as ev_ctx, \
+            tb.Context(local, ctx_options(tb, warmup=0, use_graph=0)) as cold_ctx:
+        for mib in (8, 16, 32, 64, 128, 256, 512):
+            nb = mib * MiB
+            row = {"MiB": mib}
+            for rot in (256 * MiB, 0):
+                plan = tb.rotation_plan(nb, rot)
+                src = torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda")
+                ctx.fill_source(src, nb, tb.compress_pattern(pct, 0x5EED), 0)
+                ctx.prepare_sources([src], nb, rot)
+                dst = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+                cold, warm, graph = [], [], []
+                for rep in range(3):
+                    c = []
+                    for _ in range(5):
+                        flush.fill_(rep)
+                        c.append(cold_ctx.run_transfer([src], dst, nb, iters=1,
+                                                       rotate_bytes=rot)["total_ms"])
+                    cold.append(2 * nb / (st.mean(c) / 1e3) / 1e9)
+                    warm.append(ev_ctx.run_transfer([src], dst, nb, iters=20,
+                                                    rotate_bytes=rot)["gbps"])
+                    graph.append(ctx.run_transfer([src], dst, nb, iters=20,
+                                                  rotate_bytes=rot)["gbps"])
+                tag = "on" if rot else "off"
+                row[tag] = {"K": plan.K, "cold_gbps": round(st.median(cold), 1),
+                            "warm_gbps": round(st.median(warm), 1),
+                            "w_over_c": round(st.median(warm) / st.median(cold), 3),
+                            "warm_graph_gbps": round(st.median(graph), 1)}
+                del src, dst
+            rows.append(row)
+    del flush
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_small_batch(tb, torch, local, layout, seed):
+    """One of the Mooncake RFC's small-copy shapes on seeded random pools:
+    kernel_us = kernel-only events (median of 20); device_us = events around
+    30 back-to-back calls; wall_us = one call with packing, upload, kernel
+    and stream sync (median of 20); memcpy_each = one cudaMemcpyAsync per
+    copy, wall-timed the same way (best of 2)."""
+    import statistics as st
+    src = device_random_bytes(torch, layout.src_pool_bytes, seed)
+    dst = device_random_bytes(torch, layout.dst_pool_bytes, seed + 1)
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    stream = torch.cuda.Stream()
+    moved = 2 * int(layout.total_bytes)
+    with tb.Context(local, ctx_options(tb, time_kernels=1)) as kctx, \
+            tb.Context(local, ctx_options(tb)) as ctx:
+        for _ in range(3):
+            kctx.batch_copy(desc, stream)
+        kern = []
+        for _ in range(20):
+            kctx.batch_copy(desc, stream)
+            kern.append(kctx.last_batch_kernel_ms())
+        for _ in range(3):
+            ctx.batch_copy(desc, stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        a.record(stream)
+        for _ in range(30):
+            ctx.batch_copy(desc, stream)
+        b.record(stream)
+        b.synchronize()
+        dev_ms = a.elapsed_time(b) / 30
+        walls = []
+        for _ in range(20):
+            t0 = time.perf_counter()
+            ctx.batch_copy(desc, stream)
+            stream.synchronize()
+            walls.append(time.perf_counter() - t0)
+        each = []
+        for _ in range(2):
+            t0 = time.perf_counter()
+            ctx.copy_each(desc, stream)
+            stream.synchronize()
+            each.append(time.perf_counter() - t0)
+        stats = kctx.last_batch_stats()
+    k_ms = st.median(kern)
+    wall = st.median(walls)
+    del src, dst
+    return {"workload": layout.name + " (uint8 random from seed)", "descriptors": layout.n,
+            "bytes_copied": int(layout.total_bytes),
+            "kernel_us": round(k_ms * 1e3, 2),
+            "kernel_gbps": round(moved / (k_ms / 1e3) / 1e9, 1),
+            "device_us": round(dev_ms * 1e3, 2),
+            "device_gbps": round(moved / (dev_ms / 1e3) / 1e9, 1),
+            "copies_per_s_device": round(layout.n / (dev_ms / 1e3), 1),
+            "wall_us": round(wall * 1e6, 1), "copies_per_s_wall": round(layout.n / wall, 1),
+            "memcpy_each_wall_ms": round(min(each) * 1e3, 3),
+            "speedup_vs_memcpy_each": round(min(each) / wall, 1),
+            "direct_launches": stats["direct_launches"]}
+
+
+def run_interference(tb, torch, local):
+    """A bf16 GEMM (4096^3 torch.matmul) looping on one stream for ~0.4 s, alone
+    and while the 47,540 batch is copied back to back on another stream (the
+    Mooncake RFC's interference measurement); and the 3840-page batch's wall
+    time per call on an idle GPU and under the GEMM loop, on a normal- and a
+    high-priority stream."""
+    import statistics as st
+    from copy_reduce_dst_gb300 import workloads
+    n = 4096
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    flops = 2 * n ** 3
+    gemm_s = torch.cuda.Stream()
+    copy_s = torch.cuda.Stream()
+    hi_s = torch.cuda.Stream(priority=-1)
+    reps = 2400  # ~0.4 s of 4096^3 GEMMs
+
+    def gemm_loop():
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(gemm_s)
+        with torch.cuda.stream(gemm_s):
+            for _ in range(reps):
+                torch.matmul(a, b)
+        e1.record(gemm_s)
+        return e0, e1
+
+    big = workloads.batch_head_sliced()
+    src = device_random_bytes(torch, big.src_pool_bytes, 51)
+    dst = device_random_bytes(torch, big.dst_pool_bytes, 52)
+    desc = big.descriptors(src.data_ptr(), dst.data_ptr())
+    out = {}
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        with torch.cuda.stream(gemm_s):
+            for _ in range(20):
+                torch.matmul(a, b)
+        torch.cuda.synchronize()
+        e0, e1 = gemm_loop()
+        torch.cuda.synchronize()
+        alone = reps * flops / (e0.elapsed_time(e1) / 1e3) / 1e12
+        e0, e1 = gemm_loop()
+        batches, t0 = 0, time.perf_counter()
+        while not e1.query():
+            ctx.batch_copy(desc, copy_s)
+            copy_s.synchronize()
+            batches += 1
+        wall = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        shared = reps * flops / (e0.elapsed_time(e1) / 1e3) / 1e12
+        gbps = 2 * big.total_bytes * batches / wall / 1e9
+        out.update({"gemm": "4096^3 bf16 torch.matmul", "gemm_tflops_alone": round(alone, 1),
+                    "gemm_tflops_with_batch": round(shared, 1), "batch_gbps": round(gbps, 1),
+                    "gemm_loss_pct": round(100 * (1 - shared / alone), 2),
+                    "batch": big.name + " back to back"})
+        del src, dst
+        small = workloads.batch_index_pages()
+        src = device_random_bytes(torch, small.src_pool_bytes, 53)
+        dst = device_random_bytes(torch, small.dst_pool_bytes, 54)
+        desc = small.descriptors(src.data_ptr(), dst.data_ptr())
+        for name, s in (("normal", copy_s), ("high", hi_s)):
+            for busy in (False, True):
+                torch.cuda.synchronize()
+                e1 = gemm_loop()[1] if busy else None
+                times = []
+                while len(times) < 40 and (e1 is None or not e1.query()):
+                    t = time.perf_counter()
+                    ctx.batch_copy(desc, s)
+                    s.synchronize()
+                    times.append(time.perf_counter() - t)
+                torch.cuda.synchronize()
+                key = f"index_pages_{name}_priority_{'under_gemm' if busy else 'idle'}_us"
+                out[key] = round(st.median(times) * 1e6, 1) if times else None
+        del src, dst
+    del a, b
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -1030,6 +1287,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-batch", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave out the single transfer, DMA executor, rotation sweep, small "
+                         "batches and interference keys")
     ap.add_argument("--study", action="store_true")
     ap.add_argument("--profile", choices=["reduce", "batch", "batch-short", "batch-small",
                                           "rotation"])
@@ -1055,6 +1315,17 @@ def main():
     ranks = Ranks(world, "nccl")
     red = run_reduce(args, tb, torch, ranks, local)
     batch = None if args.no_batch else run_batch(args, tb, torch, ranks, local)
+    extra = {}
+    if not args.no_extra:
+        from copy_reduce_dst_gb300 import workloads
+        extra["single_4mib_k64"] = run_single_transfer(tb, torch, local)
+        extra["dma_executor_256mib"] = run_dma_large(tb, torch, local)
+        extra["rotation_sweep"] = run_rotation_sweep(tb, torch, local)
+        extra["index_pages_3840"] = run_small_batch(tb, torch, local,
+                                                    workloads.batch_index_pages(), 31)
+        extra["block_pages_7200"] = run_small_batch(tb, torch, local,
+                                                    workloads.batch_block_pages(), 33)
+        extra["interference"] = run_interference(tb, torch, local)
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
     if rank == 0:
         line = {
@@ -1075,6 +1346,7 @@ def main():
             "roofline": red["roofline"], "cpu_baseline": cpu, "e2e": red["e2e"],
             "clocks": red["clocks"], "gpu_launches": red["gpu_launches"], "batch": batch,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
     ranks.close()
     return 0

@@ -351,6 +351,49 @@ def test_pipeline_wait_expiry_is_reported(tb):
 
 
 # ---------------------------------------------------------------------------
+# Beside compute (Mooncake RFC, "Design of #5040", interference with compute
+# on the sending GPU; "Motivation", small copies under a bf16 GEMM)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("priority", [0, -1])
+def test_batches_exact_beside_a_gemm_loop(tb, ctx, priority):
+    """The 3840-page batch and the 47,540-descriptor batch (its layout in
+    1 GiB pools) copied on a normal- or high-priority stream while a bf16
+    GEMM loop runs on another stream: both whole pools byte-exact against
+    the oracle, and the GEMM loop still running when the batches were
+    enqueued."""
+    import torch
+    layouts = [workloads.batch_index_pages(), workloads.batch_head_sliced(pool_bytes=1 << 30)]
+    pools = []
+    for j, lay in enumerate(layouts):
+        src_h = workloads.random_bytes(lay.src_pool_bytes, 300 + 2 * j)
+        dst_h = workloads.random_bytes(lay.dst_pool_bytes, 301 + 2 * j)
+        pools.append((src_h, dst_h, to_dev(src_h), to_dev(dst_h)))
+    n = 4096
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
+    gemm_s = torch.cuda.Stream()
+    copy_s = torch.cuda.Stream(priority=priority)
+    torch.cuda.synchronize()
+    done = torch.cuda.Event()
+    with torch.cuda.stream(gemm_s):
+        for _ in range(600):
+            torch.matmul(a, b, out=c)
+    done.record(gemm_s)
+    for lay, (_, _, src_d, dst_d) in zip(layouts, pools):
+        ctx.batch_copy(lay.descriptors(src_d.data_ptr(), dst_d.data_ptr()), copy_s)
+    running = not done.query()
+    copy_s.synchronize()
+    torch.cuda.synchronize()
+    assert running
+    for lay, (src_h, dst_h, _, dst_d) in zip(layouts, pools):
+        exp = dst_h.copy()
+        oracle.apply_batch(exp, src_h, lay.src_off, lay.dst_off, lay.lens)
+        mm = oracle.first_mismatch(to_host(dst_d), exp)
+        assert mm == -1, f"{lay.name}: first differing byte {mm}"
+
+
+# ---------------------------------------------------------------------------
 # Full-size layouts, in the launch configuration the bench times
 # ---------------------------------------------------------------------------
 def test_index_pages_full(tb, ctx):
