@@ -14,6 +14,13 @@ Default line (rank 0 prints one JSON object):
   batch     the 47,540-descriptor batch (47,520 head-sliced pages of
             64 B-16 KiB + 16 x 16 MiB + 4 x 8 MiB) through tb_batch_copy,
             with one cudaMemcpyAsync per copy (tb_copy_each) timed beside it;
+  single_4mib_k64, dma_executor_256mib, rotation_sweep, index_pages_3840,
+  block_pages_7200, interference
+            the other configured workloads, a few seconds in all (leave
+            them out with --no-extra): the 4 MiB K = 64 transfer on the
+            kernel and on the copy engines, the DMA executor at 256 MiB,
+            the fillCompress sweep 8-512 MiB with rotation on and off, the
+            3840- and 7200-page batches, and a bf16 GEMM beside the batches;
   roofline  achieved algorithmic GB/s of the reduce kernel against the
             measured HBM copy bandwidth (MEASURED_PEAKS.json);
   cpu_baseline  the CPU oracle on a bounded sample, one host core.
@@ -1249,8 +1256,8 @@ def profile_target(kind, args, tb, torch, local):
         with tb.Context(local, ctx_options(tb, time_kernels=1)) as ctx:
             for name, lay in (("3840 index pages", workloads.batch_index_pages()),
                               ("7200 block pages", workloads.batch_block_pages())):
-                src = torch.zeros(lay.src_pool_bytes, dtype=torch.uint8, device="cuda")
-                dst = torch.zeros(lay.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+                src = device_random_bytes(torch, lay.src_pool_bytes, 31)
+                dst = device_random_bytes(torch, lay.dst_pool_bytes, 32)
                 desc = lay.descriptors(src.data_ptr(), dst.data_ptr())
                 ms = []
                 for _ in range(5):
@@ -1265,8 +1272,8 @@ def profile_target(kind, args, tb, torch, local):
     else:
         from copy_reduce_dst_gb300 import workloads
         layout = workloads.batch_head_sliced()
-        src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
-        dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+        src = device_random_bytes(torch, layout.src_pool_bytes, 41)
+        dst = device_random_bytes(torch, layout.dst_pool_bytes, 42)
         desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
         if kind == "batch-short":  # its 47,520 short copies alone
             desc = desc[desc[:, 2] <= 16384]

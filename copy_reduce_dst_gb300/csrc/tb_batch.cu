@@ -149,6 +149,39 @@ __device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, uin
     copy_bytes(dst + done, src + done, len - done, rank, size);
 }
 
+// A short copy whose src and dst differ modulo 16, by one warp: the same
+// steps as copy_range takes for such a pair (head bytes to a 16-byte
+// destination boundary, one funnel-shifted 16-byte vector per lane and
+// round, tail bytes) without the branches a warp never reaches there, so
+// the short-copy kernels keep few registers (the general form took the
+// short-only kernel from 69 to 80 registers and into spills).
+__device__ __forceinline__ void copy_shifted_warp(uint8_t *dst, const uint8_t *src, uint64_t len,
+                                                  uint32_t lane)
+{
+    uint64_t h = (16u - ((uintptr_t)dst & 15u)) & 15u;
+    if (h > len)
+        h = len;
+    if (lane < h)
+        dst[lane] = src[lane];
+    dst += h;
+    src += h;
+    len -= h;
+    const uint64_t nv = len >> 4;
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    const uint32_t sh = (uint32_t)((uintptr_t)src & 15u);
+    const uint4 *s = reinterpret_cast<const uint4 *>(src - sh);
+    const uint32_t q = sh >> 2, rbits = (sh & 3u) * 8u;
+    for (uint64_t v = lane; v < nv; v += 32) {
+        // Both aligned words hold bytes of the range when sh != 0.
+        const uint4 lo = ld16(s + v);
+        const uint4 hi = sh ? ld16(s + v + 1) : lo;
+        st16(d + v, sh ? shift_pair(lo, hi, q, rbits) : lo);
+    }
+    const uint64_t done = nv << 4;
+    if (lane < len - done)
+        dst[done + lane] = src[done + lane];
+}
+
 __device__ __forceinline__ WorkItem load_item(const WorkItem *p)
 {
     WorkItem w;
@@ -341,11 +374,9 @@ __device__ void long_edges(const BatchArgs &a, uint32_t rank, uint32_t size)
 // short copies of 64 B - 16 KiB alone / the 47,540 batch with long copies):
 // register rounds 62.5 / 142.7 us; S = 2: U = 8 55.4, U = 4 57.0 /
 // U = 4 141.6, U = 8 143.7; S = 4: U = 4 54.5 / U = 2 141.0; S = 8: U = 2
-// 58.4 / U = 1 143.5; U = 16 (one CTA per SM) 71.1.  Short-only launches
-// take 8 KiB of slots per warp (three CTAs per SM), launches with long
-// copies 4 KiB beside the bulk stages (two per SM).
-constexpr int kShortUnits = 4;  // U of a launch of short copies only
-constexpr int kShortSlots = 4;  // S of a launch of short copies only
+// 58.4 / U = 1 143.5; U = 16 (one CTA per SM) 71.1.  Launches with long
+// copies take 4 KiB of slots per warp beside the bulk stages (two CTAs per
+// SM); launches of short copies only take one of the k_short shapes.
 constexpr int kMixedUnits = 2;  // U beside the long copies' bulk stages
 constexpr int kMixedSlots = 4;
 // Short copies a warp claims from the counter with one atomic: fewer
@@ -471,14 +502,14 @@ struct ShortPipe {
 // head bytes (lanes 0..14) and 15 tail bytes (lanes 16..30) go a byte per
 // lane, loaded before the body's pieces are pushed and stored after, so
 // their latency overlaps the pipe's; the body goes through the pipe.  Any
-// other alignment: copy_range through registers.
+// other alignment: copy_shifted_warp through registers.
 template <int U, int S>
 __device__ __forceinline__ void short_item(ShortPipe<U, S> &p, const WorkItem &w, uint32_t lane)
 {
     const uint8_t *s = reinterpret_cast<const uint8_t *>(w.src);
     uint8_t *d = reinterpret_cast<uint8_t *>(w.dst);
     if (((w.src ^ w.dst) & 15u) != 0) {
-        copy_range(d, s, w.len, lane, 32);
+        copy_shifted_warp(d, s, w.len, lane);
         return;
     }
     const uint64_t h = min((uint64_t)((16u - (w.dst & 15u)) & 15u), w.len);
@@ -544,18 +575,17 @@ __device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first,
     p.flush();
 }
 
-// A grid of up to kBatchWaves waves of resident CTAs with long copies
-// (short-lived CTAs let the scheduler balance the SMs' finishing times),
-// kShortWaves with short copies only.  U: see ShortPipe.
+// k_batch: a launch with long copies, over up to kBatchWaves waves of
+// resident CTAs (short-lived CTAs let the scheduler balance the SMs'
+// finishing times).  U, S: the short copies' ring (see ShortPipe).
 //   Long copies: their bytes form one stream of `chunks` equal chunks; CTA b
 //   owns chunks b, b + G, ... (the same number for every CTA, the grid
 //   sweeping the stream front to back).  Thread 0 moves the 16-byte-aligned
 //   bodies with a bulk-copy pipeline through shared memory; warps 1.. copy
 //   the leftover edges.
 //   Short copies (short_copies, each warp through its own shared-memory
-//   pipe): the warps free at the start (all of them, or warps 1.. when
-//   there are long chunks) take up to claim_items items each by warp
-//   index (warp w: w, w + starters); the rest are claimed kClaimBlock at a time
+//   pipe): warps 1.. take up to claim_items items each by warp index
+//   (warp w: w, w + starters); the rest are claimed kClaimBlock at a time
 //   from a counter in global memory by whichever warp is free, warp 0
 //   joining once its pipeline has drained, which balances the work without
 //   any ordering on the host.
@@ -564,46 +594,85 @@ __global__ void __launch_bounds__(kBatchThreads, 3) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    if (a.chunks > 0) {
-        if (threadIdx.x == 0) {
-            for (int s = 0; s < kStages; ++s)
-                mbar_init(smem_u32(smem) + 8 * s);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        __syncthreads();
-        if (warp == 0) {
-            if (lane == 0)
-                bulk_pipeline(a, smem_u32(smem), smem_u32(smem + kBarBytes));
-            __syncwarp();
-        } else {
-            long_edges(a, threadIdx.x - 32, blockDim.x - 32);
-        }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(smem_u32(smem) + 8 * s);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            bulk_pipeline(a, smem_u32(smem), smem_u32(smem + kBarBytes));
+        __syncwarp();
+    } else {
+        long_edges(a, threadIdx.x - 32, blockDim.x - 32);
     }
 
-    // Warps that start on short copies, and this warp's index among them.
+    // Warps 1.. start on short copies; warp 0 only claims.
     const uint32_t wpc = blockDim.x >> 5;
-    const bool busy0 = a.chunks > 0;  // warp 0 runs the bulk pipeline first
-    const uint32_t starters = gridDim.x * (busy0 ? wpc - 1 : wpc);
-    const bool starter = !(busy0 && warp == 0);
-    const uint32_t sidx = blockIdx.x * (busy0 ? wpc - 1 : wpc) + (busy0 ? warp - 1 : warp);
-    const uint32_t C = a.claim_items;
-    const uint32_t fixed = starters * C;  // items taken by index
-    const bool dynamic = fixed < a.n_short;
-    const uint32_t first = starter ? sidx : a.n_short;
-    const uint32_t pipes = smem_u32(smem) + (busy0 ? (uint32_t)kBatchSmem : 0u);
-    short_copies<U, S>(a, first, starters, fixed, dynamic, lane,
-                       pipes + warp * (uint32_t)warp_stage_bytes<U, S>());
+    const uint32_t starters = gridDim.x * (wpc - 1);
+    const uint32_t fixed = starters * a.claim_items;  // items taken by index
+    const uint32_t first = warp == 0 ? a.n_short : blockIdx.x * (wpc - 1) + warp - 1;
+    short_copies<U, S>(a, first, starters, fixed, fixed < a.n_short, lane,
+                       smem_u32(smem) + (uint32_t)kBatchSmem +
+                           warp * (uint32_t)warp_stage_bytes<U, S>());
+}
+
+// k_short: a launch of short copies only, over up to kShortWaves waves.
+// Every warp starts on short copies: up to claim_items by warp index, then
+// blocks claimed from the counter.  Its ring (U units per lane and piece, S
+// slots) and the CTAs it keeps per SM (MINB, which bounds its registers)
+// form a shape, chosen per launch (see short_shape_for).  Measured on GB300
+// (kernel events, median of 40; shapes 1 / 2 / four 1 KiB slots at 5 CTAs
+// per SM): 3840 x 2112 B 8.9-9.7 / 8.4-8.6 / 9.8-9.9 us; 7200 x 512 B-16 KiB
+// 14.5-14.6 / 14.9 / 16.6 us; 47,520 x 64 B-16 KiB 50.8 us for all three.
+// The old short-only launch (k_batch with four 2 KiB slots, 80 registers)
+// took 6.1-8.5 us on the 3840 pages by ncu, shape 2 takes 5.4-6.1.
+template <int U, int S, int MINB>
+__global__ void __launch_bounds__(kBatchThreads, MINB) k_short(const BatchArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t wpc = blockDim.x >> 5;
+    const uint32_t starters = gridDim.x * wpc;
+    const uint32_t fixed = starters * a.claim_items;
+    short_copies<U, S>(a, blockIdx.x * wpc + warp, starters, fixed, fixed < a.n_short, lane,
+                       smem_u32(smem) + warp * (uint32_t)warp_stage_bytes<U, S>());
+}
+
+// The shapes of k_short, by number (1-based; 0 names k_batch).
+struct ShapeInfo {
+    const void *kernel;
+    size_t smem;
+};
+
+template <int U, int S, int MINB>
+ShapeInfo shape_info()
+{
+    return ShapeInfo{(const void *)k_short<U, S, MINB>, short_smem_bytes<U, S>()};
+}
+
+ShapeInfo shape(int k)
+{
+    switch (k) {
+    case 1:
+        return shape_info<4, 4, 3>();  // 4 slots of 2 KiB per warp, 3 CTAs per SM
+    case 2:
+        return shape_info<4, 2, 5>();  // 2 slots of 2 KiB per warp, 5 CTAs per SM
+    default:
+        return ShapeInfo{(const void *)k_batch<kMixedUnits, kMixedSlots>,
+                         kBatchSmem + short_smem_bytes<kMixedUnits, kMixedSlots>()};
+    }
 }
 
 }  // namespace
 
-int batch_ctas_per_sm(bool with_long)
+int batch_ctas_per_sm(int k)
 {
-    if (with_long)
-        return resident_ctas((const void *)k_batch<kMixedUnits, kMixedSlots>, kBatchThreads,
-                             kBatchSmem + short_smem_bytes<kMixedUnits, kMixedSlots>());
-    return resident_ctas((const void *)k_batch<kShortUnits, kShortSlots>, kBatchThreads,
-                         short_smem_bytes<kShortUnits, kShortSlots>());
+    if (k < 0 || k > kShortShapes)
+        return 0;
+    const ShapeInfo info = shape(k);
+    return resident_ctas(info.kernel, kBatchThreads, info.smem);
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
@@ -611,7 +680,10 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
-    if (batch_ctas_per_sm(plan.chunks > 0) < 1)
+    // A launch with long copies runs k_batch, one of short copies only a
+    // k_short shape.
+    const int k = plan.chunks ? 0 : plan.shape;
+    if ((plan.chunks == 0) == (k == 0) || batch_ctas_per_sm(k) < 1)
         return cudaErrorInvalidValue;
     char *base = static_cast<char *>(const_cast<void *>(dev));
     BatchArgs a;
@@ -626,14 +698,10 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.chunks = plan.chunks;
     a.claim_items = batch_claim_items(plan);
     a.wait_ns = wait_ns;
-    if (plan.chunks)
-        k_batch<kMixedUnits, kMixedSlots><<<plan.grid, kBatchThreads,
-                                            kBatchSmem + short_smem_bytes<kMixedUnits, kMixedSlots>(),
-                                            stream>>>(a);
-    else  // short copies only: no bulk stages
-        k_batch<kShortUnits, kShortSlots><<<plan.grid, kBatchThreads,
-                                            short_smem_bytes<kShortUnits, kShortSlots>(), stream>>>(a);
-    return cudaGetLastError();
+    const ShapeInfo info = shape(k);
+    void *args[] = {&a};
+    return cudaLaunchKernel(info.kernel, dim3(plan.grid), dim3(kBatchThreads), args, info.smem,
+                            stream);
 }
 
 }  // namespace tb

@@ -77,8 +77,9 @@ struct tb_ctx {
     std::vector<Slot> slots;
     void *slot_status = nullptr;      // host-mapped status words, one per slot
     uint32_t next_slot = 0;
-    int batch_grid_long = 0;          // batch-kernel CTAs resident at once (one wave),
-    int batch_grid_short = 0;         // with long copies and with short copies only
+    // CTAs of one resident wave of each batch-kernel shape (0 = k_batch, a
+    // launch with long copies; 1.. = the k_short shapes of short-only ones).
+    int batch_grid[tb::kShortShapes + 1] = {};
     std::vector<WorkItem> longs;      // long copies of the run being packed
     tb_batch_stats last_batch{};
     std::vector<uint32_t> last_slots;  // slots the last batch launched on
@@ -201,6 +202,8 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "num_slots must be in [1, 64]");
     if (o.batch_min_copies < 0)
         return fail(ctx, TB_EINVAL, "batch_min_copies must be >= 0");
+    if (o.batch_short_shape < 0 || o.batch_short_shape > tb::kShortShapes)
+        return fail(ctx, TB_EINVAL, "batch_short_shape must be 0..%d", tb::kShortShapes);
     if (o.wait_timeout_ns == 0)
         return fail(ctx, TB_EINVAL, "wait_timeout_ns must be > 0");
     if (o.vec_bytes != 0 && o.vec_bytes != 4 && o.vec_bytes != 16 && o.vec_bytes != 32)
@@ -497,6 +500,7 @@ void tb_options_default(tb_options *o)
     o->validate_source = 0;
     o->check_overlap = 0;
     o->batch_min_copies = 0;
+    o->batch_short_shape = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -573,6 +577,7 @@ int tb_options_from_env(tb_options *o)
         env_i32("VALIDATE_SOURCE", &o->validate_source, &bad);
     env_i32("TB_CHECK_OVERLAP", &o->check_overlap, &bad);
     env_i32("TB_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
+    env_i32("TB_BATCH_SHORT_SHAPE", &o->batch_short_shape, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -662,12 +667,12 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     ctx->gate_status_dev = ctx->gate_flag_dev + 1;
     ctx->reduce_status_dev = ctx->gate_flag_dev + 2;
 
-    const int long_per_sm = tb::batch_ctas_per_sm(true);
-    const int short_per_sm = tb::batch_ctas_per_sm(false);
-    if (long_per_sm < 1 || short_per_sm < 1)
-        return bail(TB_ECUDA);
-    ctx->batch_grid_long = ctx->num_sms * long_per_sm;
-    ctx->batch_grid_short = ctx->num_sms * short_per_sm;
+    for (int k = 0; k <= tb::kShortShapes; ++k) {
+        const int per_sm = tb::batch_ctas_per_sm(k);
+        if (per_sm < 1)
+            return bail(TB_ECUDA);
+        ctx->batch_grid[k] = ctx->num_sms * per_sm;
+    }
     ctx->slots.resize(o.num_slots);
     const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items);
     void *status_dev = nullptr;
@@ -1342,8 +1347,11 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         }
         if (c.n_short + c.n_long > 0) {
             tb::BatchPlan plan;
-            const int full = c.n_long ? ctx->batch_grid_long : ctx->batch_grid_short;
-            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, full), slot.host, &plan);
+            const int shape = tb::short_shape_for(
+                c, o.batch_short_shape, (uint64_t)ctx->batch_grid[2] * (tb::kBatchThreads / 32));
+            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid[shape]),
+                             slot.host, &plan);
+            plan.shape = shape;
             ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
             // A small batch of short copies all assigned by warp index reads
             // its work list in place from the pinned staging: no upload and

@@ -126,7 +126,14 @@ struct BatchPlan {
     size_t prefix_offset;   // byte offsets of prefix[] and chunk_desc[]
     size_t chunk_offset;
     size_t upload_bytes;    // bytes of the packed buffer
+    int shape = 0;          // kernel: 0 = k_batch (long copies), 1.. = a k_short shape
 };
+
+// Shapes of the kernel of a launch of short copies only (k_short), numbered
+// 1..kShortShapes: 1 = four 2 KiB slots per warp, 3 CTAs per SM (deeper
+// rings, for batches of more copies than one round of warps); 2 = two 2 KiB
+// slots, 5 CTAs per SM (more warps, each copy in the first round).
+constexpr int kShortShapes = 2;
 
 // Start of chunk c of `chunks` equal chunks of a `total`-byte stream, on a
 // 64-byte offset; chunk `chunks` starts at total.
@@ -149,8 +156,13 @@ int count_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, BatchCou
 // buf (after the header) and the long ones to `longs` (room for n).
 int gather_batch(const tb_copy_desc *desc, size_t n, uint64_t small_max, uint64_t ce_min,
                  void *buf, WorkItem *longs, BatchCounts *c, size_t *bad);
-// CTAs for a batch: kBatchWaves full waves at most, fewer for small batches.
+// CTAs for a batch: kBatchWaves full waves at most, fewer for small batches;
+// full_grid = the CTAs of one wave of the launch's kernel shape.
 int batch_grid(const BatchCounts &c, int full_grid);
+// Kernel shape of a launch: 0 (k_batch) when it has long copies, else
+// `forced` when it names a k_short shape, else shape 2 when every short copy
+// gets a warp of shape 2's first wave (wide_warps of them), else shape 1.
+int short_shape_for(const BatchCounts &c, int forced, uint64_t wide_warps);
 // Completes a buffer gather_batch filled: header, long copies, prefix and
 // chunk table; fills *out.
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out);
@@ -185,8 +197,8 @@ int resident_ctas(const void *kernel, int threads, size_t smem);
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
                          uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull);
 
-// CTAs resident per SM for the batch kernel of a launch with long copies
-// (with_long) or of one with short copies only.
-int batch_ctas_per_sm(bool with_long);
+// CTAs resident per SM for kernel shape k (0 = k_batch, 1..kShortShapes =
+// k_short); 0 for an unknown shape or when a CUDA call fails.
+int batch_ctas_per_sm(int k);
 
 }  // namespace tb

@@ -118,6 +118,15 @@ int batch_grid(const BatchCounts &c, int full_grid)
     return (int)std::min<uint64_t>(std::min<uint64_t>((uint64_t)full_grid * waves, kMaxChunks), want);
 }
 
+int short_shape_for(const BatchCounts &c, int forced, uint64_t wide_warps)
+{
+    if (c.n_long > 0)
+        return 0;
+    if (forced >= 1 && forced <= kShortShapes)
+        return forced;
+    return c.n_short <= wide_warps ? 2 : 1;
+}
+
 void finish_batch(const BatchCounts &c, const WorkItem *longs, int grid, void *buf, BatchPlan *out)
 {
     char *base = static_cast<char *>(buf);

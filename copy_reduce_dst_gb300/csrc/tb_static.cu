@@ -64,13 +64,12 @@ alignas(4096) volatile uint32_t g_status[1024];
 bool g_status_mapped = false;
 
 // Per-device set-up: the scratch array's device address, the device's view
-// of its status word, the limit of each bounded wait, and the full grid of a
-// launch with long copies and of one with short copies only.
+// of its status word, the limit of each bounded wait, and the CTAs of one
+// resident wave of each batch-kernel shape.
 WorkItem *g_dev_items[kMaxDevices];
 uint32_t *g_dev_status[kMaxDevices];
 uint64_t g_dev_wait_ns[kMaxDevices];
-int g_dev_grid_long[kMaxDevices];
-int g_dev_grid_short[kMaxDevices];
+int g_dev_grid[kMaxDevices][tb::kShortShapes + 1];
 
 int setup_current_device(int *device)
 {
@@ -94,10 +93,13 @@ int setup_current_device(int *device)
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
         return TB_ECUDA;
-    const int long_per_sm = tb::batch_ctas_per_sm(true);
-    const int short_per_sm = tb::batch_ctas_per_sm(false);
-    if (long_per_sm < 1 || short_per_sm < 1)
-        return TB_ECUDA;
+    int grid[tb::kShortShapes + 1];
+    for (int k = 0; k <= tb::kShortShapes; ++k) {
+        const int per_sm = tb::batch_ctas_per_sm(k);
+        if (per_sm < 1)
+            return TB_ECUDA;
+        grid[k] = std::min(kMaxGrid, sms * per_sm);
+    }
     // The wait limit follows the contexts' default (environment variable
     // TB_KERNEL_WAIT_NS, else 2 s), read once here.
     tb_options o;
@@ -105,8 +107,8 @@ int setup_current_device(int *device)
     if (tb_options_from_env(&o) != TB_OK)
         return TB_EINVAL;
     g_dev_wait_ns[*device] = o.kernel_wait_ns;
-    g_dev_grid_long[*device] = std::min(kMaxGrid, sms * long_per_sm);
-    g_dev_grid_short[*device] = std::min(kMaxGrid, sms * short_per_sm);
+    for (int k = 0; k <= tb::kShortShapes; ++k)
+        g_dev_grid[*device][k] = grid[k];
     g_dev_status[*device] = static_cast<uint32_t *>(status) + *device;
     g_status[*device] = 0u;
     g_dev_items[*device] = static_cast<WorkItem *>(ptr);
@@ -156,8 +158,11 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
     // counter the kernel claims short copies from.
     tb::gather_batch(desc, n, kSmallMax, 0, g_host_items, g_longs, &c, nullptr);
     tb::BatchPlan plan;
-    const int full = c.n_long ? g_dev_grid_long[device] : g_dev_grid_short[device];
-    tb::finish_batch(c, g_longs, tb::batch_grid(c, full), g_host_items, &plan);
+    const int shape =
+        tb::short_shape_for(c, 0, (uint64_t)g_dev_grid[device][2] * (tb::kBatchThreads / 32));
+    tb::finish_batch(c, g_longs, tb::batch_grid(c, g_dev_grid[device][shape]), g_host_items,
+                     &plan);
+    plan.shape = shape;
     // The copy from pageable host memory returns once the bytes are staged,
     // so the host area is free again when this call returns.
     WorkItem *items = g_dev_items[device];

@@ -68,6 +68,7 @@ class Options(ct.Structure):
         ("validate_source", _i32),
         ("check_overlap", _i32),
         ("batch_min_copies", _i32),
+        ("batch_short_shape", _i32),
     ]
 
 

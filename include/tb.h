@@ -190,6 +190,13 @@ typedef struct {
        descriptor on `stream` instead of a kernel launch (counted in
        tb_batch_stats.ce_copies).  0 = always the kernel.  Default 0. */
     int32_t batch_min_copies;
+    /* Batched copy: the kernel shape of a launch of short copies only (the
+       per-warp ring of shared-memory slots and the CTAs kept per SM):
+       1 = four 2 KiB slots per warp, 3 CTAs per SM; 2 = two 2 KiB slots,
+       5 CTAs per SM; 0 = the library's choice (2 when every copy gets a warp
+       of one wave of shape 2, else 1).  Launches with long copies are not
+       affected.  Default 0. */
+    int32_t batch_short_shape;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -203,7 +210,7 @@ void tb_options_default(tb_options *opt);
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
      TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP, TB_BATCH_COPY_MIN
-     (batch_min_copies).
+     (batch_min_copies), TB_BATCH_SHORT_SHAPE.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);

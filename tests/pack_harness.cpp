@@ -54,6 +54,16 @@ extern "C" int harness_overlap(const tb_copy_desc *desc, size_t n, uint64_t *pai
     return found ? 1 : 0;
 }
 
+extern "C" int harness_short_shape(uint64_t n_short, uint64_t n_long, int forced,
+                                   uint64_t wide_warps)
+{
+    tb::BatchCounts c{};
+    c.n_short = n_short;
+    c.n_long = n_long;
+    c.descs = n_short + n_long;
+    return tb::short_shape_for(c, forced, wide_warps);
+}
+
 extern "C" uint64_t harness_chunk_start(uint64_t total, uint64_t chunks, uint64_t c)
 {
     return tb::chunk_start(total, chunks, c);

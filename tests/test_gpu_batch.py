@@ -350,6 +350,21 @@ def test_pipeline_wait_expiry_is_reported(tb):
         run_layout(tb, c, layout, 62)
 
 
+@pytest.mark.parametrize("shape", [1, 2])
+@pytest.mark.parametrize("seed", range(3))
+def test_short_only_shapes(tb, shape, seed):
+    """Each k_short shape forced on batches of short copies only: any byte
+    alignment (src and dst equal modulo 16 go through the warp's ring, other
+    pairs through the shifted path), 0 to 16 KiB, and the 3840-page shape;
+    whole pools byte-exact against the oracle."""
+    with tb.Context(0, tb.options(batch_short_shape=shape)) as c:
+        run_layout(tb, c, workloads.random_batch(700 + seed, 5000, 16384, 64 * MiB, align=1), seed)
+        run_layout(tb, c, workloads.random_batch(710 + seed, 3000, 4096, 16 * MiB, align=16),
+                   seed + 5, src_shift=seed, dst_shift=seed)
+        st = run_layout(tb, c, workloads.batch_index_pages(seed), seed + 9)
+        assert st["warp_items"] == 3840
+
+
 # ---------------------------------------------------------------------------
 # Beside compute (Mooncake RFC, "Design of #5040", interference with compute
 # on the sending GPU; "Motivation", small copies under a bf16 GEMM)

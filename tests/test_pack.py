@@ -30,6 +30,8 @@ def harness(tmp_path_factory):
     lib.harness_bad.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_void_p]
     lib.harness_overlap.restype = ct.c_int
     lib.harness_overlap.argtypes = [ct.c_void_p, ct.c_size_t, ct.c_void_p]
+    lib.harness_short_shape.restype = ct.c_int
+    lib.harness_short_shape.argtypes = [ct.c_uint64, ct.c_uint64, ct.c_int, ct.c_uint64]
     return lib
 
 
@@ -180,6 +182,16 @@ def test_grid_claim_items_and_coverage(harness, n, long_n, expect_grid, expect_c
     assert p["grid"] == expect_grid and p["claim"] == expect_claim
     fixed, counted = short_assignment(n, p["grid"], p["chunks"], p["claim"])
     assert sorted(fixed + counted) == list(range(n))
+
+
+@pytest.mark.parametrize("n_short,n_long,forced,shape", [
+    (3840, 0, 0, 2), (6080, 0, 0, 2), (6081, 0, 0, 1), (47520, 0, 0, 1), (1, 0, 0, 2),
+    (3840, 0, 1, 1), (47520, 0, 2, 2), (47520, 20, 1, 0), (0, 3, 2, 0), (3840, 0, 9, 2)])
+def test_short_shape_choice(harness, n_short, n_long, forced, shape):
+    """Launches with long copies run k_batch (shape 0); short-only ones take a
+    forced shape, else the wide shape 2 when every copy gets a warp of its
+    first wave (152 SMs x 5 CTAs x 8 warps = 6080 here), else shape 1."""
+    assert harness.harness_short_shape(n_short, n_long, forced, 6080) == shape
 
 
 def _conflict(d, i, j):
