@@ -1271,7 +1271,7 @@ def profile_target(kind, args, tb, torch, local):
         return 0
     else:
         from copy_reduce_dst_gb300 import workloads
-        layout = workloads.batch_head_sliced()
+        layout = workloads.batch_head_sliced(pool_bytes=args.pool_gib * GiB)
         src = device_random_bytes(torch, layout.src_pool_bytes, 41)
         dst = device_random_bytes(torch, layout.dst_pool_bytes, 42)
         desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
@@ -1303,6 +1303,9 @@ def main():
     ap.add_argument("--mib", type=int, default=16, help="--profile rotation: transfer MiB")
     ap.add_argument("--rotate-mib", type=int, default=256,
                     help="--profile rotation: SRC_ROTATE_BYTES in MiB (0 = off)")
+    ap.add_argument("--pool-gib", type=int, default=2,
+                    help="--profile batch / batch-short: size of each pool of the 47,540 "
+                         "layout in GiB (a smaller case for full ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
