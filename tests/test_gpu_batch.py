@@ -365,6 +365,17 @@ def test_short_only_shapes(tb, shape, seed):
         assert st["warp_items"] == 3840
 
 
+@pytest.mark.parametrize("shape,n", [(2, 20000), (1, 500), (2, 1)])
+def test_short_only_shapes_claims_and_few_copies(tb, shape, n):
+    """A forced shape past the copies its warps take by index (shape 2 with
+    20,000 copies: the rest claimed from the counter), with fewer copies
+    than warps (shape 1, 500 copies), and a single copy."""
+    with tb.Context(0, tb.options(batch_short_shape=shape)) as c:
+        layout = workloads.random_batch(720 + n, n, 4096, 96 * MiB, align=1, min_len=1)
+        st = run_layout(tb, c, layout, n)
+        assert st["warp_items"] == n
+
+
 # ---------------------------------------------------------------------------
 # Beside compute (Mooncake RFC, "Design of #5040", interference with compute
 # on the sending GPU; "Motivation", small copies under a bf16 GEMM)

@@ -7,8 +7,12 @@ support must be refused with TB_ENOTSUP, everything else must be bit-exact
 with dstReference and leave the guard bytes around dst untouched.
 Batched copy: 0-3000 copies of 0 B - 256 KiB at any byte alignment, with the
 short/long threshold, slot size and count, copy-count and copy-engine
-routing drawn at random; the whole destination pool must equal the oracle's
-apply of the batch.  The seeds are fixed, so a failure names its case."""
+routing and the short-only kernel shape drawn at random; the whole
+destination pool must equal the oracle's apply of the batch.
+DMA executor: one source of 1-300,000 elements in K = 1-9 rotation slices
+filled with different patterns, byte offset, warm-up, iterations, graph or
+gate drawn at random; dst must equal the slice of the last iteration.
+The seeds are fixed, so a failure names its case."""
 import numpy as np
 import pytest
 
@@ -96,7 +100,9 @@ def test_batch_fuzz(tb, seed):
                 slot_items=int(g.choice([1024, 4096, 65536])),
                 num_slots=int(g.choice([1, 2, 4])),
                 batch_min_copies=int(g.choice([0, 0, 3])),
-                ce_min_bytes=int(g.choice([0, 0, 0, 1 << 17])))
+                ce_min_bytes=int(g.choice([0, 0, 0, 1 << 17])),
+                # own generator, so the cases above stay as they were
+                batch_short_shape=int(np.random.default_rng(9000 + seed).choice([0, 0, 1, 2])))
     src_h = workloads.random_bytes(pool, 7000 + seed)
     dst_h = workloads.random_bytes(pool, 8000 + seed)
     src_d, dst_d = to_dev(src_h), to_dev(dst_h)
@@ -112,3 +118,31 @@ def test_batch_fuzz(tb, seed):
     oracle.apply_batch(exp, src_h, so, do, lens)
     mm = oracle.first_mismatch(to_host(dst_d), exp)
     assert mm == -1, f"seed {seed} {opts} n {n}: first differing byte {mm}"
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_dma_executor_fuzz(tb, seed):
+    g = np.random.default_rng(11000 + seed)
+    n = int(g.choice([1, 3, 64, int(g.integers(1, 300000))]))
+    nb = 4 * n
+    K = int(g.integers(1, 10))
+    iters = int(g.integers(1, 12))
+    off = int(g.choice([0, 0, 4, 20, 256]))
+    opts = dict(byte_offset=off, warmup=int(g.integers(0, 4)), use_graph=int(g.choice([0, 1])),
+                use_gate=int(g.choice([0, 1])))
+    plan = tb.rotation_plan(nb, K * nb if K > 1 else 0, off)
+    assert plan.K == K
+    src = dev_bytes(plan.alloc_bytes, fill=0x11)
+    slices = [finite_floats(g, n) for _ in range(K)]
+    for j, a in enumerate(slices):
+        start = off + j * plan.slice_stride
+        src[start:start + nb].copy_(to_dev(a))
+    dst = dev_bytes(nb + off + 128, fill=0xC3)
+    last = oracle.slice_for_iteration(iters - 1, K)
+    with tb.Context(0, tb.options(**opts)) as c:
+        r = c.run_transfer([src], dst, nb, iters=iters, rotate_bytes=K * nb if K > 1 else 0,
+                           expected=slices[last], executor=tb.TB_EXEC_DMA)
+    assert r["mismatch_index"] == -1 and r["executor"] == tb.TB_EXEC_DMA, (seed, opts)
+    got = to_host(dst)
+    assert np.array_equal(got[off:off + nb].view(np.uint32), slices[last].view(np.uint32))
+    assert np.all(got[:off] == 0xC3) and np.all(got[off + nb:] == 0xC3)
