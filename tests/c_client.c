@@ -3,10 +3,12 @@
  *   c_client <out_dir>
  *
  * Allocates with the CUDA runtime, fills three 16 MiB sources with the
- * default pattern, runs one 3-source reduce-copy and one batch of 1000
- * scattered copies, and writes what came back to <out_dir>/reduce.bin (the
- * destination) and <out_dir>/batch.bin (the destination pool), for the
- * caller to compare with the oracle.  The batch layout is fixed arithmetic:
+ * default pattern, runs one 3-source reduce-copy, a 2-iteration transfer of
+ * source 1 on the copy engines (DMA executor), and one batch of 1000
+ * scattered copies through tb_batch_copy and again through
+ * tb_batch_copy_noalloc, and writes what came back to <out_dir>/reduce.bin,
+ * dma.bin, batch.bin and batch_noalloc.bin, for the caller to compare with
+ * the oracle.  The batch layout is fixed arithmetic:
  * copy i moves 64 + 13 * i bytes from source offset 16384 * i + i % 13 to
  * destination offset 16384 * ((i * 7919) % 1000) + i % 5 (distinct 16 KiB
  * slots, so no two destinations overlap).  Exit status 0 on
@@ -83,6 +85,29 @@ int main(int argc, char **argv)
     if (write_file(argv[1], "reduce.bin", host, nb))
         return 1;
 
+    /* DMA executor: dst2 = src[1], one copy-engine copy per iteration. */
+    void *dst2 = NULL;
+    CHECK_CUDA(cudaMalloc(&dst2, nb));
+    CHECK_CUDA(cudaMemset(dst2, 0, nb));
+    tb_transfer t;
+    memset(&t, 0, sizeof t);
+    t.srcs = &src[1];
+    t.n_src = 1;
+    t.dst = dst2;
+    t.num_bytes = nb;
+    t.iters = 2;
+    t.rotate_bytes = 0;
+    t.executor = TB_EXEC_DMA;
+    tb_result res;
+    CHECK_TB(tb_run_transfer_ex(ctx, &t, &res));
+    if (res.executor != TB_EXEC_DMA || res.iters != 2) {
+        fprintf(stderr, "DMA result: executor %d, iters %d\n", (int)res.executor, (int)res.iters);
+        return 1;
+    }
+    CHECK_CUDA(cudaMemcpy(host, dst2, nb, cudaMemcpyDeviceToHost));
+    if (write_file(argv[1], "dma.bin", host, nb))
+        return 1;
+
     /* Batch copy from src[0] into a zeroed pool. */
     const size_t n = 1000;
     const uint64_t pool = 16384ull * 1000 + 64;
@@ -113,6 +138,21 @@ int main(int argc, char **argv)
     CHECK_CUDA(cudaMemcpy(hpool, dpool, pool, cudaMemcpyDeviceToHost));
     if (write_file(argv[1], "batch.bin", hpool, pool))
         return 1;
+
+    /* The same batch without any allocation, into a second zeroed pool. */
+    void *dpool2 = NULL;
+    CHECK_CUDA(cudaMalloc(&dpool2, pool));
+    CHECK_CUDA(cudaMemset(dpool2, 0, pool));
+    for (size_t i = 0; i < n; ++i)
+        desc[i].dst = (uint64_t)(uintptr_t)dpool2 + 16384 * ((i * 7919) % 1000) + i % 5;
+    CHECK_TB(tb_batch_copy_noalloc(desc, n, (tb_stream)s));
+    CHECK_CUDA(cudaStreamSynchronize(s));
+    CHECK_TB(tb_batch_copy_noalloc(NULL, 0, (tb_stream)s)); /* no expired wait to report */
+    CHECK_CUDA(cudaMemcpy(hpool, dpool2, pool, cudaMemcpyDeviceToHost));
+    if (write_file(argv[1], "batch_noalloc.bin", hpool, pool))
+        return 1;
+    CHECK_CUDA(cudaFree(dpool2));
+    CHECK_CUDA(cudaFree(dst2));
 
     free(desc);
     free(host);

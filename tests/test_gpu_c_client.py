@@ -1,7 +1,8 @@
 """libtb from C: tests/c_client.c, built with gcc against include/tb.h,
 libtb.so and the CUDA runtime only (no Python, no PyTorch in the client),
-runs a 3-source reduce-copy and a batch of 1000 scattered copies; both
-results must equal the oracle's."""
+runs a 3-source reduce-copy, a transfer on the copy engines (DMA executor)
+and a batch of 1000 scattered copies through tb_batch_copy and through
+tb_batch_copy_noalloc; every result must equal the oracle's."""
 import os
 import shutil
 import subprocess
@@ -39,6 +40,8 @@ def test_c_client_matches_the_oracle(tmp_path):
     refs = [oracle.prepare_reference(n, k) for k in range(3)]
     got = np.fromfile(tmp_path / "reduce.bin", dtype=np.float32)
     assert oracle.first_mismatch(got.view(np.uint32), oracle.dst_reference(refs).view(np.uint32)) == -1
+    got = np.fromfile(tmp_path / "dma.bin", dtype=np.float32)
+    assert oracle.first_mismatch(got.view(np.uint32), refs[1].view(np.uint32)) == -1
 
     i = np.arange(1000, dtype=np.uint64)
     src_off = 16384 * i + i % 13
@@ -46,5 +49,6 @@ def test_c_client_matches_the_oracle(tmp_path):
     lens = 64 + 13 * i
     pool = np.zeros(16384 * 1000 + 64, dtype=np.uint8)
     oracle.apply_batch(pool, refs[0].view(np.uint8), src_off, dst_off, lens)
-    got = np.fromfile(tmp_path / "batch.bin", dtype=np.uint8)
-    assert oracle.first_mismatch(got, pool) == -1
+    for name in ("batch.bin", "batch_noalloc.bin"):
+        got = np.fromfile(tmp_path / name, dtype=np.uint8)
+        assert oracle.first_mismatch(got, pool) == -1, name
