@@ -100,12 +100,14 @@ int setup_current_device(int *device)
             return TB_ECUDA;
         grid[k] = std::min(kMaxGrid, sms * per_sm);
     }
-    // The wait limit follows the contexts' default (environment variable
-    // TB_KERNEL_WAIT_NS, else 2 s), read once here.
+    // The wait limit follows the contexts' default: environment variable
+    // TB_KERNEL_WAIT_NS (parsed like the contexts' options), else 2 s, read
+    // once here.  No other variable is read.
     tb_options o;
     tb_options_default(&o);
-    if (tb_options_from_env(&o) != TB_OK)
-        return TB_EINVAL;
+    if (const char *v = getenv("TB_KERNEL_WAIT_NS"))
+        if (tb_parse_bytes(v, &o.kernel_wait_ns) != TB_OK)
+            return TB_EINVAL;
     g_dev_wait_ns[*device] = o.kernel_wait_ns;
     for (int k = 0; k <= tb::kShortShapes; ++k)
         g_dev_grid[*device][k] = grid[k];

@@ -543,7 +543,8 @@ int tb_copy_each(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream stre
    returns TB_ETIMEOUT, clears the word and enqueues nothing.  To learn
    whether a given batch completed, synchronize its stream and then call
    with n == 0, which copies nothing and only reports (and clears) the word.
-   Errors: TB_EINVAL for a null or wrapping range; TB_ENOTSUP when the batch
+   Errors: TB_EINVAL for a null or wrapping range, or on the first call on
+   a device when TB_KERNEL_WAIT_NS does not parse; TB_ENOTSUP when the batch
    has more than TB_NOALLOC_MAX_ITEMS descriptors with len > 0, or when
    `stream` is capturing work into a graph (the work list is copied from a
    host array that the next call rewrites); TB_ETIMEOUT as above; TB_ECUDA
