@@ -34,9 +34,10 @@ events per launch), the fillCompress sweep with rotation on and off (cold,
 warm, graphed), validation on the device against the host, end to end from
 pinned and pageable host memory, tiny batches against per-copy memcpy,
 small copies under a GEMM loop (normal and high-priority stream), the three
-batch workloads, the batch's long and short parts, copy-engine routing, and
-GEMM interference.  ``--profile reduce|batch|batch-short|batch-small|
-rotation`` runs one workload for an ncu capture (commands in ``profiles/``).
+batch workloads, the batch's long and short parts, copy-engine routing, GEMM
+interference, and GEMM interference with the batch kernel's grid capped.
+``--profile reduce|batch|batch-short|batch-small|rotation`` runs one
+workload for an ncu capture (commands in ``profiles/``).
 """
 from __future__ import annotations
 
@@ -854,6 +855,7 @@ def study(args, tb, torch, local):
     study_batch_phases(tb, torch, local)
     study_batch_routing(tb, torch, local)
     study_interference(tb, torch, local)
+    study_grid_cap(tb, torch, local)
 
 
 def study_batch_routing(tb, torch, local):
@@ -946,6 +948,68 @@ def study_interference(tb, torch, local):
                           "gemm_loss_pct": round(100 * (1 - tf / alone), 2),
                           "loss_pct_per_100gbps": round(100 * (1 - tf / alone) / max(gbps, 1e-9) * 100, 3)}),
               flush=True)
+
+
+def study_grid_cap(tb, torch, local):
+    """The Mooncake RFC's open question 4 (a CU mask or rate limit for GPUs
+    that also compute): an 8192^3 bf16 GEMM loop on one stream while the
+    47,540 batch is copied back to back on another, with the batch kernel's
+    grid capped at `batch_max_ctas` CTAs (none, 304, 152, 64, 32).  GEMM
+    TFLOP/s, copy GB/s and the GEMM's loss per 100 GB/s of copies."""
+    from copy_reduce_dst_gb300 import workloads
+    n = 8192
+    a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
+    flops = 2 * n ** 3
+    reps = 900  # ~0.5 s of GEMMs alone
+    layout = workloads.batch_head_sliced()
+    src = device_random_bytes(torch, layout.src_pool_bytes, 61)
+    dst = device_random_bytes(torch, layout.dst_pool_bytes, 62)
+    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    gemm_s = torch.cuda.Stream()
+    copy_s = torch.cuda.Stream()
+
+    def loop():
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(gemm_s)
+        with torch.cuda.stream(gemm_s):
+            for _ in range(reps):
+                torch.matmul(a, b, out=c)
+        e1.record(gemm_s)
+        return e0, e1
+
+    with torch.cuda.stream(gemm_s):
+        for _ in range(20):
+            torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    e0, e1 = loop()
+    torch.cuda.synchronize()
+    alone = reps * flops / (e0.elapsed_time(e1) / 1e3) / 1e12
+    print(json.dumps({"study": "grid cap", "cap": "no copies", "gemm_tflops": round(alone, 1)}),
+          flush=True)
+    for cap in (0, 304, 152, 64, 32):
+        with tb.Context(local, ctx_options(tb, batch_max_ctas=cap)) as ctx:
+            ctx.batch_copy(desc, copy_s)
+            copy_s.synchronize()
+            e0, e1 = loop()
+            batches, t0 = 0, time.perf_counter()
+            while not e1.query():
+                ctx.batch_copy(desc, copy_s)
+                copy_s.synchronize()
+                batches += 1
+            wall = time.perf_counter() - t0
+            torch.cuda.synchronize()
+        tf = reps * flops / (e0.elapsed_time(e1) / 1e3) / 1e12
+        gbps = 2 * layout.total_bytes * batches / wall / 1e9
+        loss = 100 * (1 - tf / alone)
+        print(json.dumps({"study": "grid cap", "cap": cap or "none", "gemm_tflops": round(tf, 1),
+                          "copy_gbps": round(gbps, 1), "gemm_loss_pct": round(loss, 2),
+                          "loss_pct_per_100gbps": round(loss / max(gbps, 1e-9) * 100, 3)}),
+              flush=True)
+    del a, b, c, src, dst
+    torch.cuda.empty_cache()
 
 
 def study_small_copies_under_compute(tb, torch, local):

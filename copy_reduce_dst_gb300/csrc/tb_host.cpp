@@ -204,6 +204,8 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "batch_min_copies must be >= 0");
     if (o.batch_short_shape < 0 || o.batch_short_shape > tb::kShortShapes)
         return fail(ctx, TB_EINVAL, "batch_short_shape must be 0..%d", tb::kShortShapes);
+    if (o.batch_max_ctas < 0)
+        return fail(ctx, TB_EINVAL, "batch_max_ctas must be >= 0");
     if (o.wait_timeout_ns == 0)
         return fail(ctx, TB_EINVAL, "wait_timeout_ns must be > 0");
     if (o.vec_bytes != 0 && o.vec_bytes != 4 && o.vec_bytes != 16 && o.vec_bytes != 32)
@@ -501,6 +503,7 @@ void tb_options_default(tb_options *o)
     o->check_overlap = 0;
     o->batch_min_copies = 0;
     o->batch_short_shape = 0;
+    o->batch_max_ctas = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -578,6 +581,7 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_CHECK_OVERLAP", &o->check_overlap, &bad);
     env_i32("TB_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
     env_i32("TB_BATCH_SHORT_SHAPE", &o->batch_short_shape, &bad);
+    env_i32("TB_BATCH_MAX_CTAS", &o->batch_max_ctas, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -1349,8 +1353,10 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             tb::BatchPlan plan;
             const int shape = tb::short_shape_for(
                 c, o.batch_short_shape, (uint64_t)ctx->batch_grid[2] * (tb::kBatchThreads / 32));
-            tb::finish_batch(c, ctx->longs.data(), tb::batch_grid(c, ctx->batch_grid[shape]),
-                             slot.host, &plan);
+            int grid = tb::batch_grid(c, ctx->batch_grid[shape]);
+            if (o.batch_max_ctas > 0 && grid > o.batch_max_ctas)
+                grid = o.batch_max_ctas;
+            tb::finish_batch(c, ctx->longs.data(), grid, slot.host, &plan);
             plan.shape = shape;
             ctx->next_slot = (ctx->next_slot + 1) % (uint32_t)ctx->slots.size();
             // A small batch of short copies all assigned by warp index reads

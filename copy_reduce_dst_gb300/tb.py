@@ -69,6 +69,7 @@ class Options(ct.Structure):
         ("check_overlap", _i32),
         ("batch_min_copies", _i32),
         ("batch_short_shape", _i32),
+        ("batch_max_ctas", _i32),
     ]
 
 

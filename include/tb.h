@@ -197,6 +197,11 @@ typedef struct {
        of one wave of shape 2, else 1).  Launches with long copies are not
        affected.  Default 0. */
     int32_t batch_short_shape;
+    /* Batched copy: most CTAs one kernel launch may use (0 = no cap), the
+       analogue of the CU mask the Mooncake RFC's open question 4 asks about
+       for GPUs that also run compute.  Fewer CTAs copy more slowly and take
+       fewer SMs at once; results do not change.  Default 0. */
+    int32_t batch_max_ctas;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -210,7 +215,7 @@ void tb_options_default(tb_options *opt);
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
      TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP, TB_BATCH_COPY_MIN
-     (batch_min_copies), TB_BATCH_SHORT_SHAPE.
+     (batch_min_copies), TB_BATCH_SHORT_SHAPE, TB_BATCH_MAX_CTAS.
    Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
    partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);

@@ -101,6 +101,7 @@ def test_options_defaults(tb):
     assert o.use_graph == 1 and o.reduce_engine == 0 and o.ce_min_bytes == 0 and o.use_pdl == 1
     assert o.time_kernels == 0 and o.vec_bytes == 0 and o.unroll == 0
     assert o.kernel_wait_ns == 2_000_000_000 and o.validate_direct == 0 and o.validate_source == 0
+    assert o.batch_short_shape == 0 and o.batch_max_ctas == 0
 
 
 def test_options_struct_matches_header(tb):
@@ -144,9 +145,12 @@ def test_options_env_new_fields(tb, monkeypatch):
     monkeypatch.setenv("TB_CE_MIN_BYTES", "1MiB")
     monkeypatch.setenv("TB_USE_PDL", "0")
     monkeypatch.setenv("TB_KERNEL_WAIT_NS", "0")
+    monkeypatch.setenv("TB_BATCH_SHORT_SHAPE", "2")
+    monkeypatch.setenv("TB_BATCH_MAX_CTAS", "64")
     o = tb.options_from_env()
     assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
     assert o.use_pdl == 0 and o.kernel_wait_ns == 0
+    assert o.batch_short_shape == 2 and o.batch_max_ctas == 64
 
 
 def test_validation_options_from_env(tb, monkeypatch):

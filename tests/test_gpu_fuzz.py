@@ -7,8 +7,8 @@ support must be refused with TB_ENOTSUP, everything else must be bit-exact
 with dstReference and leave the guard bytes around dst untouched.
 Batched copy: 0-3000 copies of 0 B - 256 KiB at any byte alignment, with the
 short/long threshold, slot size and count, copy-count and copy-engine
-routing and the short-only kernel shape drawn at random; the whole
-destination pool must equal the oracle's apply of the batch.
+routing, the short-only kernel shape and a cap on the CTAs drawn at random;
+the whole destination pool must equal the oracle's apply of the batch.
 DMA executor: one source of 1-300,000 elements in K = 1-9 rotation slices
 filled with different patterns, byte offset, warm-up, iterations, graph or
 gate drawn at random; dst must equal the slice of the last iteration.
@@ -102,7 +102,8 @@ def test_batch_fuzz(tb, seed):
                 batch_min_copies=int(g.choice([0, 0, 3])),
                 ce_min_bytes=int(g.choice([0, 0, 0, 1 << 17])),
                 # own generator, so the cases above stay as they were
-                batch_short_shape=int(np.random.default_rng(9000 + seed).choice([0, 0, 1, 2])))
+                batch_short_shape=int(np.random.default_rng(9000 + seed).choice([0, 0, 1, 2])),
+                batch_max_ctas=int(np.random.default_rng(9500 + seed).choice([0, 0, 0, 1, 7, 64])))
     src_h = workloads.random_bytes(pool, 7000 + seed)
     dst_h = workloads.random_bytes(pool, 8000 + seed)
     src_d, dst_d = to_dev(src_h), to_dev(dst_h)
