@@ -479,7 +479,10 @@ typedef struct {
    of at most small_max_bytes go to a warp each, streamed through that
    warp's ring of shared-memory slots by asynchronous 16-byte copies, the
    first ones fixed by warp index and the rest claimed four at a time by free
-   warps from a counter in the packed work list.  Addresses may also be
+   warps from a counter in the packed work list.  A launch of short copies
+   only runs a kernel without the long-copy path, in the ring shape that
+   batch_short_shape selects; batch_max_ctas caps the CTAs of any launch.
+   Addresses may also be
    pinned host memory mapped into the device's address space.  Destinations
    must not overlap one another or any source of the batch (the order of
    copies is unspecified).  TB_EINVAL for a null
