@@ -539,61 +539,73 @@ def run_rotation_sweep(tb, torch, local):
     return rows
 
 
-def run_small_batch(tb, torch, local, layout, seed):
-    """One of the Mooncake RFC's small-copy shapes on seeded random pools:
-    kernel_us = kernel-only events (median of 20); device_us = events around
-    30 back-to-back calls; wall_us = one call with packing, upload, kernel
-    and stream sync (median of 20); memcpy_each = one cudaMemcpyAsync per
-    copy, wall-timed the same way (best of 2)."""
+def run_small_batch(tb, torch, local, make_layout, seed, variants):
+    """One of the Mooncake RFC's small-copy shapes on seeded random pools.
+    A single batch of this shape touches less than the 129 MB L2, so the
+    calls cycle through `variants` layouts of the same shape (seeds seed,
+    seed + 1, ...; sources in separate regions when the source pool is
+    small), whose bytes together exceed L2: no call finds its data there.
+    kernel_us = kernel-only events (median of 40); device_us = events around
+    back-to-back calls (two passes over the variants); wall_us = one call
+    with packing, upload, kernel and stream sync (median of 40);
+    memcpy_each = one cudaMemcpyAsync per copy, wall-timed the same way
+    (best of 2, the first layout)."""
     import statistics as st
-    src = device_random_bytes(torch, layout.src_pool_bytes, seed)
-    dst = device_random_bytes(torch, layout.dst_pool_bytes, seed + 1)
-    desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
+    layouts = [make_layout(seed + r) for r in range(variants)]
+    lay0 = layouts[0]
+    own_src = lay0.src_pool_bytes * variants <= 1 << 30
+    src = device_random_bytes(torch, lay0.src_pool_bytes * (variants if own_src else 1), seed)
+    dst = device_random_bytes(torch, lay0.dst_pool_bytes, seed + 1000)
+    descs = [lay.descriptors(src.data_ptr() + (r * lay0.src_pool_bytes if own_src else 0),
+                             dst.data_ptr()) for r, lay in enumerate(layouts)]
+    touched = sum(2 * int(lay.total_bytes) for lay in layouts)
     stream = torch.cuda.Stream()
-    moved = 2 * int(layout.total_bytes)
+    moved = 2 * int(lay0.total_bytes)
     with tb.Context(local, ctx_options(tb, time_kernels=1)) as kctx, \
             tb.Context(local, ctx_options(tb)) as ctx:
-        for _ in range(3):
-            kctx.batch_copy(desc, stream)
+        for d in descs:
+            kctx.batch_copy(d, stream)
         kern = []
-        for _ in range(20):
-            kctx.batch_copy(desc, stream)
+        for i in range(40):
+            kctx.batch_copy(descs[i % variants], stream)
             kern.append(kctx.last_batch_kernel_ms())
-        for _ in range(3):
-            ctx.batch_copy(desc, stream)
+        for d in descs:
+            ctx.batch_copy(d, stream)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        calls = 2 * variants
         stream.synchronize()
         a.record(stream)
-        for _ in range(30):
-            ctx.batch_copy(desc, stream)
+        for i in range(calls):
+            ctx.batch_copy(descs[i % variants], stream)
         b.record(stream)
         b.synchronize()
-        dev_ms = a.elapsed_time(b) / 30
+        dev_ms = a.elapsed_time(b) / calls
         walls = []
-        for _ in range(20):
+        for i in range(40):
             t0 = time.perf_counter()
-            ctx.batch_copy(desc, stream)
+            ctx.batch_copy(descs[i % variants], stream)
             stream.synchronize()
             walls.append(time.perf_counter() - t0)
         each = []
         for _ in range(2):
             t0 = time.perf_counter()
-            ctx.copy_each(desc, stream)
+            ctx.copy_each(descs[0], stream)
             stream.synchronize()
             each.append(time.perf_counter() - t0)
         stats = kctx.last_batch_stats()
     k_ms = st.median(kern)
     wall = st.median(walls)
     del src, dst
-    return {"workload": layout.name + " (uint8 random from seed)", "descriptors": layout.n,
-            "bytes_copied": int(layout.total_bytes),
+    return {"workload": lay0.name + " (uint8 random from seed)", "descriptors": lay0.n,
+            "bytes_copied": int(lay0.total_bytes),
+            "variants": variants, "bytes_touched_per_cycle": touched,
             "kernel_us": round(k_ms * 1e3, 2),
             "kernel_gbps": round(moved / (k_ms / 1e3) / 1e9, 1),
             "device_us": round(dev_ms * 1e3, 2),
             "device_gbps": round(moved / (dev_ms / 1e3) / 1e9, 1),
-            "copies_per_s_device": round(layout.n / (dev_ms / 1e3), 1),
-            "wall_us": round(wall * 1e6, 1), "copies_per_s_wall": round(layout.n / wall, 1),
+            "copies_per_s_device": round(lay0.n / (dev_ms / 1e3), 1),
+            "wall_us": round(wall * 1e6, 1), "copies_per_s_wall": round(lay0.n / wall, 1),
             "memcpy_each_wall_ms": round(min(each) * 1e3, 3),
             "speedup_vs_memcpy_each": round(min(each) / wall, 1),
             "direct_launches": stats["direct_launches"]}
@@ -1401,10 +1413,10 @@ def main():
         extra["single_4mib_k64"] = run_single_transfer(tb, torch, local)
         extra["dma_executor_256mib"] = run_dma_large(tb, torch, local)
         extra["rotation_sweep"] = run_rotation_sweep(tb, torch, local)
-        extra["index_pages_3840"] = run_small_batch(tb, torch, local,
-                                                    workloads.batch_index_pages(), 31)
-        extra["block_pages_7200"] = run_small_batch(tb, torch, local,
-                                                    workloads.batch_block_pages(), 33)
+        extra["index_pages_3840"] = run_small_batch(tb, torch, local, workloads.batch_index_pages,
+                                                    31, 32)
+        extra["block_pages_7200"] = run_small_batch(tb, torch, local, workloads.batch_block_pages,
+                                                    33, 8)
         extra["interference"] = run_interference(tb, torch, local)
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
     if rank == 0:
