@@ -911,8 +911,8 @@ def study_interference(tb, torch, local):
     a = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
     b = torch.randn(n, n, dtype=torch.bfloat16, device="cuda")
     layout = workloads.batch_head_sliced()
-    src = torch.zeros(layout.src_pool_bytes, dtype=torch.uint8, device="cuda")
-    dst = torch.zeros(layout.dst_pool_bytes, dtype=torch.uint8, device="cuda")
+    src = device_random_bytes(torch, layout.src_pool_bytes, 63)
+    dst = device_random_bytes(torch, layout.dst_pool_bytes, 64)
     desc = layout.descriptors(src.data_ptr(), dst.data_ptr())
     gemm_s = torch.cuda.Stream()
     copy_s = torch.cuda.Stream()
