@@ -236,7 +236,16 @@ constexpr uint32_t kRStages = 3;      // stages of a CTA that shares its SM
 constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
 constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
-constexpr uint64_t kBulkMinBytes = 32ull << 20;  // auto engine: bulk from 32 MiB per source
+// Auto engine: bulk from 32 MiB per source, or 12 MiB for one source (a
+// relay with no adds).  Measured on GB300 (rotation on, 20 graphed
+// iterations, us per iteration, vector / bulk): 1 source 8 MiB 3.26 /
+// 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB 5.05-5.10 / 4.69, 24 MiB 8.79 /
+// 6.53; 3 sources 16 MiB 10.3 / 9.6 graphed but 15.0-15.2 / 16.1-16.4 with
+// events around every launch, 32 MiB 20.8 / 21.6 graphed.  With events
+// around every launch, or a single cold launch, one source ties at 8-16
+// MiB and favours bulk at 24 MiB (cold 16.0-17.0 / 14.0).
+constexpr uint64_t kBulkMinBytes = 32ull << 20;
+constexpr uint64_t kBulkMinBytesRelay = 12ull << 20;
 constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
 // Bytes per source of one tile.  With several sources the stages hold
@@ -590,7 +599,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
 
     // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
     // and works in 16-byte units.  It is the default from kBulkMinBytes per
-    // source up, where it keeps more bytes in flight per SM than per-thread
+    // source up (kBulkMinBytesRelay for one source), where it keeps more
+    // bytes in flight per SM than per-thread
     // vector loads; below that, its per-tile pipeline latency costs more
     // than it saves and the vector form is faster.  A CTA alone on its SM
     // with 2 to 4 sources is limited by the bulk form's per-tile adds and
@@ -603,8 +613,9 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
     const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 4;
+    const uint64_t bulk_min = n_src == 1 ? kBulkMinBytesRelay : kBulkMinBytes;
     p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
-                                 num_bytes >= kBulkMinBytes && !vector_alone))
+                                 num_bytes >= bulk_min && !vector_alone))
                     ? 2
                     : 1;
     if (p->engine == 2) {

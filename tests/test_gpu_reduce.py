@@ -207,6 +207,10 @@ def test_reduce_plan_engine_choice(tb, ctx):
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
     info = ctx.reduce_plan([p, p + 4096, p + 8192], far, big - 256)
     assert info["engine"] == 1                                    # small: vector loads
+    one = 12 << 20
+    assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: bulk from 12 MiB
+    assert ctx.reduce_plan([p], far, one - 256)["engine"] == 1
+    assert ctx.reduce_plan([p, p + 4096], far, one)["engine"] == 1  # two: from 32 MiB
     info = ctx.reduce_plan([p] * 5, far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
     info = ctx.reduce_plan([p + 4, p + 8], far, 4096)
@@ -252,8 +256,10 @@ def test_vector_grid_follows_the_work(tb, ctx):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     d = dev_bytes(64 << 20)
     p = d.data_ptr()
-    for nb in (4096, 4 << 20, 16 << 20, 24 << 20):
-        info = ctx.reduce_plan([p], p + (32 << 20), nb)
+    with tb.Context(0, tb.options(reduce_engine=1)) as vec:
+        infos = [vec.reduce_plan([p], p + (32 << 20), nb)
+                 for nb in (4096, 4 << 20, 16 << 20, 24 << 20)]
+    for info in infos:
         assert info["engine"] == 1
         rounds = -(-info["body_vectors"] // (info["block_threads"] * info["unroll"]))
         assert info["grid"] >= sms and (info["grid"] == sms or info["grid"] <= rounds)
