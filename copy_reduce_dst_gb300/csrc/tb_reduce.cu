@@ -236,16 +236,26 @@ constexpr uint32_t kRStages = 3;      // stages of a CTA that shares its SM
 constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
 constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
-// Auto engine: bulk from 32 MiB per source, or 12 MiB for one source (a
-// relay with no adds).  Measured on GB300 (rotation on, 20 graphed
-// iterations, us per iteration, vector / bulk): 1 source 8 MiB 3.26 /
-// 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB 5.05-5.10 / 4.69, 24 MiB 8.79 /
-// 6.53; 3 sources 16 MiB 10.3 / 9.6 graphed but 15.0-15.2 / 16.1-16.4 with
-// events around every launch, 32 MiB 20.8 / 21.6 graphed.  With events
-// around every launch, or a single cold launch, one source ties at 8-16
-// MiB and favours bulk at 24 MiB (cold 16.0-17.0 / 14.0).
-constexpr uint64_t kBulkMinBytes = 32ull << 20;
-constexpr uint64_t kBulkMinBytesRelay = 12ull << 20;
+// Auto engine: the bulk form from bulk_min_bytes(N) per source.  Measured
+// on GB300 (rotation on, 20 graphed iterations, us per iteration, vector /
+// bulk; per-launch events and single cold launches agree where noted):
+//   1 source   8 MiB 3.26 / 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB
+//              5.05-5.10 / 4.69, 24 MiB 8.79 / 6.53 (cold 16.0-17.0 / 14.0);
+//   2 sources  32 MiB 15.3 / 13.4, 64 MiB 29.0 / 30.7, 96 MiB 44.0 / 45.1,
+//              128 MiB 58.1 / 57.9, 192 MiB 90.0 / 86.1, 256 MiB 121.0 / 113.5;
+//   3 sources  32 MiB 20.8 / 21.6, 48 MiB 31.0 / 32.0 (cold 39.6 / 41.6),
+//              64 MiB 40.3 / 40.5, 128 MiB 77.5 / 76.3, 256 MiB 151.9 / 149.4;
+//   4 sources  32 MiB 26.4 / 28.0, 96 MiB 74.7 / 78.4, 192 MiB 145.9 / 148.9,
+//              256 MiB 192.9 / 193.7-198.5 (events and cold agree).
+// So: one source from 12 MiB, two from 32 MiB, three from 64 MiB, four
+// never by default (the bulk form stays available as reduce_engine = 2).
+__host__ __device__ constexpr uint64_t bulk_min_bytes(int n_src)
+{
+    return n_src == 1 ? 12ull << 20
+         : n_src == 2 ? 32ull << 20
+         : n_src == 3 ? 64ull << 20
+                      : UINT64_MAX;
+}
 constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
 // Bytes per source of one tile.  With several sources the stages hold
@@ -598,9 +608,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
                        (int64_t)num_subexec * ctas_per_subexec <= (int64_t)num_sms;
 
     // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
-    // and works in 16-byte units.  It is the default from kBulkMinBytes per
-    // source up (kBulkMinBytesRelay for one source), where it keeps more
-    // bytes in flight per SM than per-thread
+    // and works in 16-byte units.  It is the default from bulk_min_bytes per
+    // source up, where it keeps more bytes in flight per SM than per-thread
     // vector loads; below that, its per-tile pipeline latency costs more
     // than it saves and the vector form is faster.  A CTA alone on its SM
     // with 2 to 4 sources is limited by the bulk form's per-tile adds and
@@ -613,9 +622,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
     const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 4;
-    const uint64_t bulk_min = n_src == 1 ? kBulkMinBytesRelay : kBulkMinBytes;
     p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
-                                 num_bytes >= bulk_min && !vector_alone))
+                                 num_bytes >= bulk_min_bytes(n_src) && !vector_alone))
                     ? 2
                     : 1;
     if (p->engine == 2) {

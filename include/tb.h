@@ -130,9 +130,9 @@ typedef struct {
        2 = bulk copies (cp.async.bulk) through shared-memory stages with the
        adds done in shared memory (1 to 4 sources sharing a 16-byte
        alignment, else TB_ENOTSUP); 0 = the library's choice: 2 where it
-       applies, vec_bytes is 0 and each source has at least 32 MiB, or at
-       least 12 MiB for one source (below that the per-tile pipeline
-       latency outweighs its gain), else 1.
+       applies, vec_bytes is 0 and each source has at least 12 MiB (one
+       source), 32 MiB (two) or 64 MiB (three), else 1; four sources always
+       take 1, which measured faster at every size up to 256 MiB.
        Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy

@@ -203,14 +203,16 @@ def test_reduce_plan_engine_choice(tb, ctx):
     p = d.data_ptr()
     far = p + (1 << 36)
     big = 32 << 20
-    info = ctx.reduce_plan([p, p + 4096, p + 8192], far, big)
+    three = [p, p + 4096, p + 8192]
+    info = ctx.reduce_plan(three, far, 2 * big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
-    info = ctx.reduce_plan([p, p + 4096, p + 8192], far, big - 256)
-    assert info["engine"] == 1                                    # small: vector loads
+    assert ctx.reduce_plan(three, far, 2 * big - 256)["engine"] == 1  # three: from 64 MiB
+    assert ctx.reduce_plan(three[:2], far, big)["engine"] == 2      # two: from 32 MiB
+    assert ctx.reduce_plan(three[:2], far, big - 256)["engine"] == 1
     one = 12 << 20
-    assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: bulk from 12 MiB
+    assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: from 12 MiB
     assert ctx.reduce_plan([p], far, one - 256)["engine"] == 1
-    assert ctx.reduce_plan([p, p + 4096], far, one)["engine"] == 1  # two: from 32 MiB
+    assert ctx.reduce_plan(three + [p + 12288], far, 8 * big)["engine"] == 1  # four: vector
     info = ctx.reduce_plan([p] * 5, far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
     info = ctx.reduce_plan([p + 4, p + 8], far, 4096)
