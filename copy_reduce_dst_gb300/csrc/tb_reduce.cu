@@ -236,25 +236,37 @@ constexpr uint32_t kRStages = 3;      // stages of a CTA that shares its SM
 constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
 constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
-// Auto engine: the bulk form from bulk_min_bytes(N) per source.  Measured
-// on GB300 (rotation on, 20 graphed iterations, us per iteration, vector /
-// bulk; per-launch events and single cold launches agree where noted):
+// Auto engine: bulk_auto(N, bytes per source) picks the bulk form.
+// Measured on GB300 (20 graphed iterations, us per iteration, vector /
+// bulk; rotation on, and off where noted; per-launch events and single cold
+// launches agree where noted):
 //   1 source   8 MiB 3.26 / 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB
 //              5.05-5.10 / 4.69, 24 MiB 8.79 / 6.53 (cold 16.0-17.0 / 14.0);
-//   2 sources  32 MiB 15.3 / 13.4, 64 MiB 29.0 / 30.7, 96 MiB 44.0 / 45.1,
-//              128 MiB 58.1 / 57.9, 192 MiB 90.0 / 86.1, 256 MiB 121.0 / 113.5;
+//   2 sources  24 MiB 10.48 / 9.71, 32 MiB 14.4-15.3 / 13.4, 40 MiB 19.3 /
+//              19.3, 48 MiB 22.1 / 22.7, 64 MiB 28.6-29.0 / 30.7-31.1, 96 MiB
+//              43.8-44.1 / 45.0-45.4, 112 MiB 50.6 / 51.2, 128 MiB 58.1-58.3 /
+//              57.7-58.0, 160 MiB 73.4-73.9 / 71.8-72.2, 256 MiB 121.0 /
+//              113.5 (rotation off the same within 2%);
 //   3 sources  32 MiB 20.8 / 21.6, 48 MiB 31.0 / 32.0 (cold 39.6 / 41.6),
 //              64 MiB 40.3 / 40.5, 128 MiB 77.5 / 76.3, 256 MiB 151.9 / 149.4;
 //   4 sources  32 MiB 26.4 / 28.0, 96 MiB 74.7 / 78.4, 192 MiB 145.9 / 148.9,
 //              256 MiB 192.9 / 193.7-198.5 (events and cold agree).
-// So: one source from 12 MiB, two from 32 MiB, three from 64 MiB, four
-// never by default (the bulk form stays available as reduce_engine = 2).
-__host__ __device__ constexpr uint64_t bulk_min_bytes(int n_src)
+// So: one source from 12 MiB; two from 24 to 40 MiB and from 128 MiB;
+// three from 64 MiB; four never by default (the bulk form stays available
+// as reduce_engine = 2).
+constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
-    return n_src == 1 ? 12ull << 20
-         : n_src == 2 ? 32ull << 20
-         : n_src == 3 ? 64ull << 20
-                      : UINT64_MAX;
+    constexpr uint64_t MiB = 1ull << 20;
+    switch (n_src) {
+    case 1:
+        return bytes >= 12 * MiB;
+    case 2:
+        return (bytes >= 24 * MiB && bytes < 40 * MiB) || bytes >= 128 * MiB;
+    case 3:
+        return bytes >= 64 * MiB;
+    default:
+        return false;
+    }
 }
 constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
@@ -608,8 +620,9 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
                        (int64_t)num_subexec * ctas_per_subexec <= (int64_t)num_sms;
 
     // Engine: the bulk form needs 1..4 sources sharing a 16-byte alignment
-    // and works in 16-byte units.  It is the default from bulk_min_bytes per
-    // source up, where it keeps more bytes in flight per SM than per-thread
+    // and works in 16-byte units.  It is the default where bulk_auto says so
+    // (large enough transfers), where it keeps more bytes in flight per SM
+    // than per-thread
     // vector loads; below that, its per-tile pipeline latency costs more
     // than it saves and the vector form is faster.  A CTA alone on its SM
     // with 2 to 4 sources is limited by the bulk form's per-tile adds and
@@ -623,7 +636,7 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         return TB_ENOTSUP;
     const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 4;
     p->engine = (engine == 2 || (engine == 0 && bulk_ok && vec_bytes == 0 &&
-                                 num_bytes >= bulk_min_bytes(n_src) && !vector_alone))
+                                 bulk_auto(n_src, num_bytes) && !vector_alone))
                     ? 2
                     : 1;
     if (p->engine == 2) {

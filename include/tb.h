@@ -129,10 +129,11 @@ typedef struct {
     /* Reduce-copy engine: 1 = vector loads and stores by every thread;
        2 = bulk copies (cp.async.bulk) through shared-memory stages with the
        adds done in shared memory (1 to 4 sources sharing a 16-byte
-       alignment, else TB_ENOTSUP); 0 = the library's choice: 2 where it
-       applies, vec_bytes is 0 and each source has at least 12 MiB (one
-       source), 32 MiB (two) or 64 MiB (three), else 1; four sources always
-       take 1, which measured faster at every size up to 256 MiB.
+       alignment, else TB_ENOTSUP); 0 = the library's choice, by what
+       measured faster on GB300: 2 where it applies, vec_bytes is 0 and
+       each source holds at least 12 MiB (one source), 24 to 40 MiB or at
+       least 128 MiB (two), at least 64 MiB (three); else 1, and always 1
+       for four sources.
        Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy

@@ -207,8 +207,9 @@ def test_reduce_plan_engine_choice(tb, ctx):
     info = ctx.reduce_plan(three, far, 2 * big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
     assert ctx.reduce_plan(three, far, 2 * big - 256)["engine"] == 1  # three: from 64 MiB
-    assert ctx.reduce_plan(three[:2], far, big)["engine"] == 2      # two: from 32 MiB
-    assert ctx.reduce_plan(three[:2], far, big - 256)["engine"] == 1
+    two = three[:2]                                               # two: 24-40 MiB, >= 128 MiB
+    assert [ctx.reduce_plan(two, far, m << 20)["engine"] for m in (16, 24, 32, 40, 64, 127, 128)] \
+        == [1, 2, 2, 1, 1, 1, 2]
     one = 12 << 20
     assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: from 12 MiB
     assert ctx.reduce_plan([p], far, one - 256)["engine"] == 1
