@@ -15,12 +15,15 @@ Default line (rank 0 prints one JSON object):
             64 B-16 KiB + 16 x 16 MiB + 4 x 8 MiB) through tb_batch_copy,
             with one cudaMemcpyAsync per copy (tb_copy_each) timed beside it;
   single_4mib_k64, dma_executor_256mib, rotation_sweep, index_pages_3840,
-  block_pages_7200, interference
+  block_pages_7200, interference, multi_source_fill_compress,
+  validation_256mib
             the other configured workloads, a few seconds in all (leave
             them out with --no-extra): the 4 MiB K = 64 transfer on the
             kernel and on the copy engines, the DMA executor at 256 MiB,
             the fillCompress sweep 8-512 MiB with rotation on and off, the
-            3840- and 7200-page batches, and a bf16 GEMM beside the batches;
+            3840- and 7200-page batches, a bf16 GEMM beside the batches,
+            2-8 fillCompress sources, and validation on the device against
+            the host;
   roofline  achieved algorithmic GB/s of the reduce kernel against the
             measured HBM copy bandwidth (MEASURED_PEAKS.json);
   cpu_baseline  the CPU oracle on a bounded sample, one host core.
@@ -539,6 +542,32 @@ def run_rotation_sweep(tb, torch, local):
     return rows
 
 
+def run_multi_source_compress(tb, torch, local):
+    """Multi-source fillCompress reduce-copies (2, 4 and 8 sources of 64 MiB,
+    40/20/0/20/20 %, seed 0x5EED + k, rotation off): random floats with
+    zeroed bytes, so the adds meet subnormals and the order of the adds
+    decides the bits (bit-exactness is tested against the oracle).  GB/s
+    (read + write) of 20 graphed iterations, median of 3, and the engine."""
+    import statistics as st
+    nb = 64 * MiB
+    pct = (40, 20, 0, 20, 20)
+    rows = []
+    with tb.Context(local, ctx_options(tb)) as ctx:
+        srcs = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(8)]
+        for k, s_ in enumerate(srcs):
+            ctx.fill_source(s_, nb, tb.compress_pattern(pct, 0x5EED), k)
+        dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        for n in (2, 4, 8):
+            runs = [ctx.run_transfer(srcs[:n], dst, nb, iters=20, rotate_bytes=0)
+                    for _ in range(3)]
+            rows.append({"sources": n, "MiB_each": 64,
+                         "gbps": round(st.median(r["gbps"] for r in runs), 1),
+                         "engine": runs[0]["engine"], "ctas": runs[0]["ctas"]})
+        del srcs, dst
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_small_batch(tb, torch, local, make_layout, seed, variants):
     """One of the Mooncake RFC's small-copy shapes on seeded random pools.
     A single batch of this shape touches less than the 129 MB L2, so the
@@ -859,7 +888,7 @@ def study(args, tb, torch, local):
             row["off_over_on_warm_graph"] = round(row["off_warm_graph_gbps"] / row["on_warm_graph_gbps"], 3)
             print(json.dumps(row), flush=True)
     del flush
-    study_validation(tb, torch, local)
+    print(json.dumps(study_validation(tb, torch, local)), flush=True)
     study_host_paths(tb, torch, local)
     study_tiny_batches(tb, torch, local)
     study_small_copies_under_compute(tb, torch, local)
@@ -1188,8 +1217,9 @@ def study_validation(tb, torch, local):
                 walls[name] = (time.perf_counter() - t0) * 1e3 / (10 + 3)
             out["transfer_wall_ms_per_launch_no_validation"] = round(walls["end"], 4)
             out["transfer_wall_ms_per_launch_validating_each"] = round(walls["every_iteration"], 4)
-        print(json.dumps(out), flush=True)
         del srcs, dst, exp_dev
+    torch.cuda.empty_cache()
+    return out
 
 
 def study_batch_configs(tb, torch, local):
@@ -1418,6 +1448,8 @@ def main():
         extra["block_pages_7200"] = run_small_batch(tb, torch, local, workloads.batch_block_pages,
                                                     33, 8)
         extra["interference"] = run_interference(tb, torch, local)
+        extra["multi_source_fill_compress"] = run_multi_source_compress(tb, torch, local)
+        extra["validation_256mib"] = study_validation(tb, torch, local)
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
     if rank == 0:
         line = {

@@ -1,8 +1,9 @@
 """bench.py on the GPU: one short run prints one JSON line carrying every key
 of the bench contract and of the workloads it reports (the 3-source
 reduce-copy, the 47,540 batch, the single 4 MiB transfer, the DMA executor,
-the fillCompress rotation sweep, the 3840- and 7200-page batches and GEMM
-interference), with values in their plausible ranges."""
+the fillCompress rotation sweep, the 3840- and 7200-page batches, GEMM
+interference, multi-source fillCompress and device validation), with values
+in their plausible ranges."""
 import json
 import os
 import subprocess
@@ -68,3 +69,6 @@ def test_workload_keys(line):
         assert line[key]["descriptors"] == n and line[key]["bytes_touched_per_cycle"] > 256 << 20
     it = line["interference"]
     assert it["gemm_tflops_alone"] > 0 and it["batch_gbps"] > 0
+    assert [r["sources"] for r in line["multi_source_fill_compress"]] == [2, 4, 8]
+    v = line["validation_256mib"]
+    assert 0 < v["device_ms"] < v["host_ms"]
