@@ -771,12 +771,39 @@ def host_cpu() -> dict:
     return info
 
 
+def oracle_batch_sample(reps: int = 5):
+    """The oracle's batch apply (one memcpy per descriptor, in order) of the
+    3840- and 7200-page layouts on their host pools, single thread: one
+    untimed apply to touch the pages, then the best of `reps` for each."""
+    import numpy as np
+    import oracle
+    from copy_reduce_dst_gb300 import workloads
+    out = {"unit": "copies/s", "cores": 1, "kind": "oracle"}
+    for key, layout in (("index_pages_3840", workloads.batch_index_pages()),
+                        ("block_pages_7200", workloads.batch_block_pages())):
+        src = np.zeros(layout.src_pool_bytes, dtype=np.uint8)
+        dst = np.zeros(layout.dst_pool_bytes, dtype=np.uint8)
+        oracle.apply_batch(dst, src, layout.src_off, layout.dst_off, layout.lens)
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            oracle.apply_batch(dst, src, layout.src_off, layout.dst_off, layout.lens)
+            best = min(best, time.perf_counter() - t0)
+        out[key] = {"value": round(layout.n / best, 1), "us_per_batch": round(best * 1e6, 1),
+                    "gbps": round(2 * layout.total_bytes / best / 1e9, 3)}
+        del src, dst
+    out["value"] = out["index_pages_3840"]["value"]
+    out["sample"] = (f"the 3840- and 7200-page batches applied to their host pools, best of "
+                     f"{reps} each, single thread; value = the 3840-page batch")
+    return out
+
+
 def cpu_baseline(budget_s: float):
     gbps, reps, el = oracle_sample(budget_s)
     return {"value": round(gbps, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"dstReference[3] over 3 x 4,194,304 float32 default-pattern sources "
                       f"(64 MiB moved per call), {reps} calls in {el:.1f} s, single thread",
-            "host": host_cpu()}
+            "host": host_cpu(), "batch": oracle_batch_sample()}
 
 
 def reference_arm(args):

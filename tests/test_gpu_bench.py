@@ -46,6 +46,7 @@ def test_contract_keys(line):
     assert 0.5 < roof["frac"] < 1.3                      # a copy-bound kernel near its peak
     cpu = line["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
+    assert cpu["batch"]["unit"] == "copies/s" and cpu["batch"]["value"] > 0
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == 3 * (256 << 20)
     assert e2e["d2h_bytes_per_step"] == 256 << 20 and 0 < e2e["value"] < line["value"]
