@@ -229,10 +229,12 @@ def run_reduce(args, tb, torch, ranks, local):
     # Sub-executor sweep with the library's own per-iteration events
     # (TransferBench's loop: 3 warm-up + 20 timed iterations each).
     sweep = {}
+    peak0 = read_peaks()[0]
     for se in (1, 4, 16, 32):
         r = ctx.run_transfer(srcs, dst, nb, num_subexec=se, iters=20, rotate_bytes=rotate)
         sweep[str(se)] = {"gbps": round(r["gbps"], 1), "ctas": r["ctas"],
-                          "median_ms": round(r["median_ms"], 4)}
+                          "median_ms": round(r["median_ms"], 4),
+                          "pct_of_peak": round(r["gbps"] / peak0 * 100, 1)}
     # The timed loop runs at the best sub-executor count of the sweep (every
     # count is reported in the line's config).
     subexec = max(sweep, key=lambda k: sweep[k]["gbps"])
@@ -247,7 +249,8 @@ def run_reduce(args, tb, torch, ranks, local):
     with tb.Context(local, ctx_options(tb, ctas_per_subexec=1, warmup=1)) as c1:
         for se in (1, 4, 16, 32):
             r = c1.run_transfer(srcs, dst, nb, num_subexec=se, iters=3, rotate_bytes=rotate)
-            strict[str(se)] = {"gbps": round(r["gbps"], 1), "ctas": r["ctas"]}
+            strict[str(se)] = {"gbps": round(r["gbps"], 1), "ctas": r["ctas"],
+                               "pct_of_peak": round(r["gbps"] / peak0 * 100, 1)}
 
     def srcs_at(step):
         off = tb.slice_for_iteration(step, plan.K) * plan.slice_stride
@@ -464,6 +467,7 @@ def run_single_transfer(tb, torch, local):
                "K": k1["K"], "alloc_bytes": k1["alloc_bytes"],
                "prep_h2d_bytes": k1["prep_h2d_bytes"], "validated": bool(k1["validated"]),
                "gbps": round(k1["gbps"], 1), "us_per_iteration": round(k1["mean_ms"] * 1e3, 3),
+               "pct_of_peak": round(k1["gbps"] / read_peaks()[0] * 100, 1),
                "us_per_iteration_mean_of_runs": round(k1["mean_us"], 3),
                "graphed": bool(k1["graphed"]), "ctas": k1["ctas"],
                "gbps_64_iterations": round(k1_64["gbps"], 1),
