@@ -45,26 +45,32 @@ __device__ __forceinline__ void vload<32>(Vec<32> &v, const void *p)
         : "l"(p));
 }
 
+// Stores of the vector form, streaming (.cs: evict-first in the caches), as
+// the destination is written once per launch and read by nobody in it.
+// Measured on GB300 against L1::no_allocate stores: 4 MiB transfer with
+// rotation, 10 graphed iterations 2.43-2.44 against 2.52-2.53 us per
+// iteration (mean of 25 runs); 64 iterations, 8 MiB and 3 x 256 MiB the
+// same within 1%.
 template <int VB>
 __device__ __forceinline__ void vstore(void *p, const Vec<VB> &v);
 
 template <>
 __device__ __forceinline__ void vstore<4>(void *p, const Vec<4> &v)
 {
-    asm volatile("st.global.L1::no_allocate.b32 [%0], %1;" ::"l"(p), "r"(v.w[0]));
+    asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v.w[0]));
 }
 
 template <>
 __device__ __forceinline__ void vstore<16>(void *p, const Vec<16> &v)
 {
-    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]),
+    asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]),
                  "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]));
 }
 
 template <>
 __device__ __forceinline__ void vstore<32>(void *p, const Vec<32> &v)
 {
-    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
                  "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]),
                  "r"(v.w[6]), "r"(v.w[7]));
 }
