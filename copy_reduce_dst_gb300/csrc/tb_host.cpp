@@ -558,7 +558,8 @@ int tb_options_from_env(tb_options *o)
     env_i32("TB_WARMUP", &o->warmup, &bad);
     if (!env_i32("TB_ALWAYS_VALIDATE", &o->always_validate, &bad))
         env_i32("ALWAYS_VALIDATE", &o->always_validate, &bad);
-    env_u32("TB_MEMSET_CHAR", &o->memset_byte, &bad);
+    if (!env_u32("TB_MEMSET_CHAR", &o->memset_byte, &bad))
+        env_u32("MEMSET_CHAR", &o->memset_byte, &bad);
     env_i32("TB_CTAS_PER_SUBEXEC", &o->ctas_per_subexec, &bad);
     env_i32("TB_BLOCK_THREADS", &o->block_threads, &bad);
     env_u64("TB_SMALL_MAX_BYTES", &o->small_max_bytes, &bad);
@@ -579,7 +580,8 @@ int tb_options_from_env(tb_options *o)
     if (!env_i32("TB_VALIDATE_SOURCE", &o->validate_source, &bad))
         env_i32("VALIDATE_SOURCE", &o->validate_source, &bad);
     env_i32("TB_CHECK_OVERLAP", &o->check_overlap, &bad);
-    env_i32("TB_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
+    if (!env_i32("TB_BATCH_COPY_MIN", &o->batch_min_copies, &bad))
+        env_i32("MC_HIP_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
     env_i32("TB_BATCH_SHORT_SHAPE", &o->batch_short_shape, &bad);
     env_i32("TB_BATCH_MAX_CTAS", &o->batch_max_ctas, &bad);
     return bad ? TB_EINVAL : TB_OK;

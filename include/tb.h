@@ -211,15 +211,19 @@ void tb_options_default(tb_options *opt);
 
 /* Overrides fields of *opt from the environment:
      TB_SRC_ROTATE_BYTES (or SRC_ROTATE_BYTES), TB_BYTE_OFFSET, TB_WARMUP,
-     TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR, TB_CTAS_PER_SUBEXEC,
+     TB_ALWAYS_VALIDATE (or ALWAYS_VALIDATE), TB_MEMSET_CHAR (or MEMSET_CHAR),
+     TB_CTAS_PER_SUBEXEC,
      TB_BLOCK_THREADS, TB_SMALL_MAX_BYTES, TB_SLOT_ITEMS,
      TB_NUM_SLOTS, TB_WAIT_TIMEOUT_NS, TB_USE_GATE, TB_VEC_BYTES, TB_UNROLL,
      TB_TIME_KERNELS, TB_REDUCE_ENGINE, TB_CE_MIN_BYTES, TB_USE_GRAPH,
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
      TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP, TB_BATCH_COPY_MIN
-     (batch_min_copies), TB_BATCH_SHORT_SHAPE, TB_BATCH_MAX_CTAS.
-   Byte counts go through tb_parse_bytes.  Returns TB_EINVAL (leaving *opt
-   partly updated) if a variable does not parse. */
+     (or MC_HIP_BATCH_COPY_MIN; batch_min_copies), TB_BATCH_SHORT_SHAPE,
+     TB_BATCH_MAX_CTAS.
+   A TB_ name, when set, wins over the bare name beside it; the bare names are
+   the ones TransferBench and Mooncake read, so their users' environments
+   carry over.  Byte counts go through tb_parse_bytes.  Returns TB_EINVAL
+   (leaving *opt partly updated) if a variable does not parse. */
 int tb_options_from_env(tb_options *opt);
 
 /* Parses an unsigned byte count: decimal digits, optionally followed by one of

@@ -139,6 +139,19 @@ def test_every_option_has_an_environment_variable(tb):
         assert renamed.get(field, field.upper()) in names, field
 
 
+def test_header_environment_list_matches_the_source():
+    # every variable the header lists is one tb_options_from_env reads, and back
+    text = open(HEADER).read()
+    block = text[text.index("Overrides fields of *opt from the environment"):
+                 text.index("int tb_options_from_env")]
+    listed = set(re.findall(r"\b([A-Z][A-Z0-9]*(?:_[A-Z0-9]+)+)\b", block)) - {"TB_EINVAL"}
+    src = open(os.path.join(ROOT, "copy_reduce_dst_gb300", "csrc", "tb_host.cpp")).read()
+    body = src[src.index("int tb_options_from_env"):]
+    body = body[:body.index("\n}\n")]
+    read = set(re.findall(r'env_\w+\("([A-Z0-9_]+)"', body))
+    assert listed == read
+
+
 def test_options_env_new_fields(tb, monkeypatch):
     monkeypatch.setenv("TB_USE_GRAPH", "0")
     monkeypatch.setenv("TB_REDUCE_ENGINE", "2")
@@ -161,6 +174,21 @@ def test_validation_options_from_env(tb, monkeypatch):
     assert o.validate_direct == 1 and o.validate_source == 1
     monkeypatch.setenv("TB_VALIDATE_SOURCE", "0")
     assert tb.options_from_env().validate_source == 0
+
+
+def test_pages_variable_names_from_env(tb, monkeypatch):
+    # TransferBench's MEMSET_CHAR, Mooncake's MC_HIP_BATCH_COPY_MIN
+    monkeypatch.setenv("MEMSET_CHAR", "0x")          # does not parse
+    with pytest.raises(tb.TBError):
+        tb.options_from_env()
+    monkeypatch.setenv("MEMSET_CHAR", "90")
+    monkeypatch.setenv("MC_HIP_BATCH_COPY_MIN", "16")
+    o = tb.options_from_env()
+    assert o.memset_byte == 90 and o.batch_min_copies == 16
+    monkeypatch.setenv("TB_MEMSET_CHAR", "1")
+    monkeypatch.setenv("TB_BATCH_COPY_MIN", "0")
+    o = tb.options_from_env()
+    assert o.memset_byte == 1 and o.batch_min_copies == 0
 
 
 def test_options_from_env(tb, monkeypatch):
