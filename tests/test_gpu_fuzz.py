@@ -12,6 +12,9 @@ the whole destination pool must equal the oracle's apply of the batch.
 DMA executor: one source of 1-300,000 elements in K = 1-9 rotation slices
 filled with different patterns, byte offset, warm-up, iterations, graph or
 gate drawn at random; dst must equal the slice of the last iteration.
+Kernel executor with rotation: the same over 1-16 sources, with the engine,
+programmatic launch and sub-executors drawn too; dst must equal
+dstReference of the last iteration's slices.
 The seeds are fixed, so a failure names its case."""
 import numpy as np
 import pytest
@@ -146,4 +149,53 @@ def test_dma_executor_fuzz(tb, seed):
     assert r["mismatch_index"] == -1 and r["executor"] == tb.TB_EXEC_DMA, (seed, opts)
     got = to_host(dst)
     assert np.array_equal(got[off:off + nb].view(np.uint32), slices[last].view(np.uint32))
+    assert np.all(got[:off] == 0xC3) and np.all(got[off + nb:] == 0xC3)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_rotation_fuzz(tb, seed):
+    """The kernel executor with rotation: 1-16 sources, each a K-slice
+    allocation (K = 1-6) whose slices hold different random floats; byte
+    offset, warm-up, iterations, graph, gate, programmatic launch, engine and
+    sub-executors drawn at random.  dst must equal dstReference of every
+    source's slice (iters - 1) mod K, guard bytes untouched."""
+    g = np.random.default_rng(13000 + seed)
+    n_src = int(g.choice([1, 2, 3, 3, 4, 5, 8, 16]))
+    n = int(g.choice([1, 3, 64, 1000, int(g.integers(1, 200000))]))
+    nb = 4 * n
+    K = int(g.integers(1, 7))
+    iters = int(g.integers(1, 9))
+    off = int(g.choice([0, 0, 4, 20, 256]))
+    opts = dict(byte_offset=off, warmup=int(g.integers(0, 4)), use_graph=int(g.choice([0, 1])),
+                use_gate=int(g.choice([0, 1])), use_pdl=int(g.choice([0, 1])),
+                reduce_engine=int(g.choice([0, 0, 1, 2])),
+                ctas_per_subexec=int(g.choice([0, 0, 1])))
+    subexec = int(g.choice([0, 0, 1, 4]))
+    rotate = K * nb if K > 1 else 0
+    plan = tb.rotation_plan(nb, rotate, off)
+    assert plan.K == K
+    slices = [[finite_floats(g, n) for _ in range(K)] for _ in range(n_src)]
+    srcs = []
+    for per_src in slices:
+        b = dev_bytes(plan.alloc_bytes, fill=0x11)
+        for j, a in enumerate(per_src):
+            start = off + j * plan.slice_stride
+            b[start:start + nb].copy_(to_dev(a))
+        srcs.append(b)
+    dst = dev_bytes(nb + off + 128, fill=0xC3)
+    last = oracle.slice_for_iteration(iters - 1, K)
+    exp = oracle.dst_reference([s[last] for s in slices])
+    with tb.Context(0, tb.options(**opts)) as c:
+        try:
+            r = c.run_transfer(srcs, dst, nb, num_subexec=subexec, iters=iters,
+                               rotate_bytes=rotate, expected=exp)
+        except tb.TBError as e:
+            # only the bulk form with more than four sources may be refused
+            assert e.code == tb.TB_ENOTSUP and opts["reduce_engine"] == 2 and n_src > 4, \
+                (seed, opts, e)
+            return
+    assert r["mismatch_index"] == -1 and r["K"] == K and r["iters"] == iters, (seed, opts)
+    got = to_host(dst)
+    mm = oracle.first_mismatch(got[off:off + nb].view(np.uint32), exp.view(np.uint32))
+    assert mm == -1, f"seed {seed} {opts} subexec {subexec}: first mismatch at {mm}"
     assert np.all(got[:off] == 0xC3) and np.all(got[off + nb:] == 0xC3)
