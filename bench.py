@@ -441,7 +441,9 @@ def run_single_transfer(tb, torch, local):
     against src0 on the device.  Median (and mean) of 15 runs, on the
     reduce-copy kernel (one CUDA graph) and on the copy engines (DMA
     executor): the event timer steps by 1-2 us on a ~25 us span, so one run
-    says little; a full rotation of 64 iterations (median of 5) beside it."""
+    says little; a full rotation of 64 iterations (median of 5) beside it,
+    and the same 64-iteration loop on a 4 KiB transfer, which costs what the
+    chain of dependent launches costs by itself."""
     nb, rot = 4 * MiB, 256 * MiB
     plan = tb.rotation_plan(nb, rot)
     with tb.Context(local, ctx_options(tb)) as ctx:
@@ -462,6 +464,10 @@ def run_single_transfer(tb, torch, local):
             return r
         k1, k1_64 = med(10, tb.TB_EXEC_GPU), med(64, tb.TB_EXEC_GPU, 5)
         dma = med(10, tb.TB_EXEC_DMA)
+        # The loop's own floor: a 4 KiB transfer through the same loop (its
+        # K = 65,536 slices of 4 KiB fill the same 268,435,456 B allocation).
+        floor = sorted(ctx.run_transfer([src], dst, 4096, iters=64, rotate_bytes=rot)["mean_ms"]
+                       for _ in range(5))[2]
         out = {"workload": "1 source, 1,048,576 float32 = PrepSrcValue(0, i), SRC_ROTATE_BYTES "
                            "256 MiB, 3 warm-up + 10 timed iterations, dst == src0",
                "K": k1["K"], "alloc_bytes": k1["alloc_bytes"],
@@ -472,6 +478,7 @@ def run_single_transfer(tb, torch, local):
                "graphed": bool(k1["graphed"]), "ctas": k1["ctas"],
                "gbps_64_iterations": round(k1_64["gbps"], 1),
                "us_per_iteration_64": round(k1_64["mean_ms"] * 1e3, 3),
+               "floor_us_per_iteration_4kib_64": round(floor * 1e3, 3),
                "dma_gbps": round(dma["gbps"], 1),
                "dma_us_per_iteration": round(dma["mean_ms"] * 1e3, 3),
                "dma_us_per_iteration_mean_of_runs": round(dma["mean_us"], 3),

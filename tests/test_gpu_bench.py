@@ -60,6 +60,7 @@ def test_workload_keys(line):
     s = line["single_4mib_k64"]
     assert s["K"] == 64 and s["alloc_bytes"] == 268435456 and s["prep_h2d_bytes"] == 4 << 20
     assert s["validated"] and s["dma_validated"] and s["gbps"] > 0 and s["dma_gbps"] > 0
+    assert 0 < s["floor_us_per_iteration_4kib_64"] < 2 * s["us_per_iteration_64"]
     d = line["dma_executor_256mib"]
     assert d["kernel_gbps"] > 0 and d["dma_gbps"] > 0
     sweep = line["rotation_sweep"]
