@@ -1253,18 +1253,24 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     const tb_options &o = ctx->opt;
     const uint64_t small = o.small_max_bytes;
     const uint64_t ce_min = o.ce_min_bytes;
-    ctx->last_slots.clear();
-    tb_batch_stats st{};
     DeviceScope scope(ctx->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A captured call would leave the graph reading the slot's staging when
+    // it is replayed, after later calls have packed other work lists into
+    // it, and its completion event would never be recorded; so a capturing
+    // stream is refused before anything is queued on it.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    TB_CUDA(ctx, cudaStreamIsCapturing(s, &capture));
+    if (capture != cudaStreamCaptureStatusNone)
+        return fail(ctx, TB_ENOTSUP,
+                    "batch_copy: the stream is capturing a CUDA graph; the packed work list "
+                    "lives in staging that later calls reuse");
+    ctx->last_slots.clear();
+    tb_batch_stats st{};
     // Work lists go up on the internal upload stream, so that a call's upload
     // overlaps the kernel of the call before it; the kernel waits for it on
     // the caller's stream.  The slot is free by then: wait_slot has seen its
-    // previous kernel finish.  While the caller's stream is being captured
-    // into a graph, the upload stays on that stream.
-    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-    TB_CUDA(ctx, cudaStreamIsCapturing(s, &capture));
-    const bool side_upload = capture == cudaStreamCaptureStatusNone;
+    // previous kernel finish.
 
     // A batch that fits one slot is checked and packed in a single pass
     // straight into the slot's pinned staging.  A larger one is checked as a
@@ -1366,17 +1372,14 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             // no cross-stream event, which is most of a small call's cost.
             // The staging is not rewritten before the kernel has finished:
             // wait_slot waits for it first.
-            const bool direct = side_upload && tb::batch_direct(plan);
+            const bool direct = tb::batch_direct(plan);
             if (direct) {
                 st.direct_launches += 1;
-            } else if (side_upload) {
+            } else {
                 TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
                                              cudaMemcpyHostToDevice, ctx->up));
                 TB_CUDA(ctx, cudaEventRecord(slot.uploaded, ctx->up));
                 TB_CUDA(ctx, cudaStreamWaitEvent(s, slot.uploaded, 0));
-            } else {
-                TB_CUDA(ctx, cudaMemcpyAsync(slot.dev, slot.host, plan.upload_bytes,
-                                             cudaMemcpyHostToDevice, s));
             }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
@@ -1385,7 +1388,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             if (le != cudaSuccess) {
                 // The slot is not marked pending, so its staging may be
                 // rewritten next: let a queued upload finish reading it.
-                if (side_upload && !direct)
+                if (!direct)
                     cudaStreamSynchronize(ctx->up);
                 return cuda_fail(ctx, le, "launch of the batch kernel");
             }

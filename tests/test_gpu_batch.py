@@ -263,6 +263,40 @@ def test_user_stream_ordering(tb, ctx):
     assert np.all(to_host(dst) == 0xAB)
 
 
+def test_capturing_stream_is_refused(tb, ctx):
+    """tb_batch_copy on a stream that is capturing a CUDA graph returns
+    TB_ENOTSUP with nothing queued: the capture goes on, the graph replays
+    what else was captured (here one cudaMemcpyAsync per copy, tb_copy_each),
+    and the context copies the batch normally once capture is over."""
+    import torch
+    layout = workloads.random_batch(71, 200, 4096, 8 * MiB, align=1, min_len=1)
+    src_h = workloads.random_bytes(layout.src_pool_bytes, 72)
+    dst_h = workloads.random_bytes(layout.dst_pool_bytes, 73)
+    src_d, dst_d = to_dev(src_h), to_dev(dst_h)
+    desc = np.stack([np.uint64(src_d.data_ptr()) + layout.src_off,
+                     np.uint64(dst_d.data_ptr()) + layout.dst_off, layout.lens], axis=1)
+    exp = dst_h.copy()
+    oracle.apply_batch(exp, src_h, layout.src_off, layout.dst_off, layout.lens)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        s = torch.cuda.current_stream()
+        with pytest.raises(tb.TBError) as err:
+            ctx.batch_copy(desc, s)
+        assert err.value.code == tb.TB_ENOTSUP
+        ctx.copy_each(desc, s)
+    assert np.array_equal(to_host(dst_d), dst_h)     # capture ran nothing
+    graph.replay()
+    torch.cuda.synchronize()
+    assert oracle.first_mismatch(to_host(dst_d), exp) == -1
+    del graph
+    dst_d.copy_(to_dev(dst_h))
+    st = torch.cuda.Stream()
+    ctx.batch_copy(desc, st)
+    st.synchronize()
+    assert oracle.first_mismatch(to_host(dst_d), exp) == -1
+
+
 def test_bad_descriptors(tb, ctx):
     import torch
     d = torch.zeros(64, dtype=torch.uint8, device="cuda")
