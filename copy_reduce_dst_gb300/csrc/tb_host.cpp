@@ -1320,7 +1320,20 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
     if (ctx->longs.size() < std::min<size_t>(n, o.slot_items))
         ctx->longs.resize(std::min<size_t>(n, o.slot_items));
 
+    // Copies forked to the copy-engine stream are joined back into the
+    // caller's stream on every way out, a failed call's too, so that work
+    // queued on it afterwards comes after them.
     bool forked = false;
+    struct JoinOnExit {
+        tb_ctx *ctx;
+        cudaStream_t s;
+        const bool &forked;
+        ~JoinOnExit()
+        {
+            if (forked && cudaEventRecord(ctx->ce_join, ctx->ce) == cudaSuccess)
+                cudaStreamWaitEvent(s, ctx->ce_join, 0);
+        }
+    } join_on_exit{ctx, s, forked};
     size_t begin = 0;
     do {
         // The next run of at most slot_items descriptors.
@@ -1405,6 +1418,7 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
         begin = end;
     } while (begin < n);
     if (forked) {
+        forked = false;
         TB_CUDA(ctx, cudaEventRecord(ctx->ce_join, ctx->ce));
         TB_CUDA(ctx, cudaStreamWaitEvent(s, ctx->ce_join, 0));
     }

@@ -495,7 +495,10 @@ typedef struct {
    address with len > 0 or an address range that wraps; TB_ETIMEOUT if no
    slot came free within wait_timeout_ns, or when the previous batch that
    used the chosen slot stopped early because a bounded wait inside the
-   kernel (2 s per wait) expired; TB_ENOTSUP, with nothing queued, while
+   kernel (2 s per wait) expired (a batch of more than slot_items
+   descriptors is launched one slot at a time, so when the wait for a later
+   slot fails the launches before it stay queued and copy their part);
+   TB_ENOTSUP, with nothing queued, while
    `stream` is capturing a CUDA graph (the packed work list lives in the
    context's staging, which later calls reuse, so a replayed graph would
    read another batch's list). */

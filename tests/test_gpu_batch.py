@@ -360,6 +360,43 @@ def test_slot_wait_deadline(tb):
         st.synchronize()
 
 
+def test_failed_slot_wait_mid_batch_keeps_stream_order(tb):
+    """A batch of two slots' worth (slot_items = 1024, one slot) whose wait
+    for the second slot expires behind a busy stream: TB_ETIMEOUT; the first
+    slot's launch and its copy-engine copy stay queued and copy their part,
+    work queued on the stream after the failed call sees that copy-engine
+    copy done, and the second part is not copied."""
+    import torch
+    n = 2048
+    lens = np.full(n, 512, dtype=np.uint64)
+    lens[5] = lens[1500] = 2 * MiB                     # routed to the copy engines
+    off = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.uint64)
+    pool = int(lens.sum())
+    src_h = workloads.random_bytes(pool, 81)
+    dst_h = workloads.random_bytes(pool, 82)
+    src_d, dst_d = to_dev(src_h), to_dev(dst_h)
+    desc = np.stack([np.uint64(src_d.data_ptr()) + off, np.uint64(dst_d.data_ptr()) + off, lens],
+                    axis=1)
+    busy = torch.empty(256 * MiB, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    with tb.Context(0, tb.options(num_slots=1, slot_items=1024, wait_timeout_ns=1,
+                                  ce_min_bytes=1 * MiB)) as c:
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            for _ in range(8):
+                busy.fill_(3)                          # the first launch queues behind these
+        with pytest.raises(tb.TBError) as e:
+            c.batch_copy(desc, st)
+        assert e.value.code == tb.TB_ETIMEOUT
+        with torch.cuda.stream(st):
+            probe = dst_d[int(off[5]):int(off[5]) + 2 * MiB].clone()
+        st.synchronize()
+    assert np.array_equal(to_host(probe), src_h[int(off[5]):int(off[5]) + 2 * MiB])
+    exp = dst_h.copy()
+    oracle.apply_batch(exp, src_h, off[:1024], off[:1024], lens[:1024])
+    assert oracle.first_mismatch(to_host(dst_d), exp) == -1
+
+
 def test_pipeline_wait_expiry_is_reported(tb):
     """kernel_wait_ns = 0: the bulk pipeline of the long copies cannot meet
     its first wait; the kernel records it in the slot's status word and
