@@ -809,12 +809,51 @@ def oracle_batch_sample(reps: int = 5):
     return out
 
 
+def parallel_cpu_sample(budget_s: float, n: int = 16 * MiB):
+    """A second CPU baseline, on every host core (not the oracle): the same
+    3-source reduce-copy as numpy adds, (src0 + src1) + src2 in float32, over
+    chunks taken by a pool of threads (numpy releases the interpreter lock
+    inside its loops).  Sources of n float32 each (256 MiB moved per call,
+    above the host's last-level cache); one result is compared bit for bit
+    with the oracle's dstReference first."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
+    import oracle
+    threads = os.cpu_count() or 1
+    srcs = [oracle.prepare_reference(n, k) for k in range(3)]
+    dst = np.empty(n, dtype=np.float32)
+    step = -(-n // (4 * threads))
+    bounds = [(a, min(n, a + step)) for a in range(0, n, step)]
+
+    def part(ab):
+        a, b = ab
+        np.add(srcs[0][a:b], srcs[1][a:b], out=dst[a:b])
+        np.add(dst[a:b], srcs[2][a:b], out=dst[a:b])
+
+    with ThreadPoolExecutor(threads) as pool:
+        list(pool.map(part, bounds))
+        exact = bool(np.array_equal(dst.view(np.uint32),
+                                    oracle.dst_reference(srcs).view(np.uint32)))
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            list(pool.map(part, bounds))
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return {"value": round(4 * 4 * n * calls / el / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "numpy adds on a thread pool (not the oracle)", "bit_exact_vs_oracle": exact,
+            "sample": f"3 x {n:,} float32 default-pattern sources (256 MiB moved per call), "
+                      f"{calls} calls in {el:.1f} s, {len(bounds)} chunks on {threads} threads"}
+
+
 def cpu_baseline(budget_s: float):
     gbps, reps, el = oracle_sample(budget_s)
     return {"value": round(gbps, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"dstReference[3] over 3 x 4,194,304 float32 default-pattern sources "
                       f"(64 MiB moved per call), {reps} calls in {el:.1f} s, single thread",
-            "host": host_cpu(), "batch": oracle_batch_sample()}
+            "host": host_cpu(), "batch": oracle_batch_sample(),
+            "parallel": parallel_cpu_sample(min(2.0, budget_s))}
 
 
 def reference_arm(args):

@@ -47,6 +47,8 @@ def test_contract_keys(line):
     cpu = line["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
     assert cpu["batch"]["unit"] == "copies/s" and cpu["batch"]["value"] > 0
+    par = cpu["parallel"]
+    assert par["bit_exact_vs_oracle"] is True and par["value"] > 0 and par["cores"] >= 1
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == 3 * (256 << 20)
     assert e2e["d2h_bytes_per_step"] == 256 << 20 and 0 < e2e["value"] < line["value"]
