@@ -240,7 +240,9 @@ def run_reduce(args, tb, torch, ranks, local):
     subexec = max(sweep, key=lambda k: sweep[k]["gbps"])
     subexec = int(subexec)
     info = ctx.reduce_plan(srcs, dst, nb, subexec)
-    kernel = (f"k_reduce_bulk<{n_src}> (bulk copies through shared memory)" if info["engine"] == 2
+    kernel = (f"k_reduce_bulk<{n_src}, {info['tile_bytes']}> (bulk copies through shared memory, "
+              f"{info['stages']} stages of {info['tile_bytes'] // 1024} KiB per source)"
+              if info["engine"] == 2
               else f"k_reduce<{n_src}, {info['vec_bytes']}, {info['unroll']}> (vector loads)")
     # TransferBench's literal layout, one CTA per sub-executor (1 warm-up and
     # 3 timed iterations: a lone CTA's rate hardly varies, and at 1 GiB per
@@ -555,23 +557,26 @@ def run_rotation_sweep(tb, torch, local):
 
 def run_multi_source_compress(tb, torch, local):
     """Multi-source fillCompress reduce-copies (2, 4 and 8 sources of 64 MiB,
-    40/20/0/20/20 %, seed 0x5EED + k, rotation off): random floats with
-    zeroed bytes, so the adds meet subnormals and the order of the adds
-    decides the bits (bit-exactness is tested against the oracle).  GB/s
-    (read + write) of 20 graphed iterations, median of 3, and the engine."""
+    40/20/0/20/20 %, seed 0x5EED + k, rotation at 256 MiB, so K = 4 and every
+    iteration reads its sources from HBM): random floats with zeroed bytes,
+    so the adds meet subnormals and the order of the adds decides the bits
+    (bit-exactness is tested against the oracle).  GB/s (read + write) of 20
+    graphed iterations, median of 3, and the engine."""
     import statistics as st
-    nb = 64 * MiB
+    nb, rot = 64 * MiB, 256 * MiB
+    plan = tb.rotation_plan(nb, rot)
     pct = (40, 20, 0, 20, 20)
     rows = []
     with tb.Context(local, ctx_options(tb)) as ctx:
-        srcs = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(8)]
+        srcs = [torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda") for _ in range(8)]
         for k, s_ in enumerate(srcs):
             ctx.fill_source(s_, nb, tb.compress_pattern(pct, 0x5EED), k)
+        ctx.prepare_sources(srcs, nb, rot)
         dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
         for n in (2, 4, 8):
-            runs = [ctx.run_transfer(srcs[:n], dst, nb, iters=20, rotate_bytes=0)
+            runs = [ctx.run_transfer(srcs[:n], dst, nb, iters=20, rotate_bytes=rot)
                     for _ in range(3)]
-            rows.append({"sources": n, "MiB_each": 64,
+            rows.append({"sources": n, "MiB_each": 64, "K": runs[0]["K"],
                          "gbps": round(st.median(r["gbps"] for r in runs), 1),
                          "engine": runs[0]["engine"], "ctas": runs[0]["ctas"]})
         del srcs, dst

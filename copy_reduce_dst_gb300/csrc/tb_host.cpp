@@ -934,6 +934,8 @@ int tb_reduce_plan(tb_ctx *ctx, const void *const *srcs, int n_src, const void *
     out->body_vectors = p.nvec;
     out->tail_elems = p.n - p.head - p.nvec * ((uint64_t)p.vec_bytes / 4);
     out->smem_bytes = p.smem_bytes;
+    out->stages = p.engine == 2 ? p.stages : 0;
+    out->tile_bytes = (int32_t)tb::plan_tile_bytes(p);
     return TB_OK;
 }
 

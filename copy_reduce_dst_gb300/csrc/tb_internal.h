@@ -38,6 +38,7 @@ struct ReducePlan {
     uint32_t *status;      // nullable, device-visible: 1 if a bounded wait expired
     int pdl;               // 1 = launch with programmatic dependent launch
     int stages;            // bulk form: shared-memory pipeline stages
+    int bulk_deep;         // bulk form: 1 = the deep pipeline's tile (CTAs alone on SMs)
     uint64_t wait_ns = 2000000000ull;  // bulk form: limit of each wait for a tile's loads
     // 1 = the launch may start reading its sources before the launch ahead
     // of it on the stream has finished: only for a launch that follows
@@ -57,6 +58,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
 
 // Launches the plan on `stream` (asynchronous).
 cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream);
+// Bulk form: bytes per source of one tile of the plan's kernel; 0 otherwise.
+uint32_t plan_tile_bytes(const ReducePlan &p);
 
 // Default CTAs resident per SM for the reduce kernel of this plan shape.
 int reduce_ctas_per_sm(int n_src, int vec_bytes, int block_threads, int unroll);

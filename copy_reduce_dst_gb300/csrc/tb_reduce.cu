@@ -224,9 +224,9 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
 
 // ---------------------------------------------------------------------------
 // K1, bulk form (1 to 4 sources, every pointer sharing its address modulo
-// 16).  The body is cut into tiles of bulk_tile<N>() bytes per source.  Thread 0
-// streams each tile's N source pieces into one of kRStages shared-memory
-// stages with bulk copies (one mbarrier per stage); all threads add the
+// 16).  The body is cut into tiles of kTile bytes per source (bulk_tile).
+// Thread 0 streams each tile's N source pieces into one of the launch's
+// shared-memory stages with bulk copies (one mbarrier per stage); all threads add the
 // pieces in place, left to right with __fadd_rn, into the stage's first
 // buffer; after a proxy fence and a barrier, thread 0 writes that buffer out
 // with a bulk copy and refills the previous stage.  With one source the
@@ -237,61 +237,72 @@ constexpr uint32_t kRMaxStages = 16;  // mbarriers in the 128-byte header
 constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (227 KiB)
 constexpr int kBulkThreads = 256;
 // Auto engine: bulk_auto(N, bytes per source) picks the bulk form.
-// Measured on GB300 (20 graphed iterations, us per iteration, vector /
-// bulk; rotation on, and off where noted; per-launch events and single cold
-// launches agree where noted):
+// Measured on GB300 (20 graphed iterations, rotation on, us per iteration,
+// vector / bulk with 4 KiB tiles; median of 5, two rounds):
 //   1 source   8 MiB 3.26 / 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB
-//              5.05-5.10 / 4.69, 24 MiB 8.79 / 6.53 (cold 16.0-17.0 / 14.0);
-//   2 sources  24 MiB 10.48 / 9.71, 32 MiB 14.4-15.3 / 13.4, 40 MiB 19.3 /
-//              19.3, 48 MiB 22.1 / 22.7, 64 MiB 28.6-29.0 / 30.7-31.1, 96 MiB
-//              43.8-44.1 / 45.0-45.4, 112 MiB 50.6 / 51.2, 128 MiB 58.1-58.3 /
-//              57.7-58.0, 160 MiB 73.4-73.9 / 71.8-72.2, 256 MiB 121.0 /
-//              113.5 (rotation off the same within 2%);
-//   3 sources  32 MiB 20.8 / 21.6, 48 MiB 31.0 / 32.0 (cold 39.6 / 41.6),
-//              64 MiB 40.3 / 40.5, 128 MiB 77.5 / 76.3, 256 MiB 151.9 / 149.4;
-//   4 sources  32 MiB 26.4 / 28.0, 96 MiB 74.7 / 78.4, 192 MiB 145.9 / 148.9,
-//              256 MiB 192.9 / 193.7-198.5 (events and cold agree).
-// So: one source from 12 MiB; two from 24 to 40 MiB and from 128 MiB;
-// three from 64 MiB; four never by default (the bulk form stays available
-// as reduce_engine = 2).
+//              5.05-5.10 / 4.69, 24 MiB 8.79 / 6.53 (32 KiB tiles);
+//   2 sources  8 MiB 4.38-4.44 / 5.10-5.36, 12 MiB 7.06-7.15 / 5.61-5.77,
+//              32 MiB 14.5-14.7 / 13.1, 64 MiB 28.8 / 28.7, 128 MiB 58.2 /
+//              56.7, 256 MiB 120.5 / 112.0;
+//   3 sources  4 MiB 3.46 / 3.97, 8 MiB 5.77-5.82 / 5.41, 16 MiB 10.2-10.3 /
+//              8.9, 32 MiB 20.56 / 20.56, 64 MiB 40.2 / 39.0, 256 MiB 152.4 /
+//              146.4;
+//   4 sources  4 MiB 4.13-4.18 / 4.23, 8 MiB 7.15-7.25 / 6.53, 24 MiB 21.1-21.2
+//              / 19.7, 32 MiB 26.1 / 27.3-27.4, 40 MiB 32.75 / 32.9, 48 MiB
+//              39.3-39.4 / 39.5, 64 MiB 50.7 / 49.4, 256 MiB 193.3 / 187.2.
+// So: one or two sources from 12 MiB, three from 8 MiB, four from 8 MiB
+// except 32 to 64 MiB.
 constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
     constexpr uint64_t MiB = 1ull << 20;
     switch (n_src) {
     case 1:
-        return bytes >= 12 * MiB;
     case 2:
-        return (bytes >= 24 * MiB && bytes < 40 * MiB) || bytes >= 128 * MiB;
+        return bytes >= 12 * MiB;
     case 3:
-        return bytes >= 64 * MiB;
+        return bytes >= 8 * MiB;
+    case 4:
+        return bytes >= 8 * MiB && !(bytes >= 32 * MiB && bytes < 64 * MiB);
     default:
         return false;
     }
 }
 constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
-// Bytes per source of one tile.  With several sources the stages hold
-// N pieces each and 8 KiB keeps three CTAs (three pipelines) per SM; one
-// source is a plain relay, which moves more per SM with fewer, larger
+// Bytes per source of one tile.  With several sources the stages hold N
+// pieces each, and while CTAs share SMs 4 KiB tiles keep more, shorter
+// pipelines per SM (3 sources: six CTAs; 2: eight; 4: four) than 8 KiB
+// ones (three, four, two), measured faster on GB300 at every size and
+// source count tried, the bytes in flight per SM being about the same (20
+// graphed iterations, GB/s, 8 KiB / 4 KiB): 3 x 256 MiB 7190-7245 /
+// 7354-7355, 2 x 256 MiB 7104-7115 / 7190-7193, 3 x 64 MiB 6657-6673 /
+// 6911-6930, 2 x 32 MiB 7374-7458 / 7814-7816, 4 x 256 MiB 6813-6838 /
+// 7169-7171; 2 KiB, 6 KiB, 12 KiB and 16 KiB tiles and 4-6 stages were
+// slower.  A CTA alone on its SM (the deep pipeline below) is bound by its
+// per-tile barrier and issue instead, so it takes larger tiles (one CTA,
+// 64 MiB per source, GB/s for 2 / 3 / 4 sources): 4 KiB 37 / 38 / 42,
+// 8 KiB 49 / 59 / 65, 12 KiB 69 / 85 / 96, 16 KiB 86 / 104 / 94.
+// One source is a plain relay, which moves more per SM with fewer, larger
 // bulk copies: 32 KiB stages, two CTAs per SM (measured 3-4% faster on
-// large copies than 8 KiB with eight CTAs per SM).
-template <int N>
-__host__ __device__ constexpr uint32_t bulk_tile()
+// large copies than 8 KiB with eight CTAs per SM), alone or not.
+constexpr uint32_t kSharedTile = 4096;
+constexpr uint32_t kDeepTile = 16384;
+constexpr uint32_t kRelayTile = 32768;
+
+constexpr uint32_t bulk_tile(int n_src, bool deep)
 {
-    return N == 1 ? 32768u : 8192u;
+    return n_src == 1 ? kRelayTile : deep ? kDeepTile : kSharedTile;
 }
 
-template <int N>
-constexpr size_t bulk_smem_bytes(uint32_t stages)
+constexpr size_t bulk_smem_bytes(int n_src, uint32_t tile, uint32_t stages)
 {
-    return 128 + (size_t)stages * N * bulk_tile<N>();
+    return 128 + (size_t)stages * (size_t)n_src * tile;
 }
 
 // Most stages whose shared memory one CTA can hold (a CTA alone on its SM).
-template <int N>
-constexpr uint32_t bulk_max_stages()
+constexpr uint32_t bulk_max_stages(int n_src, uint32_t tile)
 {
-    const size_t fit = (kSmemOptIn - 128) / ((size_t)N * bulk_tile<N>());
+    const size_t fit = (kSmemOptIn - 128) / ((size_t)n_src * tile);
     return (uint32_t)(fit < kRMaxStages ? fit : kRMaxStages);
 }
 
@@ -299,11 +310,10 @@ constexpr uint32_t bulk_max_stages()
 // bulk_max_stages when each CTA has an SM to itself, so one CTA keeps more
 // bytes in flight).  Stage and phase advance incrementally: tile j uses
 // stage j mod stages, on that stage's mbarrier phase floor(j / stages).
-template <int N>
+template <int N, uint32_t kTile>
 __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr uint32_t kTile = bulk_tile<N>();
     constexpr uint32_t kTileVecs = kTile / 16;
     const uint32_t tid = threadIdx.x;
     const uint32_t nst = a.stages;
@@ -430,30 +440,17 @@ __global__ void __launch_bounds__(kBulkThreads) k_reduce_bulk(const ReduceArgs a
 
 using BulkKernel = void (*)(const ReduceArgs);
 
-BulkKernel pick_bulk(int n_src, uint32_t stages, size_t *smem)
+// The bulk kernel for n_src sources with the shared-SM tile, or the deep
+// pipeline's tile when `deep`; *smem = its shared memory at `stages`.
+BulkKernel pick_bulk(int n_src, bool deep, uint32_t stages, size_t *smem)
 {
+    *smem = bulk_smem_bytes(n_src, bulk_tile(n_src, deep), stages);
     switch (n_src) {
-    case 1: *smem = bulk_smem_bytes<1>(stages); return k_reduce_bulk<1>;
-    case 2: *smem = bulk_smem_bytes<2>(stages); return k_reduce_bulk<2>;
-    case 3: *smem = bulk_smem_bytes<3>(stages); return k_reduce_bulk<3>;
-    case 4: *smem = bulk_smem_bytes<4>(stages); return k_reduce_bulk<4>;
+    case 1: return k_reduce_bulk<1, kRelayTile>;
+    case 2: return deep ? k_reduce_bulk<2, kDeepTile> : k_reduce_bulk<2, kSharedTile>;
+    case 3: return deep ? k_reduce_bulk<3, kDeepTile> : k_reduce_bulk<3, kSharedTile>;
+    case 4: return deep ? k_reduce_bulk<4, kDeepTile> : k_reduce_bulk<4, kSharedTile>;
     default: *smem = 0; return nullptr;
-    }
-}
-
-uint32_t bulk_tile_bytes(int n_src)
-{
-    return n_src == 1 ? bulk_tile<1>() : bulk_tile<2>();
-}
-
-uint32_t bulk_deep_stages(int n_src)
-{
-    switch (n_src) {
-    case 1: return bulk_max_stages<1>();
-    case 2: return bulk_max_stages<2>();
-    case 3: return bulk_max_stages<3>();
-    case 4: return bulk_max_stages<4>();
-    default: return kRStages;
     }
 }
 
@@ -541,7 +538,7 @@ int default_unroll(int n_src, int vb)
 static int bulk_ctas_per_sm(int n_src)
 {
     size_t smem = 0;
-    BulkKernel k = pick_bulk(n_src, kRStages, &smem);
+    BulkKernel k = pick_bulk(n_src, false, kRStages, &smem);
     return k ? resident_ctas((const void *)k, kBulkThreads, smem) : 0;
 }
 
@@ -627,10 +624,10 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // than it saves and the vector form is faster.  A CTA alone on its SM
     // with 2 to 4 sources is limited by the bulk form's per-tile adds and
     // barrier instead; the vector form in a 1024-thread CTA with 32-byte
-    // vectors (two per source in flight, one for 4 sources) streams about
-    // twice as much (per CTA: 122 against 60 GB/s for 2 sources, 131
-    // against 61 for 3, 130 against 65 for 4).  One source stays bulk (a
-    // relay: 105 against 101).
+    // vectors (two per source in flight, one for 4 sources) streams more
+    // (per CTA, 64 MiB per source: 126 against 86 GB/s for 2 sources, 142
+    // against 104 for 3, 137 against 94 for 4, the bulk form with 16 KiB
+    // tiles).  One source stays bulk (a relay: 105 against 88).
     const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
@@ -706,7 +703,7 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         // 6.6 with one wave; 3 sources, 3 x 256 MiB: 7.18 against 7.11).
         // Whole waves only: a partial last wave leaves SMs idle at the end
         // (1 source, 64 MiB: 1.7 waves 6.7 TB/s, one wave 7.2).
-        const uint64_t tile_vecs = bulk_tile_bytes(n_src) / 16;
+        const uint64_t tile_vecs = bulk_tile(n_src, false) / 16;
         const uint64_t tiles = (p->nvec + tile_vecs - 1) / tile_vecs;
         const uint64_t want = (tiles + kBulkTilesPerCta - 1) / kBulkTilesPerCta;
         const uint64_t waves = std::max<uint64_t>(1, std::min<uint64_t>(want / (uint64_t)full, 4096));
@@ -732,16 +729,24 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // a lone CTA keeps several times more bytes in flight.
     if (p->engine == 2) {
         p->stages = kRStages;
+        p->bulk_deep = 0;
         if (G <= (int64_t)num_sms) {
-            const uint32_t deep = bulk_deep_stages(n_src);
+            const uint32_t deep = bulk_max_stages(n_src, bulk_tile(n_src, true));
             size_t smem = 0;
-            BulkKernel k = pick_bulk(n_src, deep, &smem);
-            if (k && resident_ctas((const void *)k, kBulkThreads, smem) >= 1)
+            BulkKernel k = pick_bulk(n_src, true, deep, &smem);
+            if (k && resident_ctas((const void *)k, kBulkThreads, smem) >= 1) {
                 p->stages = (int)deep;
+                p->bulk_deep = 1;
+            }
         }
-        pick_bulk(n_src, (uint32_t)p->stages, &p->smem_bytes);
+        pick_bulk(n_src, p->bulk_deep != 0, (uint32_t)p->stages, &p->smem_bytes);
     }
     return TB_OK;
+}
+
+uint32_t plan_tile_bytes(const ReducePlan &p)
+{
+    return p.engine == 2 ? bulk_tile(p.n_src, p.bulk_deep != 0) : 0u;
 }
 
 cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
@@ -772,7 +777,7 @@ cudaError_t launch_reduce(const ReducePlan &p, cudaStream_t stream)
     cfg.numAttrs = p.pdl ? 1 : 0;
     if (p.engine == 2) {
         size_t smem = 0;
-        BulkKernel k = pick_bulk(p.n_src, a.stages, &smem);
+        BulkKernel k = pick_bulk(p.n_src, p.bulk_deep != 0, a.stages, &smem);
         if (!k || a.stages < 2 || a.stages > kRMaxStages ||
             resident_ctas((const void *)k, kBulkThreads, smem) < 1)
             return cudaErrorInvalidValue;

@@ -123,6 +123,8 @@ class LaunchInfo(ct.Structure):
         ("body_vectors", _u64),
         ("tail_elems", _u64),
         ("smem_bytes", _u64),
+        ("stages", _i32),
+        ("tile_bytes", _i32),
     ]
 
 

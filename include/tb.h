@@ -131,9 +131,8 @@ typedef struct {
        adds done in shared memory (1 to 4 sources sharing a 16-byte
        alignment, else TB_ENOTSUP); 0 = the library's choice, by what
        measured faster on GB300: 2 where it applies, vec_bytes is 0 and
-       each source holds at least 12 MiB (one source), 24 to 40 MiB or at
-       least 128 MiB (two), at least 64 MiB (three); else 1, and always 1
-       for four sources.
+       each source holds at least 12 MiB (one or two sources), at least
+       8 MiB (three), or at least 8 MiB but not 32 to 64 MiB (four); else 1.
        Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy
@@ -365,6 +364,8 @@ typedef struct {
     uint64_t body_vectors;    /* vectors of vec_bytes in the body */
     uint64_t tail_elems;      /* scalar elements after it */
     uint64_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t stages;           /* shared-memory pipeline stages (engine 2), else 0 */
+    int32_t tile_bytes;       /* bytes per source of one tile (engine 2), else 0 */
 } tb_launch_info;
 
 /* Describes, without launching, the launch tb_reduce_copy would make for

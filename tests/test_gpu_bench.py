@@ -74,5 +74,6 @@ def test_workload_keys(line):
     it = line["interference"]
     assert it["gemm_tflops_alone"] > 0 and it["batch_gbps"] > 0
     assert [r["sources"] for r in line["multi_source_fill_compress"]] == [2, 4, 8]
+    assert all(r["K"] == 4 for r in line["multi_source_fill_compress"])
     v = line["validation_256mib"]
     assert 0 < v["device_ms"] < v["host_ms"]

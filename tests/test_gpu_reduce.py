@@ -144,9 +144,10 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
 @pytest.mark.parametrize("subexec", [1, 4, 32, 152])
 def test_bulk_deep_pipeline(tb, nsrc, subexec):
     """One CTA per sub-executor and no more CTAs than SMs: each CTA runs the
-    bulk pipeline with every stage its shared memory holds (7 to 14 instead
-    of 3).  Enough tiles per CTA that the stage ring wraps many times, a head
-    and a ragged tail; bit-exact against the oracle."""
+    bulk pipeline with the deep tiles (16 KiB per source, 32 KiB for one
+    source) and every stage its shared memory holds (3 to 7).  Enough tiles
+    per CTA that the stage ring wraps many times, a head and a ragged tail;
+    bit-exact against the oracle."""
     import torch
     if subexec > torch.cuda.get_device_properties(0).multi_processor_count:
         pytest.skip("fewer SMs than sub-executors")
@@ -157,9 +158,12 @@ def test_bulk_deep_pipeline(tb, nsrc, subexec):
         d = dev_bytes(4 * n + 64)
         far = d.data_ptr() + (1 << 36) + 4       # planning only: never accessed
         info = c.reduce_plan([d.data_ptr() + 4] * nsrc, far, 4 * n, subexec)
-        tile = 32768 if nsrc == 1 else 8192
-        stages = (info["smem_bytes"] - 128) // (nsrc * tile)
-        assert info["grid"] == subexec and stages > 3
+        tile = 32768 if nsrc == 1 else 16384
+        assert info["tile_bytes"] == tile
+        stages = info["stages"]
+        assert info["smem_bytes"] == 128 + stages * nsrc * tile
+        assert info["grid"] == subexec
+        assert stages == min(16, (232448 - 128) // (nsrc * tile)) and stages >= 3
         reduce_and_compare(tb, c, srcs, byte_offsets=[4] * nsrc, dst_offset=4,
                            num_subexec=subexec)
 
@@ -206,14 +210,25 @@ def test_reduce_plan_engine_choice(tb, ctx):
     three = [p, p + 4096, p + 8192]
     info = ctx.reduce_plan(three, far, 2 * big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
-    assert ctx.reduce_plan(three, far, 2 * big - 256)["engine"] == 1  # three: from 64 MiB
-    two = three[:2]                                               # two: 24-40 MiB, >= 128 MiB
-    assert [ctx.reduce_plan(two, far, m << 20)["engine"] for m in (16, 24, 32, 40, 64, 127, 128)] \
-        == [1, 2, 2, 1, 1, 1, 2]
+    assert (info["tile_bytes"], info["stages"]) == (4096, 3)      # short tiles, CTAs share SMs
+    assert info["smem_bytes"] == 128 + 3 * 3 * 4096
+    relay = ctx.reduce_plan([p], far, 2 * big)
+    assert (relay["tile_bytes"], relay["stages"]) == (32768, 3)
+    vec = ctx.reduce_plan([p] * 5, far, 2 * big)
+    assert vec["engine"] == 1 and (vec["tile_bytes"], vec["stages"]) == (0, 0)
+    MB = 1 << 20
+    assert ctx.reduce_plan(three, far, 8 * MB)["engine"] == 2     # three: from 8 MiB
+    assert ctx.reduce_plan(three, far, 8 * MB - 256)["engine"] == 1
+    two = three[:2]                                               # two: from 12 MiB
+    assert [ctx.reduce_plan(two, far, m)["engine"]
+            for m in (8 * MB, 12 * MB - 256, 12 * MB, 40 * MB, 256 * MB)] == [1, 1, 2, 2, 2]
     one = 12 << 20
     assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: from 12 MiB
     assert ctx.reduce_plan([p], far, one - 256)["engine"] == 1
-    assert ctx.reduce_plan(three + [p + 12288], far, 8 * big)["engine"] == 1  # four: vector
+    four = three + [p + 12288]                                    # four: 8-32 MiB, >= 64 MiB
+    assert [ctx.reduce_plan(four, far, m)["engine"]
+            for m in (4 * MB, 8 * MB - 256, 8 * MB, 32 * MB - 256, 32 * MB, 48 * MB,
+                      64 * MB - 256, 64 * MB, 256 * MB)] == [1, 1, 2, 2, 1, 1, 1, 2, 2]
     info = ctx.reduce_plan([p] * 5, far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
     info = ctx.reduce_plan([p + 4, p + 8], far, 4096)
