@@ -1529,9 +1529,11 @@ def main():
                                                     31, 32)
         extra["block_pages_7200"] = run_small_batch(tb, torch, local, workloads.batch_block_pages,
                                                     33, 8)
-        extra["interference"] = run_interference(tb, torch, local)
         extra["multi_source_fill_compress"] = run_multi_source_compress(tb, torch, local)
         extra["validation_256mib"] = study_validation(tb, torch, local)
+        # Last: its GEMM loops run the GPU at its power limit for seconds,
+        # which would slow whatever ran next.
+        extra["interference"] = run_interference(tb, torch, local)
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1) else None
     if rank == 0:
         line = {

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
 }
 
 // ---------------------------------------------------------------------------
-// K1, bulk form (1 to 4 sources, every pointer sharing its address modulo
+// K1, bulk form (1 to 8 sources, every pointer sharing its address modulo
 // 16).  The body is cut into tiles of kTile bytes per source (bulk_tile).
 // Thread 0 streams each tile's N source pieces into one of the launch's
 // shared-memory stages with bulk copies (one mbarrier per stage); all threads add the
@@ -249,9 +249,18 @@ constexpr int kBulkThreads = 256;
 //              146.4;
 //   4 sources  4 MiB 4.13-4.18 / 4.23, 8 MiB 7.15-7.25 / 6.53, 24 MiB 21.1-21.2
 //              / 19.7, 32 MiB 26.1 / 27.3-27.4, 40 MiB 32.75 / 32.9, 48 MiB
-//              39.3-39.4 / 39.5, 64 MiB 50.7 / 49.4, 256 MiB 193.3 / 187.2.
+//              39.3-39.4 / 39.5, 64 MiB 50.7 / 49.4, 256 MiB 193.3 / 187.2;
+//   5 sources  2 MiB 3.31-3.41 / 3.41-3.51, 3 MiB 4.03-4.13 / 4.13, 4 MiB
+//              7.10-7.25 / 4.80-4.90, 64 MiB 66.7 / 59.6, 256 MiB 252.6 / 234.3;
+//   6 sources  2 MiB 3.61-3.72 / 3.72, 3 MiB 4.64-4.74 / 4.44-4.48, 4 MiB
+//              8.28-8.43 / 5.33-5.41, 256 MiB 300.1 / 262.0;
+//   7 sources  2 MiB 3.82-3.87 / 4.03, 3 MiB 8.22-8.27 / 4.94-4.95, 256 MiB
+//              430.3 / 332.0;
+//   8 sources  2 MiB 4.13 / 4.23-4.24, 3 MiB 7.40-7.41 / 5.31-5.32, 16 MiB
+//              26.4 / 26.0-26.1, 256 MiB 374.7 / 362.3-362.6 (the bulk form
+//              ahead at every size from 4 to 256 MiB for 5 to 8 sources).
 // So: one or two sources from 12 MiB, three from 8 MiB, four from 8 MiB
-// except 32 to 64 MiB.
+// except 32 to 64 MiB, five from 4 MiB, six to eight from 3 MiB.
 constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
     constexpr uint64_t MiB = 1ull << 20;
@@ -263,6 +272,12 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
         return bytes >= 8 * MiB;
     case 4:
         return bytes >= 8 * MiB && !(bytes >= 32 * MiB && bytes < 64 * MiB);
+    case 5:
+        return bytes >= 4 * MiB;
+    case 6:
+    case 7:
+    case 8:
+        return bytes >= 3 * MiB;
     default:
         return false;
     }
@@ -287,11 +302,14 @@ constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bu
 // large copies than 8 KiB with eight CTAs per SM), alone or not.
 constexpr uint32_t kSharedTile = 4096;
 constexpr uint32_t kDeepTile = 16384;
+constexpr uint32_t kDeepTileMany = 8192;  // 5 to 8 sources: three or more stages still fit
 constexpr uint32_t kRelayTile = 32768;
+constexpr int kBulkMaxSrcs = 8;
 
 constexpr uint32_t bulk_tile(int n_src, bool deep)
 {
-    return n_src == 1 ? kRelayTile : deep ? kDeepTile : kSharedTile;
+    return n_src == 1 ? kRelayTile
+                      : deep ? (n_src <= 4 ? kDeepTile : kDeepTileMany) : kSharedTile;
 }
 
 constexpr size_t bulk_smem_bytes(int n_src, uint32_t tile, uint32_t stages)
@@ -450,6 +468,10 @@ BulkKernel pick_bulk(int n_src, bool deep, uint32_t stages, size_t *smem)
     case 2: return deep ? k_reduce_bulk<2, kDeepTile> : k_reduce_bulk<2, kSharedTile>;
     case 3: return deep ? k_reduce_bulk<3, kDeepTile> : k_reduce_bulk<3, kSharedTile>;
     case 4: return deep ? k_reduce_bulk<4, kDeepTile> : k_reduce_bulk<4, kSharedTile>;
+    case 5: return deep ? k_reduce_bulk<5, kDeepTileMany> : k_reduce_bulk<5, kSharedTile>;
+    case 6: return deep ? k_reduce_bulk<6, kDeepTileMany> : k_reduce_bulk<6, kSharedTile>;
+    case 7: return deep ? k_reduce_bulk<7, kDeepTileMany> : k_reduce_bulk<7, kSharedTile>;
+    case 8: return deep ? k_reduce_bulk<8, kDeepTileMany> : k_reduce_bulk<8, kSharedTile>;
     default: *smem = 0; return nullptr;
     }
 }
@@ -628,7 +650,7 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
     // (per CTA, 64 MiB per source: 126 against 86 GB/s for 2 sources, 142
     // against 104 for 3, 137 against 94 for 4, the bulk form with 16 KiB
     // tiles).  One source stays bulk (a relay: 105 against 88).
-    const bool bulk_ok = n_src >= 1 && n_src <= 4 && vb >= 16 && vec_bytes != 32;
+    const bool bulk_ok = n_src >= 1 && n_src <= kBulkMaxSrcs && vb >= 16 && vec_bytes != 32;
     if (engine == 2 && !bulk_ok)
         return TB_ENOTSUP;
     const bool vector_alone = alone && vb == 32 && n_src >= 2 && n_src <= 4;
@@ -734,7 +756,7 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
             const uint32_t deep = bulk_max_stages(n_src, bulk_tile(n_src, true));
             size_t smem = 0;
             BulkKernel k = pick_bulk(n_src, true, deep, &smem);
-            if (k && resident_ctas((const void *)k, kBulkThreads, smem) >= 1) {
+            if (k && deep >= 2 && resident_ctas((const void *)k, kBulkThreads, smem) >= 1) {
                 p->stages = (int)deep;
                 p->bulk_deep = 1;
             }

@@ -125,7 +125,7 @@ def test_reduce_parity_kernel_shapes(tb, vec, unroll, threads, nsrc):
         reduce_and_compare(tb, c, srcs, num_subexec=7)
 
 
-@pytest.mark.parametrize("nsrc", [1, 2, 3, 4])
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("n,offs,subexec", [
     (5, 0, 0), (2048, 0, 1), (2048 * 7 + 3, 4, 3), (1000003, 20, 0), (262144 * 3 + 17, 16, 32),
     (65536, 12, 1000)])
@@ -140,14 +140,14 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
                            num_subexec=subexec)
 
 
-@pytest.mark.parametrize("nsrc", [1, 2, 3, 4])
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("subexec", [1, 4, 32, 152])
 def test_bulk_deep_pipeline(tb, nsrc, subexec):
     """One CTA per sub-executor and no more CTAs than SMs: each CTA runs the
-    bulk pipeline with the deep tiles (16 KiB per source, 32 KiB for one
-    source) and every stage its shared memory holds (3 to 7).  Enough tiles
-    per CTA that the stage ring wraps many times, a head and a ragged tail;
-    bit-exact against the oracle."""
+    bulk pipeline with the deep tiles (16 KiB per source for 2 to 4 sources,
+    8 KiB for 5 to 8, 32 KiB for one source) and every stage its shared
+    memory holds (3 to 7).  Enough tiles per CTA that the stage ring wraps
+    many times, a head and a ragged tail; bit-exact against the oracle."""
     import torch
     if subexec > torch.cuda.get_device_properties(0).multi_processor_count:
         pytest.skip("fewer SMs than sub-executors")
@@ -158,7 +158,7 @@ def test_bulk_deep_pipeline(tb, nsrc, subexec):
         d = dev_bytes(4 * n + 64)
         far = d.data_ptr() + (1 << 36) + 4       # planning only: never accessed
         info = c.reduce_plan([d.data_ptr() + 4] * nsrc, far, 4 * n, subexec)
-        tile = 32768 if nsrc == 1 else 16384
+        tile = 32768 if nsrc == 1 else 16384 if nsrc <= 4 else 8192
         assert info["tile_bytes"] == tile
         stages = info["stages"]
         assert info["smem_bytes"] == 128 + stages * nsrc * tile
@@ -207,6 +207,7 @@ def test_reduce_plan_engine_choice(tb, ctx):
     p = d.data_ptr()
     far = p + (1 << 36)
     big = 32 << 20
+    MB = 1 << 20
     three = [p, p + 4096, p + 8192]
     info = ctx.reduce_plan(three, far, 2 * big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
@@ -214,9 +215,12 @@ def test_reduce_plan_engine_choice(tb, ctx):
     assert info["smem_bytes"] == 128 + 3 * 3 * 4096
     relay = ctx.reduce_plan([p], far, 2 * big)
     assert (relay["tile_bytes"], relay["stages"]) == (32768, 3)
-    vec = ctx.reduce_plan([p] * 5, far, 2 * big)
+    vec = ctx.reduce_plan([p] * 9, far, 2 * big)
     assert vec["engine"] == 1 and (vec["tile_bytes"], vec["stages"]) == (0, 0)
-    MB = 1 << 20
+    assert [ctx.reduce_plan([p] * 5, far, m)["engine"]            # five: from 4 MiB
+            for m in (4 * MB - 256, 4 * MB, 256 * MB)] == [1, 2, 2]
+    assert [ctx.reduce_plan([p] * n, far, m)["engine"]            # six to eight: from 3 MiB
+            for n in (6, 8) for m in (3 * MB - 256, 3 * MB, 256 * MB)] == [1, 2, 2] * 2
     assert ctx.reduce_plan(three, far, 8 * MB)["engine"] == 2     # three: from 8 MiB
     assert ctx.reduce_plan(three, far, 8 * MB - 256)["engine"] == 1
     two = three[:2]                                               # two: from 12 MiB
@@ -296,7 +300,7 @@ def test_bulk_engine_limits(tb):
     d = dev_bytes(1 << 16)
     with tb.Context(0, tb.options(reduce_engine=2)) as c:
         with pytest.raises(tb.TBError) as e:
-            c.reduce_copy([d.data_ptr()] * 5, d.data_ptr() + 8192, 256)    # 5 sources
+            c.reduce_copy([d.data_ptr()] * 9, d.data_ptr() + 8192, 256)    # 9 sources
         assert e.value.code == tb.TB_ENOTSUP
         with pytest.raises(tb.TBError) as e:
             c.reduce_copy([d.data_ptr() + 4], d.data_ptr() + 8192, 256)   # no common 16 B
@@ -389,7 +393,8 @@ def test_fill_rejects_bad_patterns(tb, ctx):
 
 
 @pytest.mark.parametrize("engine,nsrc", [(1, 2), (1, 3), (1, 4), (1, 5), (1, 8),
-                                         (2, 2), (2, 3), (2, 4)])    # bulk: 1 to 4 sources
+                                         (2, 2), (2, 3), (2, 4), (2, 5),
+                                         (2, 8)])    # bulk: 1 to 8 sources
 def test_multi_source_fill_compress(tb, nsrc, engine):
     """Sources k = 0..N-1 of the fillCompress pattern (every mode, 2B0
     included), written by the library's fill kernel and summed on the GPU,
