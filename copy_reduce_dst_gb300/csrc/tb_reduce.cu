@@ -238,29 +238,24 @@ constexpr size_t kSmemOptIn = 232448;  // shared memory one CTA may opt into (22
 constexpr int kBulkThreads = 256;
 // Auto engine: bulk_auto(N, bytes per source) picks the bulk form.
 // Measured on GB300 (20 graphed iterations, rotation on, us per iteration,
-// vector / bulk with 4 KiB tiles; median of 5, two rounds):
+// vector / bulk with the kSharedTile tiles; median of 5, two rounds):
 //   1 source   8 MiB 3.26 / 3.31-3.41, 12 MiB 4.54 / 4.03, 16 MiB
 //              5.05-5.10 / 4.69, 24 MiB 8.79 / 6.53 (32 KiB tiles);
-//   2 sources  8 MiB 4.38-4.44 / 5.10-5.36, 12 MiB 7.06-7.15 / 5.61-5.77,
-//              32 MiB 14.5-14.7 / 13.1, 64 MiB 28.8 / 28.7, 128 MiB 58.2 /
-//              56.7, 256 MiB 120.5 / 112.0;
-//   3 sources  4 MiB 3.46 / 3.97, 8 MiB 5.77-5.82 / 5.41, 16 MiB 10.2-10.3 /
-//              8.9, 32 MiB 20.56 / 20.56, 64 MiB 40.2 / 39.0, 256 MiB 152.4 /
-//              146.4;
-//   4 sources  4 MiB 4.13-4.18 / 4.23, 8 MiB 7.15-7.25 / 6.53, 24 MiB 21.1-21.2
-//              / 19.7, 32 MiB 26.1 / 27.3-27.4, 40 MiB 32.75 / 32.9, 48 MiB
-//              39.3-39.4 / 39.5, 64 MiB 50.7 / 49.4, 256 MiB 193.3 / 187.2;
-//   5 sources  2 MiB 3.31-3.41 / 3.41-3.51, 3 MiB 4.03-4.13 / 4.13, 4 MiB
-//              7.10-7.25 / 4.80-4.90, 64 MiB 66.7 / 59.6, 256 MiB 252.6 / 234.3;
-//   6 sources  2 MiB 3.61-3.72 / 3.72, 3 MiB 4.64-4.74 / 4.44-4.48, 4 MiB
-//              8.28-8.43 / 5.33-5.41, 256 MiB 300.1 / 262.0;
-//   7 sources  2 MiB 3.82-3.87 / 4.03, 3 MiB 8.22-8.27 / 4.94-4.95, 256 MiB
-//              430.3 / 332.0;
-//   8 sources  2 MiB 4.13 / 4.23-4.24, 3 MiB 7.40-7.41 / 5.31-5.32, 16 MiB
-//              26.4 / 26.0-26.1, 256 MiB 374.7 / 362.3-362.6 (the bulk form
-//              ahead at every size from 4 to 256 MiB for 5 to 8 sources).
-// So: one or two sources from 12 MiB, three from 8 MiB, four from 8 MiB
-// except 32 to 64 MiB, five from 4 MiB, six to eight from 3 MiB.
+//   2 sources  8 MiB 4.44 / 5.17-5.20, 12 MiB 6.95-7.05 / 5.56-5.61, 64 MiB
+//              28.7 / 28.5, 256 MiB 121.0 / 111.4;
+//   3 sources  4 MiB 3.52 / 5.00-5.05, 6 MiB 5.27-5.31 / 5.31, 8 MiB
+//              5.77-5.81 / 5.56-5.61, 64 MiB 40.0 / 38.1, 256 MiB 151.5 / 145.2;
+//   4 sources  4 MiB 4.18 / 5.11-5.20, 6 MiB 7.15-7.25 / 5.51, 32 MiB
+//              26.1-26.2 / 25.4, 256 MiB 192.4 / 183.6;
+//   5 sources  3 MiB 4.08 / 4.59-4.64, 4 MiB 7.20 / 4.90, 256 MiB 252.3 / 218.5;
+//   6 sources  2 MiB 3.92-3.93 / 4.08, 3 MiB 4.79-4.80 / 4.49-4.54, 256 MiB
+//              299.3 / 256.6;
+//   7 sources  2 MiB 3.77-3.82 / 4.03, 3 MiB 8.17 / 4.90, 256 MiB 432.4 / 302.0;
+//   8 sources  2 MiB 4.08-4.13 / 4.34-4.39, 3 MiB 7.36-7.37 / 5.36-5.41,
+//              256 MiB 370.1 / 347.8;
+// the bulk form ahead at every larger size measured (up to 256 MiB).  So:
+// one or two sources from 12 MiB, three from 8 MiB, four from 6 MiB, five
+// from 4 MiB, six to eight from 3 MiB.
 constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
     constexpr uint64_t MiB = 1ull << 20;
@@ -271,7 +266,7 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
     case 3:
         return bytes >= 8 * MiB;
     case 4:
-        return bytes >= 8 * MiB && !(bytes >= 32 * MiB && bytes < 64 * MiB);
+        return bytes >= 6 * MiB;
     case 5:
         return bytes >= 4 * MiB;
     case 6:
@@ -285,31 +280,38 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
 constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
 
 // Bytes per source of one tile.  With several sources the stages hold N
-// pieces each, and while CTAs share SMs 4 KiB tiles keep more, shorter
-// pipelines per SM (3 sources: six CTAs; 2: eight; 4: four) than 8 KiB
-// ones (three, four, two), measured faster on GB300 at every size and
-// source count tried, the bytes in flight per SM being about the same (20
-// graphed iterations, GB/s, 8 KiB / 4 KiB): 3 x 256 MiB 7190-7245 /
-// 7354-7355, 2 x 256 MiB 7104-7115 / 7190-7193, 3 x 64 MiB 6657-6673 /
-// 6911-6930, 2 x 32 MiB 7374-7458 / 7814-7816, 4 x 256 MiB 6813-6838 /
-// 7169-7171; 2 KiB, 6 KiB, 12 KiB and 16 KiB tiles and 4-6 stages were
-// slower.  A CTA alone on its SM (the deep pipeline below) is bound by its
+// pieces each.  While CTAs share SMs, small tiles keep more, shorter
+// pipelines per SM than large ones with about the same bytes in flight,
+// and the best size depends on N (20 graphed iterations, rotation on, GB/s
+// at 16 / 64 / 256 MiB per source, tiles of 4 / 3 / 2 KiB):
+//   2 sources 7357 / 7187 / 6398, 7077 / 6915 / 5718, 7206 / 7253 / 5758;
+//   3 sources 7376 / 7548 / 7062, 6893 / 7041 / 6733, 7354 / 7401 / 7015;
+//   4 sources 6895 / 7042 / 7134, 6815 / 6938 / 7020, 7173 / 7315 / 7331;
+//   5 sources 6189 / 6268 / 6884, 6758 / 6764 / 7068, 6864 / 6877 / 7366;
+//   6 sources 6106 / 6172 / 6449, 6926 / 6947 / 7082, 7181 / 7244 / 7307;
+//   7 sources 5728 / 6130 / 6222, 6280 / 6625 / 6860, 6475 / 6728 / 7192;
+//   8 sources 5821 / 6187 / 5833, 6472 / 6856 / 6454, 6649 / 7117 / 6766;
+// 8 KiB tiles (three CTAs per SM for 3 sources) ran 3 x 256 MiB at
+// 7190-7245 and 16 KiB at 6154-6162; 4-6 stages instead of 3 were slower.
+// A CTA alone on its SM (the deep pipeline below) is bound by its
 // per-tile barrier and issue instead, so it takes larger tiles (one CTA,
 // 64 MiB per source, GB/s for 2 / 3 / 4 sources): 4 KiB 37 / 38 / 42,
 // 8 KiB 49 / 59 / 65, 12 KiB 69 / 85 / 96, 16 KiB 86 / 104 / 94.
 // One source is a plain relay, which moves more per SM with fewer, larger
 // bulk copies: 32 KiB stages, two CTAs per SM (measured 3-4% faster on
 // large copies than 8 KiB with eight CTAs per SM), alone or not.
-constexpr uint32_t kSharedTile = 4096;
+constexpr int kBulkMaxSrcs = 8;
+// Tile bytes per source while CTAs share SMs, by source count (index 1 is
+// the relay's).
+constexpr uint32_t kSharedTile[kBulkMaxSrcs + 1] = {0, 32768, 4096, 3072, 2048, 2048, 2048, 2048, 3072};
 constexpr uint32_t kDeepTile = 16384;
 constexpr uint32_t kDeepTileMany = 8192;  // 5 to 8 sources: three or more stages still fit
 constexpr uint32_t kRelayTile = 32768;
-constexpr int kBulkMaxSrcs = 8;
 
 constexpr uint32_t bulk_tile(int n_src, bool deep)
 {
     return n_src == 1 ? kRelayTile
-                      : deep ? (n_src <= 4 ? kDeepTile : kDeepTileMany) : kSharedTile;
+                      : deep ? (n_src <= 4 ? kDeepTile : kDeepTileMany) : kSharedTile[n_src];
 }
 
 constexpr size_t bulk_smem_bytes(int n_src, uint32_t tile, uint32_t stages)
@@ -465,13 +467,13 @@ BulkKernel pick_bulk(int n_src, bool deep, uint32_t stages, size_t *smem)
     *smem = bulk_smem_bytes(n_src, bulk_tile(n_src, deep), stages);
     switch (n_src) {
     case 1: return k_reduce_bulk<1, kRelayTile>;
-    case 2: return deep ? k_reduce_bulk<2, kDeepTile> : k_reduce_bulk<2, kSharedTile>;
-    case 3: return deep ? k_reduce_bulk<3, kDeepTile> : k_reduce_bulk<3, kSharedTile>;
-    case 4: return deep ? k_reduce_bulk<4, kDeepTile> : k_reduce_bulk<4, kSharedTile>;
-    case 5: return deep ? k_reduce_bulk<5, kDeepTileMany> : k_reduce_bulk<5, kSharedTile>;
-    case 6: return deep ? k_reduce_bulk<6, kDeepTileMany> : k_reduce_bulk<6, kSharedTile>;
-    case 7: return deep ? k_reduce_bulk<7, kDeepTileMany> : k_reduce_bulk<7, kSharedTile>;
-    case 8: return deep ? k_reduce_bulk<8, kDeepTileMany> : k_reduce_bulk<8, kSharedTile>;
+    case 2: return deep ? k_reduce_bulk<2, kDeepTile> : k_reduce_bulk<2, kSharedTile[2]>;
+    case 3: return deep ? k_reduce_bulk<3, kDeepTile> : k_reduce_bulk<3, kSharedTile[3]>;
+    case 4: return deep ? k_reduce_bulk<4, kDeepTile> : k_reduce_bulk<4, kSharedTile[4]>;
+    case 5: return deep ? k_reduce_bulk<5, kDeepTileMany> : k_reduce_bulk<5, kSharedTile[5]>;
+    case 6: return deep ? k_reduce_bulk<6, kDeepTileMany> : k_reduce_bulk<6, kSharedTile[6]>;
+    case 7: return deep ? k_reduce_bulk<7, kDeepTileMany> : k_reduce_bulk<7, kSharedTile[7]>;
+    case 8: return deep ? k_reduce_bulk<8, kDeepTileMany> : k_reduce_bulk<8, kSharedTile[8]>;
     default: *smem = 0; return nullptr;
     }
 }

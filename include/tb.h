@@ -131,9 +131,8 @@ typedef struct {
        adds done in shared memory (1 to 8 sources sharing a 16-byte
        alignment, else TB_ENOTSUP); 0 = the library's choice, by what
        measured faster on GB300: 2 where it applies, vec_bytes is 0 and
-       each source holds at least 12 MiB (one or two sources), at least
-       8 MiB (three), at least 8 MiB but not 32 to 64 MiB (four), at least
-       4 MiB (five) or at least 3 MiB (six to eight); else 1.
+       each source holds at least 12 MiB (one or two sources), 8 MiB
+       (three), 6 MiB (four), 4 MiB (five) or 3 MiB (six to eight); else 1.
        Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy

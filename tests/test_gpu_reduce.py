@@ -211,8 +211,10 @@ def test_reduce_plan_engine_choice(tb, ctx):
     three = [p, p + 4096, p + 8192]
     info = ctx.reduce_plan(three, far, 2 * big)
     assert info["engine"] == 2 and info["vec_bytes"] == 16       # bulk where it applies
-    assert (info["tile_bytes"], info["stages"]) == (4096, 3)      # short tiles, CTAs share SMs
-    assert info["smem_bytes"] == 128 + 3 * 3 * 4096
+    assert (info["tile_bytes"], info["stages"]) == (3072, 3)      # short tiles, CTAs share SMs
+    assert info["smem_bytes"] == 128 + 3 * 3 * 3072
+    assert [ctx.reduce_plan([p] * n, far, 2 * big)["tile_bytes"] for n in range(2, 9)] \
+        == [4096, 3072, 2048, 2048, 2048, 2048, 3072]
     relay = ctx.reduce_plan([p], far, 2 * big)
     assert (relay["tile_bytes"], relay["stages"]) == (32768, 3)
     vec = ctx.reduce_plan([p] * 9, far, 2 * big)
@@ -229,10 +231,10 @@ def test_reduce_plan_engine_choice(tb, ctx):
     one = 12 << 20
     assert ctx.reduce_plan([p], far, one)["engine"] == 2          # one source: from 12 MiB
     assert ctx.reduce_plan([p], far, one - 256)["engine"] == 1
-    four = three + [p + 12288]                                    # four: 8-32 MiB, >= 64 MiB
+    four = three + [p + 12288]                                    # four: from 6 MiB
     assert [ctx.reduce_plan(four, far, m)["engine"]
-            for m in (4 * MB, 8 * MB - 256, 8 * MB, 32 * MB - 256, 32 * MB, 48 * MB,
-                      64 * MB - 256, 64 * MB, 256 * MB)] == [1, 1, 2, 2, 1, 1, 1, 2, 2]
+            for m in (4 * MB, 6 * MB - 256, 6 * MB, 32 * MB, 48 * MB, 256 * MB)] \
+        == [1, 1, 2, 2, 2, 2]
     info = ctx.reduce_plan([p] * 5, far, 4096)
     assert info["engine"] == 1 and info["vec_bytes"] == 32       # more than 4 sources
     info = ctx.reduce_plan([p + 4, p + 8], far, 4096)
