@@ -217,7 +217,10 @@ def run_reduce(args, tb, torch, ranks, local):
     n_src = 3
     rotate = 256 * MiB
     plan = tb.rotation_plan(nb, rotate)
-    ctx = tb.Context(local, ctx_options(tb))
+    # early_reads: each timed step may read its sources before the step ahead
+    # has finished, as TransferBench's loop inside tb_run_transfer does; no
+    # step writes a source (the steps write dst only).
+    ctx = tb.Context(local, ctx_options(tb, early_reads=1))
     stream = torch.cuda.current_stream()
     srcs = [torch.empty(plan.alloc_bytes, dtype=torch.uint8, device="cuda") for _ in range(n_src)]
     for k, s in enumerate(srcs):

@@ -206,6 +206,8 @@ int check_options(tb_ctx *ctx, const tb_options &o)
         return fail(ctx, TB_EINVAL, "batch_short_shape must be 0..%d", tb::kShortShapes);
     if (o.batch_max_ctas < 0)
         return fail(ctx, TB_EINVAL, "batch_max_ctas must be >= 0");
+    if (o.early_reads != 0 && o.early_reads != 1)
+        return fail(ctx, TB_EINVAL, "early_reads must be 0 or 1");
     if (o.wait_timeout_ns == 0)
         return fail(ctx, TB_EINVAL, "wait_timeout_ns must be > 0");
     if (o.vec_bytes != 0 && o.vec_bytes != 4 && o.vec_bytes != 16 && o.vec_bytes != 32)
@@ -504,6 +506,7 @@ void tb_options_default(tb_options *o)
     o->batch_min_copies = 0;
     o->batch_short_shape = 0;
     o->batch_max_ctas = 0;
+    o->early_reads = 0;
 }
 
 int tb_parse_bytes(const char *text, uint64_t *out)
@@ -584,6 +587,7 @@ int tb_options_from_env(tb_options *o)
         env_i32("MC_HIP_BATCH_COPY_MIN", &o->batch_min_copies, &bad);
     env_i32("TB_BATCH_SHORT_SHAPE", &o->batch_short_shape, &bad);
     env_i32("TB_BATCH_MAX_CTAS", &o->batch_max_ctas, &bad);
+    env_i32("TB_EARLY_READS", &o->early_reads, &bad);
     return bad ? TB_EINVAL : TB_OK;
 }
 
@@ -908,6 +912,7 @@ int tb_reduce_copy(tb_ctx *ctx, const void *const *srcs, int n_src, void *dst, u
     int rc = plan_for(ctx, &p, srcs, n_src, dst, num_bytes, num_subexec);
     if (rc != TB_OK)
         return rc;
+    p.early = ctx->opt.early_reads && p.pdl ? 1 : 0;
     TB_CUDA(ctx, tb::launch_reduce(p, static_cast<cudaStream_t>(stream)));
     return TB_OK;
 }

@@ -70,6 +70,7 @@ class Options(ct.Structure):
         ("batch_min_copies", _i32),
         ("batch_short_shape", _i32),
         ("batch_max_ctas", _i32),
+        ("early_reads", _i32),
     ]
 
 

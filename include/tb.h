@@ -203,6 +203,14 @@ typedef struct {
        for GPUs that also run compute.  Fewer CTAs copy more slowly and take
        fewer SMs at once; results do not change.  Default 0. */
     int32_t batch_max_ctas;
+    /* 1 = a tb_reduce_copy launch (with use_pdl) may start reading its
+       sources before the launch of this library queued ahead of it on the
+       stream has finished, as every launch after the first does inside
+       tb_run_transfer's loop; its writes still wait.  Only for callers whose
+       earlier work on that stream never writes this launch's sources, for
+       example successive reduce-copies over slices nothing writes: a launch
+       reading the previous one's output must keep 0.  Default 0. */
+    int32_t early_reads;
 } tb_options;
 
 /* Fills *opt with the defaults above. */
@@ -218,7 +226,7 @@ void tb_options_default(tb_options *opt);
      TB_USE_PDL, TB_KERNEL_WAIT_NS, TB_VALIDATE_DIRECT (or VALIDATE_DIRECT),
      TB_VALIDATE_SOURCE (or VALIDATE_SOURCE), TB_CHECK_OVERLAP, TB_BATCH_COPY_MIN
      (or MC_HIP_BATCH_COPY_MIN; batch_min_copies), TB_BATCH_SHORT_SHAPE,
-     TB_BATCH_MAX_CTAS.
+     TB_BATCH_MAX_CTAS, TB_EARLY_READS.
    A TB_ name, when set, wins over the bare name beside it; the bare names are
    the ones TransferBench and Mooncake read, so their users' environments
    carry over.  Byte counts go through tb_parse_bytes.  Returns TB_EINVAL

@@ -160,10 +160,11 @@ def test_options_env_new_fields(tb, monkeypatch):
     monkeypatch.setenv("TB_KERNEL_WAIT_NS", "0")
     monkeypatch.setenv("TB_BATCH_SHORT_SHAPE", "2")
     monkeypatch.setenv("TB_BATCH_MAX_CTAS", "64")
+    monkeypatch.setenv("TB_EARLY_READS", "1")
     o = tb.options_from_env()
     assert o.use_graph == 0 and o.reduce_engine == 2 and o.ce_min_bytes == 1 << 20
     assert o.use_pdl == 0 and o.kernel_wait_ns == 0
-    assert o.batch_short_shape == 2 and o.batch_max_ctas == 64
+    assert o.batch_short_shape == 2 and o.batch_max_ctas == 64 and o.early_reads == 1
 
 
 def test_validation_options_from_env(tb, monkeypatch):

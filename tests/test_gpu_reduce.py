@@ -528,6 +528,52 @@ def test_captured_chain_reads_previous_output(tb, engine):
 
 
 @pytest.mark.parametrize("graph", [1, 0])
+@pytest.mark.parametrize("nsrc,n", [(3, 3 * (1 << 20) + 5), (3, 40000 + 3), (6, 1 << 20)])
+def test_early_reads_over_unwritten_slices(tb, graph, nsrc, n):
+    """early_reads = 1: successive tb_reduce_copy launches over rotation
+    slices that nothing writes, each free to read its sources before the
+    launch ahead has finished (the bulk form at 12 MiB, the vector form at
+    160 KB): dst holds the sum of the last launch's slices, bit for bit, as
+    one captured CUDA graph and as stream launches; with 0 the same."""
+    import torch
+    K, launches = 5, 12
+    nb = 4 * n
+    plan = tb.rotation_plan(nb, K * nb)
+    g = np.random.default_rng(600 + nsrc + n % 97 + graph)
+    slices = [[finite_floats(g, n) for _ in range(K)] for _ in range(nsrc)]
+    bufs = []
+    for per_src in slices:
+        b = dev_bytes(plan.alloc_bytes)
+        for j, a in enumerate(per_src):
+            b[j * plan.slice_stride:j * plan.slice_stride + nb].copy_(to_dev(a))
+        bufs.append(b)
+    last = (launches - 1) % K
+    exp = oracle.dst_reference([per_src[last] for per_src in slices])
+    for early in (1, 0):
+        dst = dev_bytes(nb, fill=0)
+        with tb.Context(0, tb.options(early_reads=early)) as c:
+            def chain(stream):
+                for i in range(launches):
+                    off = (i % K) * plan.slice_stride
+                    c.reduce_copy([b.data_ptr() + off for b in bufs], dst, nb, 0, stream)
+            torch.cuda.synchronize()
+            if graph:
+                cap = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                with torch.cuda.graph(cap, stream=s):
+                    chain(s)
+                cap.replay()
+                torch.cuda.synchronize()
+                del cap
+            else:
+                s = torch.cuda.Stream()
+                chain(s)
+                s.synchronize()
+        mm = oracle.first_mismatch(to_host(dst).view(np.uint32), exp.view(np.uint32))
+        assert mm == -1, f"early_reads={early}: first mismatch at element {mm}"
+
+
+@pytest.mark.parametrize("graph", [1, 0])
 @pytest.mark.parametrize("iters,warmup,K", [(5, 3, 8), (1, 3, 8), (8, 0, 8), (3, 5, 4), (7, 2, 1)])
 def test_rotation_reads_slice_i_mod_k(tb, iters, warmup, K, graph):
     """Slices filled with different patterns: after the loop dst holds the
