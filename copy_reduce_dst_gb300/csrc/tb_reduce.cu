@@ -277,7 +277,15 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
         return false;
     }
 }
-constexpr uint64_t kBulkTilesPerCta = 4;         // target tiles per CTA of a bulk launch
+// Target tiles per CTA of a bulk launch (while CTAs share SMs).  GB/s at 16
+// / 64 / 256 MiB per source with 4 / 8 tiles: 3 sources 7463 / 7496, 7022 /
+// 6994, 7401 / 7350; 5 sources 6851 / 6836, 7055 / 7012, 7369 / 7295;
+// 7 sources 6218 / 6626, 6824 / 6983, 7171 / 7302; 8 sources 6208 / 6544,
+// 6785 / 7032, 7049 / 7334 (2 tiles were slower for every count).
+constexpr uint64_t bulk_tiles_per_cta(int n_src)
+{
+    return n_src >= 6 ? 8 : 4;
+}
 
 // Bytes per source of one tile.  With several sources the stages hold N
 // pieces each.  While CTAs share SMs, small tiles keep more, shorter
@@ -720,7 +728,7 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         wave = (int64_t)std::min<uint64_t>((uint64_t)full, std::max<uint64_t>((uint64_t)num_sms, rounds));
         whole_rounds = rounds >= (uint64_t)wave;
     } else {
-        // Bulk form: many short-lived CTAs of about kBulkTilesPerCta tiles
+        // Bulk form: many short-lived CTAs of about bulk_tiles_per_cta tiles
         // each rather than one resident wave with equal shares.  The CTA
         // scheduler then hands the next CTA to whichever SM finishes first,
         // so no SM ends the launch late (1 source, 2 GiB: 7.1 TB/s against
@@ -729,7 +737,8 @@ int plan_reduce(ReducePlan *p, const void *const *srcs, int n_src, void *dst, ui
         // (1 source, 64 MiB: 1.7 waves 6.7 TB/s, one wave 7.2).
         const uint64_t tile_vecs = bulk_tile(n_src, false) / 16;
         const uint64_t tiles = (p->nvec + tile_vecs - 1) / tile_vecs;
-        const uint64_t want = (tiles + kBulkTilesPerCta - 1) / kBulkTilesPerCta;
+        const uint64_t per_cta = bulk_tiles_per_cta(n_src);
+        const uint64_t want = (tiles + per_cta - 1) / per_cta;
         const uint64_t waves = std::max<uint64_t>(1, std::min<uint64_t>(want / (uint64_t)full, 4096));
         wave = (int64_t)(waves * (uint64_t)full);
     }
