@@ -50,8 +50,7 @@ __device__ __forceinline__ void vload<32>(Vec<32> &v, const void *p)
 // Measured on GB300 against L1::no_allocate stores: 4 MiB transfer with
 // rotation, 10 graphed iterations 2.43-2.44 against 2.52-2.53 us per
 // iteration (mean of 25 runs); 64 iterations, 8 MiB and 3 x 256 MiB the
-// same within 1%; one CTA alone on its SM, 3 / 4 sources of 64 MiB (the
-// 1024-thread form): 142.0 / 135.1 against 130.9 / 129.2 GB/s.
+// same within 1%.
 template <int VB>
 __device__ __forceinline__ void vstore(void *p, const Vec<VB> &v);
 
