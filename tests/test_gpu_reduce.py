@@ -140,6 +140,28 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
                            num_subexec=subexec)
 
 
+@pytest.mark.parametrize("nsrc", [2, 3, 4, 5, 6, 7, 8])
+def test_bulk_several_waves(tb, nsrc):
+    """The bulk form's own grid at 32 MiB per source (plus a 12-byte tail,
+    pointers 4 bytes past alignment): whole waves of short-lived CTAs (two
+    or three waves from three sources on; one for two), each over about 4
+    tiles (8 from six sources), the tile size its source count's; bit-exact
+    against the oracle, guard bytes untouched."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = (32 << 20) // 4 + 3
+    g = np.random.default_rng(700 + nsrc)
+    srcs = [finite_floats(g, n) for _ in range(nsrc)]
+    with tb.Context(0) as c:
+        d = dev_bytes(1 << 20)
+        far = d.data_ptr() + (1 << 36) + 4       # planning only: never accessed
+        info = c.reduce_plan([d.data_ptr() + 4] * nsrc, far, 4 * n)
+        tile = {2: 4096, 3: 3072, 4: 2048, 5: 2048, 6: 2048, 7: 2048, 8: 3072}[nsrc]
+        assert info["engine"] == 2 and info["tile_bytes"] == tile
+        assert info["grid"] % sms == 0                                 # whole waves
+        reduce_and_compare(tb, c, srcs, byte_offsets=[4] * nsrc, dst_offset=4)
+
+
 @pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("subexec", [1, 4, 32, 152])
 def test_bulk_deep_pipeline(tb, nsrc, subexec):
