@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(512) k_reduce_many(const ReduceArgs a, int n_s
 }
 
 // ---------------------------------------------------------------------------
-// K1, bulk form (1 to 8 sources, every pointer sharing its address modulo
+// K1, bulk form (1 to 16 sources, every pointer sharing its address modulo
 // 16).  The body is cut into tiles of kTile bytes per source (bulk_tile).
 // Thread 0 streams each tile's N source pieces into one of the launch's
 // shared-memory stages with bulk copies (one mbarrier per stage); all threads add the
@@ -253,9 +253,17 @@ constexpr int kBulkThreads = 256;
 //   7 sources  2 MiB 3.77-3.82 / 4.03, 3 MiB 8.17 / 4.90, 256 MiB 432.4 / 302.0;
 //   8 sources  2 MiB 4.08-4.13 / 4.34-4.39, 3 MiB 7.36-7.37 / 5.36-5.41,
 //              256 MiB 370.1 / 347.8;
-// the bulk form ahead at every larger size measured (up to 256 MiB).  So:
-// one or two sources from 12 MiB, three from 8 MiB, four from 6 MiB, five
-// from 4 MiB, six to eight from 3 MiB.
+// the bulk form ahead at every larger size measured (up to 256 MiB);
+//   9 sources  1 MiB 5.8 / 3.4, 8 MiB 17.1 / 12.8, 256 MiB 376.6 / 365.1;
+//   12 sources 2 MiB 9.0 / 5.5, 32 MiB 67.5 / 62.8, 256 MiB 490.6 / 478.4;
+//   13 sources 1 MiB 7.7 / 4.0-4.1, 64 MiB 136.6-136.9 / 144.4, 256 MiB 527.2
+//              / 562.0-562.7 (from 13 sources the 2 KiB stages fit two CTAs
+//              per SM, not three, and 1 KiB tiles measured the same);
+//   16 sources 1 MiB 9.4 / 4.5, 32 MiB 87.6 / 84.6, 64 MiB 165.9-166.0 /
+//              167.2-167.3, 256 MiB 643.4-643.7 / 646.9.
+// So: one or two sources from 12 MiB, three from 8 MiB, four from 6 MiB,
+// five from 4 MiB, six to eight from 3 MiB, nine to twelve from 1 MiB,
+// thirteen to sixteen from 1 MiB up to 32 MiB.
 constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
     constexpr uint64_t MiB = 1ull << 20;
@@ -273,6 +281,16 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
     case 7:
     case 8:
         return bytes >= 3 * MiB;
+    case 9:
+    case 10:
+    case 11:
+    case 12:
+        return bytes >= 1 * MiB;
+    case 13:
+    case 14:
+    case 15:
+    case 16:
+        return bytes >= 1 * MiB && bytes < 32 * MiB;
     default:
         return false;
     }
@@ -308,12 +326,14 @@ constexpr uint64_t bulk_tiles_per_cta(int n_src)
 // One source is a plain relay, which moves more per SM with fewer, larger
 // bulk copies: 32 KiB stages, two CTAs per SM (measured 3-4% faster on
 // large copies than 8 KiB with eight CTAs per SM), alone or not.
-constexpr int kBulkMaxSrcs = 8;
+constexpr int kBulkMaxSrcs = 16;
 // Tile bytes per source while CTAs share SMs, by source count (index 1 is
 // the relay's).
-constexpr uint32_t kSharedTile[kBulkMaxSrcs + 1] = {0, 32768, 4096, 3072, 2048, 2048, 2048, 2048, 3072};
+constexpr uint32_t kSharedTile[kBulkMaxSrcs + 1] = {0,    32768, 4096, 3072, 2048, 2048,
+                                                    2048, 2048,  3072, 2048, 2048, 2048,
+                                                    2048, 2048,  2048, 2048, 2048};
 constexpr uint32_t kDeepTile = 16384;
-constexpr uint32_t kDeepTileMany = 8192;  // 5 to 8 sources: three or more stages still fit
+constexpr uint32_t kDeepTileMany = 8192;  // 5 or more sources: two or more stages fit up to 14
 constexpr uint32_t kRelayTile = 32768;
 
 constexpr uint32_t bulk_tile(int n_src, bool deep)
@@ -482,6 +502,14 @@ BulkKernel pick_bulk(int n_src, bool deep, uint32_t stages, size_t *smem)
     case 6: return deep ? k_reduce_bulk<6, kDeepTileMany> : k_reduce_bulk<6, kSharedTile[6]>;
     case 7: return deep ? k_reduce_bulk<7, kDeepTileMany> : k_reduce_bulk<7, kSharedTile[7]>;
     case 8: return deep ? k_reduce_bulk<8, kDeepTileMany> : k_reduce_bulk<8, kSharedTile[8]>;
+    case 9: return deep ? k_reduce_bulk<9, kDeepTileMany> : k_reduce_bulk<9, kSharedTile[9]>;
+    case 10: return deep ? k_reduce_bulk<10, kDeepTileMany> : k_reduce_bulk<10, kSharedTile[10]>;
+    case 11: return deep ? k_reduce_bulk<11, kDeepTileMany> : k_reduce_bulk<11, kSharedTile[11]>;
+    case 12: return deep ? k_reduce_bulk<12, kDeepTileMany> : k_reduce_bulk<12, kSharedTile[12]>;
+    case 13: return deep ? k_reduce_bulk<13, kDeepTileMany> : k_reduce_bulk<13, kSharedTile[13]>;
+    case 14: return deep ? k_reduce_bulk<14, kDeepTileMany> : k_reduce_bulk<14, kSharedTile[14]>;
+    case 15: return deep ? k_reduce_bulk<15, kDeepTileMany> : k_reduce_bulk<15, kSharedTile[15]>;
+    case 16: return deep ? k_reduce_bulk<16, kDeepTileMany> : k_reduce_bulk<16, kSharedTile[16]>;
     default: *smem = 0; return nullptr;
     }
 }

@@ -125,7 +125,7 @@ def test_reduce_parity_kernel_shapes(tb, vec, unroll, threads, nsrc):
         reduce_and_compare(tb, c, srcs, num_subexec=7)
 
 
-@pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("nsrc", [1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 16])
 @pytest.mark.parametrize("n,offs,subexec", [
     (5, 0, 0), (2048, 0, 1), (2048 * 7 + 3, 4, 3), (1000003, 20, 0), (262144 * 3 + 17, 16, 32),
     (65536, 12, 1000)])
@@ -140,7 +140,7 @@ def test_reduce_parity_bulk_engine(tb, nsrc, n, offs, subexec):
                            num_subexec=subexec)
 
 
-@pytest.mark.parametrize("nsrc", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("nsrc", [2, 3, 4, 5, 6, 7, 8, 12])
 def test_bulk_several_waves(tb, nsrc):
     """The bulk form's own grid at 32 MiB per source (plus a 12-byte tail,
     pointers 4 bytes past alignment): whole waves of short-lived CTAs (two
@@ -156,7 +156,7 @@ def test_bulk_several_waves(tb, nsrc):
         d = dev_bytes(1 << 20)
         far = d.data_ptr() + (1 << 36) + 4       # planning only: never accessed
         info = c.reduce_plan([d.data_ptr() + 4] * nsrc, far, 4 * n)
-        tile = {2: 4096, 3: 3072, 4: 2048, 5: 2048, 6: 2048, 7: 2048, 8: 3072}[nsrc]
+        tile = {2: 4096, 3: 3072, 4: 2048, 5: 2048, 6: 2048, 7: 2048, 8: 3072, 12: 2048}[nsrc]
         assert info["engine"] == 2 and info["tile_bytes"] == tile
         assert info["grid"] % sms == 0                                 # whole waves
         reduce_and_compare(tb, c, srcs, byte_offsets=[4] * nsrc, dst_offset=4)
@@ -239,8 +239,11 @@ def test_reduce_plan_engine_choice(tb, ctx):
         == [4096, 3072, 2048, 2048, 2048, 2048, 3072]
     relay = ctx.reduce_plan([p], far, 2 * big)
     assert (relay["tile_bytes"], relay["stages"]) == (32768, 3)
-    vec = ctx.reduce_plan([p] * 9, far, 2 * big)
+    vec = ctx.reduce_plan([p] * 16, far, 2 * big)
     assert vec["engine"] == 1 and (vec["tile_bytes"], vec["stages"]) == (0, 0)
+    assert [ctx.reduce_plan([p] * n, far, m)["engine"]            # nine to sixteen
+            for n in (9, 12, 13, 16) for m in (MB - 256, MB, 32 * MB - 256, 32 * MB)] \
+        == [1, 2, 2, 2] * 2 + [1, 2, 2, 1] * 2
     assert [ctx.reduce_plan([p] * 5, far, m)["engine"]            # five: from 4 MiB
             for m in (4 * MB - 256, 4 * MB, 256 * MB)] == [1, 2, 2]
     assert [ctx.reduce_plan([p] * n, far, m)["engine"]            # six to eight: from 3 MiB
@@ -324,8 +327,8 @@ def test_bulk_engine_limits(tb):
     d = dev_bytes(1 << 16)
     with tb.Context(0, tb.options(reduce_engine=2)) as c:
         with pytest.raises(tb.TBError) as e:
-            c.reduce_copy([d.data_ptr()] * 9, d.data_ptr() + 8192, 256)    # 9 sources
-        assert e.value.code == tb.TB_ENOTSUP
+            c.reduce_copy([d.data_ptr()] * 17, d.data_ptr() + 8192, 256)   # 17 sources
+        assert e.value.code == tb.TB_EINVAL
         with pytest.raises(tb.TBError) as e:
             c.reduce_copy([d.data_ptr() + 4], d.data_ptr() + 8192, 256)   # no common 16 B
         assert e.value.code == tb.TB_ENOTSUP
