@@ -194,13 +194,13 @@ _sig("tb_run_transfer", ct.c_int, _vp, _P(_vp), ct.c_int, _vp, _u64, ct.c_int, c
      _P(Result))
 _sig("tb_reduce_copy_host", ct.c_int, _vp, _P(_vp), ct.c_int, _vp, _u64, _P(_vp), _vp, ct.c_int,
      _vp)
-_sig("tb_batch_copy", ct.c_int, _vp, _P(CopyDesc), ct.c_size_t, _vp)
+_sig("tb_batch_copy", ct.c_int, _vp, _vp, ct.c_size_t, _vp)  # desc: a CopyDesc array's address
 _sig("tb_last_batch_stats", ct.c_int, _vp, _P(BatchStats))
 _sig("tb_last_batch_kernel_ms", ct.c_int, _vp, _P(ct.c_double))
-_sig("tb_copy_each", ct.c_int, _vp, _P(CopyDesc), ct.c_size_t, _vp)
+_sig("tb_copy_each", ct.c_int, _vp, _vp, ct.c_size_t, _vp)  # desc: a CopyDesc array's address
 _sig("tb_validate", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
 _sig("tb_validate_device", ct.c_int, _vp, _vp, _vp, _u64, _u32, _P(Mismatch))
-_sig("tb_batch_copy_noalloc", ct.c_int, _P(CopyDesc), ct.c_size_t, _vp)
+_sig("tb_batch_copy_noalloc", ct.c_int, _vp, ct.c_size_t, _vp)  # desc: as tb_batch_copy
 
 TB_NOALLOC_MAX_ITEMS = 65536
 TB_EXEC_GPU = 0
@@ -424,16 +424,24 @@ class Context:
     # -- batched copy ------------------------------------------------------
     @staticmethod
     def descriptor_array(descs):
-        """(pointer, count, keep-alive) for a ctypes CopyDesc array or an
-        (n, 3) uint64 array of (src, dst, len) rows."""
+        """(address, count, keep-alive) for a ctypes CopyDesc array or an
+        (n, 3) uint64 array of (src, dst, len) rows.  The address is taken
+        without a ctypes pointer object, which would cost more than the rest
+        of a small call's host work."""
         if isinstance(descs, ct.Array):
-            return ct.cast(descs, ct.POINTER(CopyDesc)), len(descs), descs
+            return ct.addressof(descs), len(descs), descs
         import numpy as np
         a = np.ascontiguousarray(descs, dtype=np.uint64)
         if a.ndim != 2 or a.shape[1] != 3:
             raise ValueError("descriptors must be an (n, 3) array of (src, dst, len)")
         n = a.shape[0]
-        return (ct.cast(a.ctypes.data, ct.POINTER(CopyDesc)) if n else None), n, a
+        if n == 0:
+            return None, 0, a
+        try:
+            ptr = ct.addressof(ct.c_uint64.from_buffer(a))
+        except (TypeError, ValueError):  # a read-only array
+            ptr = a.ctypes.data
+        return ptr, n, a
 
     def batch_copy(self, descs, stream=None):
         """tb_batch_copy of (src, dst, len) descriptors (see descriptor_array)."""
