@@ -60,7 +60,7 @@ extern "C" {
 #define TB_ECUDA      (-3)  /* a CUDA call failed; tb_last_error() has the text */
 #define TB_EVALIDATE  (-4)  /* destination differs from the expected bytes */
 #define TB_ETIMEOUT   (-5)  /* a bounded wait (descriptor slot, gate) expired */
-#define TB_ENOTSUP    (-6)  /* request outside what this build supports */
+#define TB_ENOTSUP    (-6)  /* request outside what the library supports */
 
 /* Most sources one reduce-copy accepts. */
 #define TB_MAX_SRCS 16
