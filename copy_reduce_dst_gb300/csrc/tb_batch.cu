@@ -203,7 +203,24 @@ struct BatchArgs {
     uint32_t chunks;
     uint32_t claim_items;        // short copies a warp takes by its index: 1 or 2
     uint64_t wait_ns;            // limit of each wait for a block's load
+    uint32_t *done_count;        // nullable: completion signal (BatchDone)
+    uint32_t *done_word;
+    uint32_t done_base;
+    uint32_t done_seq;
 };
+
+// The completion signal: called by every thread of a CTA at its end.  Every
+// warp's reads of the work list have returned their values (they were used)
+// before the barrier, so thread 0's add comes after all of them; the add
+// that returns done_base + grid - 1 is the launch's last.
+__device__ __forceinline__ void signal_done(const BatchArgs &a)
+{
+    if (!a.done_count)
+        return;
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(a.done_count, 1u) == a.done_base + gridDim.x - 1u)
+        *reinterpret_cast<volatile uint32_t *>(a.done_word) = a.done_seq;
+}
 
 // ---------------------------------------------------------------------------
 // Bulk (TMA) copies through shared memory: cp.async.bulk global -> shared
@@ -616,6 +633,7 @@ __global__ void __launch_bounds__(kBatchThreads, 3) k_batch(const BatchArgs a)
     short_copies<U, S>(a, first, starters, fixed, fixed < a.n_short, lane,
                        smem_u32(smem) + (uint32_t)kBatchSmem +
                            warp * (uint32_t)warp_stage_bytes<U, S>());
+    signal_done(a);
 }
 
 // k_short: a launch of short copies only, over up to kShortWaves waves.
@@ -638,6 +656,7 @@ __global__ void __launch_bounds__(kBatchThreads, MINB) k_short(const BatchArgs a
     const uint32_t fixed = starters * a.claim_items;
     short_copies<U, S>(a, blockIdx.x * wpc + warp, starters, fixed, fixed < a.n_short, lane,
                        smem_u32(smem) + warp * (uint32_t)warp_stage_bytes<U, S>());
+    signal_done(a);
 }
 
 // The shapes of k_short, by number (1-based; 0 names k_batch).
@@ -676,7 +695,7 @@ int batch_ctas_per_sm(int k)
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
-                         uint32_t *status, uint64_t wait_ns)
+                         uint32_t *status, uint64_t wait_ns, const BatchDone &done)
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
@@ -698,6 +717,10 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.chunks = plan.chunks;
     a.claim_items = batch_claim_items(plan);
     a.wait_ns = wait_ns;
+    a.done_count = done.count && done.word ? done.count : nullptr;
+    a.done_word = done.word;
+    a.done_base = done.base;
+    a.done_seq = done.seq;
     const ShapeInfo info = shape(k);
     void *args[] = {&a};
     return cudaLaunchKernel(info.kernel, dim3(plan.grid), dim3(kBatchThreads), args, info.smem,

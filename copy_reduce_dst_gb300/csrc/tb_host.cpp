@@ -35,13 +35,21 @@ struct Slot {
     void *dev = nullptr;       // device copy of one packed launch
     void *host = nullptr;      // pinned staging of it (mapped)
     void *host_dev = nullptr;  // device address of the staging
-    cudaEvent_t done = nullptr;
+    cudaEvent_t done_event = nullptr;
     cudaEvent_t uploaded = nullptr;  // the work list is on the device (upload stream)
-    bool pending = false;      // `done` recorded and maybe not reached yet
+    bool pending = false;      // `done_event` recorded and maybe not reached yet
     cudaEvent_t t0 = nullptr;  // kernel timing (time_kernels only)
     cudaEvent_t t1 = nullptr;
     volatile uint32_t *status = nullptr;  // host-mapped: 1 if a kernel wait expired
     uint32_t *status_dev = nullptr;
+    // Completion signal (tb::BatchDone): the launch's last CTA writes `seq`
+    // into the host-mapped `done_word`, so wait_slot usually learns the slot
+    // is free from one read of host memory instead of an event query.
+    volatile uint32_t *done_word = nullptr;
+    uint32_t *done_word_dev = nullptr;
+    uint32_t *count_dev = nullptr;        // device counter of finished CTAs (only grows)
+    uint32_t count = 0;                   // its value once every launch so far has finished
+    uint32_t seq = 0;                     // of the slot's latest launch
 };
 
 // Chunk size of the staged tb_reduce_copy_host pipeline.
@@ -75,7 +83,8 @@ struct tb_ctx {
     std::vector<float> iter_ms;
 
     std::vector<Slot> slots;
-    void *slot_status = nullptr;      // host-mapped status words, one per slot
+    void *slot_status = nullptr;      // host-mapped status and done words, two per slot
+    uint32_t *slot_counts = nullptr;  // device counters of the completion signal, one per slot
     uint32_t next_slot = 0;
     // CTAs of one resident wave of each batch-kernel shape (0 = k_batch, a
     // launch with long copies; 1.. = the k_short shapes of short-only ones).
@@ -241,8 +250,11 @@ int wait_slot(tb_ctx *ctx, Slot &s)
     if (!s.pending)
         return TB_OK;
     const uint64_t deadline = now_ns() + ctx->opt.wait_timeout_ns;
-    for (;;) {
-        cudaError_t e = cudaEventQuery(s.done);
+    // The kernel's completion word first (one read of host memory), the
+    // slot's event as the fallback: the launch may still be running, or
+    // may not have written the word (a kernel without the signal).
+    while (*s.done_word != s.seq) {
+        cudaError_t e = cudaEventQuery(s.done_event);
         if (e == cudaSuccess)
             break;
         if (e != cudaErrorNotReady)
@@ -686,14 +698,23 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
     ctx->slots.resize(o.num_slots);
     const size_t slot_bytes = tb::batch_buffer_bytes(o.slot_items);
     void *status_dev = nullptr;
-    if (cudaHostAlloc(&ctx->slot_status, o.num_slots * sizeof(uint32_t), cudaHostAllocMapped) !=
+    if (cudaHostAlloc(&ctx->slot_status, 2 * o.num_slots * sizeof(uint32_t), cudaHostAllocMapped) !=
             cudaSuccess ||
         cudaHostGetDevicePointer(&status_dev, ctx->slot_status, 0) != cudaSuccess)
         return bail(TB_ENOMEM);
+    if (cudaMalloc(&ctx->slot_counts, o.num_slots * sizeof(uint32_t)) != cudaSuccess)
+        return bail(TB_ENOMEM);
+    if (cudaMemset(ctx->slot_counts, 0, o.num_slots * sizeof(uint32_t)) != cudaSuccess)
+        return bail(TB_ECUDA);
     for (uint32_t i = 0; i < o.num_slots; ++i) {
-        ctx->slots[i].status = static_cast<volatile uint32_t *>(ctx->slot_status) + i;
-        ctx->slots[i].status_dev = static_cast<uint32_t *>(status_dev) + i;
-        *ctx->slots[i].status = 0u;
+        Slot &sl = ctx->slots[i];
+        sl.status = static_cast<volatile uint32_t *>(ctx->slot_status) + i;
+        sl.status_dev = static_cast<uint32_t *>(status_dev) + i;
+        sl.done_word = static_cast<volatile uint32_t *>(ctx->slot_status) + o.num_slots + i;
+        sl.done_word_dev = static_cast<uint32_t *>(status_dev) + o.num_slots + i;
+        sl.count_dev = ctx->slot_counts + i;
+        *sl.status = 0u;
+        *sl.done_word = 0u;
     }
     for (Slot &s : ctx->slots) {
         if (cudaMalloc(&s.dev, slot_bytes) != cudaSuccess)
@@ -702,7 +723,7 @@ int tb_create(tb_ctx **out, int device, const tb_options *opt)
             return bail(TB_ENOMEM);
         if (cudaHostGetDevicePointer(&s.host_dev, s.host, 0) != cudaSuccess)
             return bail(TB_ECUDA);
-        if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess ||
+        if (cudaEventCreateWithFlags(&s.done_event, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&s.uploaded, cudaEventDisableTiming) != cudaSuccess)
             return bail(TB_ECUDA);
         if (o.time_kernels &&
@@ -722,15 +743,15 @@ void tb_destroy(tb_ctx *ctx)
     // (an upload may be queued on `up` even when its launch failed), and
     // only then free what they may still read or write.
     for (Slot &s : ctx->slots)
-        if (s.done && s.pending)
-            cudaEventSynchronize(s.done);
+        if (s.done_event && s.pending)
+            cudaEventSynchronize(s.done_event);
     for (cudaStream_t s : {ctx->stream, ctx->up, ctx->ce, ctx->pipe.h2d, ctx->pipe.cmp,
                            ctx->pipe.d2h})
         if (s)
             cudaStreamSynchronize(s);
     for (Slot &s : ctx->slots) {
-        if (s.done)
-            cudaEventDestroy(s.done);
+        if (s.done_event)
+            cudaEventDestroy(s.done_event);
         if (s.uploaded)
             cudaEventDestroy(s.uploaded);
         if (s.t0)
@@ -765,6 +786,8 @@ void tb_destroy(tb_ctx *ctx)
         cudaFreeHost((void *)ctx->gate_flag);
     if (ctx->slot_status)
         cudaFreeHost(ctx->slot_status);
+    if (ctx->slot_counts)
+        cudaFree(ctx->slot_counts);
     if (ctx->val_stage)
         cudaFreeHost(ctx->val_stage);
     if (ctx->direct_expected)
@@ -1403,8 +1426,13 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             }
             if (slot.t0)
                 TB_CUDA(ctx, cudaEventRecord(slot.t0, s));
+            tb::BatchDone done;
+            done.count = slot.count_dev;
+            done.word = slot.done_word_dev;
+            done.base = slot.count;
+            done.seq = slot.seq + 1;
             const cudaError_t le = tb::launch_batch(direct ? slot.host_dev : slot.dev, plan, s,
-                                                    slot.status_dev, o.kernel_wait_ns);
+                                                    slot.status_dev, o.kernel_wait_ns, done);
             if (le != cudaSuccess) {
                 // The slot is not marked pending, so its staging may be
                 // rewritten next: let a queued upload finish reading it.
@@ -1412,11 +1440,15 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
                     cudaStreamSynchronize(ctx->up);
                 return cuda_fail(ctx, le, "launch of the batch kernel");
             }
+            // The kernel runs: the slot's staging stays untouched until it
+            // has signalled (or its event has been reached).
+            slot.seq = done.seq;
+            slot.count += plan.grid;
+            slot.pending = true;
+            ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
             if (slot.t1)
                 TB_CUDA(ctx, cudaEventRecord(slot.t1, s));
-            TB_CUDA(ctx, cudaEventRecord(slot.done, s));
-            ctx->last_slots.push_back((uint32_t)(&slot - ctx->slots.data()));
-            slot.pending = true;
+            TB_CUDA(ctx, cudaEventRecord(slot.done_event, s));
             st.launches += 1;
             st.warp_items += plan.n_short;
             st.cta_items += plan.chunks;

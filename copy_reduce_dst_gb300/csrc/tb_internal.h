@@ -193,12 +193,27 @@ bool batch_direct(const BatchPlan &plan);
 // (device, kernel, threads, smem); 0 when a CUDA call fails.
 int resident_ctas(const void *kernel, int threads, size_t smem);
 
+// Completion signal of a batch launch (all fields null: none).  Every CTA
+// adds one to *count (device memory that only grows) once it has finished
+// reading the work list; the CTA whose add returns base + grid - 1 (base:
+// the count before the launch, which the host tracks) is the last, and
+// writes seq to *word (the device address of a host-mapped word), so the
+// host learns with one read of host memory that the launch no longer reads
+// its work list.
+struct BatchDone {
+    uint32_t *count = nullptr;
+    uint32_t *word = nullptr;
+    uint32_t base = 0;
+    uint32_t seq = 0;
+};
+
 // Launches k_batch over a packed buffer (device copy at `dev`).  status
 // (nullable, device-visible) is set to 1 if a bounded wait inside the kernel
 // expired; wait_ns limits each wait of its bulk pipeline for a block's load
 // (0: one non-blocking probe).
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
-                         uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull);
+                         uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull,
+                         const BatchDone &done = BatchDone{});
 
 // CTAs resident per SM for kernel shape k (0 = k_batch, 1..kShortShapes =
 // k_short); 0 for an unknown shape or when a CUDA call fails.

@@ -169,6 +169,39 @@ def test_more_launches_than_slots(tb):
             run_layout(tb, c, workloads.random_batch(30 + i, 3000, 4000, 64 * MiB), 40 + i)
 
 
+@pytest.mark.parametrize("with_long", [0, 1])
+def test_one_slot_back_to_back(tb, with_long):
+    """200 calls queued without a sync on one slot, call i copying its own
+    source region into its own destination region (64 copies of 2112 B, plus
+    one 64 KiB copy that makes the launch upload its work list): the slot is
+    reused only after the launch before it has finished reading the work
+    list, so every region ends equal to its source."""
+    import torch
+    calls, per, size, big = 200, 64, 2112, 65536
+    region = per * 4224 + (big if with_long else 0)
+    src_h = workloads.random_bytes(calls * region, 91)
+    dst_h = workloads.random_bytes(calls * region, 92)
+    src_d, dst_d = to_dev(src_h), to_dev(dst_h)
+    exp = dst_h.copy()
+    with tb.Context(0, tb.options(num_slots=1)) as c:
+        st = torch.cuda.Stream()
+        for i in range(calls):
+            base = i * region
+            off = np.uint64(base) + np.arange(per, dtype=np.uint64) * np.uint64(4224)
+            lens = np.full(per, size, dtype=np.uint64)
+            if with_long:
+                off = np.append(off, np.uint64(base + per * 4224))
+                lens = np.append(lens, np.uint64(big))
+            desc = np.stack([np.uint64(src_d.data_ptr()) + off, np.uint64(dst_d.data_ptr()) + off,
+                             lens], axis=1)
+            c.batch_copy(desc, st)
+            oracle.apply_batch(exp, src_h, off, off, lens)
+        stats = c.last_batch_stats()
+        st.synchronize()
+    assert stats["direct_launches"] == (0 if with_long else 1)
+    assert oracle.first_mismatch(to_host(dst_d), exp) == -1
+
+
 @pytest.mark.parametrize("small", [1, 64, 1000, 16384, 1 << 20, 16 << 20])
 def test_size_bins(tb, small):
     with tb.Context(0, tb.options(small_max_bytes=small)) as c:
