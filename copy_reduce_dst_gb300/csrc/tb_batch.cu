@@ -578,6 +578,11 @@ __device__ __forceinline__ void short_copies(const BatchArgs &a, uint32_t first,
         return;
     ShortPipe<U, S> p(pipe_smem, lane);
     WorkItem w = load_item(a.shorts + cur);
+    // A launch that follows another on its stream may have started early
+    // (programmatic dependent launch): its own work list is read already,
+    // but no source or destination byte is touched before the launch ahead
+    // has finished and its writes are visible.
+    pdl_wait_prerequisite();
     for (;;) {
         const uint32_t nx = after(cur);
         WorkItem wn{0, 0, 0};
@@ -610,6 +615,8 @@ template <int U, int S>
 __global__ void __launch_bounds__(kBatchThreads, 3) k_batch(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_launch_dependents();
+    pdl_wait_prerequisite();
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -650,6 +657,7 @@ template <int U, int S, int MINB>
 __global__ void __launch_bounds__(kBatchThreads, MINB) k_short(const BatchArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_launch_dependents();
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t wpc = blockDim.x >> 5;
     const uint32_t starters = gridDim.x * wpc;
@@ -695,7 +703,7 @@ int batch_ctas_per_sm(int k)
 }
 
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
-                         uint32_t *status, uint64_t wait_ns, const BatchDone &done)
+                         uint32_t *status, uint64_t wait_ns, const BatchDone &done, bool pdl)
 {
     if (plan.n_short == 0 && plan.n_long == 0)
         return cudaSuccess;
@@ -723,8 +731,17 @@ cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t st
     a.done_seq = done.seq;
     const ShapeInfo info = shape(k);
     void *args[] = {&a};
-    return cudaLaunchKernel(info.kernel, dim3(plan.grid), dim3(kBatchThreads), args, info.smem,
-                            stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kBatchThreads);
+    cfg.dynamicSmemBytes = info.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, info.kernel, args);
 }
 
 }  // namespace tb

@@ -1432,7 +1432,8 @@ int tb_batch_copy(tb_ctx *ctx, const tb_copy_desc *desc, size_t n, tb_stream str
             done.base = slot.count;
             done.seq = slot.seq + 1;
             const cudaError_t le = tb::launch_batch(direct ? slot.host_dev : slot.dev, plan, s,
-                                                    slot.status_dev, o.kernel_wait_ns, done);
+                                                    slot.status_dev, o.kernel_wait_ns, done,
+                                                    o.use_pdl != 0);
             if (le != cudaSuccess) {
                 // The slot is not marked pending, so its staging may be
                 // rewritten next: let a queued upload finish reading it.

@@ -211,9 +211,12 @@ struct BatchDone {
 // (nullable, device-visible) is set to 1 if a bounded wait inside the kernel
 // expired; wait_ns limits each wait of its bulk pipeline for a block's load
 // (0: one non-blocking probe).
+// With pdl the launch may be scheduled before the kernel ahead of it on the
+// stream has finished (programmatic dependent launch): it reads its work
+// list early, and every access to the copies' bytes waits for that kernel.
 cudaError_t launch_batch(const void *dev, const BatchPlan &plan, cudaStream_t stream,
                          uint32_t *status = nullptr, uint64_t wait_ns = 2000000000ull,
-                         const BatchDone &done = BatchDone{});
+                         const BatchDone &done = BatchDone{}, bool pdl = false);
 
 // CTAs resident per SM for kernel shape k (0 = k_batch, 1..kShortShapes =
 // k_short); 0 for an unknown shape or when a CUDA call fails.

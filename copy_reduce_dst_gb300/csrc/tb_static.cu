@@ -171,7 +171,8 @@ extern "C" int tb_batch_copy_noalloc(const tb_copy_desc *desc, size_t n, tb_stre
     if (cudaMemcpyAsync(items, g_host_items, plan.upload_bytes, cudaMemcpyHostToDevice, s) !=
         cudaSuccess)
         return TB_ECUDA;
-    if (tb::launch_batch(items, plan, s, g_dev_status[device], g_dev_wait_ns[device]) !=
+    if (tb::launch_batch(items, plan, s, g_dev_status[device], g_dev_wait_ns[device],
+                         tb::BatchDone{}, true) !=
         cudaSuccess)
         return TB_ECUDA;
     return TB_OK;

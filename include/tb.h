@@ -151,14 +151,16 @@ typedef struct {
        with always_validate, which needs the host between iterations.
        Default 1. */
     int32_t use_graph;
-    /* 1 = reduce-copy kernels are launched with programmatic dependent
-       launch: a launch may be scheduled while the previous kernel on its
-       stream drains, and every CTA waits for that kernel to complete and its
-       writes to be visible before it touches memory, so the results are
-       those of serialised launches with less idle time between them.
-       Inside tb_run_transfer, where the launch before is one of the same
-       transfer (same sources, writing only dst), a launch starts reading
-       its sources before that wait; only its writes wait.  Default 1. */
+    /* 1 = reduce-copy and batched-copy kernels are launched with
+       programmatic dependent launch: a launch may be scheduled while the
+       previous kernel on its stream drains, and every CTA waits for that
+       kernel to complete and its writes to be visible before it touches the
+       copies' bytes, so the results are those of serialised launches with
+       less idle time between them.  A batched-copy launch reads its own
+       work list before that wait.  Inside tb_run_transfer, where the launch
+       before is one of the same transfer (same sources, writing only dst),
+       a launch starts reading its sources before that wait; only its writes
+       wait.  Default 1. */
     int32_t use_pdl;
     /* Limit, in nanoseconds, of each wait inside the kernels' shared-memory
        pipelines (bulk reduce-copy, batched copy) for a load to land.  A wait

@@ -169,6 +169,37 @@ def test_more_launches_than_slots(tb):
             run_layout(tb, c, workloads.random_batch(30 + i, 3000, 4000, 64 * MiB), 40 + i)
 
 
+@pytest.mark.parametrize("pdl", [1, 0])
+@pytest.mark.parametrize("with_long", [0, 1])
+def test_batch_chain_reads_previous_output(tb, pdl, with_long):
+    """20 batches queued on one stream, batch i copying region i into
+    region i + 1 (the next batch's sources): with programmatic dependent
+    launch a batch may start while the one before drains and reads its work
+    list early, yet every copy still sees the previous batch's output; the
+    pool ends as the oracle's batches applied in order."""
+    import torch
+    steps, per, size, big = 20, 64, 2112, 65536
+    region = per * 4224 + (big if with_long else 0)
+    pool_h = workloads.random_bytes((steps + 1) * region, 93)
+    pool_d = to_dev(pool_h)
+    exp = pool_h.copy()
+    inner = np.arange(per, dtype=np.uint64) * np.uint64(4224)
+    lens = np.full(per, size, dtype=np.uint64)
+    if with_long:
+        inner = np.append(inner, np.uint64(per * 4224))
+        lens = np.append(lens, np.uint64(big))
+    with tb.Context(0, tb.options(use_pdl=pdl, num_slots=2)) as c:
+        st = torch.cuda.Stream()
+        for i in range(steps):
+            so = np.uint64(i * region) + inner
+            do = np.uint64((i + 1) * region) + inner
+            base = np.uint64(pool_d.data_ptr())
+            c.batch_copy(np.stack([base + so, base + do, lens], axis=1), st)
+            oracle.apply_batch(exp, exp.copy(), so, do, lens)
+        st.synchronize()
+    assert oracle.first_mismatch(to_host(pool_d), exp) == -1
+
+
 @pytest.mark.parametrize("with_long", [0, 1])
 def test_one_slot_back_to_back(tb, with_long):
     """200 calls queued without a sync on one slot, call i copying its own
