@@ -256,14 +256,17 @@ constexpr int kBulkThreads = 256;
 // the bulk form ahead at every larger size measured (up to 256 MiB);
 //   9 sources  1 MiB 5.8 / 3.4, 8 MiB 17.1 / 12.8, 256 MiB 376.6 / 365.1;
 //   12 sources 2 MiB 9.0 / 5.5, 32 MiB 67.5 / 62.8, 256 MiB 490.6 / 478.4;
-//   13 sources 1 MiB 7.7 / 4.0-4.1, 64 MiB 136.6-136.9 / 144.4, 256 MiB 527.2
-//              / 562.0-562.7 (from 13 sources the 2 KiB stages fit two CTAs
-//              per SM, not three, and 1 KiB tiles measured the same);
-//   16 sources 1 MiB 9.4 / 4.5, 32 MiB 87.6 / 84.6, 64 MiB 165.9-166.0 /
-//              167.2-167.3, 256 MiB 643.4-643.7 / 646.9.
+//   13 sources 1 MiB 7.5-7.6 / 4.1, 64 MiB 137.8-138.0 / 136.1-136.2, 256 MiB
+//              532.3 / 522.2 (1 KiB tiles from 13 sources: 2 KiB stages fit
+//              two CTAs per SM, not three, and ran 256 MiB in 562.0-562.7);
+//   14 sources 1 MiB 8.1-8.2 / 4.2, 256 MiB 571.5-571.7 / 556.4;
+//   15 sources 1 MiB 8.7 / 4.4, 64 MiB 157.4-157.6 / 161.5, 256 MiB
+//              610.8-610.9 / 620.7-620.8;
+//   16 sources 1 MiB 9.3-9.4 / 4.5-4.6, 32 MiB 87.6 / 84.6, 64 MiB 167.3 /
+//              168.9-169.0, 256 MiB 650.0-650.2 / 647.5-647.6.
 // So: one or two sources from 12 MiB, three from 8 MiB, four from 6 MiB,
-// five from 4 MiB, six to eight from 3 MiB, nine to twelve from 1 MiB,
-// thirteen to sixteen from 1 MiB up to 32 MiB.
+// five from 4 MiB, six to eight from 3 MiB, nine to fourteen from 1 MiB,
+// fifteen and sixteen from 1 MiB up to 32 MiB.
 constexpr bool bulk_auto(int n_src, uint64_t bytes)
 {
     constexpr uint64_t MiB = 1ull << 20;
@@ -285,9 +288,9 @@ constexpr bool bulk_auto(int n_src, uint64_t bytes)
     case 10:
     case 11:
     case 12:
-        return bytes >= 1 * MiB;
     case 13:
     case 14:
+        return bytes >= 1 * MiB;
     case 15:
     case 16:
         return bytes >= 1 * MiB && bytes < 32 * MiB;
@@ -331,7 +334,7 @@ constexpr int kBulkMaxSrcs = 16;
 // the relay's).
 constexpr uint32_t kSharedTile[kBulkMaxSrcs + 1] = {0,    32768, 4096, 3072, 2048, 2048,
                                                     2048, 2048,  3072, 2048, 2048, 2048,
-                                                    2048, 2048,  2048, 2048, 2048};
+                                                    2048, 1024,  1024, 1024, 1024};
 constexpr uint32_t kDeepTile = 16384;
 constexpr uint32_t kDeepTileMany = 8192;  // 5 or more sources: two or more stages fit up to 14
 constexpr uint32_t kRelayTile = 32768;

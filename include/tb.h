@@ -132,8 +132,8 @@ typedef struct {
        TB_ENOTSUP); 0 = the library's choice, by what measured faster on
        GB300: 2 where it applies, vec_bytes is 0 and each source holds at
        least 12 MiB (one or two sources), 8 MiB (three), 6 MiB (four),
-       4 MiB (five), 3 MiB (six to eight), 1 MiB (nine to twelve), or 1 to
-       32 MiB (thirteen to sixteen); else 1.
+       4 MiB (five), 3 MiB (six to eight), 1 MiB (nine to fourteen), or 1
+       to 32 MiB (fifteen and sixteen); else 1.
        Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy

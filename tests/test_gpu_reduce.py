@@ -242,8 +242,10 @@ def test_reduce_plan_engine_choice(tb, ctx):
     vec = ctx.reduce_plan([p] * 16, far, 2 * big)
     assert vec["engine"] == 1 and (vec["tile_bytes"], vec["stages"]) == (0, 0)
     assert [ctx.reduce_plan([p] * n, far, m)["engine"]            # nine to sixteen
-            for n in (9, 12, 13, 16) for m in (MB - 256, MB, 32 * MB - 256, 32 * MB)] \
-        == [1, 2, 2, 2] * 2 + [1, 2, 2, 1] * 2
+            for n in (9, 12, 14, 15, 16) for m in (MB - 256, MB, 32 * MB - 256, 32 * MB)] \
+        == [1, 2, 2, 2] * 3 + [1, 2, 2, 1] * 2
+    assert [ctx.reduce_plan([p] * n, far, 8 * MB)["tile_bytes"] for n in (12, 13, 16)] \
+        == [2048, 1024, 1024]
     assert [ctx.reduce_plan([p] * 5, far, m)["engine"]            # five: from 4 MiB
             for m in (4 * MB - 256, 4 * MB, 256 * MB)] == [1, 2, 2]
     assert [ctx.reduce_plan([p] * n, far, m)["engine"]            # six to eight: from 3 MiB
