@@ -133,8 +133,10 @@ typedef struct {
        GB300: 2 where it applies, vec_bytes is 0 and each source holds at
        least 12 MiB (one or two sources), 8 MiB (three), 6 MiB (four),
        4 MiB (five), 3 MiB (six to eight), 1 MiB (nine to fourteen), or 1
-       to 32 MiB (fifteen and sixteen); else 1.
-       Default 0. */
+       to 32 MiB (fifteen and sixteen); else 1.  A split of at most one CTA
+       per SM (ctas_per_subexec with few sub-executors) with 2 to 4 sources
+       sharing a 32-byte alignment takes 1 in 1024-thread CTAs, which stream
+       more per SM than a lone bulk pipeline.  Default 0. */
     int32_t reduce_engine;
     /* Batched copy: descriptors of at least this many bytes go to the copy
        engines (one cudaMemcpyAsync each, on an internal stream forked from
